@@ -1,0 +1,332 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 tensor-core GEMM path.
+
+One step = the three square GEMMs the study measures at N = 8192 ("Hand-Written
+PTX Tensor-Core GEMM Kernels: A Multi-Precision Study on NVIDIA L4", Tables II
+and III): FP16 -> FP32 (operands normal(0,1)/sqrt(K)), INT8 -> INT32 and packed
+INT4 -> INT32 (operands uniform over their ranges), on seeded synthetic inputs
+already resident in HBM.  The working set of a step (~1.2 GB) is far larger
+than L2, so no flush is needed between steps.
+
+Reported (one JSON line from rank 0):
+  value        2*N^3 multiply-adds counted as operations, summed over the three
+               GEMMs of every step of every rank, divided by the max-over-ranks
+               device time of the timed steps  [TOPS]
+  per_precision  TFLOP/s (FP16) and TOPS (INT8, INT4) of each call, averaged
+               over the timed steps (CUDA events on the launching stream)
+  roofline     the FP16 GEMM kernel (one launch per gemm_f16 call) against the
+               measured bf16 tensor-core peak (FP16 runs at the bf16 rate)
+  e2e          the same metric through the public API with pinned host
+               buffers: H2D of the operands, the GEMMs, D2H of the results
+  cpu_baseline the CPU oracle on a bounded row sample of the same workload
+  clocks       SM clocks and throttle reasons sampled during the timed region
+
+--impl reference times the CPU oracle as the reference arm.
+Multi-GPU: one process per GPU under torchrun; every rank runs the full step
+on its own data (independent problems, weak scaling); only the timing
+barrier and a max-reduction of the elapsed time cross ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s / TOPS at N=8192 (FP16, INT8, INT4); fraction of GB300 dense peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=300)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--n", type=int, default=8192)
+    p.add_argument("--e2e-steps", type=int, default=0, help="0: min(steps, 20)")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline budget")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- inputs
+def make_inputs(n):
+    import datagen
+    A16, B16 = datagen.f16_operands(n, "normal")
+    A8, B8 = datagen.s8_operands(n)
+    A4, B4 = datagen.s4_operands(n)
+    return {"f16": (A16.view(np.float16), B16.view(np.float16)),
+            "s8": (A8, B8), "s4": (A4, B4)}
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = [r.split(", ") for r in out.strip().splitlines() if r.count(",") >= 8]
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        pw = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].strip() == "Active"})
+        busy = [s for s in sm if s > 0.5 * (max(sm) if sm else 1)]
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(pw) if pw else None,
+                "samples": len(rows), "reasons": reasons}
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world, dist):
+    import torch
+    import __graft_entry__
+    import precision_tensor_core_gb300 as ptc
+
+    __graft_entry__.build()
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    n = args.n
+    host = make_inputs(n)
+    d = {k: (torch.from_numpy(np.ascontiguousarray(a)).to(dev),
+             torch.from_numpy(np.ascontiguousarray(b)).to(dev)) for k, (a, b) in host.items()}
+    C16 = torch.empty((n, n), dtype=torch.float32, device=dev)
+    C8 = torch.empty((n, n), dtype=torch.int32, device=dev)
+    C4 = torch.empty((n, n), dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        ptc.matmul_f16(d["f16"][0], d["f16"][1], out=C16)
+        if ev is not None:
+            ev[1].record(stream)
+        ptc.matmul_s8(d["s8"][0], d["s8"][1], out=C8)
+        if ev is not None:
+            ev[2].record(stream)
+        ptc.matmul_s4(d["s4"][0], d["s4"][1], n, out=C4)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert ptc.gemm_poll_device_error() == ptc.PTC_OK
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = ptc.ptc_kernel_launch_count()
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    launches = ptc.ptc_kernel_launch_count() - launches0
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    elapsed_ms = start.elapsed_time(stop)
+    t16 = [e[0].elapsed_time(e[1]) for e in evs]
+    t8 = [e[1].elapsed_time(e[2]) for e in evs]
+    t4 = [e[2].elapsed_time(e[3]) for e in evs]
+    assert ptc.gemm_poll_device_error() == ptc.PTC_OK
+    if dist:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+
+    ops = 2.0 * n ** 3
+    value = 3 * ops * args.steps * world / (elapsed_ms * 1e-3) / 1e12
+    per = {"fp16_tflops": ops / (statistics.mean(t16) * 1e-3) / 1e12,
+           "int8_tops": ops / (statistics.mean(t8) * 1e-3) / 1e12,
+           "int4_tops": ops / (statistics.mean(t4) * 1e-3) / 1e12,
+           "ms": {"fp16": statistics.mean(t16), "int8": statistics.mean(t8), "int4": statistics.mean(t4)}}
+
+    # e2e through the public API with pinned host buffers
+    e2e_steps = args.e2e_steps or min(args.steps, 20)
+    hp = {k: (torch.from_numpy(np.ascontiguousarray(a)).pin_memory(),
+              torch.from_numpy(np.ascontiguousarray(b)).pin_memory()) for k, (a, b) in host.items()}
+    h16 = torch.empty((n, n), dtype=torch.float32, pin_memory=True)
+    h8 = torch.empty((n, n), dtype=torch.int32, pin_memory=True)
+    h4 = torch.empty((n, n), dtype=torch.int32, pin_memory=True)
+
+    def e2e_step():
+        ptc.matmul_f16(hp["f16"][0], hp["f16"][1], out=h16)
+        ptc.matmul_s8(hp["s8"][0], hp["s8"][1], out=h8)
+        ptc.matmul_s4(hp["s4"][0], hp["s4"][1], n, out=h4)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = sum(a.numel() * a.element_size() + b.numel() * b.element_size() for a, b in hp.values())
+    d2h = sum(x.numel() * x.element_size() for x in (h16, h8, h4))
+    e2e = {"value": 3 * ops * e2e_steps * world / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS",
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
+
+    peaks, src = load_peaks()
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    achieved = per["fp16_tflops"]
+    roofline = {"bound": "tensor", "kernel": "gemm_kernel<F16, B MN-major, f32 out> (gemm_f16)",
+                "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "peak_source": f"bf16_tflops_sustained of {src} MEASURED_PEAKS.json (FP16 = bf16 rate)",
+                "traffic": None,
+                "int8_frac_of_f16_peak": per["int8_tops"] / peak,
+                "int4_frac_of_fp8_peak": per["int4_tops"] / (2 * peak)}
+    return {"value": value, "elapsed_ms": elapsed_ms, "per": per, "e2e": e2e, "roofline": roofline,
+            "clocks": clocks, "launches": int(launches)}
+
+
+# ---------------------------------------------------------------- oracle timing
+def oracle_sample(host, n, rows, nthreads):
+    """Run the CPU oracle on the first `rows` output rows of each precision's
+    GEMM; returns (seconds, operations)."""
+    import oracle
+    t0 = time.perf_counter()
+    A16, B16 = host["f16"]
+    oracle.gemm_f16(A16[:rows].view(np.uint16), B16.view(np.uint16), nthreads=nthreads)
+    A8, B8 = host["s8"]
+    oracle.gemm_s8(A8[:rows], B8, nthreads=nthreads)
+    A4, B4 = host["s4"]
+    oracle.gemm_s4(A4[:rows], B4, n, nthreads=nthreads)
+    return time.perf_counter() - t0, 3 * 2.0 * rows * n * n
+
+
+def cpu_baseline(host, n, budget_s):
+    cores = os.cpu_count() or 1
+    rows = cores
+    secs, ops = oracle_sample(host, n, rows, cores)
+    if secs < budget_s / 3:
+        rows = max(rows, min(n, int(rows * (budget_s / 2) / max(secs, 1e-3))) // cores * cores)
+        secs, ops = oracle_sample(host, n, rows, cores)
+    return {"value": ops / secs / 1e12, "unit": "TOPS", "cores": cores, "kind": "oracle",
+            "sample": f"first {rows} output rows of each of the FP16, INT8 and INT4 N={n} GEMMs "
+                      f"({ops:.3g} ops, {secs:.1f} s, {cores} threads)"}
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle, as it stands, on bounded row samples."""
+    n = args.n
+    host = make_inputs(n)
+    cores = os.cpu_count() or 1
+    secs, _ = oracle_sample(host, n, 1, cores)
+    per_step_budget = max(0.05, 150.0 / max(1, args.steps + args.warmup))
+    rows = int(max(1, min(n, per_step_budget / max(secs, 1e-4))))
+    for _ in range(args.warmup):
+        oracle_sample(host, n, rows, cores)
+    total_s, total_ops = 0.0, 0.0
+    for _ in range(args.steps):
+        s, o = oracle_sample(host, n, rows, cores)
+        total_s += s
+        total_ops += o
+    value = total_ops / total_s / 1e12
+    sample = f"first {rows} output rows of each of the FP16, INT8 and INT4 N={n} GEMMs per step"
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_s / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16->f64, s8->s64, s4->s64 (CPU oracle)", "data": "synthetic",
+        "config": {"workload": f"square GEMM N={n}: FP16 normal/sqrt(K), INT8 and INT4 uniform; "
+                               "reference arm = CPU oracle on a row sample", "N": n},
+        "cpu_baseline": {"value": value, "unit": "TOPS", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    res = run_ours(args, rank, world, dist)
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world >= 1:
+            cpu = cpu_baseline(make_inputs(args.n), args.n, args.cpu_seconds)
+        line = {
+            "metric": METRIC, "value": res["value"], "unit": "TOPS", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": res["elapsed_ms"] / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": "f16->f32, s8->s32, s4->s32", "data": "synthetic",
+            "config": {"workload": f"square GEMMs N={args.n}: FP16 (normal/sqrt(K)) -> FP32, "
+                                   "INT8 (uniform) -> INT32, packed INT4 (uniform) -> INT32; "
+                                   "one step = one GEMM of each",
+                       "N": args.n, "l2": "inputs larger than L2 (~1.2 GB per step), no flush",
+                       "parallelism": f"replicas x{world}"},
+            "per_precision": res["per"], "roofline": res["roofline"], "cpu_baseline": cpu,
+            "e2e": res["e2e"], "gpu_launches": res["launches"], "clocks": res["clocks"],
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,167 @@
+/*
+ * ptc.h -- C ABI of libptc: dense tensor-core matrix products C = A.B on one
+ * NVIDIA GB300 (sm_103), in the three precisions of "Hand-Written PTX
+ * Tensor-Core GEMM Kernels: A Multi-Precision Study on NVIDIA L4"
+ * (Borowski & Osinski):
+ *
+ *   gemm_f16  FP16 operands, FP32 accumulation, FP32 result
+ *             (section IV-A and Table VI: FP16 family with f32 accumulators;
+ *             section IV-A's ~537 MB working set at N = 8192 is two FP16
+ *             operands plus an FP32 C)
+ *   gemm_s8   INT8 operands, INT32 accumulation, INT32 result (section IV-B)
+ *   gemm_s4   packed INT4 operands, INT32 accumulation, INT32 result
+ *             (section IV-C, Listings 1-2: mma ... .s32.s4.s4.s32)
+ *
+ * All three compute C <- A.B exactly as the plain sum over k, with C
+ * overwritten and no scaling, bias or dequantisation (section VI "Scope":
+ * INT32 accumulations without in-kernel dequantization or scaling).  The
+ * paper's problems are square (section III-B, N = 512 ... 8192); general
+ * M, N, K >= 0 are accepted.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - A, B, C are DEVICE pointers owned by the caller (any allocator).  The
+ *   library keeps no pointer after the call returns.
+ * - Sizes and leading dimensions are counted in ELEMENTS (for packed INT4:
+ *   in 4-bit elements, i.e. nibbles).
+ * - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
+ *   is asynchronous on that stream and never synchronises the host.  Errors
+ *   raised by the device after launch surface at the caller's next
+ *   synchronisation, or through gemm_poll_device_error().
+ * - The call runs on the calling thread's current CUDA device, which must be
+ *   a compute-capability 10.3 GPU (GB300).  There is no CPU fallback: any
+ *   unsupported case returns an error code and computes nothing.
+ * - M == 0 or N == 0: no-op, returns PTC_OK (pointers may be NULL).
+ *   K == 0: C is filled with zeros (the empty sum), A and B are not read.
+ * - Return value: PTC_OK (0) on success, else one of the PTC_ERR_* codes below.
+ *   Arguments are checked in this order, before any CUDA call:
+ *     PTC_ERR_INVALID  negative or too-large size (each of M, N, K must be
+ *                      <= 2^30, and C must have fewer than 2^31 output tiles
+ *                      of 128 x 256), NULL pointer where data is needed, a leading
+ *                      dimension below its minimum, an odd INT4 leading
+ *                      dimension
+ *     PTC_ERR_ALIGN    a base pointer not 16-byte aligned, or a row pitch in
+ *                      bytes that is not a multiple of 16
+ *     PTC_ERR_OVERLAP  C's byte range intersects A's or B's
+ *   and then, at execution:
+ *     PTC_ERR_DEVICE   no current device, or it is not compute capability 10.3
+ *     PTC_ERR_ALLOC    the stream-ordered workspace could not be obtained
+ *     PTC_ERR_LAUNCH   a CUDA runtime or driver call failed (text available
+ *                      from gemm_status_string(PTC_ERR_LAUNCH) on this thread)
+ *     PTC_ERR_TIMEOUT  (device side, reported by gemm_poll_device_error) a
+ *                      pipeline wait inside a kernel exceeded its time limit;
+ *                      the kernel stopped early and C is incomplete
+ */
+#ifndef PTC_H
+#define PTC_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PTC_OK 0
+#define PTC_ERR_INVALID 1
+#define PTC_ERR_ALIGN 2
+#define PTC_ERR_OVERLAP 3
+#define PTC_ERR_DEVICE 4
+#define PTC_ERR_LAUNCH 5
+#define PTC_ERR_TIMEOUT 6
+#define PTC_ERR_ALLOC 7
+
+/*
+ * FP16 GEMM: C[M x N] (float32) = A[M x K] (binary16) . B[K x N] (binary16),
+ * products accumulated in FP32 on the tensor cores.
+ *   A  row-major, element (i,k) at A[i*lda + k]; lda >= K, lda % 8 == 0
+ *   B  row-major, element (k,j) at B[k*ldb + j]; ldb >= N, ldb % 8 == 0
+ *      (the paper's FP16 kernels load B with ldmatrix .trans, Table VI)
+ *   C  row-major, element (i,j) at C[i*ldc + j]; ldc >= N, ldc % 4 == 0
+ * Accuracy: each element is the FP32 tensor-core sum of exact products; it is
+ * not bitwise reproducible against a sequential sum.
+ */
+int gemm_f16(int64_t M, int64_t N, int64_t K,
+             const void *A, int64_t lda,
+             const void *B, int64_t ldb,
+             float *C, int64_t ldc,
+             void *stream);
+
+/*
+ * INT8 GEMM: C[M x N] (int32) = A[M x K] (int8) . B[K x N] (int8), exact.
+ *   A  row-major,    element (i,k) at A[i*lda + k]; lda >= K, lda % 16 == 0
+ *   B  column-major, element (k,j) at B[j*ldb + k]; ldb >= K, ldb % 16 == 0
+ *      (K-contiguous "non-transposed" B of the paper's .row.col MMAs;
+ *      section IV-D shows a transposed B collapses coalescing)
+ *   C  row-major, element (i,j) at C[i*ldc + j];    ldc >= N, ldc % 4 == 0
+ * Result: bit-exact sum_k A_ik B_kj, wrapped modulo 2^32 if it leaves the
+ * int32 range (unreachable for K <= 131072).
+ * Uses a stream-ordered device workspace of about 2*(M+N)*K bytes, taken
+ * from and returned to a library-owned memory pool on `stream`.
+ */
+int gemm_s8(int64_t M, int64_t N, int64_t K,
+            const int8_t *A, int64_t lda,
+            const int8_t *B, int64_t ldb,
+            int32_t *C, int64_t ldc,
+            void *stream);
+
+/*
+ * Packed INT4 GEMM: C[M x N] (int32) = A[M x K] (s4) . B[K x N] (s4), exact.
+ * Two signed 4-bit values per byte, element 2t of a row in bits 0..3 of byte
+ * t and element 2t+1 in bits 4..7 (low nibble = even k); Listing 1 addresses
+ * A's byte (row, k) at row*(K/2) + k/2.
+ *   A  row-major,    element (i,k) in byte A[i*lda/2 + k/2]; lda >= K,
+ *                    lda even, lda % 32 == 0 (16-byte row pitch)
+ *   B  column-major, element (k,j) in byte B[j*ldb/2 + k/2]; ldb >= K,
+ *                    ldb even, ldb % 32 == 0
+ *   C  row-major int32, ldc >= N, ldc % 4 == 0
+ * Odd K is allowed: the high nibble of a row's last byte is then ignored.
+ * Result: bit-exact sum_k A_ik B_kj (|C| <= 64*K, no overflow for K < 2^25).
+ * Uses a stream-ordered device workspace of about (M+N)*K bytes, as gemm_s8.
+ */
+int gemm_s4(int64_t M, int64_t N, int64_t K,
+            const void *A, int64_t lda,
+            const void *B, int64_t ldb,
+            int32_t *C, int64_t ldc,
+            void *stream);
+
+/* Human-readable text of a status code.  For PTC_ERR_LAUNCH the text of the
+ * failing CUDA call on the calling thread is appended.  Never NULL; the
+ * string stays valid until the next call on the same thread. */
+const char *gemm_status_string(int status);
+
+/* Reads and clears the device-side error word of the current device that the
+ * GEMM kernels set when a pipeline wait times out.  Synchronises the device.
+ * Returns PTC_OK when no kernel reported an error, PTC_ERR_TIMEOUT when one
+ * did, PTC_ERR_DEVICE / PTC_ERR_LAUNCH when the device cannot be queried. */
+int gemm_poll_device_error(void);
+
+/* Number of kernels this library has launched in this process (all devices,
+ * all threads).  Lets callers count the GPU work behind a sequence of calls. */
+uint64_t ptc_kernel_launch_count(void);
+
+/* Test hook, not for production use.  Sets the pipeline-wait time limit (in
+ * nanoseconds, 0 restores the default of one second) and, when stall_tile >= 0,
+ * makes the next launched GEMM kernel withhold the operands of output tile
+ * `stall_tile`, so that the wait for them runs out and the kernel reports
+ * PTC_ERR_TIMEOUT through gemm_poll_device_error().  The stall applies to one
+ * launch only.  Returns PTC_OK. */
+int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile);
+
+/* Tuning and test knobs, process-wide.  Returns PTC_OK, or PTC_ERR_INVALID for
+ * an unknown key or a value out of range.  Keys:
+ *   "group_m"      output-tile rows per raster group of the persistent
+ *                  scheduler (L2 reuse), default 16
+ *   "s8_chunk_kb"  INT8 route: K blocks (64 values each) whose FP32 partial
+ *                  sum is folded into int32 at a time, default 8 (512 values:
+ *                  |partial| <= 2^23, so every FP32 partial sum is an exact
+ *                  integer)
+ *   "s4_chunk_kb"  INT4 route: K blocks (128 values each) per fold, default 2
+ * Values above the defaults can make gemm_s8 / gemm_s4 inexact for adversarial
+ * inputs; they exist to measure the tensor cores' accumulation width. */
+int ptc_set_tuning(const char *key, int64_t value);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PTC_H */

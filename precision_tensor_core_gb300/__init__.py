@@ -1,0 +1,199 @@
+"""Python binding of libptc, the GB300 (sm_103a) tensor-core GEMM library.
+
+Dense matrix products C = A.B in the three precisions of "Hand-Written PTX
+Tensor-Core GEMM Kernels: A Multi-Precision Study on NVIDIA L4"
+(Borowski & Osinski): FP16 -> FP32, INT8 -> INT32 and packed INT4 -> INT32.
+
+Two layers, both argument marshalling only (every arithmetic step runs in the
+library's CUDA kernels):
+
+* ``gemm_f16``, ``gemm_s8``, ``gemm_s4``, ``gemm_status_string``,
+  ``gemm_poll_device_error``, ``ptc_kernel_launch_count``,
+  ``ptc_debug_set_wait_limit``, ``ptc_set_tuning``: the C ABI of
+  ``include/ptc.h`` under the same names, taking integers (sizes, leading
+  dimensions, device addresses, a cudaStream_t handle).  A nonzero status
+  raises :class:`PtcError`.
+* ``matmul_f16``, ``matmul_s8``, ``matmul_s4``: the same calls on torch
+  tensors.  Device tensors run on the current CUDA stream; CPU tensors are
+  copied to the device and the result is copied back (end-to-end use).
+
+There is no CPU fallback: if ``libptc.so`` has not been built the first call
+raises, and on a machine without a compute-capability 10.3 GPU every GEMM call
+raises ``PtcError`` with status ``PTC_ERR_DEVICE``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libptc.so")
+
+PTC_OK = 0
+PTC_ERR_INVALID = 1
+PTC_ERR_ALIGN = 2
+PTC_ERR_OVERLAP = 3
+PTC_ERR_DEVICE = 4
+PTC_ERR_LAUNCH = 5
+PTC_ERR_TIMEOUT = 6
+PTC_ERR_ALLOC = 7
+
+_i64 = ctypes.c_int64
+_vp = ctypes.c_void_p
+_lib = None
+
+
+class PtcError(RuntimeError):
+    """A libptc call returned a nonzero status."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"[{status}] {message}")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load libptc.so (built in-tree by ``__graft_entry__.build()``)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libptc.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name in ("gemm_f16", "gemm_s8", "gemm_s4"):
+            fn = getattr(L, name)
+            fn.restype = ctypes.c_int
+            fn.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]
+        L.gemm_status_string.restype = ctypes.c_char_p
+        L.gemm_status_string.argtypes = [ctypes.c_int]
+        L.gemm_poll_device_error.restype = ctypes.c_int
+        L.gemm_poll_device_error.argtypes = []
+        L.ptc_kernel_launch_count.restype = ctypes.c_uint64
+        L.ptc_kernel_launch_count.argtypes = []
+        L.ptc_debug_set_wait_limit.restype = ctypes.c_int
+        L.ptc_debug_set_wait_limit.argtypes = [ctypes.c_uint64, _i64]
+        L.ptc_set_tuning.restype = ctypes.c_int
+        L.ptc_set_tuning.argtypes = [ctypes.c_char_p, _i64]
+        _lib = L
+    return _lib
+
+
+def _check(status: int) -> int:
+    if status != PTC_OK:
+        raise PtcError(status, gemm_status_string(status))
+    return status
+
+
+def gemm_status_string(status: int) -> str:
+    return lib().gemm_status_string(int(status)).decode()
+
+
+# ---------------------------------------------------------------- C ABI layer
+def gemm_f16(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    """C[MxN] f32 = A[MxK] f16 (row-major) . B[KxN] f16 (row-major); device addresses."""
+    return _check(lib().gemm_f16(M, N, K, A, lda, B, ldb, C, ldc, stream))
+
+
+def gemm_s8(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    """C[MxN] s32 = A[MxK] s8 (row-major) . B[KxN] s8 (column-major); device addresses."""
+    return _check(lib().gemm_s8(M, N, K, A, lda, B, ldb, C, ldc, stream))
+
+
+def gemm_s4(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    """C[MxN] s32 = A[MxK] packed s4 . B[KxN] packed s4 (column-major); lda/ldb in nibbles."""
+    return _check(lib().gemm_s4(M, N, K, A, lda, B, ldb, C, ldc, stream))
+
+
+def gemm_poll_device_error() -> int:
+    """Status of the device error word (read and cleared); synchronises the device."""
+    return int(lib().gemm_poll_device_error())
+
+
+def ptc_kernel_launch_count() -> int:
+    return int(lib().ptc_kernel_launch_count())
+
+
+def ptc_debug_set_wait_limit(timeout_ns: int, stall_tile: int = -1) -> int:
+    return _check(lib().ptc_debug_set_wait_limit(int(timeout_ns), int(stall_tile)))
+
+
+def ptc_set_tuning(key: str, value: int) -> int:
+    return _check(lib().ptc_set_tuning(key.encode(), int(value)))
+
+
+# ---------------------------------------------------------------- torch layer
+def _stream(stream):
+    import torch
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _rowmajor(t, name):
+    """Row pitch in elements of a 2-D tensor with unit column stride.  A single
+    row has no pitch; the smallest one that meets every alignment rule is used."""
+    if t.dim() != 2 or (t.shape[1] > 1 and t.stride(1) != 1):
+        raise ValueError(f"{name} must be a 2-D tensor with unit column stride")
+    if t.shape[0] > 1:
+        return t.stride(0)
+    return max(32, (t.shape[1] + 31) // 32 * 32)
+
+
+def _run(fn, A, B, out, out_shape, out_dtype, M, N, K, lda_scale, stream):
+    import torch
+    host = A.device.type == "cpu"
+    if host != (B.device.type == "cpu"):
+        raise ValueError("A and B must both be on the host or both on the device")
+    if host:
+        dev = torch.device("cuda", torch.cuda.current_device())
+        Ad = A.to(dev, non_blocking=True)
+        Bd = B.to(dev, non_blocking=True)
+        Cd = torch.empty(out_shape, dtype=out_dtype, device=dev)
+    else:
+        Ad, Bd = A, B
+        Cd = out if out is not None else torch.empty(out_shape, dtype=out_dtype, device=A.device)
+    lda = _rowmajor(Ad, "A") * lda_scale
+    ldb = _rowmajor(Bd, "B") * lda_scale
+    ldc = _rowmajor(Cd, "C")
+    fn(M, N, K, Ad.data_ptr(), lda, Bd.data_ptr(), ldb, Cd.data_ptr(), ldc, _stream(stream))
+    if host:
+        if out is None:
+            out = torch.empty(out_shape, dtype=out_dtype, pin_memory=True)
+        out.copy_(Cd, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return out
+    return Cd
+
+
+def matmul_f16(A, B, out=None, stream=None):
+    """FP16 A (M,K) @ B (K,N) -> float32 (M,N) on the tensor cores."""
+    import torch
+    if A.dtype != torch.float16 or B.dtype != torch.float16:
+        raise TypeError("matmul_f16 takes float16 operands")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    return _run(gemm_f16, A, B, out, (M, N), torch.float32, M, N, K, 1, stream)
+
+
+def matmul_s8(A, Bt, out=None, stream=None):
+    """INT8 A (M,K) @ B where B (K,N) is column-major, given as Bt (N,K) -> int32 (M,N)."""
+    import torch
+    if A.dtype != torch.int8 or Bt.dtype != torch.int8:
+        raise TypeError("matmul_s8 takes int8 operands")
+    M, K = A.shape
+    N, K2 = Bt.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    return _run(gemm_s8, A, Bt, out, (M, N), torch.int32, M, N, K, 1, stream)
+
+
+def matmul_s4(A, Bt, K, out=None, stream=None):
+    """Packed INT4 A (M, >=K/2 bytes) @ B, B column-major given as Bt (N, >=K/2 bytes),
+    two values per byte with the low nibble first -> int32 (M,N)."""
+    import torch
+    if A.dtype != torch.uint8 or Bt.dtype != torch.uint8:
+        raise TypeError("matmul_s4 takes packed uint8 operands")
+    M, N = A.shape[0], Bt.shape[0]
+    return _run(gemm_s4, A, Bt, out, (M, N), torch.int32, M, N, int(K), 2, stream)

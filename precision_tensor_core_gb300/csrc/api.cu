@@ -1,0 +1,433 @@
+// api.cu -- the C ABI of libptc (declared in include/ptc.h): argument checks,
+// tensor maps, workspace, launches.  Host code only.
+//
+// Each call validates its arguments without touching CUDA, checks the device
+// (compute capability 10.3), encodes TMA tensor maps for the operands, and
+// launches on the caller's stream:
+//   gemm_f16: one persistent tensor-core kernel (FP16 x FP16 -> FP32).
+//   gemm_s8 : s8 -> f16 conversion of A and B into a stream-ordered workspace,
+//             then the tensor-core kernel with exact chunked int32 folding.
+//   gemm_s4 : packed s4 -> E4M3 conversion, then the same with E4M3 MMAs.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "internal.h"
+#include "ptc.h"
+
+namespace {
+
+using ptc::GemmArgs;
+using ptc::Kind;
+
+constexpr int64_t kMaxDim = int64_t(1) << 30;
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;  // 1 s per pipeline wait
+constexpr int kMaxDevices = 64;
+
+std::atomic<uint64_t> g_launches{0};
+thread_local char g_msg[512];
+
+// Tunables (process-wide).  Integer routes fold the FP32 partial sums into
+// int32 every kb_per_chunk K blocks of 128 bytes; see gemm_tc.cu.
+std::atomic<int> g_chunk_s8{8};   // 512 K values: |partial| <= 512 * 2^14 = 2^23
+std::atomic<int> g_chunk_s4{2};   // 256 K values: |partial| <= 256 * 2^6  = 2^14
+std::atomic<int> g_group_m{16};
+std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
+std::atomic<int64_t> g_stall_tile{-1};
+
+int fail_cuda(cudaError_t e, const char *what) {
+    std::snprintf(g_msg, sizeof(g_msg), "CUDA call failed: %s: %s", what, cudaGetErrorString(e));
+    cudaGetLastError();  // clear a sticky-free error so the next call starts clean
+    return PTC_ERR_LAUNCH;
+}
+
+// ------------------------------------------------------------ device info
+struct DevInfo {
+    std::once_flag once;
+    int ok = 0;      // 1: compute capability 10.3
+    int sms = 0;
+    cudaMemPool_t pool = nullptr;
+    int pool_ok = 0;
+};
+DevInfo g_dev[kMaxDevices];
+
+int current_device(int *dev_out, DevInfo **info_out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        std::snprintf(g_msg, sizeof(g_msg), "no usable current CUDA device");
+        return PTC_ERR_DEVICE;
+    }
+    DevInfo &d = g_dev[dev];
+    std::call_once(d.once, [&] {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return;
+        }
+        d.sms = sms;
+        d.ok = (major == 10 && minor == 3 && sms > 0) ? 1 : 0;
+        if (!d.ok) return;
+        cudaMemPoolProps props;
+        std::memset(&props, 0, sizeof(props));
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        if (cudaMemPoolCreate(&d.pool, &props) == cudaSuccess) {
+            uint64_t keep = UINT64_MAX;  // keep freed workspace cached in the pool
+            cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+            d.pool_ok = 1;
+        } else {
+            cudaGetLastError();
+        }
+    });
+    if (!d.ok) {
+        std::snprintf(g_msg, sizeof(g_msg), "device %d is not a compute capability 10.3 GPU", dev);
+        return PTC_ERR_DEVICE;
+    }
+    *dev_out = dev;
+    *info_out = &d;
+    return PTC_OK;
+}
+
+// ------------------------------------------------------------ tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// 2-D row-major view: `inner` contiguous elements per row, `outer` rows,
+// `pitch` bytes between rows; boxes of box_inner x box_outer elements with the
+// 128-byte swizzle; out-of-range elements of a box read as zero.
+int make_tmap(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner,
+              uint64_t outer, uint64_t pitch, uint32_t box_inner, uint32_t box_outer) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) {
+        std::snprintf(g_msg, sizeof(g_msg), "cuTensorMapEncodeTiled unavailable");
+        return PTC_ERR_LAUNCH;
+    }
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {pitch};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        std::snprintf(g_msg, sizeof(g_msg), "cuTensorMapEncodeTiled failed (CUresult %d)", int(r));
+        return PTC_ERR_LAUNCH;
+    }
+    return PTC_OK;
+}
+
+// ------------------------------------------------------------ validation
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void *a, uint64_t alen, const void *b, uint64_t blen) {
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + blen && b0 < a0 + alen;
+}
+
+// Bytes spanned by `rows` rows of `cols` elements at `ld` elements pitch, for
+// an element of `num`/`den` bytes (den = 2 for nibbles).
+uint64_t span_bytes(int64_t rows, int64_t cols, int64_t ld, int num, int den) {
+    const int64_t elems = (rows - 1) * ld + cols;
+    return uint64_t((elems * num + den - 1) / den);
+}
+
+int check_sizes(int64_t M, int64_t N, int64_t K) {
+    if (M < 0 || N < 0 || K < 0 || M > kMaxDim || N > kMaxDim || K > kMaxDim) {
+        std::snprintf(g_msg, sizeof(g_msg), "sizes must satisfy 0 <= M, N, K <= 2^30");
+        return PTC_ERR_INVALID;
+    }
+    const int64_t tiles = ((M + ptc::kBM - 1) / ptc::kBM) * ((N + ptc::kBN - 1) / ptc::kBN);
+    if (tiles >= (int64_t(1) << 31)) {
+        std::snprintf(g_msg, sizeof(g_msg), "too many output tiles");
+        return PTC_ERR_INVALID;
+    }
+    return PTC_OK;
+}
+
+int fail(int code, const char *text) {
+    std::snprintf(g_msg, sizeof(g_msg), "%s", text);
+    return code;
+}
+
+// ------------------------------------------------------------ launches
+GemmArgs base_args(int64_t M, int64_t N, int64_t K, int k_elems_per_block, void *C, int64_t ldc) {
+    GemmArgs a;
+    std::memset(&a, 0, sizeof(a));
+    a.C = C;
+    a.ldc = ldc;
+    a.M = int(M);
+    a.N = int(N);
+    a.K = int(K);
+    a.tiles_m = int((M + ptc::kBM - 1) / ptc::kBM);
+    a.tiles_n = int((N + ptc::kBN - 1) / ptc::kBN);
+    a.num_tiles = a.tiles_m * a.tiles_n;
+    a.num_kb = int((K + k_elems_per_block - 1) / k_elems_per_block);
+    a.kb_per_chunk = a.num_kb;
+    a.group_m = g_group_m.load() > 0 ? g_group_m.load() : 1;
+    a.stall_tile = int(g_stall_tile.exchange(-1));
+    a.wait_limit_ns = g_wait_ns.load();
+    return a;
+}
+
+int launch_gemm_checked(Kind kind, bool b_mn, bool int_out, const CUtensorMap &ta,
+                        const CUtensorMap &tb, const GemmArgs &args, const DevInfo &d,
+                        cudaStream_t stream) {
+    const int grid = args.num_tiles < d.sms ? args.num_tiles : d.sms;
+    cudaError_t e = ptc::launch_gemm(kind, b_mn, int_out, ta, tb, args, grid, stream);
+    if (e != cudaSuccess) return fail_cuda(e, "GEMM kernel launch");
+    g_launches.fetch_add(1);
+    return PTC_OK;
+}
+
+int zero_c(void *C, int64_t ldc, int64_t M, int64_t N, const DevInfo &d, cudaStream_t stream) {
+    cudaError_t e = ptc::launch_zero_fill(C, ldc, int(M), int(N), d.sms * 4, stream);
+    if (e != cudaSuccess) return fail_cuda(e, "zero-fill launch");
+    g_launches.fetch_add(1);
+    return PTC_OK;
+}
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+}  // namespace
+
+extern "C" {
+
+int gemm_f16(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+             int64_t ldb, float *C, int64_t ldc, void *stream) {
+    g_msg[0] = 0;
+    int rc = check_sizes(M, N, K);
+    if (rc) return rc;
+    if (M == 0 || N == 0) return PTC_OK;
+    if (!C || ldc < N) return fail(PTC_ERR_INVALID, "C is NULL or ldc < N");
+    if (K > 0 && (!A || !B)) return fail(PTC_ERR_INVALID, "A or B is NULL");
+    if (K > 0 && (lda < K || ldb < N)) return fail(PTC_ERR_INVALID, "lda < K or ldb < N");
+    if (!aligned16(C) || ldc % 4) return fail(PTC_ERR_ALIGN, "C must be 16-byte aligned, ldc % 4 == 0");
+    if (K > 0 && (!aligned16(A) || !aligned16(B) || lda % 8 || ldb % 8))
+        return fail(PTC_ERR_ALIGN, "A, B must be 16-byte aligned, lda % 8 == 0, ldb % 8 == 0");
+    const uint64_t cbytes = span_bytes(M, N, ldc, 4, 1);
+    if (K > 0 && (overlaps(C, cbytes, A, span_bytes(M, K, lda, 2, 1)) ||
+                  overlaps(C, cbytes, B, span_bytes(K, N, ldb, 2, 1))))
+        return fail(PTC_ERR_OVERLAP, "C overlaps A or B");
+
+    int dev;
+    DevInfo *d;
+    if ((rc = current_device(&dev, &d))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) return zero_c(C, ldc, M, N, *d, s);
+
+    CUtensorMap ta, tb;
+    if ((rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, uint64_t(lda) * 2, 64, ptc::kBM)))
+        return rc;
+    if ((rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, N, K, uint64_t(ldb) * 2, 64, 64)))
+        return rc;
+    GemmArgs args = base_args(M, N, K, 64, C, ldc);
+    return launch_gemm_checked(Kind::F16, true, false, ta, tb, args, *d, s);
+}
+
+int gemm_s8(int64_t M, int64_t N, int64_t K, const int8_t *A, int64_t lda, const int8_t *B,
+            int64_t ldb, int32_t *C, int64_t ldc, void *stream) {
+    g_msg[0] = 0;
+    int rc = check_sizes(M, N, K);
+    if (rc) return rc;
+    if (M == 0 || N == 0) return PTC_OK;
+    if (!C || ldc < N) return fail(PTC_ERR_INVALID, "C is NULL or ldc < N");
+    if (K > 0 && (!A || !B)) return fail(PTC_ERR_INVALID, "A or B is NULL");
+    if (K > 0 && (lda < K || ldb < K)) return fail(PTC_ERR_INVALID, "lda < K or ldb < K");
+    if (!aligned16(C) || ldc % 4) return fail(PTC_ERR_ALIGN, "C must be 16-byte aligned, ldc % 4 == 0");
+    if (K > 0 && (!aligned16(A) || !aligned16(B) || lda % 16 || ldb % 16))
+        return fail(PTC_ERR_ALIGN, "A, B must be 16-byte aligned, lda % 16 == 0, ldb % 16 == 0");
+    const uint64_t cbytes = span_bytes(M, N, ldc, 4, 1);
+    if (K > 0 && (overlaps(C, cbytes, A, span_bytes(M, K, lda, 1, 1)) ||
+                  overlaps(C, cbytes, B, span_bytes(N, K, ldb, 1, 1))))
+        return fail(PTC_ERR_OVERLAP, "C overlaps A or B");
+
+    int dev;
+    DevInfo *d;
+    if ((rc = current_device(&dev, &d))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) return zero_c(C, ldc, M, N, *d, s);
+    if (!d->pool_ok) return fail(PTC_ERR_ALLOC, "workspace memory pool unavailable");
+
+    // Workspace: A and B as binary16 rows of K, pitch rounded to 128 bytes.
+    const int64_t ldw = round_up(K, 64);
+    const int64_t a_bytes = round_up(M * ldw * 2, 1024);
+    const int64_t b_bytes = round_up(N * ldw * 2, 1024);
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, size_t(a_bytes + b_bytes), d->pool, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PTC_ERR_ALLOC, "workspace allocation failed");
+    }
+    uint16_t *aw = static_cast<uint16_t *>(ws);
+    uint16_t *bw = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + a_bytes);
+    const int cgrid = d->sms * 8;
+    rc = PTC_OK;
+    if ((e = ptc::launch_s8_to_f16(A, lda, int(M), int(K), aw, ldw, cgrid, s)) != cudaSuccess)
+        rc = fail_cuda(e, "s8 conversion launch");
+    else
+        g_launches.fetch_add(1);
+    if (!rc) {
+        if ((e = ptc::launch_s8_to_f16(B, ldb, int(N), int(K), bw, ldw, cgrid, s)) != cudaSuccess)
+            rc = fail_cuda(e, "s8 conversion launch");
+        else
+            g_launches.fetch_add(1);
+    }
+    CUtensorMap ta, tb;
+    if (!rc) rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, aw, K, M, uint64_t(ldw) * 2, 64, ptc::kBM);
+    if (!rc) rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bw, K, N, uint64_t(ldw) * 2, 64, ptc::kBN);
+    if (!rc) {
+        GemmArgs args = base_args(M, N, K, 64, C, ldc);
+        const int ch = g_chunk_s8.load();
+        args.kb_per_chunk = ch > 0 ? ch : 1;
+        rc = launch_gemm_checked(Kind::F16, false, true, ta, tb, args, *d, s);
+    }
+    cudaFreeAsync(ws, s);
+    return rc;
+}
+
+int gemm_s4(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+            int64_t ldb, int32_t *C, int64_t ldc, void *stream) {
+    g_msg[0] = 0;
+    int rc = check_sizes(M, N, K);
+    if (rc) return rc;
+    if (M == 0 || N == 0) return PTC_OK;
+    if (!C || ldc < N) return fail(PTC_ERR_INVALID, "C is NULL or ldc < N");
+    if (K > 0 && (!A || !B)) return fail(PTC_ERR_INVALID, "A or B is NULL");
+    if (K > 0 && (lda < K || ldb < K || (lda & 1) || (ldb & 1)))
+        return fail(PTC_ERR_INVALID, "lda, ldb must be even and >= K (counted in nibbles)");
+    if (!aligned16(C) || ldc % 4) return fail(PTC_ERR_ALIGN, "C must be 16-byte aligned, ldc % 4 == 0");
+    if (K > 0 && (!aligned16(A) || !aligned16(B) || lda % 32 || ldb % 32))
+        return fail(PTC_ERR_ALIGN, "A, B must be 16-byte aligned, lda % 32 == 0, ldb % 32 == 0");
+    const uint64_t cbytes = span_bytes(M, N, ldc, 4, 1);
+    if (K > 0 && (overlaps(C, cbytes, A, span_bytes(M, K, lda, 1, 2)) ||
+                  overlaps(C, cbytes, B, span_bytes(N, K, ldb, 1, 2))))
+        return fail(PTC_ERR_OVERLAP, "C overlaps A or B");
+
+    int dev;
+    DevInfo *d;
+    if ((rc = current_device(&dev, &d))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) return zero_c(C, ldc, M, N, *d, s);
+    if (!d->pool_ok) return fail(PTC_ERR_ALLOC, "workspace memory pool unavailable");
+
+    // Workspace: A and B as E4M3 rows of K, pitch rounded to 128 bytes.
+    const int64_t ldw = round_up(K, 128);
+    const int64_t a_bytes = round_up(M * ldw, 1024);
+    const int64_t b_bytes = round_up(N * ldw, 1024);
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, size_t(a_bytes + b_bytes), d->pool, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PTC_ERR_ALLOC, "workspace allocation failed");
+    }
+    uint8_t *aw = static_cast<uint8_t *>(ws);
+    uint8_t *bw = aw + a_bytes;
+    const int cgrid = d->sms * 8;
+    rc = PTC_OK;
+    if ((e = ptc::launch_s4_to_e4m3(static_cast<const uint8_t *>(A), lda / 2, int(M), int(K), aw, ldw,
+                                    cgrid, s)) != cudaSuccess)
+        rc = fail_cuda(e, "s4 conversion launch");
+    else
+        g_launches.fetch_add(1);
+    if (!rc) {
+        if ((e = ptc::launch_s4_to_e4m3(static_cast<const uint8_t *>(B), ldb / 2, int(N), int(K), bw,
+                                        ldw, cgrid, s)) != cudaSuccess)
+            rc = fail_cuda(e, "s4 conversion launch");
+        else
+            g_launches.fetch_add(1);
+    }
+    CUtensorMap ta, tb;
+    if (!rc) rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, aw, K, M, uint64_t(ldw), 128, ptc::kBM);
+    if (!rc) rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, bw, K, N, uint64_t(ldw), 128, ptc::kBN);
+    if (!rc) {
+        GemmArgs args = base_args(M, N, K, 128, C, ldc);
+        const int ch = g_chunk_s4.load();
+        args.kb_per_chunk = ch > 0 ? ch : 1;
+        rc = launch_gemm_checked(Kind::E4M3, false, true, ta, tb, args, *d, s);
+    }
+    cudaFreeAsync(ws, s);
+    return rc;
+}
+
+const char *gemm_status_string(int status) {
+    static const char *names[] = {"PTC_OK",           "PTC_ERR_INVALID: invalid argument",
+                                  "PTC_ERR_ALIGN: misaligned pointer or row pitch",
+                                  "PTC_ERR_OVERLAP: C overlaps an input",
+                                  "PTC_ERR_DEVICE: no compute capability 10.3 device",
+                                  "PTC_ERR_LAUNCH: CUDA call failed",
+                                  "PTC_ERR_TIMEOUT: a kernel pipeline wait timed out",
+                                  "PTC_ERR_ALLOC: workspace allocation failed"};
+    thread_local char buf[640];
+    const char *base = (status >= 0 && status <= 7) ? names[status] : "unknown status";
+    if (status != PTC_OK && g_msg[0])
+        std::snprintf(buf, sizeof(buf), "%s (%s)", base, g_msg);
+    else
+        std::snprintf(buf, sizeof(buf), "%s", base);
+    return buf;
+}
+
+int gemm_poll_device_error(void) {
+    int dev;
+    DevInfo *d;
+    int rc = current_device(&dev, &d);
+    if (rc) return rc;
+    uint32_t w = 0;
+    cudaError_t e = ptc::read_and_clear_error_word(&w);
+    if (e != cudaSuccess) return fail_cuda(e, "reading the device error word");
+    return w ? PTC_ERR_TIMEOUT : PTC_OK;
+}
+
+uint64_t ptc_kernel_launch_count(void) { return g_launches.load(); }
+
+int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile) {
+    g_wait_ns.store(timeout_ns ? timeout_ns : kDefaultWaitNs);
+    g_stall_tile.store(stall_tile);
+    return PTC_OK;
+}
+
+int ptc_set_tuning(const char *key, int64_t value) {
+    if (!key) return fail(PTC_ERR_INVALID, "key is NULL");
+    if (std::strcmp(key, "s8_chunk_kb") == 0 && value > 0 && value < (1 << 30)) {
+        g_chunk_s8.store(int(value));
+        return PTC_OK;
+    }
+    if (std::strcmp(key, "s4_chunk_kb") == 0 && value > 0 && value < (1 << 30)) {
+        g_chunk_s4.store(int(value));
+        return PTC_OK;
+    }
+    if (std::strcmp(key, "group_m") == 0 && value > 0 && value < (1 << 20)) {
+        g_group_m.store(int(value));
+        return PTC_OK;
+    }
+    return fail(PTC_ERR_INVALID, "unknown tuning key or value out of range");
+}
+
+}  // extern "C"

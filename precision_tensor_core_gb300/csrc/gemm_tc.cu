@@ -1,0 +1,396 @@
+// gemm_tc.cu -- persistent, warp-specialised tensor-core GEMM for sm_103a.
+//
+// The method is the tiled tensor-core GEMM of "Hand-Written PTX Tensor-Core
+// GEMM Kernels: A Multi-Precision Study on NVIDIA L4" (section III-A: output
+// tiles per block, a K loop that stages A/B tiles in shared memory while the
+// tensor cores consume the previous ones, Listing 1), rebuilt for GB300:
+//
+//   warp 0      TMA producer: one thread streams 128-byte-wide K blocks of A
+//               and B into a STAGES-deep shared-memory ring (128-byte swizzle),
+//               completing on per-stage "full" mbarriers (replaces cp.async +
+//               commit_group / wait_group + __syncthreads buffer rotation).
+//   warp 1      allocates all 512 tensor-memory columns, then one thread
+//               issues tcgen05.mma (M = 128, N = 256, K = 32 bytes per
+//               instruction) into a double-buffered tensor-memory accumulator
+//               and frees ring stages with tcgen05.commit -> "empty" barriers
+//               (replaces ldmatrix + mma.sync and register accumulators).
+//   warps 2-9   epilogue: tcgen05.ld tensor memory -> registers -> global C,
+//               overlapped with the next tile's MMAs through the second
+//               accumulator buffer.
+//
+// Integer routes: sm_103a has no integer tcgen05 MMA, so INT8 runs on the
+// FP16 kind (every s8 value is an exact binary16) and INT4 on the E4M3 kind
+// (every s4 value is an exact E4M3).  Products are exact and the FP32 sums are
+// exact integers while |partial sum| < 2^24, so the K loop is cut into chunks
+// of kb_per_chunk K blocks, each summed in its own accumulator buffer; the
+// epilogue converts each chunk's (integral) FP32 sums to int32 and adds them
+// in registers.  The int32 result is therefore the exact sum modulo 2^32.
+//
+// Tiles are spread over a persistent grid of at most one CTA per SM with no
+// inter-CTA dependency (no grid-wide spin barrier).  Every wait is bounded by
+// a %globaltimer limit: on expiry the CTA raises an abort flag, records
+// PTC_ERR_TIMEOUT in a device error word, drains its in-flight copies and
+// MMAs, frees tensor memory and exits.
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace ptc {
+
+__device__ uint32_t g_error_word;
+
+namespace {
+
+constexpr int STAGES = 4;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int A_STAGE_BYTES = kBM * kRowBytes;  // 16 KiB
+constexpr int B_STAGE_BYTES = kBN * kRowBytes;  // 32 KiB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int TMEM_COLS = 512;                  // two accumulators of kBN columns
+constexpr int KSTEP_BYTES = 32;                 // K bytes per tcgen05.mma (16 f16 / 32 e4m3)
+constexpr int KSTEPS = kRowBytes / KSTEP_BYTES; // MMAs per stage
+
+struct SharedTail {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    AbortState abort;
+};
+
+constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + sizeof(SharedTail);
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+__device__ __forceinline__ void tile_coords(int t, const GemmArgs &a, int &mb, int &nb) {
+    const int per_group = a.group_m * a.tiles_n;
+    const int g = t / per_group;
+    const int first_m = g * a.group_m;
+    const int gsz = min(a.tiles_m - first_m, a.group_m);
+    const int r = t - g * per_group;
+    mb = first_m + r % gsz;
+    nb = r / gsz;
+}
+
+// Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, AbortState *ab,
+                                          uint64_t limit, int lane) {
+    uint32_t ok = 0;
+    if (lane == 0) ok = mbar_wait(bar, parity, ab, &g_error_word, limit) ? 1u : 0u;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+template <typename T>
+__device__ __forceinline__ void store_32(T *dst, const uint32_t (&v)[32], int valid) {
+    if (valid >= 32) {
+        uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) d[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    } else {
+        uint32_t *d = reinterpret_cast<uint32_t *>(dst);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j < valid) d[j] = v[j];
+    }
+}
+
+template <Kind KIND, bool B_MN, bool INT_OUT>
+__global__ void __launch_bounds__(THREADS, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const GemmArgs args) {
+    static_assert(!(B_MN && KIND == Kind::E4M3), "MN-major B is used by the FP16 path only");
+    extern __shared__ uint8_t smem_raw[];
+    // 128-byte swizzle atoms must sit on 1024-byte boundaries.
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+    uint8_t *a_ring = smem;
+    uint8_t *b_ring = smem + STAGES * A_STAGE_BYTES;
+    SharedTail *st = reinterpret_cast<SharedTail *>(smem + STAGES * STAGE_BYTES);
+
+    const int warp = threadIdx.x / 32;
+    const int lane = threadIdx.x % 32;
+    const uint64_t limit = args.wait_limit_ns;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&st->full[s], 1);
+            mbar_init(&st->empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&st->acc_full[b], 1);
+            mbar_init(&st->acc_empty[b], EPI_WARPS);
+        }
+        mbar_init(&st->drain, 1);
+        st->abort.flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(&st->tmem_base, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = st->tmem_base;
+
+    const int nchunks = (args.num_kb + args.kb_per_chunk - 1) / args.kb_per_chunk;
+    constexpr int K_ELEMS = (KIND == Kind::F16) ? kRowBytes / 2 : kRowBytes;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int s = 0;
+            uint32_t ph = 0;
+            uint32_t outstanding = 0, out_phase = 0;  // per-stage bits of issued copies
+            bool ok = true;
+            for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
+                int mb, nb;
+                tile_coords(t, args, mb, nb);
+                const int m0 = mb * kBM, n0 = nb * kBN;
+                for (int kb = 0; kb < args.num_kb; ++kb) {
+                    if (!mbar_wait(&st->empty[s], ph ^ 1u, &st->abort, &g_error_word, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    outstanding &= ~(1u << s);
+                    if (!(t == args.stall_tile && kb == 0)) {
+                        mbar_arrive_expect_tx(&st->full[s], STAGE_BYTES);
+                        tma_load_2d(a_ring + s * A_STAGE_BYTES, &tmA, &st->full[s], kb * K_ELEMS, m0);
+                        if constexpr (B_MN) {
+#pragma unroll
+                            for (int i = 0; i < kBN / 64; ++i)
+                                tma_load_2d(b_ring + s * B_STAGE_BYTES + i * (K_ELEMS * 128), &tmB,
+                                            &st->full[s], n0 + 64 * i, kb * K_ELEMS);
+                        } else {
+                            tma_load_2d(b_ring + s * B_STAGE_BYTES, &tmB, &st->full[s], kb * K_ELEMS, n0);
+                        }
+                        outstanding |= 1u << s;
+                        out_phase = (out_phase & ~(1u << s)) | (ph << s);
+                    }
+                    if (++s == STAGES) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Abort: let every copy this thread issued land before the CTA exits.
+                for (int q = 0; q < STAGES; ++q)
+                    if (outstanding & (1u << q))
+                        mbar_wait(&st->full[q], (out_phase >> q) & 1u, nullptr, nullptr, limit);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t IDESC =
+                instr_desc(0u, 0u, B_MN, kBM, kBN);  // F16 x F16 or E4M3 x E4M3 -> F32
+            const uint32_t a_base = smem_u32(a_ring);
+            const uint32_t b_base = smem_u32(b_ring);
+            int s = 0;
+            uint32_t ph = 0;
+            int abuf = 0;
+            uint32_t aph = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
+                for (int ch = 0; ch < nchunks && ok; ++ch) {
+                    if (!mbar_wait(&st->acc_empty[abuf], aph ^ 1u, &st->abort, &g_error_word, limit)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t d_tmem = tmem_base + uint32_t(abuf * kBN);
+                    const int kb0 = ch * args.kb_per_chunk;
+                    const int kb1 = min(args.num_kb, kb0 + args.kb_per_chunk);
+                    for (int kb = kb0; kb < kb1; ++kb) {
+                        if (!mbar_wait(&st->full[s], ph, &st->abort, &g_error_word, limit)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        const uint32_t a_addr = a_base + s * A_STAGE_BYTES;
+                        const uint32_t b_addr = b_base + s * B_STAGE_BYTES;
+#pragma unroll
+                        for (int k = 0; k < KSTEPS; ++k) {
+                            const uint64_t adesc = smem_desc_sw128(a_addr + k * KSTEP_BYTES, 16, 1024);
+                            uint64_t bdesc;
+                            if constexpr (B_MN)
+                                bdesc = smem_desc_sw128(b_addr + k * (16 * 128), K_ELEMS * 128, 1024);
+                            else
+                                bdesc = smem_desc_sw128(b_addr + k * KSTEP_BYTES, 16, 1024);
+                            const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
+                            if constexpr (KIND == Kind::F16)
+                                mma_f16(d_tmem, adesc, bdesc, IDESC, acc);
+                            else
+                                mma_f8(d_tmem, adesc, bdesc, IDESC, acc);
+                        }
+                        mma_commit(&st->empty[s]);
+                        if (++s == STAGES) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(&st->acc_full[abuf]);
+                    if (++abuf == 2) {
+                        abuf = 0;
+                        aph ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Abort: wait for the MMAs already issued before tensor memory is freed.
+                mma_commit(&st->drain);
+                mbar_wait(&st->drain, 0, nullptr, nullptr, limit);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------ epilogue
+        const int q = warp & 3;             // tensor-memory lane quarter
+        const int h = (warp - 2) >> 2;      // column half of the tile
+        const uint32_t t_lane = tmem_base + (uint32_t(32 * q) << 16) + uint32_t(h * (kBN / 2));
+        int abuf = 0;
+        uint32_t aph = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
+            int mb, nb;
+            tile_coords(t, args, mb, nb);
+            const int row = mb * kBM + 32 * q + lane;
+            const int col0 = nb * kBN + h * (kBN / 2);
+            if constexpr (INT_OUT) {
+                int32_t acc[kBN / 2];
+#pragma unroll
+                for (int j = 0; j < kBN / 2; ++j) acc[j] = 0;
+                for (int ch = 0; ch < nchunks; ++ch) {
+                    if (!warp_wait(&st->acc_full[abuf], aph, &st->abort, limit, lane)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        uint32_t r[16];
+                        tmem_ld_16cols(t_lane + uint32_t(abuf * kBN + 16 * c), r);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) acc[16 * c + j] += __float2int_rn(__uint_as_float(r[j]));
+                    }
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&st->acc_empty[abuf]);
+                    if (++abuf == 2) {
+                        abuf = 0;
+                        aph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if (row < args.M) {
+                    int32_t *crow = reinterpret_cast<int32_t *>(args.C) + int64_t(row) * args.ldc;
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t v[32];
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] = static_cast<uint32_t>(acc[32 * c + j]);
+                        const int cc = col0 + 32 * c;
+                        if (cc < args.N) store_32(crow + cc, v, args.N - cc);
+                    }
+                }
+            } else {
+                if (!warp_wait(&st->acc_full[abuf], aph, &st->abort, limit, lane)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                float *crow = reinterpret_cast<float *>(args.C) + int64_t(row) * args.ldc;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t r[32];
+                    tmem_ld_32cols(t_lane + uint32_t(abuf * kBN + 32 * c), r);
+                    tmem_ld_wait();
+                    const int cc = col0 + 32 * c;
+                    if (row < args.M && cc < args.N) store_32(crow + cc, r, args.N - cc);
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&st->acc_empty[abuf]);
+                if (++abuf == 2) {
+                    abuf = 0;
+                    aph ^= 1u;
+                }
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+}
+
+__global__ void zero_fill_kernel(uint32_t *C, int64_t ldc, int M, int N) {
+    const int64_t total = int64_t(M) * N;
+    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
+         i += int64_t(gridDim.x) * blockDim.x) {
+        const int64_t r = i / N, c = i - r * N;
+        C[r * ldc + c] = 0u;
+    }
+}
+
+template <Kind KIND, bool B_MN, bool INT_OUT>
+cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args,
+                       int grid, cudaStream_t stream) {
+    auto *fn = gemm_kernel<KIND, B_MN, INT_OUT>;
+    // The attribute is per device; setting it on every launch costs ~1 us and
+    // keeps multi-device use correct.
+    static thread_local int last_dev = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev != last_dev) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES));
+        if (e != cudaSuccess) return e;
+        last_dev = dev;
+    }
+    fn<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, args);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_smem_bytes() { return SMEM_BYTES; }
+
+cudaError_t launch_gemm(Kind kind, bool b_mn_major, bool int_out, const CUtensorMap &ta,
+                        const CUtensorMap &tb, const GemmArgs &args, int grid,
+                        cudaStream_t stream) {
+    if (kind == Kind::F16 && b_mn_major && !int_out)
+        return launch_one<Kind::F16, true, false>(ta, tb, args, grid, stream);
+    if (kind == Kind::F16 && !b_mn_major && int_out)
+        return launch_one<Kind::F16, false, true>(ta, tb, args, grid, stream);
+    if (kind == Kind::E4M3 && !b_mn_major && int_out)
+        return launch_one<Kind::E4M3, false, true>(ta, tb, args, grid, stream);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_zero_fill(void *C, int64_t ldc, int M, int N, int grid, cudaStream_t stream) {
+    zero_fill_kernel<<<grid, 256, 0, stream>>>(static_cast<uint32_t *>(C), ldc, M, N);
+    return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_error_word(uint32_t *out) {
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_error_word, sizeof(v));
+    if (e != cudaSuccess) return e;
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero));
+    *out = v;
+    return e;
+}
+
+}  // namespace ptc

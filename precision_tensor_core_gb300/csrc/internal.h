@@ -1,0 +1,61 @@
+// internal.h -- declarations shared by the host side of libptc (not part of
+// the public C ABI; see include/ptc.h for that).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace ptc {
+
+// Output tile of one CTA and one tensor-memory accumulator buffer.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+// Bytes of K held per operand row per pipeline stage: one 128-byte swizzle row
+// (64 FP16 or 128 E4M3 elements).
+constexpr int kRowBytes = 128;
+
+enum class Kind : int { F16 = 0, E4M3 = 1 };
+
+// Arguments of one GEMM kernel launch (the tensor maps travel separately).
+struct GemmArgs {
+    void *C;               // float (FP16 path) or int32 (integer paths), row-major
+    int64_t ldc;           // elements
+    int M, N, K;           // K in operand elements
+    int tiles_m, tiles_n;  // output tiles of kBM x kBN
+    int num_tiles;
+    int num_kb;            // K blocks of kRowBytes bytes
+    int kb_per_chunk;      // K blocks summed in one accumulator buffer before the
+                           // epilogue folds the partial sum into int32 registers
+    int group_m;           // tiles of M per raster group (L2 reuse)
+    int stall_tile;        // test hook: withhold this tile's operands (-1: none)
+    uint64_t wait_limit_ns;
+};
+
+// Dynamic shared memory the GEMM kernel needs.
+size_t gemm_smem_bytes();
+
+// Launch the persistent tensor-core GEMM.
+//   F16  + B MN-major + float output:  gemm_f16
+//   F16  + B K-major  + int32 output:  gemm_s8 (operands converted s8 -> f16)
+//   E4M3 + B K-major  + int32 output:  gemm_s4 (operands converted s4 -> e4m3)
+cudaError_t launch_gemm(Kind kind, bool b_mn_major, bool int_out, const CUtensorMap &ta,
+                        const CUtensorMap &tb, const GemmArgs &args, int grid,
+                        cudaStream_t stream);
+
+// C[M x N] (4-byte elements) = 0.
+cudaError_t launch_zero_fill(void *C, int64_t ldc, int M, int N, int grid, cudaStream_t stream);
+
+// Reads and clears the device error word of the current device.
+cudaError_t read_and_clear_error_word(uint32_t *out);
+
+// Operand preparation for the integer routes: exact element conversion into a
+// dense, 128-byte-pitched workspace matrix of `rows` x `cols`.
+//   s8 -> binary16: src row pitch lds bytes, dst pitch ldd elements (2 bytes)
+cudaError_t launch_s8_to_f16(const int8_t *src, int64_t lds, int rows, int cols, uint16_t *dst,
+                             int64_t ldd, int grid, cudaStream_t stream);
+//   packed s4 -> E4M3: src row pitch lds BYTES, dst pitch ldd elements (bytes)
+cudaError_t launch_s4_to_e4m3(const uint8_t *src, int64_t lds, int rows, int cols, uint8_t *dst,
+                              int64_t ldd, int grid, cudaStream_t stream);
+
+}  // namespace ptc

@@ -1,0 +1,138 @@
+"""The C ABI without a GPU: the library loads, exports every entry point that
+include/ptc.h declares, and rejects bad arguments with the documented status
+codes before making any CUDA call.
+
+Addresses passed here are never dereferenced: every case is rejected by the
+host-side checks (and the one case that gets past them only runs where no GPU
+is present, where it must stop at the device check)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import precision_tensor_core_gb300 as ptc
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ptc.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    import __graft_entry__
+    __graft_entry__.build()
+    return ptc.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert {"gemm_f16", "gemm_s8", "gemm_s4", "gemm_status_string",
+            "gemm_poll_device_error"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in ptc.h but not exported"
+        # C linkage: the plain name resolves, no mangling
+        ctypes.cast(getattr(L, n), ctypes.c_void_p)
+
+
+def test_python_binding_has_same_names():
+    for n in declared_functions():
+        assert callable(getattr(ptc, n)), n
+
+
+BASE = 1 << 40  # fake, 16-byte aligned, never dereferenced
+
+
+def call(L, name, M, N, K, A, lda, B, ldb, C, ldc):
+    return getattr(L, name)(M, N, K, A, lda, B, ldb, C, ldc, None)
+
+
+def good_args(name, M=64, N=64, K=64):
+    A = BASE
+    B = BASE + (1 << 30)
+    C = BASE + (1 << 31)
+    if name == "gemm_f16":
+        return dict(M=M, N=N, K=K, A=A, lda=K, B=B, ldb=N, C=C, ldc=N)
+    return dict(M=M, N=N, K=K, A=A, lda=K, B=B, ldb=K, C=C, ldc=N)
+
+
+NAMES = ["gemm_f16", "gemm_s8", "gemm_s4"]
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_invalid_sizes_and_pointers(L, name):
+    g = good_args(name)
+    for bad in [dict(M=-1), dict(N=-5), dict(K=-1), dict(M=(1 << 30) + 1), dict(K=(1 << 31))]:
+        assert call(L, name, **{**g, **bad}) == ptc.PTC_ERR_INVALID, bad
+    assert call(L, name, **{**g, "C": None}) == ptc.PTC_ERR_INVALID
+    assert call(L, name, **{**g, "A": None}) == ptc.PTC_ERR_INVALID
+    assert call(L, name, **{**g, "B": None}) == ptc.PTC_ERR_INVALID
+    assert call(L, name, **{**g, "lda": g["K"] - 1}) == ptc.PTC_ERR_INVALID
+    assert call(L, name, **{**g, "ldc": g["N"] - 4}) == ptc.PTC_ERR_INVALID
+    bad_ldb = g["N"] - 1 if name == "gemm_f16" else g["K"] - 1
+    assert call(L, name, **{**g, "ldb": bad_ldb}) == ptc.PTC_ERR_INVALID
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_empty_problems_are_noops(L, name):
+    g = good_args(name)
+    # M == 0 or N == 0: nothing to do, pointers may be NULL, no CUDA call
+    assert call(L, name, **{**g, "M": 0, "A": None, "B": None, "C": None}) == ptc.PTC_OK
+    assert call(L, name, **{**g, "N": 0, "A": None, "B": None, "C": None}) == ptc.PTC_OK
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_alignment(L, name):
+    g = good_args(name)
+    assert call(L, name, **{**g, "A": BASE + 8}) == ptc.PTC_ERR_ALIGN
+    assert call(L, name, **{**g, "B": g["B"] + 4}) == ptc.PTC_ERR_ALIGN
+    assert call(L, name, **{**g, "C": g["C"] + 4}) == ptc.PTC_ERR_ALIGN
+    assert call(L, name, **{**g, "ldc": 66}) == ptc.PTC_ERR_ALIGN
+    pitch_bad = {"gemm_f16": 68, "gemm_s8": 72, "gemm_s4": 80}[name]
+    assert call(L, name, **{**g, "lda": pitch_bad}) == ptc.PTC_ERR_ALIGN
+
+
+def test_s4_odd_leading_dimension_is_invalid(L):
+    g = good_args("gemm_s4", K=63)
+    assert call(L, "gemm_s4", **{**g, "lda": 65}) == ptc.PTC_ERR_INVALID
+    assert call(L, "gemm_s4", **{**g, "ldb": 65}) == ptc.PTC_ERR_INVALID
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_overlap(L, name):
+    g = good_args(name)
+    assert call(L, name, **{**g, "C": g["A"]}) == ptc.PTC_ERR_OVERLAP
+    assert call(L, name, **{**g, "C": g["B"] + 64}) == ptc.PTC_ERR_OVERLAP
+    # adjacent but disjoint is fine up to the device check
+    esize = {"gemm_f16": 2, "gemm_s8": 1, "gemm_s4": 0.5}[name]
+    a_end = g["A"] + int(((g["M"] - 1) * g["lda"] + g["K"]) * esize)
+    r = call(L, name, **{**g, "C": (a_end + 15) // 16 * 16})
+    assert r != ptc.PTC_ERR_OVERLAP
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path only")
+@pytest.mark.parametrize("name", NAMES)
+def test_no_device_is_reported(L, name):
+    assert call(L, name, **good_args(name)) == ptc.PTC_ERR_DEVICE
+    assert "PTC_ERR_DEVICE" in ptc.gemm_status_string(ptc.PTC_ERR_DEVICE)
+    with pytest.raises(ptc.PtcError) as e:
+        getattr(ptc, name)(**good_args(name))
+    assert e.value.status == ptc.PTC_ERR_DEVICE
+
+
+def test_status_strings_and_tuning(L):
+    for s in range(8):
+        assert ptc.gemm_status_string(s)
+    assert "unknown" in ptc.gemm_status_string(99)
+    with pytest.raises(ptc.PtcError):
+        ptc.ptc_set_tuning("no_such_key", 3)
+    with pytest.raises(ptc.PtcError):
+        ptc.ptc_set_tuning("s8_chunk_kb", 0)
+    assert ptc.ptc_set_tuning("group_m", 16) == 0
+    assert isinstance(ptc.ptc_kernel_launch_count(), int)
