@@ -228,7 +228,7 @@ def test_mma_lab_worked_example(golden_dir):
 def test_guard_bands_untouched(prec):
     """Output slots outside the M x N block (row padding and rows past M) keep
     the sentinel 0xdeadbeef."""
-    M, N, K = 130, 260, 96
+    M, N, K = 130, 264, 96
     ldc = 272
     sentinel = np.int32(np.uint32(0xDEADBEEF).view(np.int32))
     Cd = torch.full((M + 3, ldc), int(sentinel), dtype=torch.int32, device=DEV)
@@ -275,7 +275,8 @@ def test_strided_operands_padding_not_read():
     A8p = np.full((M, 128), 127, np.int8); A8p[:, :K] = A8
     B8p = np.full((N, 144), -128, np.int8); B8p[:, :K] = Bt8
     Ci = torch.empty((M, 272), dtype=torch.int32, device=DEV)
-    ptc.gemm_s8(M, N, K, int_dev(A8p).data_ptr(), 128, int_dev(B8p).data_ptr(), 144, Ci.data_ptr(), 272, 0)
+    A8d, B8d = int_dev(A8p), int_dev(B8p)  # keep the device copies alive across the call
+    ptc.gemm_s8(M, N, K, A8d.data_ptr(), 128, B8d.data_ptr(), 144, Ci.data_ptr(), 272, 0)
     torch.cuda.synchronize()
     assert np.array_equal(Ci.cpu().numpy()[:, :N], oracle.wrap_s32(oracle.gemm_s8(A8, Bt8)))
 
@@ -352,7 +353,7 @@ def test_side_stream_and_launch_count():
 
 
 def test_host_tensors_end_to_end():
-    A, B = datagen.f16_operands(300, "uniform", m=200, k=120)
+    A, B = datagen.f16_operands(296, "uniform", m=200, k=120)
     C = ptc.matmul_f16(torch.from_numpy(A.view(np.float16)).pin_memory(),
                        torch.from_numpy(B.view(np.float16)).pin_memory())
     assert C.device.type == "cpu"
