@@ -124,6 +124,30 @@ int gemm_s4(int64_t M, int64_t N, int64_t K,
             int32_t *C, int64_t ldc,
             void *stream);
 
+/*
+ * gemm_s8 without any memory allocation.  The paper has no counterpart: it is
+ * an addition for callers that cannot let a library allocate device memory,
+ * such as an application whose own allocator has reserved the GPU's memory
+ * and forbids other allocations, or a latency-bound path where an allocation
+ * could block or fail at an arbitrary moment.
+ * Same arguments, layouts, result and errors as gemm_s8; the binary16
+ * workspace lives in a fixed 32 MiB array in the library's device image
+ * (held on every GPU that loads the library until the process exits) instead
+ * of the memory pool.  The workspace must fit:
+ *     (M + N) * roundup(K, 64) * 2 bytes <= 32 MiB   (e.g. M = N = K = 2048),
+ * otherwise the call returns PTC_ERR_INVALID and launches nothing.
+ * The first call on each device (with that device current) looks up the
+ * array's device address with cudaGetSymbolAddress; make it before any stream
+ * capture begins.  Every call uses the same array: calls whose kernels
+ * overlap on the GPU (other streams, other host threads) race on it and give
+ * wrong results, so serialise them.
+ */
+int gemm_s8_noalloc(int64_t M, int64_t N, int64_t K,
+                    const int8_t *A, int64_t lda,
+                    const int8_t *B, int64_t ldb,
+                    int32_t *C, int64_t ldc,
+                    void *stream);
+
 /* Human-readable text of a status code.  For PTC_ERR_LAUNCH the text of the
  * failing CUDA call on the calling thread is appended.  Never NULL; the
  * string stays valid until the next call on the same thread. */

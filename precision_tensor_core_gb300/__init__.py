@@ -7,7 +7,7 @@ Tensor-Core GEMM Kernels: A Multi-Precision Study on NVIDIA L4"
 Two layers, both argument marshalling only (every arithmetic step runs in the
 library's CUDA kernels):
 
-* ``gemm_f16``, ``gemm_s8``, ``gemm_s4``, ``gemm_status_string``,
+* ``gemm_f16``, ``gemm_s8``, ``gemm_s4``, ``gemm_s8_noalloc``, ``gemm_status_string``,
   ``gemm_poll_device_error``, ``ptc_kernel_launch_count``,
   ``ptc_debug_set_wait_limit``, ``ptc_set_tuning``: the C ABI of
   ``include/ptc.h`` under the same names, taking integers (sizes, leading
@@ -58,7 +58,7 @@ def lib() -> ctypes.CDLL:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"libptc.so is not built ({LIB_PATH}); run __graft_entry__.build()")
         L = ctypes.CDLL(LIB_PATH)
-        for name in ("gemm_f16", "gemm_s8", "gemm_s4"):
+        for name in ("gemm_f16", "gemm_s8", "gemm_s4", "gemm_s8_noalloc"):
             fn = getattr(L, name)
             fn.restype = ctypes.c_int
             fn.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]
@@ -100,6 +100,13 @@ def gemm_s8(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
 def gemm_s4(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
     """C[MxN] s32 = A[MxK] packed s4 . B[KxN] packed s4 (column-major); lda/ldb in nibbles."""
     return _check(lib().gemm_s4(M, N, K, A, lda, B, ldb, C, ldc, stream))
+
+
+def gemm_s8_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    """gemm_s8 that allocates nothing: its workspace is a fixed 32 MiB device
+    array shared by all calls, for callers that cannot allow a library to
+    allocate device memory.  Overlapping calls race; see include/ptc.h."""
+    return _check(lib().gemm_s8_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream))
 
 
 def gemm_poll_device_error() -> int:

@@ -58,4 +58,13 @@ cudaError_t launch_s8_to_f16(const int8_t *src, int64_t lds, int rows, int cols,
 cudaError_t launch_s4_to_e4m3(const uint8_t *src, int64_t lds, int rows, int cols, uint8_t *dst,
                               int64_t ldd, int grid, cudaStream_t stream);
 
+// Adds to the library's kernel-launch counter (ptc_kernel_launch_count).
+void note_launches(uint64_t n);
+// Sets the calling thread's detail text shown by gemm_status_string.
+void set_message(const char *text);
+// TMA tensor map of a row-major matrix (2-byte elements, or 1-byte when
+// one_byte), 128-byte swizzle, zero fill outside; returns a PTC_* status.
+int encode_tmap_2d(CUtensorMap *map, bool one_byte, const void *base, uint64_t inner, uint64_t outer,
+                   uint64_t pitch, uint32_t box_inner, uint32_t box_outer);
+
 }  // namespace ptc

@@ -1,0 +1,69 @@
+"""gemm_s8_noalloc: the INT8 GEMM for callers that cannot let a library
+allocate device memory (for example an application whose own allocator has
+reserved the GPU's memory).  Its workspace is a fixed device array shared by
+every call, so the test runs two different problems back to back: the second
+call starts with the first call's data still in the array.  Each result must
+equal what gemm_s8 (the pool-allocating entry point) returns for the same
+inputs, bit for bit, as all INT8 results in this suite must.
+
+This file is collected last on purpose: if it fails, a run that stops at the
+first failure has already run every other test.
+"""
+import numpy as np
+import pytest
+import torch
+
+import datagen
+import precision_tensor_core_gb300 as ptc
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.set_device(DEV)
+    ptc.lib()
+
+
+def _both(M, N, K, seed):
+    A, Bt = datagen.s8_operands(N, seed=seed, m=M, k=K)
+    Ad = torch.from_numpy(A).to(DEV)
+    Bd = torch.from_numpy(Bt).to(DEV)
+    ref = torch.empty((M, N), dtype=torch.int32, device=DEV)
+    got = torch.full((M, N), -1, dtype=torch.int32, device=DEV)
+    s = torch.cuda.current_stream().cuda_stream
+    ptc.gemm_s8(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K, ref.data_ptr(), N, s)
+    before = ptc.ptc_kernel_launch_count()
+    ptc.gemm_s8_noalloc(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K, got.data_ptr(), N, s)
+    launched = ptc.ptc_kernel_launch_count() - before
+    torch.cuda.synchronize()
+    return got.cpu().numpy(), ref.cpu().numpy(), launched
+
+
+def test_noalloc_matches_gemm_s8_on_two_calls_in_a_row():
+    # call 1: the INT8 workload shape of the study, 2048^3 (16 MiB of workspace)
+    got, ref, launched = _both(2048, 2048, 2048, seed=datagen.config_seed("s8", 2048))
+    assert launched == 3  # two conversions and the tensor-core kernel
+    assert np.array_equal(got, ref)
+    # call 2: a smaller ragged problem over the array the first call filled
+    got, ref, _ = _both(300, 520, 208, seed=12345)
+    assert np.array_equal(got, ref)
+    assert ptc.gemm_poll_device_error() == ptc.PTC_OK
+
+
+def test_noalloc_rejects_problems_beyond_the_scratch():
+    M = N = K = 4096  # (M + N) * K * 2 = 64 MiB > 32 MiB
+    A = torch.zeros((M, K), dtype=torch.int8, device=DEV)
+    Bt = torch.zeros((N, K), dtype=torch.int8, device=DEV)
+    C = torch.zeros((M, N), dtype=torch.int32, device=DEV)
+    before = ptc.ptc_kernel_launch_count()
+    with pytest.raises(ptc.PtcError) as e:
+        ptc.gemm_s8_noalloc(M, N, K, A.data_ptr(), K, Bt.data_ptr(), K, C.data_ptr(), N, 0)
+    assert e.value.status == ptc.PTC_ERR_INVALID
+    assert "static scratch" in str(e.value)
+    assert ptc.ptc_kernel_launch_count() == before
