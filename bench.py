@@ -42,6 +42,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "GEMM TFLOP/s / TOPS at N=8192 (FP16, INT8, INT4); fraction of GB300 dense peak"
+# DRAM read + write bytes of one launch of the FP16 GEMM kernel at N = 8192, from
+# the ncu capture summarised in profiles/gemm_f16_n8192.md (set to None whenever
+# that kernel changes, until it is captured again).
+F16_KERNEL_DRAM_BYTES = 1.004e9 + 0.246e9
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -222,11 +226,12 @@ def run_ours(args, rank, world, dist):
 
     peaks, src = load_peaks()
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    traffic = F16_KERNEL_DRAM_BYTES if n == 8192 else None
     achieved = per["fp16_tflops"]
     roofline = {"bound": "tensor", "kernel": "gemm_kernel<F16, B MN-major, f32 out> (gemm_f16)",
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "peak_source": f"bf16_tflops_sustained of {src} MEASURED_PEAKS.json (FP16 = bf16 rate)",
-                "traffic": None,
+                "traffic": traffic,
                 "int8_frac_of_f16_peak": per["int8_tops"] / peak,
                 "int4_frac_of_fp8_peak": per["int4_tops"] / (2 * peak)}
     return {"value": value, "elapsed_ms": elapsed_ms, "per": per, "e2e": e2e, "roofline": roofline,

@@ -176,10 +176,11 @@ int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile);
  *   "group_m"      output-tile rows per raster group of the persistent
  *                  scheduler (L2 reuse), default 16
  *   "s8_chunk_kb"  INT8 route: K blocks (64 values each) whose FP32 partial
- *                  sum is folded into int32 at a time, default 8 (512 values:
- *                  |partial| <= 2^23, so every FP32 partial sum is an exact
- *                  integer)
- *   "s4_chunk_kb"  INT4 route: K blocks (128 values each) per fold, default 2
+ *                  sum is folded into int32 at a time, default 16 (1024
+ *                  values: |partial| <= 2^24, so every FP32 partial sum is an
+ *                  exactly representable integer)
+ *   "s4_chunk_kb"  INT4 route: K blocks (128 values each) per fold, default 16
+ *                  (2048 values: |partial| <= 2^17)
  * Values above the defaults can make gemm_s8 / gemm_s4 inexact for adversarial
  * inputs; they exist to measure the tensor cores' accumulation width. */
 int ptc_set_tuning(const char *key, int64_t value);

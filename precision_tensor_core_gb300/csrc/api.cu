@@ -34,8 +34,8 @@ thread_local char g_msg[512];
 
 // Tunables (process-wide).  Integer routes fold the FP32 partial sums into
 // int32 every kb_per_chunk K blocks of 128 bytes; see gemm_tc.cu.
-std::atomic<int> g_chunk_s8{8};   // 512 K values: |partial| <= 512 * 2^14 = 2^23
-std::atomic<int> g_chunk_s4{2};   // 256 K values: |partial| <= 256 * 2^6  = 2^14
+std::atomic<int> g_chunk_s8{16};  // 1024 K values: |partial| <= 1024 * 2^14 = 2^24
+std::atomic<int> g_chunk_s4{16};  // 2048 K values: |partial| <= 2048 * 2^6  = 2^17
 std::atomic<int> g_group_m{16};
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 std::atomic<int64_t> g_stall_tile{-1};

@@ -320,6 +320,38 @@ def test_int4_extremes_and_cancellation_k8192():
     assert np.array_equal(run_s4(Ap, Bp, K), oracle.wrap_s32(oracle.gemm_s4(Ap, Bp, K)))
 
 
+def test_int8_odd_partial_sums_up_to_2_24():
+    """Every fold of the INT8 route sums 1024 K values; with A = 127 and B = 127
+    except one 126 per 16 values, each 16-product group sums to an odd number
+    and the partial sums climb to 64 * 257937 = 16,507,968 < 2^24 through odd
+    values, so any accumulation narrower than 24 bits drops a unit."""
+    K, M, N = 8192, 128, 256
+    A = np.full((M, K), 127, np.int8)
+    Bt = np.full((N, K), 127, np.int8)
+    for j in range(N):
+        Bt[j, (np.arange(K) % 16) == (j % 16)] = 126
+        if j % 2:
+            Bt[j] = -Bt[j]
+    C = run_s8(A, Bt)
+    assert np.array_equal(C, oracle.wrap_s32(oracle.gemm_s8(A, Bt)))
+
+
+def test_int4_odd_partial_sums():
+    """INT4 route: A = 7, B = 7 except one 6 per 32 values, so each 32-product
+    group sums to the odd 1561 and the running sums stay odd-valued as they
+    grow; with a wrap pattern per column."""
+    K, M, N = 8192, 128, 256
+    Av = np.full((M, K), 7, np.int8)
+    Bv = np.full((N, K), 7, np.int8)
+    for j in range(N):
+        Bv[j, (np.arange(K) % 32) == (j % 32)] = 6
+        if j % 3 == 1:
+            Bv[j] = -Bv[j]
+    Av[1::2] = -8
+    Ap, Bp = datagen.pack_s4_rows(Av), datagen.pack_s4_rows(Bv)
+    assert np.array_equal(run_s4(Ap, Bp, K), oracle.wrap_s32(oracle.gemm_s4(Ap, Bp, K)))
+
+
 # ---------------------------------------------------------------- runtime behaviour
 @pytest.mark.parametrize("prec", ["f16", "s8", "s4"])
 def test_deterministic(prec):
