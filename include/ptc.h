@@ -181,6 +181,11 @@ int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile);
  *                  exactly representable integer)
  *   "s4_chunk_kb"  INT4 route: K blocks (128 values each) per fold, default 16
  *                  (2048 values: |partial| <= 2^17)
+ *   "cta_pair"     0 (default): one CTA per 128 x 256 output tile while such
+ *                  tiles leave SMs idle, else clusters of two CTAs sharing
+ *                  256 x 256 tiles (tcgen05 cta_group::2); 1: always one CTA;
+ *                  2: always CTA pairs.  Results do not depend on the choice
+ *                  except through the FP16 summation order.
  * Values above the defaults can make gemm_s8 / gemm_s4 inexact for adversarial
  * inputs; they exist to measure the tensor cores' accumulation width. */
 int ptc_set_tuning(const char *key, int64_t value);

@@ -37,6 +37,7 @@ thread_local char g_msg[512];
 std::atomic<int> g_chunk_s8{16};  // 1024 K values: |partial| <= 1024 * 2^14 = 2^24
 std::atomic<int> g_chunk_s4{16};  // 2048 K values: |partial| <= 2048 * 2^6  = 2^17
 std::atomic<int> g_group_m{16};
+std::atomic<int> g_cta_pair{0};   // 0: by problem size, 1: one CTA per tile, 2: CTA pairs
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 std::atomic<int64_t> g_stall_tile{-1};
 
@@ -178,7 +179,18 @@ int fail(int code, const char *text) {
 }
 
 // ------------------------------------------------------------ launches
-GemmArgs base_args(int64_t M, int64_t N, int64_t K, int k_elems_per_block, void *C, int64_t ldc) {
+// One CTA per 128 x 256 tile while that leaves SMs idle; CTA pairs on
+// 256 x 256 tiles (half the B traffic per CTA, deeper ring) once the one-CTA
+// tiles cover every SM.
+int choose_ctas(int64_t M, int64_t N, int sms) {
+    const int forced = g_cta_pair.load();
+    if (forced == 1 || forced == 2) return forced;
+    const int64_t tiles1 = ((M + ptc::kBM - 1) / ptc::kBM) * ((N + ptc::kBN - 1) / ptc::kBN);
+    return tiles1 >= sms ? 2 : 1;
+}
+
+GemmArgs base_args(int64_t M, int64_t N, int64_t K, int k_elems_per_block, void *C, int64_t ldc,
+                   int ctas) {
     GemmArgs a;
     std::memset(&a, 0, sizeof(a));
     a.C = C;
@@ -186,7 +198,8 @@ GemmArgs base_args(int64_t M, int64_t N, int64_t K, int k_elems_per_block, void 
     a.M = int(M);
     a.N = int(N);
     a.K = int(K);
-    a.tiles_m = int((M + ptc::kBM - 1) / ptc::kBM);
+    const int64_t tile_m = int64_t(ptc::kBM) * ctas;
+    a.tiles_m = int((M + tile_m - 1) / tile_m);
     a.tiles_n = int((N + ptc::kBN - 1) / ptc::kBN);
     a.num_tiles = a.tiles_m * a.tiles_n;
     a.num_kb = int((K + k_elems_per_block - 1) / k_elems_per_block);
@@ -197,11 +210,10 @@ GemmArgs base_args(int64_t M, int64_t N, int64_t K, int k_elems_per_block, void 
     return a;
 }
 
-int launch_gemm_checked(Kind kind, bool b_mn, bool int_out, const CUtensorMap &ta,
+int launch_gemm_checked(Kind kind, bool b_mn, bool int_out, int ctas, const CUtensorMap &ta,
                         const CUtensorMap &tb, const GemmArgs &args, const DevInfo &d,
                         cudaStream_t stream) {
-    const int grid = args.num_tiles < d.sms ? args.num_tiles : d.sms;
-    cudaError_t e = ptc::launch_gemm(kind, b_mn, int_out, ta, tb, args, grid, stream);
+    cudaError_t e = ptc::launch_gemm(kind, b_mn, int_out, ctas, ta, tb, args, d.sms, stream);
     if (e != cudaSuccess) return fail_cuda(e, "GEMM kernel launch");
     g_launches.fetch_add(1);
     return PTC_OK;
@@ -253,13 +265,14 @@ int gemm_f16(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0) return zero_c(C, ldc, M, N, *d, s);
 
+    const int ctas = choose_ctas(M, N, d->sms);
     CUtensorMap ta, tb;
     if ((rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, uint64_t(lda) * 2, 64, ptc::kBM)))
         return rc;
     if ((rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, N, K, uint64_t(ldb) * 2, 64, 64)))
         return rc;
-    GemmArgs args = base_args(M, N, K, 64, C, ldc);
-    return launch_gemm_checked(Kind::F16, true, false, ta, tb, args, *d, s);
+    GemmArgs args = base_args(M, N, K, 64, C, ldc, ctas);
+    return launch_gemm_checked(Kind::F16, true, false, ctas, ta, tb, args, *d, s);
 }
 
 int gemm_s8(int64_t M, int64_t N, int64_t K, const int8_t *A, int64_t lda, const int8_t *B,
@@ -310,14 +323,16 @@ int gemm_s8(int64_t M, int64_t N, int64_t K, const int8_t *A, int64_t lda, const
         else
             g_launches.fetch_add(1);
     }
+    const int ctas = choose_ctas(M, N, d->sms);
     CUtensorMap ta, tb;
     if (!rc) rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, aw, K, M, uint64_t(ldw) * 2, 64, ptc::kBM);
-    if (!rc) rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bw, K, N, uint64_t(ldw) * 2, 64, ptc::kBN);
+    if (!rc)
+        rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bw, K, N, uint64_t(ldw) * 2, 64, ptc::kBN / ctas);
     if (!rc) {
-        GemmArgs args = base_args(M, N, K, 64, C, ldc);
+        GemmArgs args = base_args(M, N, K, 64, C, ldc, ctas);
         const int ch = g_chunk_s8.load();
         args.kb_per_chunk = ch > 0 ? ch : 1;
-        rc = launch_gemm_checked(Kind::F16, false, true, ta, tb, args, *d, s);
+        rc = launch_gemm_checked(Kind::F16, false, true, ctas, ta, tb, args, *d, s);
     }
     cudaFreeAsync(ws, s);
     return rc;
@@ -374,14 +389,15 @@ int gemm_s4(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const v
         else
             g_launches.fetch_add(1);
     }
+    const int ctas = choose_ctas(M, N, d->sms);
     CUtensorMap ta, tb;
     if (!rc) rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, aw, K, M, uint64_t(ldw), 128, ptc::kBM);
-    if (!rc) rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, bw, K, N, uint64_t(ldw), 128, ptc::kBN);
+    if (!rc) rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, bw, K, N, uint64_t(ldw), 128, ptc::kBN / ctas);
     if (!rc) {
-        GemmArgs args = base_args(M, N, K, 128, C, ldc);
+        GemmArgs args = base_args(M, N, K, 128, C, ldc, ctas);
         const int ch = g_chunk_s4.load();
         args.kb_per_chunk = ch > 0 ? ch : 1;
-        rc = launch_gemm_checked(Kind::E4M3, false, true, ta, tb, args, *d, s);
+        rc = launch_gemm_checked(Kind::E4M3, false, true, ctas, ta, tb, args, *d, s);
     }
     cudaFreeAsync(ws, s);
     return rc;
@@ -435,6 +451,10 @@ int ptc_set_tuning(const char *key, int64_t value) {
     }
     if (std::strcmp(key, "group_m") == 0 && value > 0 && value < (1 << 20)) {
         g_group_m.store(int(value));
+        return PTC_OK;
+    }
+    if (std::strcmp(key, "cta_pair") == 0 && value >= 0 && value <= 2) {
+        g_cta_pair.store(int(value));
         return PTC_OK;
     }
     return fail(PTC_ERR_INVALID, "unknown tuning key or value out of range");

@@ -10,28 +10,38 @@
 //               completing on per-stage "full" mbarriers (replaces cp.async +
 //               commit_group / wait_group + __syncthreads buffer rotation).
 //   warp 1      allocates all 512 tensor-memory columns, then one thread
-//               issues tcgen05.mma (M = 128, N = 256, K = 32 bytes per
-//               instruction) into a double-buffered tensor-memory accumulator
-//               and frees ring stages with tcgen05.commit -> "empty" barriers
-//               (replaces ldmatrix + mma.sync and register accumulators).
+//               issues tcgen05.mma (N = 256, K = 32 bytes per instruction)
+//               into a double-buffered tensor-memory accumulator and frees
+//               ring stages with tcgen05.commit -> "empty" barriers (replaces
+//               ldmatrix + mma.sync and register accumulators).
 //   warps 2-9   epilogue: tcgen05.ld tensor memory -> registers -> global C,
 //               overlapped with the next tile's MMAs through the second
 //               accumulator buffer.
 //
+// Two shapes of the same kernel:
+//   CTAS = 1    one CTA per 128 x 256 output tile (M = 128 MMAs), 4 stages.
+//   CTAS = 2    a cluster of two CTAs per 256 x 256 output tile
+//               (tcgen05 cta_group::2, M = 256 MMAs issued by the even CTA):
+//               each CTA stages its own 128 rows of A and half of B, so a CTA
+//               moves 32 KiB per stage instead of 48 KiB and the ring holds 6
+//               stages.
+//
 // Integer routes: sm_103a has no integer tcgen05 MMA, so INT8 runs on the
 // FP16 kind (every s8 value is an exact binary16) and INT4 on the E4M3 kind
 // (every s4 value is an exact E4M3).  Products are exact and the FP32 sums are
-// exact integers while |partial sum| < 2^24, so the K loop is cut into chunks
+// exact integers while |partial sum| <= 2^24, so the K loop is cut into chunks
 // of kb_per_chunk K blocks, each summed in its own accumulator buffer; the
 // epilogue converts each chunk's (integral) FP32 sums to int32 and adds them
 // in registers.  The int32 result is therefore the exact sum modulo 2^32.
 //
 // Tiles are spread over a persistent grid of at most one CTA per SM with no
-// inter-CTA dependency (no grid-wide spin barrier).  Every wait is bounded by
-// a %globaltimer limit: on expiry the CTA raises an abort flag, records
-// PTC_ERR_TIMEOUT in a device error word, drains its in-flight copies and
-// MMAs, frees tensor memory and exits.
+// dependency between clusters (no grid-wide spin barrier).  Every wait is
+// bounded by a %globaltimer limit: on expiry the CTA raises an abort flag,
+// records PTC_ERR_TIMEOUT in a device error word, lets its in-flight copies
+// and MMAs land, frees tensor memory and exits.
 #include <cuda_runtime.h>
+
+#include <cstring>
 
 #include "internal.h"
 #include "ptx.cuh"
@@ -42,16 +52,25 @@ __device__ uint32_t g_error_word;
 
 namespace {
 
-constexpr int STAGES = 4;
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
-constexpr int A_STAGE_BYTES = kBM * kRowBytes;  // 16 KiB
-constexpr int B_STAGE_BYTES = kBN * kRowBytes;  // 32 KiB
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
 constexpr int TMEM_COLS = 512;                  // two accumulators of kBN columns
 constexpr int KSTEP_BYTES = 32;                 // K bytes per tcgen05.mma (16 f16 / 32 e4m3)
 constexpr int KSTEPS = kRowBytes / KSTEP_BYTES; // MMAs per stage
 
+// Per-CTA shapes of the two variants.  A CTA stages 128 rows of A; alone it
+// stages all 256 rows of B (4 stages of 48 KiB), in a pair it stages half of
+// B (6 stages of 32 KiB: the pair's MMAs read B from both CTAs).
+template <int CTAS>
+struct Cfg {
+    static constexpr int STAGES = CTAS == 1 ? 4 : 6;
+    static constexpr int B_ROWS = kBN / CTAS;
+    static constexpr int A_STAGE = kBM * kRowBytes;
+    static constexpr int B_STAGE = B_ROWS * kRowBytes;
+    static constexpr int STAGE = A_STAGE + B_STAGE;
+};
+
+template <int STAGES>
 struct SharedTail {
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
@@ -62,8 +81,12 @@ struct SharedTail {
     AbortState abort;
 };
 
-constexpr size_t SMEM_BYTES = 1024 + size_t(STAGES) * STAGE_BYTES + sizeof(SharedTail);
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+template <int CTAS>
+constexpr size_t smem_bytes() {
+    return 1024 + size_t(Cfg<CTAS>::STAGES) * Cfg<CTAS>::STAGE +
+           sizeof(SharedTail<Cfg<CTAS>::STAGES>);
+}
+static_assert(smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448, "shared memory budget");
 
 __device__ __forceinline__ void tile_coords(int t, const GemmArgs &a, int &mb, int &nb) {
     const int per_group = a.group_m * a.tiles_n;
@@ -83,6 +106,14 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, AbortS
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// Bounded pause (abort path of a CTA pair, whose copies complete on the even
+// CTA's barrier and cannot be awaited locally).
+__device__ __forceinline__ void pause_ns(uint64_t ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < ns) {
+    }
+}
+
 template <typename T>
 __device__ __forceinline__ void store_32(T *dst, const uint32_t (&v)[32], int valid) {
     if (valid >= 32) {
@@ -97,22 +128,32 @@ __device__ __forceinline__ void store_32(T *dst, const uint32_t (&v)[32], int va
     }
 }
 
-template <Kind KIND, bool B_MN, bool INT_OUT>
+// CTA r of a pair owns rows 128 r .. 128 r + 127 of the 256 x 256 tile and
+// stages B rows 128 r .. 128 r + 127.  The even CTA issues the MMAs for both;
+// its full barriers collect both CTAs' copies, its commits arrive on both
+// CTAs' empty / accumulator-full barriers, and both CTAs' epilogues release
+// accumulator buffers on its acc_empty barriers.
+template <Kind KIND, bool B_MN, bool INT_OUT, int CTAS>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmArgs args) {
     static_assert(!(B_MN && KIND == Kind::E4M3), "MN-major B is used by the FP16 path only");
+    using C_ = Cfg<CTAS>;
+    constexpr int STAGES = C_::STAGES;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzle atoms must sit on 1024-byte boundaries.
     const uint32_t raw_addr = smem_u32(smem_raw);
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     uint8_t *a_ring = smem;
-    uint8_t *b_ring = smem + STAGES * A_STAGE_BYTES;
-    SharedTail *st = reinterpret_cast<SharedTail *>(smem + STAGES * STAGE_BYTES);
+    uint8_t *b_ring = smem + STAGES * C_::A_STAGE;
+    SharedTail<STAGES> *st = reinterpret_cast<SharedTail<STAGES> *>(smem + STAGES * C_::STAGE);
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const uint64_t limit = args.wait_limit_ns;
+    const uint32_t rank = (CTAS == 1) ? 0u : cluster_ctarank();
+    const int cluster = blockIdx.x / CTAS;
+    const int nclusters = gridDim.x / CTAS;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -121,7 +162,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&st->acc_full[b], 1);
-            mbar_init(&st->acc_empty[b], EPI_WARPS);
+            mbar_init(&st->acc_empty[b], EPI_WARPS * CTAS);
         }
         mbar_init(&st->drain, 1);
         st->abort.flag = 0;
@@ -130,11 +171,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc(&st->tmem_base, TMEM_COLS);
-        tmem_relinquish();
+        tmem_alloc<CTAS>(&st->tmem_base, TMEM_COLS);
+        tmem_relinquish<CTAS>();
     }
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (CTAS == 1)
+        __syncthreads();
+    else
+        cluster_sync();
     tc_fence_after_sync();
     const uint32_t tmem_base = st->tmem_base;
 
@@ -148,29 +192,49 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t ph = 0;
             uint32_t outstanding = 0, out_phase = 0;  // per-stage bits of issued copies
             bool ok = true;
-            for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
+            for (int t = cluster; t < args.num_tiles && ok; t += nclusters) {
                 int mb, nb;
                 tile_coords(t, args, mb, nb);
-                const int m0 = mb * kBM, n0 = nb * kBN;
+                const int m0 = mb * (kBM * CTAS) + int(rank) * kBM;
+                const int n0 = nb * kBN + int(rank) * C_::B_ROWS;
                 for (int kb = 0; kb < args.num_kb; ++kb) {
                     if (!mbar_wait(&st->empty[s], ph ^ 1u, &st->abort, &g_error_word, limit)) {
                         ok = false;
                         break;
                     }
                     outstanding &= ~(1u << s);
-                    if (!(t == args.stall_tile && kb == 0)) {
-                        mbar_arrive_expect_tx(&st->full[s], STAGE_BYTES);
-                        tma_load_2d(a_ring + s * A_STAGE_BYTES, &tmA, &st->full[s], kb * K_ELEMS, m0);
-                        if constexpr (B_MN) {
+                    const bool stall = (t == args.stall_tile && kb == 0 && rank == 0);
+                    if (!stall) {
+                        uint8_t *a_dst = a_ring + s * C_::A_STAGE;
+                        uint8_t *b_dst = b_ring + s * C_::B_STAGE;
+                        if constexpr (CTAS == 1) {
+                            mbar_arrive_expect_tx(&st->full[s], C_::STAGE);
+                            tma_load_2d(a_dst, &tmA, &st->full[s], kb * K_ELEMS, m0);
+                            if constexpr (B_MN) {
 #pragma unroll
-                            for (int i = 0; i < kBN / 64; ++i)
-                                tma_load_2d(b_ring + s * B_STAGE_BYTES + i * (K_ELEMS * 128), &tmB,
-                                            &st->full[s], n0 + 64 * i, kb * K_ELEMS);
+                                for (int i = 0; i < C_::B_ROWS / 64; ++i)
+                                    tma_load_2d(b_dst + i * (K_ELEMS * 128), &tmB, &st->full[s],
+                                                n0 + 64 * i, kb * K_ELEMS);
+                            } else {
+                                tma_load_2d(b_dst, &tmB, &st->full[s], kb * K_ELEMS, n0);
+                            }
+                            outstanding |= 1u << s;
+                            out_phase = (out_phase & ~(1u << s)) | (ph << s);
                         } else {
-                            tma_load_2d(b_ring + s * B_STAGE_BYTES, &tmB, &st->full[s], kb * K_ELEMS, n0);
+                            // Both CTAs' copies complete on the even CTA's full barrier,
+                            // which alone expects the pair's bytes.
+                            const uint32_t bar = mapa_shared(smem_u32(&st->full[s]), 0);
+                            if (rank == 0) mbar_arrive_expect_tx(&st->full[s], CTAS * C_::STAGE);
+                            tma_load_2d_pair(a_dst, &tmA, bar, kb * K_ELEMS, m0);
+                            if constexpr (B_MN) {
+#pragma unroll
+                                for (int i = 0; i < C_::B_ROWS / 64; ++i)
+                                    tma_load_2d_pair(b_dst + i * (K_ELEMS * 128), &tmB, bar,
+                                                     n0 + 64 * i, kb * K_ELEMS);
+                            } else {
+                                tma_load_2d_pair(b_dst, &tmB, bar, kb * K_ELEMS, n0);
+                            }
                         }
-                        outstanding |= 1u << s;
-                        out_phase = (out_phase & ~(1u << s)) | (ph << s);
                     }
                     if (++s == STAGES) {
                         s = 0;
@@ -180,17 +244,21 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (!ok) {
                 // Abort: let every copy this thread issued land before the CTA exits.
-                for (int q = 0; q < STAGES; ++q)
-                    if (outstanding & (1u << q))
-                        mbar_wait(&st->full[q], (out_phase >> q) & 1u, nullptr, nullptr, limit);
+                if constexpr (CTAS == 1) {
+                    for (int q = 0; q < STAGES; ++q)
+                        if (outstanding & (1u << q))
+                            mbar_wait(&st->full[q], (out_phase >> q) & 1u, nullptr, nullptr, limit);
+                } else {
+                    pause_ns(200000);  // copies complete on the even CTA's barrier: allow 200 us
+                }
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
             constexpr uint32_t IDESC =
-                instr_desc(0u, 0u, B_MN, kBM, kBN);  // F16 x F16 or E4M3 x E4M3 -> F32
+                instr_desc(0u, 0u, B_MN, kBM * CTAS, kBN);  // F16 x F16 or E4M3 x E4M3 -> F32
             const uint32_t a_base = smem_u32(a_ring);
             const uint32_t b_base = smem_u32(b_ring);
             int s = 0;
@@ -198,7 +266,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             int abuf = 0;
             uint32_t aph = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
+            for (int t = cluster; t < args.num_tiles && ok; t += nclusters) {
                 for (int ch = 0; ch < nchunks && ok; ++ch) {
                     if (!mbar_wait(&st->acc_empty[abuf], aph ^ 1u, &st->abort, &g_error_word, limit)) {
                         ok = false;
@@ -214,8 +282,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                             break;
                         }
                         tc_fence_after_sync();
-                        const uint32_t a_addr = a_base + s * A_STAGE_BYTES;
-                        const uint32_t b_addr = b_base + s * B_STAGE_BYTES;
+                        const uint32_t a_addr = a_base + s * C_::A_STAGE;
+                        const uint32_t b_addr = b_base + s * C_::B_STAGE;
 #pragma unroll
                         for (int k = 0; k < KSTEPS; ++k) {
                             const uint64_t adesc = smem_desc_sw128(a_addr + k * KSTEP_BYTES, 16, 1024);
@@ -225,19 +293,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                             else
                                 bdesc = smem_desc_sw128(b_addr + k * KSTEP_BYTES, 16, 1024);
                             const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
-                            if constexpr (KIND == Kind::F16)
-                                mma_f16(d_tmem, adesc, bdesc, IDESC, acc);
-                            else
-                                mma_f8(d_tmem, adesc, bdesc, IDESC, acc);
+                            mma<CTAS, KIND == Kind::E4M3>(d_tmem, adesc, bdesc, IDESC, acc);
                         }
-                        mma_commit(&st->empty[s]);
+                        if constexpr (CTAS == 1)
+                            mma_commit<1>(&st->empty[s]);
+                        else
+                            mma_commit_pair(&st->empty[s], 0x3);
                         if (++s == STAGES) {
                             s = 0;
                             ph ^= 1u;
                         }
                     }
                     if (!ok) break;
-                    mma_commit(&st->acc_full[abuf]);
+                    if constexpr (CTAS == 1)
+                        mma_commit<1>(&st->acc_full[abuf]);
+                    else
+                        mma_commit_pair(&st->acc_full[abuf], 0x3);
                     if (++abuf == 2) {
                         abuf = 0;
                         aph ^= 1u;
@@ -246,7 +317,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (!ok) {
                 // Abort: wait for the MMAs already issued before tensor memory is freed.
-                mma_commit(&st->drain);
+                mma_commit<CTAS>(&st->drain);
                 mbar_wait(&st->drain, 0, nullptr, nullptr, limit);
             }
         }
@@ -256,13 +327,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int q = warp & 3;             // tensor-memory lane quarter
         const int h = (warp - 2) >> 2;      // column half of the tile
         const uint32_t t_lane = tmem_base + (uint32_t(32 * q) << 16) + uint32_t(h * (kBN / 2));
+        // Accumulator buffers are released on the issuing (even) CTA's barriers.
+        uint32_t release0 = 0u, release1 = 0u;
+        if constexpr (CTAS == 2) {
+            release0 = mapa_shared(smem_u32(&st->acc_empty[0]), 0);
+            release1 = mapa_shared(smem_u32(&st->acc_empty[1]), 0);
+        }
         int abuf = 0;
         uint32_t aph = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < args.num_tiles && ok; t += gridDim.x) {
+        for (int t = cluster; t < args.num_tiles && ok; t += nclusters) {
             int mb, nb;
             tile_coords(t, args, mb, nb);
-            const int row = mb * kBM + 32 * q + lane;
+            const int row = mb * (kBM * CTAS) + int(rank) * kBM + 32 * q + lane;
             const int col0 = nb * kBN + h * (kBN / 2);
             if constexpr (INT_OUT) {
                 int32_t acc[kBN / 2];
@@ -284,7 +361,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     tc_fence_before_sync();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&st->acc_empty[abuf]);
+                    if (lane == 0) {
+                        if constexpr (CTAS == 1)
+                            mbar_arrive(&st->acc_empty[abuf]);
+                        else
+                            mbar_arrive_cluster(abuf ? release1 : release0);
+                    }
                     if (++abuf == 2) {
                         abuf = 0;
                         aph ^= 1u;
@@ -319,7 +401,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&st->acc_empty[abuf]);
+                if (lane == 0) {
+                    if constexpr (CTAS == 1)
+                        mbar_arrive(&st->acc_empty[abuf]);
+                    else
+                        mbar_arrive_cluster(abuf ? release1 : release0);
+                }
                 if (++abuf == 2) {
                     abuf = 0;
                     aph ^= 1u;
@@ -329,9 +416,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
 
     tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (CTAS == 1)
+        __syncthreads();
+    else
+        cluster_sync();
     tc_fence_after_sync();
-    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+    if (warp == 1) tmem_dealloc<CTAS>(tmem_base, TMEM_COLS);
 }
 
 __global__ void zero_fill_kernel(uint32_t *C, int64_t ldc, int M, int N) {
@@ -343,38 +433,71 @@ __global__ void zero_fill_kernel(uint32_t *C, int64_t ldc, int M, int N) {
     }
 }
 
-template <Kind KIND, bool B_MN, bool INT_OUT>
+struct LaunchCache {
+    int dev = -1;
+    int max_clusters = 0;
+};
+
+template <Kind KIND, bool B_MN, bool INT_OUT, int CTAS>
 cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args,
-                       int grid, cudaStream_t stream) {
-    auto *fn = gemm_kernel<KIND, B_MN, INT_OUT>;
-    // The attribute is per device; setting it on every launch costs ~1 us and
-    // keeps multi-device use correct.
-    static thread_local int last_dev = -1;
+                       int sms, cudaStream_t stream) {
+    auto *fn = gemm_kernel<KIND, B_MN, INT_OUT, CTAS>;
+    constexpr size_t SMEM = smem_bytes<CTAS>();
+    static thread_local LaunchCache cache;  // per device (re-queried when it changes)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev != last_dev) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM_BYTES));
-        if (e != cudaSuccess) return e;
-        last_dev = dev;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute attr[1];
+    std::memset(attr, 0, sizeof(attr));
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = SMEM;
+    cfg.stream = stream;
+    if constexpr (CTAS == 2) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
     }
-    fn<<<grid, THREADS, SMEM_BYTES, stream>>>(ta, tb, args);
+    if (dev != cache.dev) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM));
+        if (e != cudaSuccess) return e;
+        int clusters = sms / CTAS;
+        if constexpr (CTAS == 2) {
+            cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+            int n = 0;
+            e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+            if (e != cudaSuccess) return e;
+            if (n <= 0) return cudaErrorInvalidConfiguration;
+            if (n < clusters) clusters = n;
+        }
+        cache.max_clusters = clusters;
+        cache.dev = dev;
+    }
+    const int clusters = args.num_tiles < cache.max_clusters ? args.num_tiles : cache.max_clusters;
+    cfg.gridDim = dim3(CTAS * clusters, 1, 1);
+    e = cudaLaunchKernelEx(&cfg, fn, ta, tb, args);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t gemm_smem_bytes() { return SMEM_BYTES; }
+size_t gemm_smem_bytes(int ctas) { return ctas == 2 ? smem_bytes<2>() : smem_bytes<1>(); }
 
-cudaError_t launch_gemm(Kind kind, bool b_mn_major, bool int_out, const CUtensorMap &ta,
-                        const CUtensorMap &tb, const GemmArgs &args, int grid,
+cudaError_t launch_gemm(Kind kind, bool b_mn_major, bool int_out, int ctas, const CUtensorMap &ta,
+                        const CUtensorMap &tb, const GemmArgs &args, int sms,
                         cudaStream_t stream) {
-    if (kind == Kind::F16 && b_mn_major && !int_out)
-        return launch_one<Kind::F16, true, false>(ta, tb, args, grid, stream);
-    if (kind == Kind::F16 && !b_mn_major && int_out)
-        return launch_one<Kind::F16, false, true>(ta, tb, args, grid, stream);
-    if (kind == Kind::E4M3 && !b_mn_major && int_out)
-        return launch_one<Kind::E4M3, false, true>(ta, tb, args, grid, stream);
+#define PTC_LAUNCH(K, BMN, IO)                                              \
+    return ctas == 2 ? launch_one<K, BMN, IO, 2>(ta, tb, args, sms, stream) \
+                     : launch_one<K, BMN, IO, 1>(ta, tb, args, sms, stream)
+    if (kind == Kind::F16 && b_mn_major && !int_out) PTC_LAUNCH(Kind::F16, true, false);
+    if (kind == Kind::F16 && !b_mn_major && int_out) PTC_LAUNCH(Kind::F16, false, true);
+    if (kind == Kind::E4M3 && !b_mn_major && int_out) PTC_LAUNCH(Kind::E4M3, false, true);
+#undef PTC_LAUNCH
     return cudaErrorInvalidValue;
 }
 

@@ -32,15 +32,18 @@ struct GemmArgs {
     uint64_t wait_limit_ns;
 };
 
-// Dynamic shared memory the GEMM kernel needs.
-size_t gemm_smem_bytes();
+// Dynamic shared memory the GEMM kernel needs (ctas = 1: one CTA per
+// 128 x 256 tile; ctas = 2: a CTA pair per 256 x 256 tile).
+size_t gemm_smem_bytes(int ctas);
 
-// Launch the persistent tensor-core GEMM.
+// Launch the persistent tensor-core GEMM on at most `sms` SMs.
 //   F16  + B MN-major + float output:  gemm_f16
 //   F16  + B K-major  + int32 output:  gemm_s8 (operands converted s8 -> f16)
 //   E4M3 + B K-major  + int32 output:  gemm_s4 (operands converted s4 -> e4m3)
-cudaError_t launch_gemm(Kind kind, bool b_mn_major, bool int_out, const CUtensorMap &ta,
-                        const CUtensorMap &tb, const GemmArgs &args, int grid,
+// args.tiles_m counts tiles of kBM * ctas rows.  The tensor map of A has boxes
+// of kBM rows; that of B boxes of kBN / ctas rows (K-major) or 64 x 64 (MN-major).
+cudaError_t launch_gemm(Kind kind, bool b_mn_major, bool int_out, int ctas, const CUtensorMap &ta,
+                        const CUtensorMap &tb, const GemmArgs &args, int sms,
                         cudaStream_t stream);
 
 // C[M x N] (4-byte elements) = 0.

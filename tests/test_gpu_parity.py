@@ -30,6 +30,15 @@ def built():
     assert ptc.gemm_poll_device_error() == ptc.PTC_OK
 
 
+@pytest.fixture(params=[1, 2], ids=["cta1", "cta2"])
+def cta_mode(request):
+    """Run the test with one CTA per 128 x 256 tile, then with CTA pairs on
+    256 x 256 tiles (tcgen05 cta_group::2), whatever the problem size."""
+    ptc.ptc_set_tuning("cta_pair", request.param)
+    yield request.param
+    ptc.ptc_set_tuning("cta_pair", 0)
+
+
 def run_f16(A, B):
     C = ptc.matmul_f16(f16_dev(A), f16_dev(B))
     torch.cuda.synchronize()
@@ -123,7 +132,7 @@ RAGGED = [(1, 1, 1), (15, 17, 9), (31, 33, 64), (33, 31, 65), (127, 255, 63), (1
 
 
 @pytest.mark.parametrize("M,N,K", RAGGED)
-def test_ragged_f16(M, N, K):
+def test_ragged_f16(M, N, K, cta_mode):
     A, B = datagen.f16_operands(N, "uniform", seed=M * 7919 + K, m=M, k=K)
     A, B = pad_cols(A, 8), pad_cols(B, 8)
     Cd = torch.empty((M, max(4, (N + 3) // 4 * 4)), dtype=torch.float32, device=DEV)
@@ -135,7 +144,7 @@ def test_ragged_f16(M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", RAGGED)
-def test_ragged_s8(M, N, K):
+def test_ragged_s8(M, N, K, cta_mode):
     A, Bt = datagen.s8_operands(N, seed=M * 31 + K, m=M, k=K)
     A, Bt = pad_cols(A, 16), pad_cols(Bt, 16)
     Cd = torch.empty((M, max(4, (N + 3) // 4 * 4)), dtype=torch.int32, device=DEV)
@@ -148,7 +157,7 @@ def test_ragged_s8(M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", RAGGED)
-def test_ragged_s4(M, N, K):
+def test_ragged_s4(M, N, K, cta_mode):
     rng = np.random.default_rng(M * 131 + N + K)
     Av = rng.integers(-8, 8, size=(M, K)).astype(np.int8)
     Bv = rng.integers(-8, 8, size=(N, K)).astype(np.int8)
@@ -163,7 +172,7 @@ def test_ragged_s4(M, N, K):
 
 
 @pytest.mark.parametrize("K", [63, 64, 65, 127, 128, 129, 255, 256, 257, 511, 512, 513, 1023, 1024, 1025])
-def test_k_boundaries_int(K):
+def test_k_boundaries_int(K, cta_mode):
     M, N = 136, 264
     A, Bt = datagen.s8_operands(N, seed=K, m=M, k=K)
     A, Bt = pad_cols(A, 16), pad_cols(Bt, 16)
@@ -182,7 +191,7 @@ def test_k_boundaries_int(K):
 
 
 @pytest.mark.parametrize("prec", ["f16", "s8", "s4"])
-def test_zero_k_writes_zeros(prec):
+def test_zero_k_writes_zeros(prec, cta_mode):
     M, N = 70, 90
     dt = torch.float32 if prec == "f16" else torch.int32
     Cd = torch.full((M, 92), 7, dtype=dt, device=DEV)
@@ -193,7 +202,7 @@ def test_zero_k_writes_zeros(prec):
     assert np.all(c[:, :N] == 0) and np.all(c[:, N:] == 7)
 
 
-def test_identity_and_permutation_exact():
+def test_identity_and_permutation_exact(cta_mode):
     K = N = 384
     M = 256
     A = np.zeros((M, K))
@@ -210,7 +219,7 @@ def test_identity_and_permutation_exact():
     assert np.array_equal(C4, Bt4.T[perm].astype(np.int32))
 
 
-def test_mma_lab_worked_example(golden_dir):
+def test_mma_lab_worked_example(golden_dir, cta_mode):
     import os
     from tests.test_oracle_pins import _read_golden
     g = _read_golden(os.path.join(golden_dir, "mma_lab_m16n8k16.txt"))
@@ -225,7 +234,7 @@ def test_mma_lab_worked_example(golden_dir):
 
 
 @pytest.mark.parametrize("prec", ["f16", "s8", "s4"])
-def test_guard_bands_untouched(prec):
+def test_guard_bands_untouched(prec, cta_mode):
     """Output slots outside the M x N block (row padding and rows past M) keep
     the sentinel 0xdeadbeef."""
     M, N, K = 130, 264, 96
@@ -257,7 +266,7 @@ def test_guard_bands_untouched(prec):
         assert np.array_equal(c[:M, :N], oracle.wrap_s32(oracle.gemm_s4(A, Bt, K)))
 
 
-def test_strided_operands_padding_not_read():
+def test_strided_operands_padding_not_read(cta_mode):
     """Leading dimensions larger than the logical width; the padding holds
     values that would change the result if they were read."""
     M, N, K = 150, 270, 100
@@ -282,7 +291,7 @@ def test_strided_operands_padding_not_read():
 
 
 # ---------------------------------------------------------------- integer exactness
-def test_int8_extremes_and_cancellation_k8192():
+def test_int8_extremes_and_cancellation_k8192(cta_mode):
     """(-128)(-128) summed over K = 8192 is 2^27 (FP32 alone would round it);
     the cancellation adversary has exact result 0 with partial sums ~2^26."""
     K, M, N = 8192, 130, 260
@@ -301,7 +310,7 @@ def test_int8_extremes_and_cancellation_k8192():
     assert np.array_equal(C, oracle.wrap_s32(oracle.gemm_s8(A, Bt)))
 
 
-def test_int4_extremes_and_cancellation_k8192():
+def test_int4_extremes_and_cancellation_k8192(cta_mode):
     K, M, N = 8192, 130, 260
     pk = lambda v, r: datagen.pack_s4_rows(np.full((r, K), v, np.int8))
     C = run_s4(pk(-8, M), pk(-8, N), K)
@@ -320,7 +329,7 @@ def test_int4_extremes_and_cancellation_k8192():
     assert np.array_equal(run_s4(Ap, Bp, K), oracle.wrap_s32(oracle.gemm_s4(Ap, Bp, K)))
 
 
-def test_int8_odd_partial_sums_up_to_2_24():
+def test_int8_odd_partial_sums_up_to_2_24(cta_mode):
     """Every fold of the INT8 route sums 1024 K values; with A = 127 and B = 127
     except one 126 per 16 values, each 16-product group sums to an odd number
     and the partial sums climb to 64 * 257937 = 16,507,968 < 2^24 through odd
@@ -336,7 +345,7 @@ def test_int8_odd_partial_sums_up_to_2_24():
     assert np.array_equal(C, oracle.wrap_s32(oracle.gemm_s8(A, Bt)))
 
 
-def test_int4_odd_partial_sums():
+def test_int4_odd_partial_sums(cta_mode):
     """INT4 route: A = 7, B = 7 except one 6 per 32 values, so each 32-product
     group sums to the odd 1561 and the running sums stay odd-valued as they
     grow; with a wrap pattern per column."""
@@ -392,7 +401,7 @@ def test_host_tensors_end_to_end():
     check_f16(C.numpy(), A, B)
 
 
-def test_wait_timeout_is_reported_and_context_survives():
+def test_wait_timeout_is_reported_and_context_survives(cta_mode):
     """A kernel whose operands for one tile are withheld gives up after the
     (shortened) wait limit, reports PTC_ERR_TIMEOUT, and the context stays
     usable for the next call."""
