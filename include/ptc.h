@@ -174,13 +174,16 @@ int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile);
 /* Tuning and test knobs, process-wide.  Returns PTC_OK, or PTC_ERR_INVALID for
  * an unknown key or a value out of range.  Keys:
  *   "group_m"      output-tile rows per raster group of the persistent
- *                  scheduler (L2 reuse), default 16
+ *                  scheduler (L2 reuse), default 8
  *   "s8_chunk_kb"  INT8 route: K blocks (64 values each) whose FP32 partial
  *                  sum is folded into int32 at a time, default 16 (1024
  *                  values: |partial| <= 2^24, so every FP32 partial sum is an
  *                  exactly representable integer)
  *   "s4_chunk_kb"  INT4 route: K blocks (128 values each) per fold, default 16
  *                  (2048 values: |partial| <= 2^17)
+ *   "l2_hint"      L2 eviction policy of operand loads: 0 (default) none;
+ *                  1 A evict-last / B evict-first; 2 A evict-last; 3 both
+ *                  evict-normal (all measured slower than 0 on GB300)
  *   "cta_pair"     0 (default): one CTA per 128 x 256 output tile while such
  *                  tiles leave SMs idle, else clusters of two CTAs sharing
  *                  256 x 256 tiles (tcgen05 cta_group::2); 1: always one CTA;

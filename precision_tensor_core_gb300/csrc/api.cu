@@ -36,7 +36,8 @@ thread_local char g_msg[512];
 // int32 every kb_per_chunk K blocks of 128 bytes; see gemm_tc.cu.
 std::atomic<int> g_chunk_s8{16};  // 1024 K values: |partial| <= 1024 * 2^14 = 2^24
 std::atomic<int> g_chunk_s4{16};  // 2048 K values: |partial| <= 2048 * 2^6  = 2^17
-std::atomic<int> g_group_m{16};
+std::atomic<int> g_group_m{8};
+std::atomic<int> g_l2_hint{0};
 std::atomic<int> g_cta_pair{0};   // 0: by problem size, 1: one CTA per tile, 2: CTA pairs
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 std::atomic<int64_t> g_stall_tile{-1};
@@ -206,6 +207,7 @@ GemmArgs base_args(int64_t M, int64_t N, int64_t K, int k_elems_per_block, void 
     a.kb_per_chunk = a.num_kb;
     a.group_m = g_group_m.load() > 0 ? g_group_m.load() : 1;
     a.stall_tile = int(g_stall_tile.exchange(-1));
+    a.l2_hint = g_l2_hint.load();
     a.wait_limit_ns = g_wait_ns.load();
     return a;
 }
@@ -313,16 +315,11 @@ int gemm_s8(int64_t M, int64_t N, int64_t K, const int8_t *A, int64_t lda, const
     uint16_t *bw = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + a_bytes);
     const int cgrid = d->sms * 8;
     rc = PTC_OK;
-    if ((e = ptc::launch_s8_to_f16(A, lda, int(M), int(K), aw, ldw, cgrid, s)) != cudaSuccess)
+    if ((e = ptc::launch_s8_to_f16_pair(A, lda, int(M), B, ldb, int(N), int(K), aw, bw, ldw, cgrid, s)) !=
+        cudaSuccess)
         rc = fail_cuda(e, "s8 conversion launch");
     else
         g_launches.fetch_add(1);
-    if (!rc) {
-        if ((e = ptc::launch_s8_to_f16(B, ldb, int(N), int(K), bw, ldw, cgrid, s)) != cudaSuccess)
-            rc = fail_cuda(e, "s8 conversion launch");
-        else
-            g_launches.fetch_add(1);
-    }
     const int ctas = choose_ctas(M, N, d->sms);
     CUtensorMap ta, tb;
     if (!rc) rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, aw, K, M, uint64_t(ldw) * 2, 64, ptc::kBM);
@@ -377,18 +374,12 @@ int gemm_s4(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const v
     uint8_t *bw = aw + a_bytes;
     const int cgrid = d->sms * 8;
     rc = PTC_OK;
-    if ((e = ptc::launch_s4_to_e4m3(static_cast<const uint8_t *>(A), lda / 2, int(M), int(K), aw, ldw,
-                                    cgrid, s)) != cudaSuccess)
+    if ((e = ptc::launch_s4_to_e4m3_pair(static_cast<const uint8_t *>(A), lda / 2, int(M),
+                                         static_cast<const uint8_t *>(B), ldb / 2, int(N), int(K), aw, bw,
+                                         ldw, cgrid, s)) != cudaSuccess)
         rc = fail_cuda(e, "s4 conversion launch");
     else
         g_launches.fetch_add(1);
-    if (!rc) {
-        if ((e = ptc::launch_s4_to_e4m3(static_cast<const uint8_t *>(B), ldb / 2, int(N), int(K), bw,
-                                        ldw, cgrid, s)) != cudaSuccess)
-            rc = fail_cuda(e, "s4 conversion launch");
-        else
-            g_launches.fetch_add(1);
-    }
     const int ctas = choose_ctas(M, N, d->sms);
     CUtensorMap ta, tb;
     if (!rc) rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, aw, K, M, uint64_t(ldw), 128, ptc::kBM);
@@ -451,6 +442,10 @@ int ptc_set_tuning(const char *key, int64_t value) {
     }
     if (std::strcmp(key, "group_m") == 0 && value > 0 && value < (1 << 20)) {
         g_group_m.store(int(value));
+        return PTC_OK;
+    }
+    if (std::strcmp(key, "l2_hint") == 0 && value >= 0 && value <= 3) {
+        g_l2_hint.store(int(value));
         return PTC_OK;
     }
     if (std::strcmp(key, "cta_pair") == 0 && value >= 0 && value <= 2) {

@@ -39,16 +39,28 @@ __device__ __forceinline__ uint16_t s8_to_f16_bits(int8_t v) {
     return __half_as_ushort(__int2half_rn(static_cast<int>(v)));
 }
 
-__global__ void s8_to_f16_kernel(const int8_t *__restrict__ src, int64_t lds, int rows, int cols,
-                                 uint16_t *__restrict__ dst, int64_t ldd) {
+// Converts rows [0, rows_a) of A and then rows [0, rows_b) of B, cols
+// elements each, in one grid-stride pass over (row, 16-element vector) pairs.
+__global__ void s8_to_f16_kernel(const int8_t *__restrict__ src_a, int64_t lds_a, int rows_a,
+                                 const int8_t *__restrict__ src_b, int64_t lds_b, int rows_b,
+                                 int cols, uint16_t *__restrict__ dst_a, uint16_t *__restrict__ dst_b,
+                                 int64_t ldd) {
     const int vpr = (cols + 15) / 16;  // 16-element vectors per row
-    const int64_t total = int64_t(rows) * vpr;
+    const int64_t total = int64_t(rows_a + rows_b) * vpr;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
          i += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t r = i / vpr;
+        int64_t r = i / vpr;
         const int c0 = int(i - r * vpr) * 16;
-        const int8_t *s = src + r * lds + c0;
-        uint16_t *d = dst + r * ldd + c0;
+        const int8_t *s;
+        uint16_t *d;
+        if (r < rows_a) {
+            s = src_a + r * lds_a + c0;
+            d = dst_a + r * ldd + c0;
+        } else {
+            r -= rows_a;
+            s = src_b + r * lds_b + c0;
+            d = dst_b + r * ldd + c0;
+        }
         if (c0 + 16 <= cols) {
             const uint4 x = __ldcs(reinterpret_cast<const uint4 *>(s));
             uint4 o0, o1;
@@ -107,16 +119,27 @@ __device__ __forceinline__ uint8_t s4_to_e4m3_byte(uint32_t nib) {
     return static_cast<uint8_t>(s4x4_to_e4m3x4(nib & 0xFu) & 0xFFu);
 }
 
-__global__ void s4_to_e4m3_kernel(const uint8_t *__restrict__ src, int64_t lds, int rows, int cols,
-                                  uint8_t *__restrict__ dst, int64_t ldd) {
+// As s8_to_f16_kernel: rows of A, then rows of B, 32-element vectors.
+__global__ void s4_to_e4m3_kernel(const uint8_t *__restrict__ src_a, int64_t lds_a, int rows_a,
+                                  const uint8_t *__restrict__ src_b, int64_t lds_b, int rows_b,
+                                  int cols, uint8_t *__restrict__ dst_a, uint8_t *__restrict__ dst_b,
+                                  int64_t ldd) {
     const int vpr = (cols + 31) / 32;  // 32-element (16-byte packed) vectors per row
-    const int64_t total = int64_t(rows) * vpr;
+    const int64_t total = int64_t(rows_a + rows_b) * vpr;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
          i += int64_t(gridDim.x) * blockDim.x) {
-        const int64_t r = i / vpr;
+        int64_t r = i / vpr;
         const int c0 = int(i - r * vpr) * 32;
-        const uint8_t *s = src + r * lds + c0 / 2;
-        uint8_t *d = dst + r * ldd + c0;
+        const uint8_t *s;
+        uint8_t *d;
+        if (r < rows_a) {
+            s = src_a + r * lds_a + c0 / 2;
+            d = dst_a + r * ldd + c0;
+        } else {
+            r -= rows_a;
+            s = src_b + r * lds_b + c0 / 2;
+            d = dst_b + r * ldd + c0;
+        }
         if (c0 + 32 <= cols) {
             const uint4 x = __ldcs(reinterpret_cast<const uint4 *>(s));
             const uint32_t w[4] = {x.x, x.y, x.z, x.w};
@@ -141,13 +164,21 @@ __global__ void s4_to_e4m3_kernel(const uint8_t *__restrict__ src, int64_t lds, 
 
 cudaError_t launch_s8_to_f16(const int8_t *src, int64_t lds, int rows, int cols, uint16_t *dst,
                              int64_t ldd, int grid, cudaStream_t stream) {
-    s8_to_f16_kernel<<<grid, 256, 0, stream>>>(src, lds, rows, cols, dst, ldd);
+    s8_to_f16_kernel<<<grid, 256, 0, stream>>>(src, lds, rows, src, lds, 0, cols, dst, dst, ldd);
     return cudaGetLastError();
 }
 
-cudaError_t launch_s4_to_e4m3(const uint8_t *src, int64_t lds, int rows, int cols, uint8_t *dst,
-                              int64_t ldd, int grid, cudaStream_t stream) {
-    s4_to_e4m3_kernel<<<grid, 256, 0, stream>>>(src, lds, rows, cols, dst, ldd);
+cudaError_t launch_s8_to_f16_pair(const int8_t *a, int64_t lda, int rows_a, const int8_t *b,
+                                  int64_t ldb, int rows_b, int cols, uint16_t *dst_a, uint16_t *dst_b,
+                                  int64_t ldd, int grid, cudaStream_t stream) {
+    s8_to_f16_kernel<<<grid, 256, 0, stream>>>(a, lda, rows_a, b, ldb, rows_b, cols, dst_a, dst_b, ldd);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_s4_to_e4m3_pair(const uint8_t *a, int64_t lda, int rows_a, const uint8_t *b,
+                                   int64_t ldb, int rows_b, int cols, uint8_t *dst_a, uint8_t *dst_b,
+                                   int64_t ldd, int grid, cudaStream_t stream) {
+    s4_to_e4m3_kernel<<<grid, 256, 0, stream>>>(a, lda, rows_a, b, ldb, rows_b, cols, dst_a, dst_b, ldd);
     return cudaGetLastError();
 }
 

@@ -23,7 +23,7 @@
 //   CTAS = 2    a cluster of two CTAs per 256 x 256 output tile
 //               (tcgen05 cta_group::2, M = 256 MMAs issued by the even CTA):
 //               each CTA stages its own 128 rows of A and half of B, so a CTA
-//               moves 32 KiB per stage instead of 48 KiB and the ring holds 6
+//               moves 32 KiB per stage instead of 48 KiB and the ring holds 7
 //               stages.
 //
 // Integer routes: sm_103a has no integer tcgen05 MMA, so INT8 runs on the
@@ -60,10 +60,10 @@ constexpr int KSTEPS = kRowBytes / KSTEP_BYTES; // MMAs per stage
 
 // Per-CTA shapes of the two variants.  A CTA stages 128 rows of A; alone it
 // stages all 256 rows of B (4 stages of 48 KiB), in a pair it stages half of
-// B (6 stages of 32 KiB: the pair's MMAs read B from both CTAs).
+// B (7 stages of 32 KiB: the pair's MMAs read B from both CTAs).
 template <int CTAS>
 struct Cfg {
-    static constexpr int STAGES = CTAS == 1 ? 4 : 6;
+    static constexpr int STAGES = CTAS == 1 ? 4 : 7;
     static constexpr int B_ROWS = kBN / CTAS;
     static constexpr int A_STAGE = kBM * kRowBytes;
     static constexpr int B_STAGE = B_ROWS * kRowBytes;
@@ -188,6 +188,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
+            // L2 policies: A panels are re-read by every N tile of a raster group,
+            // B panels only by the M tiles of one group running at the same time.
+            const bool hint = args.l2_hint != 0;
+            uint64_t pol_a = 0, pol_b = 0;
+            if (args.l2_hint == 1 || args.l2_hint == 2) pol_a = l2_policy_evict_last();
+            if (args.l2_hint == 1) pol_b = l2_policy_evict_first();
+            if (args.l2_hint == 2) pol_b = l2_policy_evict_normal();
+            if (args.l2_hint == 3) pol_a = pol_b = l2_policy_evict_normal();
             int s = 0;
             uint32_t ph = 0;
             uint32_t outstanding = 0, out_phase = 0;  // per-stage bits of issued copies
@@ -209,14 +217,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                         uint8_t *b_dst = b_ring + s * C_::B_STAGE;
                         if constexpr (CTAS == 1) {
                             mbar_arrive_expect_tx(&st->full[s], C_::STAGE);
-                            tma_load_2d(a_dst, &tmA, &st->full[s], kb * K_ELEMS, m0);
+                            auto load = [&](void *dst, const CUtensorMap *map, int x, int y, uint64_t pol) {
+                                if (hint)
+                                    tma_load_2d_hint(dst, map, &st->full[s], x, y, pol);
+                                else
+                                    tma_load_2d(dst, map, &st->full[s], x, y);
+                            };
+                            load(a_dst, &tmA, kb * K_ELEMS, m0, pol_a);
                             if constexpr (B_MN) {
 #pragma unroll
                                 for (int i = 0; i < C_::B_ROWS / 64; ++i)
-                                    tma_load_2d(b_dst + i * (K_ELEMS * 128), &tmB, &st->full[s],
-                                                n0 + 64 * i, kb * K_ELEMS);
+                                    load(b_dst + i * (K_ELEMS * 128), &tmB, n0 + 64 * i, kb * K_ELEMS, pol_b);
                             } else {
-                                tma_load_2d(b_dst, &tmB, &st->full[s], kb * K_ELEMS, n0);
+                                load(b_dst, &tmB, kb * K_ELEMS, n0, pol_b);
                             }
                             outstanding |= 1u << s;
                             out_phase = (out_phase & ~(1u << s)) | (ph << s);
@@ -225,14 +238,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                             // which alone expects the pair's bytes.
                             const uint32_t bar = mapa_shared(smem_u32(&st->full[s]), 0);
                             if (rank == 0) mbar_arrive_expect_tx(&st->full[s], CTAS * C_::STAGE);
-                            tma_load_2d_pair(a_dst, &tmA, bar, kb * K_ELEMS, m0);
+                            auto load = [&](void *dst, const CUtensorMap *map, int x, int y, uint64_t pol) {
+                                if (hint)
+                                    tma_load_2d_pair_hint(dst, map, bar, x, y, pol);
+                                else
+                                    tma_load_2d_pair(dst, map, bar, x, y);
+                            };
+                            load(a_dst, &tmA, kb * K_ELEMS, m0, pol_a);
                             if constexpr (B_MN) {
 #pragma unroll
                                 for (int i = 0; i < C_::B_ROWS / 64; ++i)
-                                    tma_load_2d_pair(b_dst + i * (K_ELEMS * 128), &tmB, bar,
-                                                     n0 + 64 * i, kb * K_ELEMS);
+                                    load(b_dst + i * (K_ELEMS * 128), &tmB, n0 + 64 * i, kb * K_ELEMS, pol_b);
                             } else {
-                                tma_load_2d_pair(b_dst, &tmB, bar, kb * K_ELEMS, n0);
+                                load(b_dst, &tmB, kb * K_ELEMS, n0, pol_b);
                             }
                         }
                     }

@@ -29,6 +29,8 @@ struct GemmArgs {
                            // epilogue folds the partial sum into int32 registers
     int group_m;           // tiles of M per raster group (L2 reuse)
     int stall_tile;        // test hook: withhold this tile's operands (-1: none)
+    int l2_hint;           // L2 policy of operand loads: 0 none, 1 A evict-last and
+                           // B evict-first, 2 A evict-last, 3 both evict-normal
     uint64_t wait_limit_ns;
 };
 
@@ -52,14 +54,19 @@ cudaError_t launch_zero_fill(void *C, int64_t ldc, int M, int N, int grid, cudaS
 // Reads and clears the device error word of the current device.
 cudaError_t read_and_clear_error_word(uint32_t *out);
 
-// Operand preparation for the integer routes: exact element conversion into a
-// dense, 128-byte-pitched workspace matrix of `rows` x `cols`.
-//   s8 -> binary16: src row pitch lds bytes, dst pitch ldd elements (2 bytes)
+// Operand preparation for the integer routes: exact element conversion into
+// dense, 128-byte-pitched workspace matrices of `cols` columns.
+//   s8 -> binary16: source pitches in bytes, destination pitch ldd elements
 cudaError_t launch_s8_to_f16(const int8_t *src, int64_t lds, int rows, int cols, uint16_t *dst,
                              int64_t ldd, int grid, cudaStream_t stream);
-//   packed s4 -> E4M3: src row pitch lds BYTES, dst pitch ldd elements (bytes)
-cudaError_t launch_s4_to_e4m3(const uint8_t *src, int64_t lds, int rows, int cols, uint8_t *dst,
-                              int64_t ldd, int grid, cudaStream_t stream);
+//   both operands in one launch: rows_a rows of A, then rows_b rows of B
+cudaError_t launch_s8_to_f16_pair(const int8_t *a, int64_t lda, int rows_a, const int8_t *b,
+                                  int64_t ldb, int rows_b, int cols, uint16_t *dst_a, uint16_t *dst_b,
+                                  int64_t ldd, int grid, cudaStream_t stream);
+//   packed s4 -> E4M3, both operands: source pitches in BYTES, ldd in elements
+cudaError_t launch_s4_to_e4m3_pair(const uint8_t *a, int64_t lda, int rows_a, const uint8_t *b,
+                                   int64_t ldb, int rows_b, int cols, uint8_t *dst_a, uint8_t *dst_b,
+                                   int64_t ldd, int grid, cudaStream_t stream);
 
 // Adds to the library's kernel-launch counter (ptc_kernel_launch_count).
 void note_launches(uint64_t n);
