@@ -71,6 +71,22 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+# ---------------------------------------------------------------- ranks
+def reduce_max(dist, x: float, device) -> float:
+    """Max of x over all ranks (x itself without a process group)."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def throughput_tops(ops_per_step: float, steps: int, world: int, elapsed_ms: float) -> float:
+    """Whole-job TOPS: the operations every rank did, over the slowest rank's time."""
+    return ops_per_step * steps * world / (elapsed_ms * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- inputs
 def make_inputs(n):
     import datagen
@@ -178,13 +194,10 @@ def run_ours(args, rank, world, dist):
     t8 = [e[1].elapsed_time(e[2]) for e in evs]
     t4 = [e[2].elapsed_time(e[3]) for e in evs]
     assert ptc.gemm_poll_device_error() == ptc.PTC_OK
-    if dist:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = reduce_max(dist, elapsed_ms, dev)
 
     ops = 2.0 * n ** 3
-    value = 3 * ops * args.steps * world / (elapsed_ms * 1e-3) / 1e12
+    value = throughput_tops(3 * ops, args.steps, world, elapsed_ms)
     per = {"fp16_tflops": ops / (statistics.mean(t16) * 1e-3) / 1e12,
            "int8_tops": ops / (statistics.mean(t8) * 1e-3) / 1e12,
            "int4_tops": ops / (statistics.mean(t4) * 1e-3) / 1e12,
@@ -214,14 +227,10 @@ def run_ours(args, rank, world, dist):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max(dist, e0.elapsed_time(e1), dev)
     h2d = sum(a.numel() * a.element_size() + b.numel() * b.element_size() for a, b in hp.values())
     d2h = sum(x.numel() * x.element_size() for x in (h16, h8, h4))
-    e2e = {"value": 3 * ops * e2e_steps * world / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS",
+    e2e = {"value": throughput_tops(3 * ops, e2e_steps, world, e2e_ms), "unit": "TOPS",
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": e2e_steps}
 
     peaks, src = load_peaks()

@@ -1,0 +1,82 @@
+"""bench.py without a GPU: the multi-rank timing path on two gloo ranks, the
+whole-job throughput formula, and the reference arm's JSON line (CPU oracle on
+a small problem; under torchrun only rank 0 prints)."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        dist.barrier()
+        slowest = bench.reduce_max(dist, 10.0 * (rank + 1), "cpu")
+        value = bench.throughput_tops(3 * 2.0 * 8192 ** 3, 4, world, slowest)
+        q.put((rank, slowest, value))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_slowest_rank():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(world))
+    expect = 3 * 2.0 * 8192 ** 3 * 4 * 2 / 20e-3 / 1e12
+    for rank, slowest, value in got:
+        assert slowest == 20.0
+        assert value == pytest.approx(expect)
+
+
+def test_throughput_formula_single_rank():
+    assert bench.reduce_max(None, 3.5, "cpu") == 3.5
+    # 2 N^3 ops in 1 ms at N = 1000 is 2 TOPS
+    assert bench.throughput_tops(2e9, 1, 1, 1.0) == pytest.approx(2.0)
+
+
+def _run_bench(args, env_extra):
+    env = dict(os.environ, **env_extra)
+    return subprocess.run([sys.executable, os.path.join(ROOT, "bench.py")] + args,
+                          capture_output=True, text=True, env=env, timeout=300)
+
+
+def test_reference_arm_json_line():
+    r = _run_bench(["--impl", "reference", "--n", "256", "--steps", "2", "--warmup", "1"], {})
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "TOPS" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+    assert d["steps"] == 2 and d["warmup"] == 1 and d["higher_is_better"] is True
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    r = _run_bench(["--impl", "reference", "--n", "256", "--steps", "2", "--warmup", "1"],
+                   {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
+    assert r.returncode == 0 and r.stdout.strip() == ""
