@@ -179,8 +179,10 @@ int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile);
  *                  sum is folded into int32 at a time, default 16 (1024
  *                  values: |partial| <= 2^24, so every FP32 partial sum is an
  *                  exactly representable integer)
- *   "s4_chunk_kb"  INT4 route: K blocks (128 values each) per fold, default 16
- *                  (2048 values: |partial| <= 2^17)
+ *   "s4_chunk_kb"  INT4 route: K blocks (128 values each) per fold, default 64
+ *                  (8192 values: |partial| <= 2^19)
+ *   "prefetch_kb"  L2 prefetch of the operands this many K blocks ahead of
+ *                  the loads; 0 (default) off (measured much slower on GB300)
  *   "l2_hint"      L2 eviction policy of operand loads: 0 (default) none;
  *                  1 A evict-last / B evict-first; 2 A evict-last; 3 both
  *                  evict-normal (all measured slower than 0 on GB300)

@@ -35,9 +35,10 @@ thread_local char g_msg[512];
 // Tunables (process-wide).  Integer routes fold the FP32 partial sums into
 // int32 every kb_per_chunk K blocks of 128 bytes; see gemm_tc.cu.
 std::atomic<int> g_chunk_s8{16};  // 1024 K values: |partial| <= 1024 * 2^14 = 2^24
-std::atomic<int> g_chunk_s4{16};  // 2048 K values: |partial| <= 2048 * 2^6  = 2^17
+std::atomic<int> g_chunk_s4{64};  // 8192 K values: |partial| <= 8192 * 2^6  = 2^19
 std::atomic<int> g_group_m{8};
 std::atomic<int> g_l2_hint{0};
+std::atomic<int> g_prefetch_kb{0};
 std::atomic<int> g_cta_pair{0};   // 0: by problem size, 1: one CTA per tile, 2: CTA pairs
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 std::atomic<int64_t> g_stall_tile{-1};
@@ -208,6 +209,7 @@ GemmArgs base_args(int64_t M, int64_t N, int64_t K, int k_elems_per_block, void 
     a.group_m = g_group_m.load() > 0 ? g_group_m.load() : 1;
     a.stall_tile = int(g_stall_tile.exchange(-1));
     a.l2_hint = g_l2_hint.load();
+    a.prefetch_kb = g_prefetch_kb.load();
     a.wait_limit_ns = g_wait_ns.load();
     return a;
 }
@@ -442,6 +444,10 @@ int ptc_set_tuning(const char *key, int64_t value) {
     }
     if (std::strcmp(key, "group_m") == 0 && value > 0 && value < (1 << 20)) {
         g_group_m.store(int(value));
+        return PTC_OK;
+    }
+    if (std::strcmp(key, "prefetch_kb") == 0 && value >= 0 && value <= 1024) {
+        g_prefetch_kb.store(int(value));
         return PTC_OK;
     }
     if (std::strcmp(key, "l2_hint") == 0 && value >= 0 && value <= 3) {

@@ -194,6 +194,7 @@ extern "C" int gemm_s8_noalloc(int64_t M, int64_t N, int64_t K, const int8_t *A,
     args.group_m = kGroupM;
     args.stall_tile = -1;
     args.l2_hint = 0;
+    args.prefetch_kb = 0;
     args.wait_limit_ns = kWaitNs;
     if ((e = ptc::launch_gemm(ptc::Kind::F16, false, true, 1, ta, tb, args, d->sms, s)) != cudaSuccess) {
         cudaGetLastError();

@@ -200,12 +200,32 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t ph = 0;
             uint32_t outstanding = 0, out_phase = 0;  // per-stage bits of issued copies
             bool ok = true;
+            int seq = 0;  // position in this CTA's sequence of (tile, K block) loads
             for (int t = cluster; t < args.num_tiles && ok; t += nclusters) {
                 int mb, nb;
                 tile_coords(t, args, mb, nb);
                 const int m0 = mb * (kBM * CTAS) + int(rank) * kBM;
                 const int n0 = nb * kBN + int(rank) * C_::B_ROWS;
-                for (int kb = 0; kb < args.num_kb; ++kb) {
+                for (int kb = 0; kb < args.num_kb; ++kb, ++seq) {
+                    if (args.prefetch_kb > 0) {
+                        // Warm L2 with the operands this CTA loads prefetch_kb K blocks later.
+                        const int p = seq + args.prefetch_kb;
+                        const int lt = p / args.num_kb, kbp = p - lt * args.num_kb;
+                        const int tp = cluster + lt * nclusters;
+                        if (tp < args.num_tiles) {
+                            int mbp, nbp;
+                            tile_coords(tp, args, mbp, nbp);
+                            tma_prefetch_2d(&tmA, kbp * K_ELEMS, mbp * (kBM * CTAS) + int(rank) * kBM);
+                            const int n0p = nbp * kBN + int(rank) * C_::B_ROWS;
+                            if constexpr (B_MN) {
+#pragma unroll
+                                for (int i = 0; i < C_::B_ROWS / 64; ++i)
+                                    tma_prefetch_2d(&tmB, n0p + 64 * i, kbp * K_ELEMS);
+                            } else {
+                                tma_prefetch_2d(&tmB, kbp * K_ELEMS, n0p);
+                            }
+                        }
+                    }
                     if (!mbar_wait(&st->empty[s], ph ^ 1u, &st->abort, &g_error_word, limit)) {
                         ok = false;
                         break;

@@ -29,6 +29,7 @@ struct GemmArgs {
                            // epilogue folds the partial sum into int32 registers
     int group_m;           // tiles of M per raster group (L2 reuse)
     int stall_tile;        // test hook: withhold this tile's operands (-1: none)
+    int prefetch_kb;       // L2 prefetch distance in K blocks ahead of the loads (0: off)
     int l2_hint;           // L2 policy of operand loads: 0 none, 1 A evict-last and
                            // B evict-first, 2 A evict-last, 3 both evict-normal
     uint64_t wait_limit_ns;

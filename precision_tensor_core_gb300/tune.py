@@ -1,0 +1,152 @@
+"""Tuning and size sweeps of the GEMM entry points on cuda:0.
+
+    python -m precision_tensor_core_gb300.tune --mode knobs --n 8192
+    python -m precision_tensor_core_gb300.tune --mode sizes --sizes 512,1024,2048,4096,8192
+
+`knobs` times gemm_f16 / gemm_s8 / gemm_s4 at one size under each setting of
+the library's tuning knobs (ptc_set_tuning: CTA pairs, raster group, L2
+eviction policy, INT fold length), one knob at a time from the defaults: the
+ablation that shows the defaults are a local optimum.  `sizes` times the three
+entry points at each size with the library defaults.
+
+Calls are captured in a CUDA graph (`--graph`, default on) and the graph is
+replayed, so that the host-side cost of a Python call does not hide the GPU
+time at small sizes; times are CUDA-event times of the replay divided by the
+calls in it.  Inputs are the benchmark's seeded operands.  These are tuning
+measurements, not the benchmark's reported numbers.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import sys
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULTS = {"cta_pair": 0, "group_m": 8, "l2_hint": 0, "prefetch_kb": 0, "s8_chunk_kb": 16,
+            "s4_chunk_kb": 64}
+KNOBS = {"cta_pair": [1, 2], "group_m": [4, 16, 32], "l2_hint": [1, 2, 3],
+         "prefetch_kb": [4, 8, 16, 32], "s8_chunk_kb": [4, 8], "s4_chunk_kb": [2, 8, 16, 128]}
+
+
+def main():
+    p = argparse.ArgumentParser()
+    p.add_argument("--mode", choices=["knobs", "sizes"], default="sizes")
+    p.add_argument("--n", type=int, default=8192)
+    p.add_argument("--sizes", default="512,1024,2048,4096,8192")
+    p.add_argument("--calls", type=int, default=0, help="calls per timing (0: by size)")
+    p.add_argument("--no-graph", action="store_true")
+    p.add_argument("--json", default="")
+    p.add_argument("--only", default="", help="comma-separated knob names to sweep (default: all)")
+    a = p.parse_args()
+
+    import torch
+
+    import datagen
+    import precision_tensor_core_gb300 as ptc
+    from precision_tensor_core_gb300 import build as ptc_build
+
+    ptc_build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+
+    def operands(n):
+        A, B = datagen.f16_operands(n, "normal")
+        A8, B8 = datagen.s8_operands(n)
+        A4, B4 = datagen.s4_operands(n)
+        t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).to(dev)
+        return {"f16": (t(A.view(np.float16)), t(B.view(np.float16)),
+                        torch.empty((n, n), dtype=torch.float32, device=dev)),
+                "s8": (t(A8), t(B8), torch.empty((n, n), dtype=torch.int32, device=dev)),
+                "s4": (t(A4), t(B4), torch.empty((n, n), dtype=torch.int32, device=dev))}
+
+    def call(prec, ops, n):
+        A, B, C = ops[prec]
+        if prec == "f16":
+            return lambda: ptc.matmul_f16(A, B, out=C)
+        if prec == "s8":
+            return lambda: ptc.matmul_s8(A, B, out=C)
+        return lambda: ptc.matmul_s4(A, B, n, out=C)
+
+    def time_ms(fn, calls):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g = None
+        if not a.no_graph:
+            try:
+                g = torch.cuda.CUDAGraph()
+                s = torch.cuda.Stream()
+                s.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(s):
+                    with torch.cuda.graph(g, stream=s):
+                        for _ in range(calls):
+                            fn()
+                torch.cuda.current_stream().wait_stream(s)
+                g.replay()
+                torch.cuda.synchronize()
+            except Exception as exc:  # capture unsupported for this call: time eagerly
+                print(f"  (graph capture failed: {exc}; timing eager calls)", flush=True)
+                torch.cuda.synchronize()
+                g = None
+        e0.record()
+        if g is not None:
+            g.replay()
+        else:
+            for _ in range(calls):
+                fn()
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / calls
+
+    def measure(n, ops):
+        calls = a.calls or max(4, min(200, int(2e13 / (2.0 * n ** 3))))
+        out = {}
+        for prec in ("f16", "s8", "s4"):
+            ms = time_ms(call(prec, ops, n), calls)
+            out[prec] = {"ms": ms, "tops": 2.0 * n ** 3 / (ms * 1e-3) / 1e12}
+        return out
+
+    results = {}
+    if a.mode == "sizes":
+        for k, v in DEFAULTS.items():
+            ptc.ptc_set_tuning(k, v)
+        print(f"{'N':>6} {'FP16 TFLOP/s':>13} {'INT8 TOPS':>10} {'INT4 TOPS':>10}   (ms per call)")
+        for n in [int(x) for x in a.sizes.split(",")]:
+            r = measure(n, operands(n))
+            results[str(n)] = r
+            print(f"{n:>6} {r['f16']['tops']:>13.1f} {r['s8']['tops']:>10.1f} {r['s4']['tops']:>10.1f}"
+                  f"   ({r['f16']['ms']:.4f} / {r['s8']['ms']:.4f} / {r['s4']['ms']:.4f})", flush=True)
+    else:
+        ops = operands(a.n)
+        chosen = [k for k in KNOBS if not a.only or k in a.only.split(",")]
+        settings = [("defaults", None, None)] + [(k, k, v) for k in chosen for v in KNOBS[k]]
+        print(f"{'setting':>18} {'FP16 TFLOP/s':>13} {'INT8 TOPS':>10} {'INT4 TOPS':>10} {'sum ms':>8}")
+        for label, key, val in settings:
+            for k, v in DEFAULTS.items():
+                ptc.ptc_set_tuning(k, v)
+            name = "defaults" if key is None else f"{key}={val}"
+            if key is not None:
+                ptc.ptc_set_tuning(key, val)
+            r = measure(a.n, ops)
+            results[name] = r
+            total = sum(r[p]["ms"] for p in r)
+            print(f"{name:>18} {r['f16']['tops']:>13.1f} {r['s8']['tops']:>10.1f} {r['s4']['tops']:>10.1f}"
+                  f" {total:>8.3f}", flush=True)
+        for k, v in DEFAULTS.items():
+            ptc.ptc_set_tuning(k, v)
+    status = ptc.gemm_poll_device_error()
+    if a.json:
+        with open(a.json, "w") as f:
+            json.dump(results, f, indent=1)
+    sys.exit(0 if status == ptc.PTC_OK else 1)
+
+
+if __name__ == "__main__":
+    main()
