@@ -125,6 +125,44 @@ int gemm_s4(int64_t M, int64_t N, int64_t K,
             void *stream);
 
 /*
+ * Integer GEMM with a dequantising epilogue.  The paper leaves scaling out of
+ * its kernels ("INT32 accumulations without in-kernel dequantization or
+ * scaling", section VI "Scope"); this is the per-channel-scaled form such
+ * INT8 / INT4 products take in quantised LLM inference (section V), built on
+ * the same exact integer sums:
+ *
+ *   acc[i][j] = sum_k A_ik B_kj                (exact, wrapped to int32)
+ *   C[i][j]   = out( rn(rn(rn(float(acc)) * scale_a[i]) * scale_b[j]) )
+ *
+ * in FP32 with round-to-nearest-even at each step, in that order and without
+ * fused multiply-add, then rounded to nearest-even into the output type
+ * (PTC_OUT_F32: no further rounding).  scale_a (M floats) and scale_b
+ * (N floats) are device pointers, 4-byte aligned; NULL means all ones.
+ * K == 0 writes +0 everywhere.  A, B, lda, ldb as gemm_s8 (INT8) and gemm_s4
+ * (packed INT4, nibbles); C row-major with ldc >= N elements of the output
+ * type and a row pitch that is a multiple of 16 bytes.  Errors as gemm_s8,
+ * plus PTC_ERR_INVALID for an unknown out_type and PTC_ERR_OVERLAP when C
+ * overlaps a scale vector.
+ */
+#define PTC_OUT_F32 0
+#define PTC_OUT_BF16 1
+#define PTC_OUT_F16 2
+
+int gemm_s8_scaled(int64_t M, int64_t N, int64_t K,
+                   const int8_t *A, int64_t lda,
+                   const int8_t *B, int64_t ldb,
+                   const float *scale_a, const float *scale_b,
+                   void *C, int64_t ldc, int out_type,
+                   void *stream);
+
+int gemm_s4_scaled(int64_t M, int64_t N, int64_t K,
+                   const void *A, int64_t lda,
+                   const void *B, int64_t ldb,
+                   const float *scale_a, const float *scale_b,
+                   void *C, int64_t ldc, int out_type,
+                   void *stream);
+
+/*
  * gemm_s8 without any memory allocation.  The paper has no counterpart: it is
  * an addition for callers that cannot let a library allocate device memory,
  * such as an application whose own allocator has reserved the GPU's memory

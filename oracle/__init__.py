@@ -32,7 +32,7 @@ def build(force: bool = False) -> str:
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
         subprocess.check_call(["gcc", "-O2", "-std=c11", "-Wall", "-fPIC", "-shared",
-                               "-pthread", _SRC, "-o", tmp, "-lm"])
+                               "-ffp-contract=off", "-pthread", _SRC, "-o", tmp, "-lm"])
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -65,6 +65,11 @@ def _load(path: str):
     L.oracle_gemm_s4_at.argtypes = [_i64, _vp, _i64, _vp, _i64, _i64, _vp, _vp, _vp]
     L.oracle_wrap_s32.restype = ctypes.c_int32
     L.oracle_wrap_s32.argtypes = [_i64]
+    L.oracle_f32_to_bf16.restype = ctypes.c_uint16
+    L.oracle_f32_to_bf16.argtypes = [ctypes.c_float]
+    L.oracle_f32_to_f16.restype = ctypes.c_uint16
+    L.oracle_f32_to_f16.argtypes = [ctypes.c_float]
+    L.oracle_dequant.argtypes = [_i64, _i64, _vp, _i64, _vp, _vp, ctypes.c_int, _vp, _i64]
     return L
 
 
@@ -204,6 +209,34 @@ def gemm_s4_at(A: np.ndarray, Bt: np.ndarray, K: int, ii, jj) -> np.ndarray:
     lib().oracle_gemm_s4_at(K, _ptr(A), 2 * A.shape[1], _ptr(Bt), 2 * Bt.shape[1],
                             ii.size, _ptr(ii), _ptr(jj), _ptr(C))
     return C
+
+
+OUT_F32, OUT_BF16, OUT_F16 = 0, 1, 2
+
+
+def dequant(acc: np.ndarray, scale_a=None, scale_b=None, out_type: int = OUT_F32) -> np.ndarray:
+    """Scaled integer GEMM epilogue applied to exact sums (int64, M x N).
+    Returns bit patterns: uint32 (binary32) for OUT_F32, uint16 otherwise."""
+    acc = np.ascontiguousarray(acc, dtype=np.int64)
+    M, N = acc.shape
+    sa = None if scale_a is None else np.ascontiguousarray(scale_a, dtype=np.float32)
+    sb = None if scale_b is None else np.ascontiguousarray(scale_b, dtype=np.float32)
+    out = np.empty((M, N), dtype=np.uint32 if out_type == OUT_F32 else np.uint16)
+    lib().oracle_dequant(M, N, _ptr(acc), N, None if sa is None else _ptr(sa),
+                         None if sb is None else _ptr(sb), out_type, _ptr(out), N)
+    return out
+
+
+def f32_to_bf16(x) -> np.ndarray:
+    L = lib()
+    x = np.asarray(x, dtype=np.float32)
+    return np.array([L.oracle_f32_to_bf16(float(v)) for v in x.reshape(-1)], dtype=np.uint16).reshape(x.shape)
+
+
+def f32_to_f16(x) -> np.ndarray:
+    L = lib()
+    x = np.asarray(x, dtype=np.float32)
+    return np.array([L.oracle_f32_to_f16(float(v)) for v in x.reshape(-1)], dtype=np.uint16).reshape(x.shape)
 
 
 def wrap_s32(C: np.ndarray) -> np.ndarray:

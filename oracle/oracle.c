@@ -253,6 +253,79 @@ void oracle_gemm_s4_at(int64_t K, const uint8_t *A, int64_t lda, const uint8_t *
         C[p] = dot_s4(K, A, lda, B, ldb, ii[p], jj[p]);
 }
 
+/* ---------------------------------------------------------------------------
+ * Scaled integer GEMM (dequantisation epilogue).  This is the form the INT8 /
+ * INT4 products take in quantised inference (paper section V), which the
+ * paper's own kernels leave out (section VI): per-row scales of A, per-column
+ * scales of B.  Definition, per element, in IEEE binary32 with
+ * round-to-nearest-even at every step and no fused multiply-add:
+ *     v = acc wrapped to int32;  t = (float)v;  t = t * sa[i];  t = t * sb[j]
+ * then rounded to nearest-even into the output type.
+ * ------------------------------------------------------------------------- */
+
+/* binary32 -> bfloat16 (the top 16 bits of binary32), round to nearest,
+ * ties to even; NaN stays NaN. */
+uint16_t oracle_f32_to_bf16(float x)
+{
+    uint32_t b;
+    memcpy(&b, &x, 4);
+    if ((b & 0x7f800000u) == 0x7f800000u && (b & 0x007fffffu))
+        return (uint16_t)((b >> 16) | 0x0040u);          /* quiet NaN */
+    uint32_t keep = b >> 16, rest = b & 0xffffu;
+    if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u)))
+        keep += 1;                                        /* may carry into the exponent: correct */
+    return (uint16_t)keep;
+}
+
+/* binary32 -> binary16, round to nearest, ties to even, from the binary16
+ * definition: normal values (1 + f/1024) 2^e for -14 <= e <= 15, subnormals
+ * f 2^-24, overflow to infinity. */
+uint16_t oracle_f32_to_f16(float x)
+{
+    double v = (double)x;
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    double a = fabs(v);
+    if (isnan(v)) return (uint16_t)(sign | 0x7e00u);
+    if (isinf(v)) return (uint16_t)(sign | 0x7c00u);
+    if (a < ldexp(1.0, -14)) {                            /* subnormal range, quantum 2^-24 */
+        double q = nearbyint(a * ldexp(1.0, 24));         /* ties to even (default mode) */
+        return (uint16_t)(sign | (uint16_t)q);            /* q == 1024 is the smallest normal */
+    }
+    int e;
+    frexp(a, &e);                                         /* a = m 2^e, 0.5 <= m < 1 */
+    e -= 1;                                               /* a = (1 + f) 2^e */
+    double q = nearbyint(ldexp(a, 10 - e));               /* 1024 <= q <= 2048 */
+    if (q >= 2048.0) { q = 1024.0; e += 1; }
+    if (e > 15) return (uint16_t)(sign | 0x7c00u);
+    return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)(q - 1024.0));
+}
+
+/* out_type 0: binary32 bit patterns (uint32); 1: bfloat16; 2: binary16
+ * (uint16).  acc holds exact sums (int64), M x N with pitch lda; sa / sb may
+ * be NULL (all ones). */
+void oracle_dequant(int64_t M, int64_t N, const int64_t *acc, int64_t lda, const float *sa,
+                    const float *sb, int out_type, void *out, int64_t ldo)
+{
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t j = 0; j < N; ++j) {
+            int32_t v = (int32_t)(uint32_t)(uint64_t)acc[i * lda + j];
+            volatile float t = (float)v;
+            t = t * (sa ? sa[i] : 1.0f);
+            t = t * (sb ? sb[j] : 1.0f);
+            if (out_type == 0) {
+                uint32_t b;
+                float tf = t;
+                memcpy(&b, &tf, 4);
+                ((uint32_t *)out)[i * ldo + j] = b;
+            } else if (out_type == 1) {
+                ((uint16_t *)out)[i * ldo + j] = oracle_f32_to_bf16(t);
+            } else {
+                ((uint16_t *)out)[i * ldo + j] = oracle_f32_to_f16(t);
+            }
+        }
+    }
+}
+
 /* Two's-complement wrap of an exact sum to 32 bits (reading adopted where the
  * paper is silent on INT32 overflow: .s32 accumulation without saturation). */
 int32_t oracle_wrap_s32(int64_t v)

@@ -7,13 +7,15 @@ Tensor-Core GEMM Kernels: A Multi-Precision Study on NVIDIA L4"
 Two layers, both argument marshalling only (every arithmetic step runs in the
 library's CUDA kernels):
 
-* ``gemm_f16``, ``gemm_s8``, ``gemm_s4``, ``gemm_s8_noalloc``, ``gemm_status_string``,
+* ``gemm_f16``, ``gemm_s8``, ``gemm_s4``, ``gemm_s8_scaled``, ``gemm_s4_scaled``,
+  ``gemm_s8_noalloc``, ``gemm_status_string``,
   ``gemm_poll_device_error``, ``ptc_kernel_launch_count``,
   ``ptc_debug_set_wait_limit``, ``ptc_set_tuning``: the C ABI of
   ``include/ptc.h`` under the same names, taking integers (sizes, leading
   dimensions, device addresses, a cudaStream_t handle).  A nonzero status
   raises :class:`PtcError`.
-* ``matmul_f16``, ``matmul_s8``, ``matmul_s4``: the same calls on torch
+* ``matmul_f16``, ``matmul_s8``, ``matmul_s4``, ``matmul_s8_scaled``,
+  ``matmul_s4_scaled``: the same calls on torch
   tensors.  Device tensors run on the current CUDA stream; CPU tensors are
   copied to the device and the result is copied back (end-to-end use).
 
@@ -37,6 +39,10 @@ PTC_ERR_DEVICE = 4
 PTC_ERR_LAUNCH = 5
 PTC_ERR_TIMEOUT = 6
 PTC_ERR_ALLOC = 7
+
+PTC_OUT_F32 = 0
+PTC_OUT_BF16 = 1
+PTC_OUT_F16 = 2
 
 _i64 = ctypes.c_int64
 _vp = ctypes.c_void_p
@@ -62,6 +68,10 @@ def lib() -> ctypes.CDLL:
             fn = getattr(L, name)
             fn.restype = ctypes.c_int
             fn.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]
+        for name in ("gemm_s8_scaled", "gemm_s4_scaled"):
+            fn = getattr(L, name)
+            fn.restype = ctypes.c_int
+            fn.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i64, ctypes.c_int, _vp]
         L.gemm_status_string.restype = ctypes.c_char_p
         L.gemm_status_string.argtypes = [ctypes.c_int]
         L.gemm_poll_device_error.restype = ctypes.c_int
@@ -100,6 +110,16 @@ def gemm_s8(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
 def gemm_s4(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
     """C[MxN] s32 = A[MxK] packed s4 . B[KxN] packed s4 (column-major); lda/ldb in nibbles."""
     return _check(lib().gemm_s4(M, N, K, A, lda, B, ldb, C, ldc, stream))
+
+
+def gemm_s8_scaled(M, N, K, A, lda, B, ldb, scale_a, scale_b, C, ldc, out_type, stream=0) -> int:
+    """C = out(rn(rn(float(sum_k A_ik B_kj) * scale_a[i]) * scale_b[j])), INT8 operands."""
+    return _check(lib().gemm_s8_scaled(M, N, K, A, lda, B, ldb, scale_a, scale_b, C, ldc, out_type, stream))
+
+
+def gemm_s4_scaled(M, N, K, A, lda, B, ldb, scale_a, scale_b, C, ldc, out_type, stream=0) -> int:
+    """As gemm_s8_scaled with packed INT4 operands (lda, ldb in nibbles)."""
+    return _check(lib().gemm_s4_scaled(M, N, K, A, lda, B, ldb, scale_a, scale_b, C, ldc, out_type, stream))
 
 
 def gemm_s8_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
@@ -204,3 +224,47 @@ def matmul_s4(A, Bt, K, out=None, stream=None):
         raise TypeError("matmul_s4 takes packed uint8 operands")
     M, N = A.shape[0], Bt.shape[0]
     return _run(gemm_s4, A, Bt, out, (M, N), torch.int32, M, N, int(K), 2, stream)
+
+
+def _out_type(dtype):
+    import torch
+    table = {torch.float32: PTC_OUT_F32, torch.bfloat16: PTC_OUT_BF16, torch.float16: PTC_OUT_F16}
+    if dtype not in table:
+        raise TypeError("scaled outputs are float32, bfloat16 or float16")
+    return table[dtype]
+
+
+def _scaled(fn, A, Bt, K, scale_a, scale_b, out_dtype, out, stream, lda_scale):
+    import torch
+    M, N = A.shape[0], Bt.shape[0]
+    if A.device.type == "cpu" or Bt.device.type == "cpu":
+        raise ValueError("scaled products take device tensors")
+    C = out if out is not None else torch.empty((M, N), dtype=out_dtype, device=A.device)
+    for v, n, name in ((scale_a, M, "scale_a"), (scale_b, N, "scale_b")):
+        if v is not None and (v.dtype != torch.float32 or v.numel() != n or not v.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous float32 vector of {n} elements")
+    fn(M, N, K, A.data_ptr(), _rowmajor(A, "A") * lda_scale, Bt.data_ptr(), _rowmajor(Bt, "B") * lda_scale,
+       None if scale_a is None else scale_a.data_ptr(), None if scale_b is None else scale_b.data_ptr(),
+       C.data_ptr(), _rowmajor(C, "C"), _out_type(C.dtype), _stream(stream))
+    return C
+
+
+def matmul_s8_scaled(A, Bt, scale_a=None, scale_b=None, out_dtype=None, out=None, stream=None):
+    """(A (M,K) int8 @ B, B column-major as Bt (N,K) int8) * scale_a[:,None] * scale_b[None,:]
+    -> float32 / bfloat16 / float16 (M,N), with the rounding order of gemm_s8_scaled."""
+    import torch
+    if A.dtype != torch.int8 or Bt.dtype != torch.int8:
+        raise TypeError("matmul_s8_scaled takes int8 operands")
+    if A.shape[1] != Bt.shape[1]:
+        raise ValueError("inner dimensions differ")
+    dt = out.dtype if out is not None else (out_dtype or torch.float32)
+    return _scaled(gemm_s8_scaled, A, Bt, A.shape[1], scale_a, scale_b, dt, out, stream, 1)
+
+
+def matmul_s4_scaled(A, Bt, K, scale_a=None, scale_b=None, out_dtype=None, out=None, stream=None):
+    """As matmul_s8_scaled with packed INT4 operands (two per byte, low nibble first)."""
+    import torch
+    if A.dtype != torch.uint8 or Bt.dtype != torch.uint8:
+        raise TypeError("matmul_s4_scaled takes packed uint8 operands")
+    dt = out.dtype if out is not None else (out_dtype or torch.float32)
+    return _scaled(gemm_s4_scaled, A, Bt, int(K), scale_a, scale_b, dt, out, stream, 2)

@@ -223,8 +223,8 @@ int launch_gemm_checked(Kind kind, bool b_mn, bool int_out, int ctas, const CUte
     return PTC_OK;
 }
 
-int zero_c(void *C, int64_t ldc, int64_t M, int64_t N, const DevInfo &d, cudaStream_t stream) {
-    cudaError_t e = ptc::launch_zero_fill(C, ldc, int(M), int(N), d.sms * 4, stream);
+int zero_c(void *C, int64_t ldc, int64_t M, int64_t N, int esize, const DevInfo &d, cudaStream_t stream) {
+    cudaError_t e = ptc::launch_zero_fill(C, ldc, int(M), int(N), esize, d.sms * 4, stream);
     if (e != cudaSuccess) return fail_cuda(e, "zero-fill launch");
     g_launches.fetch_add(1);
     return PTC_OK;
@@ -267,7 +267,7 @@ int gemm_f16(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const 
     DevInfo *d;
     if ((rc = current_device(&dev, &d))) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (K == 0) return zero_c(C, ldc, M, N, *d, s);
+    if (K == 0) return zero_c(C, ldc, M, N, 4, *d, s);
 
     const int ctas = choose_ctas(M, N, d->sms);
     CUtensorMap ta, tb;
@@ -279,93 +279,59 @@ int gemm_f16(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const 
     return launch_gemm_checked(Kind::F16, true, false, ctas, ta, tb, args, *d, s);
 }
 
-int gemm_s8(int64_t M, int64_t N, int64_t K, const int8_t *A, int64_t lda, const int8_t *B,
-            int64_t ldb, int32_t *C, int64_t ldc, void *stream) {
-    g_msg[0] = 0;
+}  // extern "C"
+
+namespace {
+
+// Bytes of one output element of an integer-route mode.
+int out_bytes(int mode) { return (mode == ptc::OUT_BF16 || mode == ptc::OUT_F16) ? 2 : 4; }
+
+// The integer routes: validation, operand conversion into a stream-ordered
+// workspace, then the tensor-core kernel whose epilogue folds the FP32 chunk
+// sums into int32 and writes int32 or scaled FP32 / BF16 / FP16.
+//   s4 == false: INT8, lda / ldb in bytes; s4 == true: packed INT4, in nibbles.
+int int_gemm(bool s4, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+             int64_t ldb, void *C, int64_t ldc, int mode, const float *sa, const float *sb,
+             void *stream) {
     int rc = check_sizes(M, N, K);
     if (rc) return rc;
     if (M == 0 || N == 0) return PTC_OK;
+    const int eb = out_bytes(mode);
     if (!C || ldc < N) return fail(PTC_ERR_INVALID, "C is NULL or ldc < N");
     if (K > 0 && (!A || !B)) return fail(PTC_ERR_INVALID, "A or B is NULL");
     if (K > 0 && (lda < K || ldb < K)) return fail(PTC_ERR_INVALID, "lda < K or ldb < K");
-    if (!aligned16(C) || ldc % 4) return fail(PTC_ERR_ALIGN, "C must be 16-byte aligned, ldc % 4 == 0");
-    if (K > 0 && (!aligned16(A) || !aligned16(B) || lda % 16 || ldb % 16))
-        return fail(PTC_ERR_ALIGN, "A, B must be 16-byte aligned, lda % 16 == 0, ldb % 16 == 0");
-    const uint64_t cbytes = span_bytes(M, N, ldc, 4, 1);
-    if (K > 0 && (overlaps(C, cbytes, A, span_bytes(M, K, lda, 1, 1)) ||
-                  overlaps(C, cbytes, B, span_bytes(N, K, ldb, 1, 1))))
+    if (s4 && K > 0 && ((lda & 1) || (ldb & 1)))
+        return fail(PTC_ERR_INVALID, "lda, ldb must be even (counted in nibbles)");
+    if (!aligned16(C) || (ldc * eb) % 16)
+        return fail(PTC_ERR_ALIGN, "C must be 16-byte aligned with a row pitch that is a multiple of 16 bytes");
+    const int pitch_mult = s4 ? 32 : 16;
+    if (K > 0 && (!aligned16(A) || !aligned16(B) || lda % pitch_mult || ldb % pitch_mult))
+        return fail(PTC_ERR_ALIGN, s4 ? "A, B must be 16-byte aligned, lda % 32 == 0, ldb % 32 == 0"
+                                      : "A, B must be 16-byte aligned, lda % 16 == 0, ldb % 16 == 0");
+    if ((sa && (reinterpret_cast<uintptr_t>(sa) & 3u)) || (sb && (reinterpret_cast<uintptr_t>(sb) & 3u)))
+        return fail(PTC_ERR_ALIGN, "scale vectors must be 4-byte aligned");
+    const uint64_t cbytes = span_bytes(M, N, ldc, eb, 1);
+    const int den = s4 ? 2 : 1;
+    if (K > 0 && (overlaps(C, cbytes, A, span_bytes(M, K, lda, 1, den)) ||
+                  overlaps(C, cbytes, B, span_bytes(N, K, ldb, 1, den))))
         return fail(PTC_ERR_OVERLAP, "C overlaps A or B");
+    if ((sa && overlaps(C, cbytes, sa, uint64_t(M) * 4)) || (sb && overlaps(C, cbytes, sb, uint64_t(N) * 4)))
+        return fail(PTC_ERR_OVERLAP, "C overlaps a scale vector");
 
     int dev;
     DevInfo *d;
     if ((rc = current_device(&dev, &d))) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (K == 0) return zero_c(C, ldc, M, N, *d, s);
+    if (K == 0) return zero_c(C, ldc, M, N, eb, *d, s);
     if (!d->pool_ok) return fail(PTC_ERR_ALLOC, "workspace memory pool unavailable");
 
-    // Workspace: A and B as binary16 rows of K, pitch rounded to 128 bytes.
-    const int64_t ldw = round_up(K, 64);
-    const int64_t a_bytes = round_up(M * ldw * 2, 1024);
-    const int64_t b_bytes = round_up(N * ldw * 2, 1024);
-    void *ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, size_t(a_bytes + b_bytes), d->pool, s);
-    if (e != cudaSuccess) {
-        cudaGetLastError();
-        return fail(PTC_ERR_ALLOC, "workspace allocation failed");
-    }
-    uint16_t *aw = static_cast<uint16_t *>(ws);
-    uint16_t *bw = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + a_bytes);
-    const int cgrid = d->sms * 8;
-    rc = PTC_OK;
-    if ((e = ptc::launch_s8_to_f16_pair(A, lda, int(M), B, ldb, int(N), int(K), aw, bw, ldw, cgrid, s)) !=
-        cudaSuccess)
-        rc = fail_cuda(e, "s8 conversion launch");
-    else
-        g_launches.fetch_add(1);
-    const int ctas = choose_ctas(M, N, d->sms);
-    CUtensorMap ta, tb;
-    if (!rc) rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, aw, K, M, uint64_t(ldw) * 2, 64, ptc::kBM);
-    if (!rc)
-        rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bw, K, N, uint64_t(ldw) * 2, 64, ptc::kBN / ctas);
-    if (!rc) {
-        GemmArgs args = base_args(M, N, K, 64, C, ldc, ctas);
-        const int ch = g_chunk_s8.load();
-        args.kb_per_chunk = ch > 0 ? ch : 1;
-        rc = launch_gemm_checked(Kind::F16, false, true, ctas, ta, tb, args, *d, s);
-    }
-    cudaFreeAsync(ws, s);
-    return rc;
-}
-
-int gemm_s4(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
-            int64_t ldb, int32_t *C, int64_t ldc, void *stream) {
-    g_msg[0] = 0;
-    int rc = check_sizes(M, N, K);
-    if (rc) return rc;
-    if (M == 0 || N == 0) return PTC_OK;
-    if (!C || ldc < N) return fail(PTC_ERR_INVALID, "C is NULL or ldc < N");
-    if (K > 0 && (!A || !B)) return fail(PTC_ERR_INVALID, "A or B is NULL");
-    if (K > 0 && (lda < K || ldb < K || (lda & 1) || (ldb & 1)))
-        return fail(PTC_ERR_INVALID, "lda, ldb must be even and >= K (counted in nibbles)");
-    if (!aligned16(C) || ldc % 4) return fail(PTC_ERR_ALIGN, "C must be 16-byte aligned, ldc % 4 == 0");
-    if (K > 0 && (!aligned16(A) || !aligned16(B) || lda % 32 || ldb % 32))
-        return fail(PTC_ERR_ALIGN, "A, B must be 16-byte aligned, lda % 32 == 0, ldb % 32 == 0");
-    const uint64_t cbytes = span_bytes(M, N, ldc, 4, 1);
-    if (K > 0 && (overlaps(C, cbytes, A, span_bytes(M, K, lda, 1, 2)) ||
-                  overlaps(C, cbytes, B, span_bytes(N, K, ldb, 1, 2))))
-        return fail(PTC_ERR_OVERLAP, "C overlaps A or B");
-
-    int dev;
-    DevInfo *d;
-    if ((rc = current_device(&dev, &d))) return rc;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (K == 0) return zero_c(C, ldc, M, N, *d, s);
-    if (!d->pool_ok) return fail(PTC_ERR_ALLOC, "workspace memory pool unavailable");
-
-    // Workspace: A and B as E4M3 rows of K, pitch rounded to 128 bytes.
-    const int64_t ldw = round_up(K, 128);
-    const int64_t a_bytes = round_up(M * ldw, 1024);
-    const int64_t b_bytes = round_up(N * ldw, 1024);
+    // Workspace: A and B as rows of K in the MMA input type (binary16 for
+    // INT8, E4M3 for INT4), pitch rounded to 128 bytes, blocks 1024-aligned.
+    const int k_elems = s4 ? 128 : 64;  // elements per 128-byte K block
+    const int wsize = s4 ? 1 : 2;       // workspace bytes per element
+    const int64_t ldw = round_up(K, k_elems);
+    const int64_t a_bytes = round_up(M * ldw * wsize, 1024);
+    const int64_t b_bytes = round_up(N * ldw * wsize, 1024);
     void *ws = nullptr;
     cudaError_t e = cudaMallocFromPoolAsync(&ws, size_t(a_bytes + b_bytes), d->pool, s);
     if (e != cudaSuccess) {
@@ -376,24 +342,78 @@ int gemm_s4(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const v
     uint8_t *bw = aw + a_bytes;
     const int cgrid = d->sms * 8;
     rc = PTC_OK;
-    if ((e = ptc::launch_s4_to_e4m3_pair(static_cast<const uint8_t *>(A), lda / 2, int(M),
-                                         static_cast<const uint8_t *>(B), ldb / 2, int(N), int(K), aw, bw,
-                                         ldw, cgrid, s)) != cudaSuccess)
-        rc = fail_cuda(e, "s4 conversion launch");
+    if (s4)
+        e = ptc::launch_s4_to_e4m3_pair(static_cast<const uint8_t *>(A), lda / 2, int(M),
+                                        static_cast<const uint8_t *>(B), ldb / 2, int(N), int(K), aw, bw,
+                                        ldw, cgrid, s);
+    else
+        e = ptc::launch_s8_to_f16_pair(static_cast<const int8_t *>(A), lda, int(M),
+                                       static_cast<const int8_t *>(B), ldb, int(N), int(K),
+                                       reinterpret_cast<uint16_t *>(aw), reinterpret_cast<uint16_t *>(bw),
+                                       ldw, cgrid, s);
+    if (e != cudaSuccess)
+        rc = fail_cuda(e, "operand conversion launch");
     else
         g_launches.fetch_add(1);
     const int ctas = choose_ctas(M, N, d->sms);
+    const CUtensorMapDataType dt = s4 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap ta, tb;
-    if (!rc) rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, aw, K, M, uint64_t(ldw), 128, ptc::kBM);
-    if (!rc) rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, bw, K, N, uint64_t(ldw), 128, ptc::kBN / ctas);
+    if (!rc) rc = make_tmap(&ta, dt, aw, K, M, uint64_t(ldw) * wsize, k_elems, ptc::kBM);
+    if (!rc) rc = make_tmap(&tb, dt, bw, K, N, uint64_t(ldw) * wsize, k_elems, ptc::kBN / ctas);
     if (!rc) {
-        GemmArgs args = base_args(M, N, K, 128, C, ldc, ctas);
-        const int ch = g_chunk_s4.load();
+        GemmArgs args = base_args(M, N, K, k_elems, C, ldc, ctas);
+        const int ch = s4 ? g_chunk_s4.load() : g_chunk_s8.load();
         args.kb_per_chunk = ch > 0 ? ch : 1;
-        rc = launch_gemm_checked(Kind::E4M3, false, true, ctas, ta, tb, args, *d, s);
+        args.out_mode = mode;
+        args.scale_a = sa;
+        args.scale_b = sb;
+        rc = launch_gemm_checked(s4 ? Kind::E4M3 : Kind::F16, false, true, ctas, ta, tb, args, *d, s);
     }
     cudaFreeAsync(ws, s);
     return rc;
+}
+
+int scaled_mode(int out_type) {
+    switch (out_type) {
+        case PTC_OUT_F32: return ptc::OUT_F32;
+        case PTC_OUT_BF16: return ptc::OUT_BF16;
+        case PTC_OUT_F16: return ptc::OUT_F16;
+        default: return -1;
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_s8(int64_t M, int64_t N, int64_t K, const int8_t *A, int64_t lda, const int8_t *B,
+            int64_t ldb, int32_t *C, int64_t ldc, void *stream) {
+    g_msg[0] = 0;
+    return int_gemm(false, M, N, K, A, lda, B, ldb, C, ldc, ptc::OUT_S32, nullptr, nullptr, stream);
+}
+
+int gemm_s4(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+            int64_t ldb, int32_t *C, int64_t ldc, void *stream) {
+    g_msg[0] = 0;
+    return int_gemm(true, M, N, K, A, lda, B, ldb, C, ldc, ptc::OUT_S32, nullptr, nullptr, stream);
+}
+
+int gemm_s8_scaled(int64_t M, int64_t N, int64_t K, const int8_t *A, int64_t lda, const int8_t *B,
+                   int64_t ldb, const float *scale_a, const float *scale_b, void *C, int64_t ldc,
+                   int out_type, void *stream) {
+    g_msg[0] = 0;
+    const int mode = scaled_mode(out_type);
+    if (mode < 0) return fail(PTC_ERR_INVALID, "out_type must be PTC_OUT_F32, PTC_OUT_BF16 or PTC_OUT_F16");
+    return int_gemm(false, M, N, K, A, lda, B, ldb, C, ldc, mode, scale_a, scale_b, stream);
+}
+
+int gemm_s4_scaled(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                   int64_t ldb, const float *scale_a, const float *scale_b, void *C, int64_t ldc,
+                   int out_type, void *stream) {
+    g_msg[0] = 0;
+    const int mode = scaled_mode(out_type);
+    if (mode < 0) return fail(PTC_ERR_INVALID, "out_type must be PTC_OUT_F32, PTC_OUT_BF16 or PTC_OUT_F16");
+    return int_gemm(true, M, N, K, A, lda, B, ldb, C, ldc, mode, scale_a, scale_b, stream);
 }
 
 const char *gemm_status_string(int status) {

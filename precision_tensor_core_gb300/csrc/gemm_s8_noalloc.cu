@@ -154,7 +154,7 @@ extern "C" int gemm_s8_noalloc(int64_t M, int64_t N, int64_t K, const int8_t *A,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
     if (K == 0) {
-        if ((e = ptc::launch_zero_fill(C, ldc, int(M), int(N), d->sms * 4, s)) != cudaSuccess) {
+        if ((e = ptc::launch_zero_fill(C, ldc, int(M), int(N), 4, d->sms * 4, s)) != cudaSuccess) {
             cudaGetLastError();
             return reject(PTC_ERR_LAUNCH, cudaGetErrorString(e));
         }
@@ -195,6 +195,9 @@ extern "C" int gemm_s8_noalloc(int64_t M, int64_t N, int64_t K, const int8_t *A,
     args.stall_tile = -1;
     args.l2_hint = 0;
     args.prefetch_kb = 0;
+    args.out_mode = ptc::OUT_S32;
+    args.scale_a = nullptr;
+    args.scale_b = nullptr;
     args.wait_limit_ns = kWaitNs;
     if ((e = ptc::launch_gemm(ptc::Kind::F16, false, true, 1, ta, tb, args, d->sms, s)) != cudaSuccess) {
         cudaGetLastError();

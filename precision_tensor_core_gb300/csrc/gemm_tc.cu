@@ -39,6 +39,8 @@
 // bounded by a %globaltimer limit: on expiry the CTA raises an abort flag,
 // records PTC_ERR_TIMEOUT in a device error word, lets its in-flight copies
 // and MMAs land, frees tensor memory and exits.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -125,6 +127,58 @@ __device__ __forceinline__ void store_32(T *dst, const uint32_t (&v)[32], int va
 #pragma unroll
         for (int j = 0; j < 32; ++j)
             if (j < valid) d[j] = v[j];
+    }
+}
+
+// Scaled integer epilogue (dequantisation): for the 128 columns col0 .. of
+// `row`, value = rn(rn(rn(float(acc)) * sa) * sb) in FP32, in that order and
+// without contraction, then rounded to nearest-even in the output type.
+// Columns at or beyond N are not written.
+__device__ __forceinline__ void store_scaled_row(const GemmArgs &args, int row, int col0,
+                                                 const int32_t (&acc)[kBN / 2]) {
+    const float sa = args.scale_a ? __ldg(args.scale_a + row) : 1.0f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const int cc = col0 + 32 * c;
+        if (cc >= args.N) break;
+        const int valid = min(32, args.N - cc);
+        float f[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float sb = (args.scale_b && j < valid) ? __ldg(args.scale_b + cc + j) : 1.0f;
+            f[j] = __fmul_rn(__fmul_rn(__int2float_rn(acc[32 * c + j]), sa), sb);
+        }
+        if (args.out_mode == OUT_F32) {
+            uint32_t v[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(f[j]);
+            store_32(reinterpret_cast<float *>(args.C) + int64_t(row) * args.ldc + cc, v, valid);
+        } else {
+            // 16-bit outputs: pairs packed into 32-bit words, 64 bytes per 32 columns.
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                uint32_t lo, hi;
+                if (args.out_mode == OUT_BF16) {
+                    lo = __bfloat16_as_ushort(__float2bfloat16_rn(f[2 * j]));
+                    hi = __bfloat16_as_ushort(__float2bfloat16_rn(f[2 * j + 1]));
+                } else {
+                    lo = __half_as_ushort(__float2half_rn(f[2 * j]));
+                    hi = __half_as_ushort(__float2half_rn(f[2 * j + 1]));
+                }
+                w[j] = lo | (hi << 16);
+            }
+            uint16_t *dst = reinterpret_cast<uint16_t *>(args.C) + int64_t(row) * args.ldc + cc;
+            if (valid == 32) {
+                uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (j < valid) dst[j] = static_cast<uint16_t>(w[j >> 1] >> ((j & 1) * 16));
+            }
+        }
     }
 }
 
@@ -412,14 +466,18 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
                 if (!ok) break;
                 if (row < args.M) {
-                    int32_t *crow = reinterpret_cast<int32_t *>(args.C) + int64_t(row) * args.ldc;
+                    if (args.out_mode == OUT_S32) {
+                        int32_t *crow = reinterpret_cast<int32_t *>(args.C) + int64_t(row) * args.ldc;
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t v[32];
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t v[32];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = static_cast<uint32_t>(acc[32 * c + j]);
-                        const int cc = col0 + 32 * c;
-                        if (cc < args.N) store_32(crow + cc, v, args.N - cc);
+                            for (int j = 0; j < 32; ++j) v[j] = static_cast<uint32_t>(acc[32 * c + j]);
+                            const int cc = col0 + 32 * c;
+                            if (cc < args.N) store_32(crow + cc, v, args.N - cc);
+                        }
+                    } else {
+                        store_scaled_row(args, row, col0, acc);
                     }
                 }
             } else {
@@ -462,12 +520,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (warp == 1) tmem_dealloc<CTAS>(tmem_base, TMEM_COLS);
 }
 
-__global__ void zero_fill_kernel(uint32_t *C, int64_t ldc, int M, int N) {
+template <typename T>
+__global__ void zero_fill_kernel(T *C, int64_t ldc, int M, int N) {
     const int64_t total = int64_t(M) * N;
     for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
          i += int64_t(gridDim.x) * blockDim.x) {
         const int64_t r = i / N, c = i - r * N;
-        C[r * ldc + c] = 0u;
+        C[r * ldc + c] = T(0);
     }
 }
 
@@ -539,8 +598,11 @@ cudaError_t launch_gemm(Kind kind, bool b_mn_major, bool int_out, int ctas, cons
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_zero_fill(void *C, int64_t ldc, int M, int N, int grid, cudaStream_t stream) {
-    zero_fill_kernel<<<grid, 256, 0, stream>>>(static_cast<uint32_t *>(C), ldc, M, N);
+cudaError_t launch_zero_fill(void *C, int64_t ldc, int M, int N, int esize, int grid, cudaStream_t stream) {
+    if (esize == 2)
+        zero_fill_kernel<uint16_t><<<grid, 256, 0, stream>>>(static_cast<uint16_t *>(C), ldc, M, N);
+    else
+        zero_fill_kernel<uint32_t><<<grid, 256, 0, stream>>>(static_cast<uint32_t *>(C), ldc, M, N);
     return cudaGetLastError();
 }
 

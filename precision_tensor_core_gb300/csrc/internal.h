@@ -33,7 +33,15 @@ struct GemmArgs {
     int l2_hint;           // L2 policy of operand loads: 0 none, 1 A evict-last and
                            // B evict-first, 2 A evict-last, 3 both evict-normal
     uint64_t wait_limit_ns;
+    // Integer routes only: output of the epilogue.
+    int out_mode;          // OUT_S32, or OUT_F32 / OUT_BF16 / OUT_F16 (scaled)
+    const float *scale_a;  // M row scales (scaled modes; NULL: 1)
+    const float *scale_b;  // N column scales (scaled modes; NULL: 1)
 };
+
+// Epilogue outputs of the integer routes.  The scaled modes write
+// rn(rn(rn(float(acc)) * scale_a[i]) * scale_b[j]) rounded to the output type.
+enum OutMode : int { OUT_S32 = 0, OUT_F32 = 1, OUT_BF16 = 2, OUT_F16 = 3 };
 
 // Dynamic shared memory the GEMM kernel needs (ctas = 1: one CTA per
 // 128 x 256 tile; ctas = 2: a CTA pair per 256 x 256 tile).
@@ -49,8 +57,8 @@ cudaError_t launch_gemm(Kind kind, bool b_mn_major, bool int_out, int ctas, cons
                         const CUtensorMap &tb, const GemmArgs &args, int sms,
                         cudaStream_t stream);
 
-// C[M x N] (4-byte elements) = 0.
-cudaError_t launch_zero_fill(void *C, int64_t ldc, int M, int N, int grid, cudaStream_t stream);
+// C[M x N] = 0 for elements of esize (2 or 4) bytes, ldc in elements.
+cudaError_t launch_zero_fill(void *C, int64_t ldc, int M, int N, int esize, int grid, cudaStream_t stream);
 
 // Reads and clears the device error word of the current device.
 cudaError_t read_and_clear_error_word(uint32_t *out);

@@ -5,7 +5,9 @@ Each mutant (all of them stay in bounds) is a textual edit of oracle.c compiled 
 the pin tests of test_oracle_pins.py then run against it and at least one must
 fail.  This shows the pins are sensitive to the plausible mistakes: a dropped
 term, a wrong sign, a wrong index, a transposed operand, a swapped nibble order
-and a wrong binary16 exponent or subnormal scale.
+a wrong binary16 exponent or subnormal scale, and, in the scaled epilogue,
+truncating or ties-away 16-bit rounding, a missing overflow, swapped scale
+order and a missing 32-bit wrap.
 """
 import os
 import subprocess
@@ -14,6 +16,7 @@ import sys
 import pytest
 
 import oracle
+from tests import test_oracle_dequant as dq
 from tests import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
@@ -43,6 +46,16 @@ MUTANTS = [
     ("s4_row_off_by_one", "const uint8_t *arow = A + i * (lda / 2);",
      "const uint8_t *arow = A + (i > 0 ? i - 1 : 0) * (lda / 2);"),
     ("rows_skipped_by_threads", "jobs[t].r0 = t * per;", "jobs[t].r0 = t * per + (t > 0);"),
+    ("bf16_truncates", "if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u)))", "if (0)"),
+    ("bf16_ties_away", "if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u)))",
+     "if (rest >= 0x8000u)"),
+    ("f16_subnormal_quantum", "double q = nearbyint(a * ldexp(1.0, 24));",
+     "double q = nearbyint(a * ldexp(1.0, 23));"),
+    ("f16_no_overflow", "if (e > 15) return (uint16_t)(sign | 0x7c00u);", "if (e > 16) return (uint16_t)(sign | 0x7c00u);"),
+    ("dequant_scales_swapped", "t = t * (sa ? sa[i] : 1.0f);\n            t = t * (sb ? sb[j] : 1.0f);",
+     "t = t * (sb ? sb[j] : 1.0f);\n            t = t * (sa ? sa[i] : 1.0f);"),
+    ("dequant_no_wrap", "int32_t v = (int32_t)(uint32_t)(uint64_t)acc[i * lda + j];",
+     "int64_t v = acc[i * lda + j];"),
 ]
 
 PIN_CALLS = [
@@ -59,6 +72,11 @@ PIN_CALLS = [
     lambda g: pins.test_s4_nibble_order_and_roundtrip(),
     lambda g: pins.test_brute_force_int(7, 9, 11),
     lambda g: pins.test_brute_force_f16_fraction(7, 9, 11),
+    lambda g: dq.test_bf16_rounding_against_torch(),
+    lambda g: dq.test_f16_rounding_against_numpy(),
+    lambda g: dq.test_dequant_matches_exact_stepwise_rounding(),
+    lambda g: dq.test_dequant_order_matters_and_is_a_then_b(),
+    lambda g: dq.test_dequant_identity_scales(),
 ]
 
 
@@ -94,7 +112,7 @@ def test_pins_catch_planted_mistake(name, old, new, oracle_src, tmp_path, golden
     src.write_text(oracle_src.replace(old, new))
     so = tmp_path / f"liboracle_{name}.so"
     subprocess.check_call(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-pthread",
-                           str(src), "-o", str(so), "-lm"])
+                           "-ffp-contract=off", str(src), "-o", str(so), "-lm"])
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     code = CHILD.format(root=root, so=str(so), golden=str(golden_dir))
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
