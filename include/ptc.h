@@ -87,6 +87,22 @@ int gemm_f16(int64_t M, int64_t N, int64_t K,
              void *stream);
 
 /*
+ * FP16 GEMM with FP16 accumulators: C[M x N] (binary16) = A . B, the tensor
+ * cores accumulating in binary16 (the paper's fp16_ptx_fp16acc variant,
+ * section IV-A and Table VI: f16 accumulators instead of f32).  A and B as
+ * gemm_f16; C row-major binary16 with ldc >= N and ldc % 8 == 0.  Each output
+ * is the binary16 running sum of the products, so its error grows with K:
+ * the bound the tests use is |C - sum| <= (ceil(K/16) + 1) * 2^-10 *
+ * sum_k |A_ik B_kj| + ceil(K/16) * 2^-24.  Values beyond the binary16 range
+ * become infinities.
+ */
+int gemm_f16_f16acc(int64_t M, int64_t N, int64_t K,
+                    const void *A, int64_t lda,
+                    const void *B, int64_t ldb,
+                    void *C, int64_t ldc,
+                    void *stream);
+
+/*
  * INT8 GEMM: C[M x N] (int32) = A[M x K] (int8) . B[K x N] (int8), exact.
  *   A  row-major,    element (i,k) at A[i*lda + k]; lda >= K, lda % 16 == 0
  *   B  column-major, element (k,j) at B[j*ldb + k]; ldb >= K, ldb % 16 == 0

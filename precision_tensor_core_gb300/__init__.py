@@ -7,14 +7,14 @@ Tensor-Core GEMM Kernels: A Multi-Precision Study on NVIDIA L4"
 Two layers, both argument marshalling only (every arithmetic step runs in the
 library's CUDA kernels):
 
-* ``gemm_f16``, ``gemm_s8``, ``gemm_s4``, ``gemm_s8_scaled``, ``gemm_s4_scaled``,
+* ``gemm_f16``, ``gemm_f16_f16acc``, ``gemm_s8``, ``gemm_s4``, ``gemm_s8_scaled``, ``gemm_s4_scaled``,
   ``gemm_s8_noalloc``, ``gemm_status_string``,
   ``gemm_poll_device_error``, ``ptc_kernel_launch_count``,
   ``ptc_debug_set_wait_limit``, ``ptc_set_tuning``: the C ABI of
   ``include/ptc.h`` under the same names, taking integers (sizes, leading
   dimensions, device addresses, a cudaStream_t handle).  A nonzero status
   raises :class:`PtcError`.
-* ``matmul_f16``, ``matmul_s8``, ``matmul_s4``, ``matmul_s8_scaled``,
+* ``matmul_f16``, ``matmul_f16_f16acc``, ``matmul_s8``, ``matmul_s4``, ``matmul_s8_scaled``,
   ``matmul_s4_scaled``: the same calls on torch
   tensors.  Device tensors run on the current CUDA stream; CPU tensors are
   copied to the device and the result is copied back (end-to-end use).
@@ -64,7 +64,7 @@ def lib() -> ctypes.CDLL:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"libptc.so is not built ({LIB_PATH}); run __graft_entry__.build()")
         L = ctypes.CDLL(LIB_PATH)
-        for name in ("gemm_f16", "gemm_s8", "gemm_s4", "gemm_s8_noalloc"):
+        for name in ("gemm_f16", "gemm_f16_f16acc", "gemm_s8", "gemm_s4", "gemm_s8_noalloc"):
             fn = getattr(L, name)
             fn.restype = ctypes.c_int
             fn.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]
@@ -100,6 +100,11 @@ def gemm_status_string(status: int) -> str:
 def gemm_f16(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
     """C[MxN] f32 = A[MxK] f16 (row-major) . B[KxN] f16 (row-major); device addresses."""
     return _check(lib().gemm_f16(M, N, K, A, lda, B, ldb, C, ldc, stream))
+
+
+def gemm_f16_f16acc(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    """C[MxN] f16 = A[MxK] f16 . B[KxN] f16 with FP16 accumulators; device addresses."""
+    return _check(lib().gemm_f16_f16acc(M, N, K, A, lda, B, ldb, C, ldc, stream))
 
 
 def gemm_s8(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
@@ -202,6 +207,18 @@ def matmul_f16(A, B, out=None, stream=None):
     if K != K2:
         raise ValueError("inner dimensions differ")
     return _run(gemm_f16, A, B, out, (M, N), torch.float32, M, N, K, 1, stream)
+
+
+def matmul_f16_f16acc(A, B, out=None, stream=None):
+    """FP16 A (M,K) @ B (K,N) -> float16 (M,N), accumulated in FP16 on the tensor cores."""
+    import torch
+    if A.dtype != torch.float16 or B.dtype != torch.float16:
+        raise TypeError("matmul_f16_f16acc takes float16 operands")
+    M, K = A.shape
+    K2, N = B.shape
+    if K != K2:
+        raise ValueError("inner dimensions differ")
+    return _run(gemm_f16_f16acc, A, B, out, (M, N), torch.float16, M, N, K, 1, stream)
 
 
 def matmul_s8(A, Bt, out=None, stream=None):

@@ -214,10 +214,10 @@ GemmArgs base_args(int64_t M, int64_t N, int64_t K, int k_elems_per_block, void 
     return a;
 }
 
-int launch_gemm_checked(Kind kind, bool b_mn, bool int_out, int ctas, const CUtensorMap &ta,
+int launch_gemm_checked(Kind kind, bool b_mn, int epi, int ctas, const CUtensorMap &ta,
                         const CUtensorMap &tb, const GemmArgs &args, const DevInfo &d,
                         cudaStream_t stream) {
-    cudaError_t e = ptc::launch_gemm(kind, b_mn, int_out, ctas, ta, tb, args, d.sms, stream);
+    cudaError_t e = ptc::launch_gemm(kind, b_mn, epi, ctas, ta, tb, args, d.sms, stream);
     if (e != cudaSuccess) return fail_cuda(e, "GEMM kernel launch");
     g_launches.fetch_add(1);
     return PTC_OK;
@@ -244,21 +244,24 @@ int encode_tmap_2d(CUtensorMap *map, bool one_byte, const void *base, uint64_t i
 }
 }  // namespace ptc
 
-extern "C" {
+namespace {
 
-int gemm_f16(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
-             int64_t ldb, float *C, int64_t ldc, void *stream) {
-    g_msg[0] = 0;
+// FP16 operands: validation, tensor maps, one kernel launch.  epi is
+// EPI_F32 (FP32 accumulators, FP32 C) or EPI_F16ACC (FP16 accumulators, FP16 C).
+int f16_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
+             void *C, int64_t ldc, int epi, void *stream) {
     int rc = check_sizes(M, N, K);
     if (rc) return rc;
     if (M == 0 || N == 0) return PTC_OK;
+    const int eb = epi == ptc::EPI_F16ACC ? 2 : 4;
     if (!C || ldc < N) return fail(PTC_ERR_INVALID, "C is NULL or ldc < N");
     if (K > 0 && (!A || !B)) return fail(PTC_ERR_INVALID, "A or B is NULL");
     if (K > 0 && (lda < K || ldb < N)) return fail(PTC_ERR_INVALID, "lda < K or ldb < N");
-    if (!aligned16(C) || ldc % 4) return fail(PTC_ERR_ALIGN, "C must be 16-byte aligned, ldc % 4 == 0");
+    if (!aligned16(C) || (ldc * eb) % 16)
+        return fail(PTC_ERR_ALIGN, "C must be 16-byte aligned with a row pitch that is a multiple of 16 bytes");
     if (K > 0 && (!aligned16(A) || !aligned16(B) || lda % 8 || ldb % 8))
         return fail(PTC_ERR_ALIGN, "A, B must be 16-byte aligned, lda % 8 == 0, ldb % 8 == 0");
-    const uint64_t cbytes = span_bytes(M, N, ldc, 4, 1);
+    const uint64_t cbytes = span_bytes(M, N, ldc, eb, 1);
     if (K > 0 && (overlaps(C, cbytes, A, span_bytes(M, K, lda, 2, 1)) ||
                   overlaps(C, cbytes, B, span_bytes(K, N, ldb, 2, 1))))
         return fail(PTC_ERR_OVERLAP, "C overlaps A or B");
@@ -267,7 +270,7 @@ int gemm_f16(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const 
     DevInfo *d;
     if ((rc = current_device(&dev, &d))) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (K == 0) return zero_c(C, ldc, M, N, 4, *d, s);
+    if (K == 0) return zero_c(C, ldc, M, N, eb, *d, s);
 
     const int ctas = choose_ctas(M, N, d->sms);
     CUtensorMap ta, tb;
@@ -276,7 +279,23 @@ int gemm_f16(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const 
     if ((rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, N, K, uint64_t(ldb) * 2, 64, 64)))
         return rc;
     GemmArgs args = base_args(M, N, K, 64, C, ldc, ctas);
-    return launch_gemm_checked(Kind::F16, true, false, ctas, ta, tb, args, *d, s);
+    return launch_gemm_checked(Kind::F16, true, epi, ctas, ta, tb, args, *d, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+int gemm_f16(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+             int64_t ldb, float *C, int64_t ldc, void *stream) {
+    g_msg[0] = 0;
+    return f16_gemm(M, N, K, A, lda, B, ldb, C, ldc, ptc::EPI_F32, stream);
+}
+
+int gemm_f16_f16acc(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                    int64_t ldb, void *C, int64_t ldc, void *stream) {
+    g_msg[0] = 0;
+    return f16_gemm(M, N, K, A, lda, B, ldb, C, ldc, ptc::EPI_F16ACC, stream);
 }
 
 }  // extern "C"
@@ -367,7 +386,7 @@ int int_gemm(bool s4, int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
         args.out_mode = mode;
         args.scale_a = sa;
         args.scale_b = sb;
-        rc = launch_gemm_checked(s4 ? Kind::E4M3 : Kind::F16, false, true, ctas, ta, tb, args, *d, s);
+        rc = launch_gemm_checked(s4 ? Kind::E4M3 : Kind::F16, false, ptc::EPI_INT, ctas, ta, tb, args, *d, s);
     }
     cudaFreeAsync(ws, s);
     return rc;

@@ -187,11 +187,12 @@ __device__ __forceinline__ void store_scaled_row(const GemmArgs &args, int row, 
 // its full barriers collect both CTAs' copies, its commits arrive on both
 // CTAs' empty / accumulator-full barriers, and both CTAs' epilogues release
 // accumulator buffers on its acc_empty barriers.
-template <Kind KIND, bool B_MN, bool INT_OUT, int CTAS>
+template <Kind KIND, bool B_MN, int EPI, int CTAS>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmArgs args) {
     static_assert(!(B_MN && KIND == Kind::E4M3), "MN-major B is used by the FP16 path only");
+    constexpr bool INT_OUT = EPI == EPI_INT;
     using C_ = Cfg<CTAS>;
     constexpr int STAGES = C_::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -350,7 +351,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------ MMA issuer
         if (lane == 0 && rank == 0) {
             constexpr uint32_t IDESC =
-                instr_desc(0u, 0u, B_MN, kBM * CTAS, kBN);  // F16 x F16 or E4M3 x E4M3 -> F32
+                instr_desc(EPI == EPI_F16ACC ? 0u : 1u, 0u, 0u, B_MN, kBM * CTAS,
+                           kBN);  // F16 x F16 or E4M3 x E4M3 -> F32 (or F16 accumulators)
             const uint32_t a_base = smem_u32(a_ring);
             const uint32_t b_base = smem_u32(b_ring);
             int s = 0;
@@ -493,7 +495,28 @@ __global__ void __launch_bounds__(THREADS, 1)
                     tmem_ld_32cols(t_lane + uint32_t(abuf * kBN + 32 * c), r);
                     tmem_ld_wait();
                     const int cc = col0 + 32 * c;
-                    if (row < args.M && cc < args.N) store_32(crow + cc, r, args.N - cc);
+                    if constexpr (EPI == EPI_F16ACC) {
+                        // An FP16 accumulator occupies the low half of its 32-bit column.
+                        if (row < args.M && cc < args.N) {
+                            uint16_t *dst = reinterpret_cast<uint16_t *>(args.C) + int64_t(row) * args.ldc + cc;
+                            const int valid = min(32, args.N - cc);
+                            if (valid == 32) {
+                                uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    d[i] = make_uint4((r[8 * i] & 0xFFFFu) | (r[8 * i + 1] << 16),
+                                                      (r[8 * i + 2] & 0xFFFFu) | (r[8 * i + 3] << 16),
+                                                      (r[8 * i + 4] & 0xFFFFu) | (r[8 * i + 5] << 16),
+                                                      (r[8 * i + 6] & 0xFFFFu) | (r[8 * i + 7] << 16));
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    if (j < valid) dst[j] = static_cast<uint16_t>(r[j]);
+                            }
+                        }
+                    } else {
+                        if (row < args.M && cc < args.N) store_32(crow + cc, r, args.N - cc);
+                    }
                 }
                 tc_fence_before_sync();
                 __syncwarp();
@@ -535,10 +558,10 @@ struct LaunchCache {
     int max_clusters = 0;
 };
 
-template <Kind KIND, bool B_MN, bool INT_OUT, int CTAS>
+template <Kind KIND, bool B_MN, int EPI, int CTAS>
 cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args,
                        int sms, cudaStream_t stream) {
-    auto *fn = gemm_kernel<KIND, B_MN, INT_OUT, CTAS>;
+    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS>;
     constexpr size_t SMEM = smem_bytes<CTAS>();
     static thread_local LaunchCache cache;  // per device (re-queried when it changes)
     int dev = 0;
@@ -585,15 +608,16 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
 
 size_t gemm_smem_bytes(int ctas) { return ctas == 2 ? smem_bytes<2>() : smem_bytes<1>(); }
 
-cudaError_t launch_gemm(Kind kind, bool b_mn_major, bool int_out, int ctas, const CUtensorMap &ta,
+cudaError_t launch_gemm(Kind kind, bool b_mn_major, int epi, int ctas, const CUtensorMap &ta,
                         const CUtensorMap &tb, const GemmArgs &args, int sms,
                         cudaStream_t stream) {
-#define PTC_LAUNCH(K, BMN, IO)                                              \
-    return ctas == 2 ? launch_one<K, BMN, IO, 2>(ta, tb, args, sms, stream) \
-                     : launch_one<K, BMN, IO, 1>(ta, tb, args, sms, stream)
-    if (kind == Kind::F16 && b_mn_major && !int_out) PTC_LAUNCH(Kind::F16, true, false);
-    if (kind == Kind::F16 && !b_mn_major && int_out) PTC_LAUNCH(Kind::F16, false, true);
-    if (kind == Kind::E4M3 && !b_mn_major && int_out) PTC_LAUNCH(Kind::E4M3, false, true);
+#define PTC_LAUNCH(K, BMN, E)                                              \
+    return ctas == 2 ? launch_one<K, BMN, E, 2>(ta, tb, args, sms, stream) \
+                     : launch_one<K, BMN, E, 1>(ta, tb, args, sms, stream)
+    if (kind == Kind::F16 && b_mn_major && epi == EPI_F32) PTC_LAUNCH(Kind::F16, true, EPI_F32);
+    if (kind == Kind::F16 && b_mn_major && epi == EPI_F16ACC) PTC_LAUNCH(Kind::F16, true, EPI_F16ACC);
+    if (kind == Kind::F16 && !b_mn_major && epi == EPI_INT) PTC_LAUNCH(Kind::F16, false, EPI_INT);
+    if (kind == Kind::E4M3 && !b_mn_major && epi == EPI_INT) PTC_LAUNCH(Kind::E4M3, false, EPI_INT);
 #undef PTC_LAUNCH
     return cudaErrorInvalidValue;
 }

@@ -47,13 +47,21 @@ enum OutMode : int { OUT_S32 = 0, OUT_F32 = 1, OUT_BF16 = 2, OUT_F16 = 3 };
 // 128 x 256 tile; ctas = 2: a CTA pair per 256 x 256 tile).
 size_t gemm_smem_bytes(int ctas);
 
+// Epilogues of the tensor-core GEMM kernel.
+enum Epi : int {
+    EPI_F32 = 0,     // FP32 accumulators -> FP32 C
+    EPI_INT = 1,     // FP32 chunk sums folded into int32 -> int32 or scaled output
+    EPI_F16ACC = 2,  // FP16 accumulators -> FP16 C
+};
+
 // Launch the persistent tensor-core GEMM on at most `sms` SMs.
-//   F16  + B MN-major + float output:  gemm_f16
-//   F16  + B K-major  + int32 output:  gemm_s8 (operands converted s8 -> f16)
-//   E4M3 + B K-major  + int32 output:  gemm_s4 (operands converted s4 -> e4m3)
+//   F16  + B MN-major + EPI_F32:     gemm_f16
+//   F16  + B MN-major + EPI_F16ACC:  gemm_f16_f16acc
+//   F16  + B K-major  + EPI_INT:     gemm_s8 (operands converted s8 -> f16)
+//   E4M3 + B K-major  + EPI_INT:     gemm_s4 (operands converted s4 -> e4m3)
 // args.tiles_m counts tiles of kBM * ctas rows.  The tensor map of A has boxes
 // of kBM rows; that of B boxes of kBN / ctas rows (K-major) or 64 x 64 (MN-major).
-cudaError_t launch_gemm(Kind kind, bool b_mn_major, bool int_out, int ctas, const CUtensorMap &ta,
+cudaError_t launch_gemm(Kind kind, bool b_mn_major, int epi, int ctas, const CUtensorMap &ta,
                         const CUtensorMap &tb, const GemmArgs &args, int sms,
                         cudaStream_t stream);
 

@@ -350,13 +350,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
 }
 
 // Instruction descriptor for kind::f16 and kind::f8f6f4 (dense):
-//   bits  4-5   D format (1 = F32)
+//   bits  4-5   D format (0 = F16, 1 = F32)
 //   bits  7-9   A format, bits 10-12 B format (kind::f16: 0 = F16;
 //               kind::f8f6f4: 0 = E4M3)
 //   bit  15     A major (0 = K-major), bit 16 B major (1 = MN-major)
 //   bits 17-22  N >> 3, bits 24-28 M >> 4
-__host__ __device__ constexpr uint32_t instr_desc(uint32_t afmt, uint32_t bfmt, bool b_mn_major, int m, int n) {
-    return (1u << 4) | (afmt << 7) | (bfmt << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+__host__ __device__ constexpr uint32_t instr_desc(uint32_t dfmt, uint32_t afmt, uint32_t bfmt, bool b_mn_major,
+                                                  int m, int n) {
+    return (dfmt << 4) | (afmt << 7) | (bfmt << 10) | ((b_mn_major ? 1u : 0u) << 16) |
            (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 

@@ -3,6 +3,8 @@
     python -m precision_tensor_core_gb300.tune --mode knobs --n 8192
     python -m precision_tensor_core_gb300.tune --mode sizes --sizes 512,1024,2048,4096,8192
 
+`variants` times gemm_f16_f16acc against gemm_f16, and gemm_s8_scaled /
+gemm_s4_scaled (each output type) against gemm_s8 / gemm_s4, at one size.
 `knobs` times gemm_f16 / gemm_s8 / gemm_s4 at one size under each setting of
 the library's tuning knobs (ptc_set_tuning: CTA pairs, raster group, L2
 eviction policy, INT fold length), one knob at a time from the defaults: the
@@ -36,7 +38,7 @@ KNOBS = {"cta_pair": [1, 2], "group_m": [4, 16, 32], "l2_hint": [1, 2, 3],
 
 def main():
     p = argparse.ArgumentParser()
-    p.add_argument("--mode", choices=["knobs", "sizes"], default="sizes")
+    p.add_argument("--mode", choices=["knobs", "sizes", "variants"], default="sizes")
     p.add_argument("--n", type=int, default=8192)
     p.add_argument("--sizes", default="512,1024,2048,4096,8192")
     p.add_argument("--calls", type=int, default=0, help="calls per timing (0: by size)")
@@ -114,7 +116,35 @@ def main():
         return out
 
     results = {}
-    if a.mode == "sizes":
+    if a.mode == "variants":
+        n = a.n
+        ops = operands(n)
+        sa = torch.rand(n, device=dev) + 0.5
+        sb = torch.rand(n, device=dev) + 0.5
+        calls = a.calls or max(4, min(200, int(2e13 / (2.0 * n ** 3))))
+        print(f"{'call':>24} {'TOPS':>8} {'ms':>8}")
+        A, B, C = ops["f16"]
+        Ch = torch.empty((n, n), dtype=torch.float16, device=dev)
+        for key, fn in (("gemm_f16 -> f32", call("f16", ops, n)),
+                        ("gemm_f16_f16acc -> f16", lambda: ptc.matmul_f16_f16acc(A, B, out=Ch))):
+            ms = time_ms(fn, calls)
+            results[key] = {"ms": ms, "tops": 2.0 * n ** 3 / (ms * 1e-3) / 1e12}
+            print(f"{key:>24} {results[key]['tops']:>8.1f} {ms:>8.4f}", flush=True)
+        for prec in ("s8", "s4"):
+            A, B, C = ops[prec]
+            rows = [("int32", call(prec, ops, n))]
+            for name, dt in (("f32", torch.float32), ("bf16", torch.bfloat16), ("f16", torch.float16)):
+                Co = torch.empty((n, n), dtype=dt, device=dev)
+                if prec == "s8":
+                    rows.append((name, lambda Co=Co: ptc.matmul_s8_scaled(A, B, sa, sb, out=Co)))
+                else:
+                    rows.append((name, lambda Co=Co: ptc.matmul_s4_scaled(A, B, n, sa, sb, out=Co)))
+            for name, fn in rows:
+                ms = time_ms(fn, calls)
+                key = f"gemm_{prec}{'' if name == 'int32' else '_scaled'} -> {name}"
+                results[key] = {"ms": ms, "tops": 2.0 * n ** 3 / (ms * 1e-3) / 1e12}
+                print(f"{key:>24} {results[key]['tops']:>8.1f} {ms:>8.4f}", flush=True)
+    elif a.mode == "sizes":
         for k, v in DEFAULTS.items():
             ptc.ptc_set_tuning(k, v)
         print(f"{'N':>6} {'FP16 TFLOP/s':>13} {'INT8 TOPS':>10} {'INT4 TOPS':>10}   (ms per call)")
