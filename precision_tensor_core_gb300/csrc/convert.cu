@@ -41,37 +41,54 @@ __device__ __forceinline__ uint16_t s8_to_f16_bits(int8_t v) {
 
 // Converts rows [0, rows_a) of A and then rows [0, rows_b) of B, cols
 // elements each, in one grid-stride pass over (row, 16-element vector) pairs.
+// Each thread takes UNROLL vectors per pass and issues all their loads before
+// converting, so that several 16-byte loads per thread are in flight.
+constexpr int UNROLL = 4;
+
 __global__ void s8_to_f16_kernel(const int8_t *__restrict__ src_a, int64_t lds_a, int rows_a,
                                  const int8_t *__restrict__ src_b, int64_t lds_b, int rows_b,
                                  int cols, uint16_t *__restrict__ dst_a, uint16_t *__restrict__ dst_b,
                                  int64_t ldd) {
     const int vpr = (cols + 15) / 16;  // 16-element vectors per row
     const int64_t total = int64_t(rows_a + rows_b) * vpr;
-    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
-         i += int64_t(gridDim.x) * blockDim.x) {
-        int64_t r = i / vpr;
-        const int c0 = int(i - r * vpr) * 16;
-        const int8_t *s;
-        uint16_t *d;
-        if (r < rows_a) {
-            s = src_a + r * lds_a + c0;
-            d = dst_a + r * ldd + c0;
-        } else {
-            r -= rows_a;
-            s = src_b + r * lds_b + c0;
-            d = dst_b + r * ldd + c0;
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t base = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; base < total;
+         base += stride * UNROLL) {
+        uint4 x[UNROLL];
+        const int8_t *s[UNROLL];
+        uint16_t *d[UNROLL];
+        int c0[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int64_t i = base + u * stride;
+            s[u] = nullptr;
+            if (i >= total) continue;
+            int64_t r = i / vpr;
+            c0[u] = int(i - r * vpr) * 16;
+            if (r < rows_a) {
+                s[u] = src_a + r * lds_a + c0[u];
+                d[u] = dst_a + r * ldd + c0[u];
+            } else {
+                r -= rows_a;
+                s[u] = src_b + r * lds_b + c0[u];
+                d[u] = dst_b + r * ldd + c0[u];
+            }
+            if (c0[u] + 16 <= cols) x[u] = __ldcs(reinterpret_cast<const uint4 *>(s[u]));
         }
-        if (c0 + 16 <= cols) {
-            const uint4 x = __ldcs(reinterpret_cast<const uint4 *>(s));
-            uint4 o0, o1;
-            s8x4_to_f16x4(x.x, o0.x, o0.y);
-            s8x4_to_f16x4(x.y, o0.z, o0.w);
-            s8x4_to_f16x4(x.z, o1.x, o1.y);
-            s8x4_to_f16x4(x.w, o1.z, o1.w);
-            reinterpret_cast<uint4 *>(d)[0] = o0;
-            reinterpret_cast<uint4 *>(d)[1] = o1;
-        } else {
-            for (int j = 0; j < cols - c0; ++j) d[j] = s8_to_f16_bits(s[j]);
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            if (s[u] == nullptr) continue;
+            if (c0[u] + 16 <= cols) {
+                uint4 o0, o1;
+                s8x4_to_f16x4(x[u].x, o0.x, o0.y);
+                s8x4_to_f16x4(x[u].y, o0.z, o0.w);
+                s8x4_to_f16x4(x[u].z, o1.x, o1.y);
+                s8x4_to_f16x4(x[u].w, o1.z, o1.w);
+                reinterpret_cast<uint4 *>(d[u])[0] = o0;
+                reinterpret_cast<uint4 *>(d[u])[1] = o1;
+            } else {
+                for (int j = 0; j < cols - c0[u]; ++j) d[u][j] = s8_to_f16_bits(s[u][j]);
+            }
         }
     }
 }
@@ -126,35 +143,48 @@ __global__ void s4_to_e4m3_kernel(const uint8_t *__restrict__ src_a, int64_t lds
                                   int64_t ldd) {
     const int vpr = (cols + 31) / 32;  // 32-element (16-byte packed) vectors per row
     const int64_t total = int64_t(rows_a + rows_b) * vpr;
-    for (int64_t i = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; i < total;
-         i += int64_t(gridDim.x) * blockDim.x) {
-        int64_t r = i / vpr;
-        const int c0 = int(i - r * vpr) * 32;
-        const uint8_t *s;
-        uint8_t *d;
-        if (r < rows_a) {
-            s = src_a + r * lds_a + c0 / 2;
-            d = dst_a + r * ldd + c0;
-        } else {
-            r -= rows_a;
-            s = src_b + r * lds_b + c0 / 2;
-            d = dst_b + r * ldd + c0;
-        }
-        if (c0 + 32 <= cols) {
-            const uint4 x = __ldcs(reinterpret_cast<const uint4 *>(s));
-            const uint32_t w[4] = {x.x, x.y, x.z, x.w};
-            uint32_t o[8];
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t base = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; base < total;
+         base += stride * UNROLL) {
+        uint4 x[UNROLL];
+        const uint8_t *s[UNROLL];
+        uint8_t *d[UNROLL];
+        int c0[UNROLL];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                o[2 * q] = s4x4_to_e4m3x4(w[q] & 0xFFFFu);
-                o[2 * q + 1] = s4x4_to_e4m3x4(w[q] >> 16);
+        for (int u = 0; u < UNROLL; ++u) {
+            const int64_t i = base + u * stride;
+            s[u] = nullptr;
+            if (i >= total) continue;
+            int64_t r = i / vpr;
+            c0[u] = int(i - r * vpr) * 32;
+            if (r < rows_a) {
+                s[u] = src_a + r * lds_a + c0[u] / 2;
+                d[u] = dst_a + r * ldd + c0[u];
+            } else {
+                r -= rows_a;
+                s[u] = src_b + r * lds_b + c0[u] / 2;
+                d[u] = dst_b + r * ldd + c0[u];
             }
-            reinterpret_cast<uint4 *>(d)[0] = make_uint4(o[0], o[1], o[2], o[3]);
-            reinterpret_cast<uint4 *>(d)[1] = make_uint4(o[4], o[5], o[6], o[7]);
-        } else {
-            for (int j = 0; j < cols - c0; ++j) {
-                const uint32_t b = s[j >> 1];
-                d[j] = s4_to_e4m3_byte((j & 1) ? (b >> 4) : b);
+            if (c0[u] + 32 <= cols) x[u] = __ldcs(reinterpret_cast<const uint4 *>(s[u]));
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            if (s[u] == nullptr) continue;
+            if (c0[u] + 32 <= cols) {
+                const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+                uint32_t o[8];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    o[2 * q] = s4x4_to_e4m3x4(w[q] & 0xFFFFu);
+                    o[2 * q + 1] = s4x4_to_e4m3x4(w[q] >> 16);
+                }
+                reinterpret_cast<uint4 *>(d[u])[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                reinterpret_cast<uint4 *>(d[u])[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            } else {
+                for (int j = 0; j < cols - c0[u]; ++j) {
+                    const uint32_t b = s[u][j >> 1];
+                    d[u][j] = s4_to_e4m3_byte((j & 1) ? (b >> 4) : b);
+                }
             }
         }
     }
