@@ -202,6 +202,41 @@ int gemm_s8_noalloc(int64_t M, int64_t N, int64_t K,
                     int32_t *C, int64_t ldc,
                     void *stream);
 
+/*
+ * The same three products with HOST-resident operands and result: A, B and C
+ * are host pointers (pinned memory from cudaHostAlloc / cudaHostRegister gives
+ * asynchronous copies; pageable memory works but its copies are staged
+ * synchronously by the driver).  Layouts, leading dimensions and errors as
+ * gemm_f16 / gemm_s8 / gemm_s4 (host pointers must also be 16-byte aligned).
+ * Asynchronous on `stream`: the call enqueues the work and returns; A and B
+ * must stay unchanged and C unread until `stream` has completed.  The work is
+ * pipelined over row panels of 2048 rows once M >= 8192: B and the A panels
+ * are copied to the device on a library-owned stream, each panel's kernels
+ * run on `stream` as soon as its operands arrived, and each C panel is copied
+ * back on a second library-owned stream as soon as it is done, so the two
+ * copy directions and the tensor cores work at the same time.  All of it is
+ * ordered after the work already queued on `stream`, and `stream` waits for
+ * the last copy.  Device buffers come from the library's stream-ordered pool.
+ * The paper has no counterpart (its matrices are device-resident).
+ */
+int gemm_f16_host(int64_t M, int64_t N, int64_t K,
+                  const void *A, int64_t lda,
+                  const void *B, int64_t ldb,
+                  float *C, int64_t ldc,
+                  void *stream);
+
+int gemm_s8_host(int64_t M, int64_t N, int64_t K,
+                 const int8_t *A, int64_t lda,
+                 const int8_t *B, int64_t ldb,
+                 int32_t *C, int64_t ldc,
+                 void *stream);
+
+int gemm_s4_host(int64_t M, int64_t N, int64_t K,
+                 const void *A, int64_t lda,
+                 const void *B, int64_t ldb,
+                 int32_t *C, int64_t ldc,
+                 void *stream);
+
 /* Human-readable text of a status code.  For PTC_ERR_LAUNCH the text of the
  * failing CUDA call on the calling thread is appended.  Never NULL; the
  * string stays valid until the next call on the same thread. */

@@ -15,9 +15,10 @@ library's CUDA kernels):
   dimensions, device addresses, a cudaStream_t handle).  A nonzero status
   raises :class:`PtcError`.
 * ``matmul_f16``, ``matmul_f16_f16acc``, ``matmul_s8``, ``matmul_s4``, ``matmul_s8_scaled``,
-  ``matmul_s4_scaled``: the same calls on torch
-  tensors.  Device tensors run on the current CUDA stream; CPU tensors are
-  copied to the device and the result is copied back (end-to-end use).
+  ``matmul_s4_scaled``: the same calls on torch tensors.  Device tensors run
+  on the current CUDA stream; host (CPU) tensors of ``matmul_f16`` /
+  ``matmul_s8`` / ``matmul_s4`` go through the host-buffer entry points
+  (``gemm_*_host``), which pipeline the copies inside the library.
 
 There is no CPU fallback: if ``libptc.so`` has not been built the first call
 raises, and on a machine without a compute-capability 10.3 GPU every GEMM call
@@ -64,7 +65,8 @@ def lib() -> ctypes.CDLL:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"libptc.so is not built ({LIB_PATH}); run __graft_entry__.build()")
         L = ctypes.CDLL(LIB_PATH)
-        for name in ("gemm_f16", "gemm_f16_f16acc", "gemm_s8", "gemm_s4", "gemm_s8_noalloc"):
+        for name in ("gemm_f16", "gemm_f16_f16acc", "gemm_s8", "gemm_s4", "gemm_s8_noalloc",
+                     "gemm_f16_host", "gemm_s8_host", "gemm_s4_host"):
             fn = getattr(L, name)
             fn.restype = ctypes.c_int
             fn.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]
@@ -134,6 +136,21 @@ def gemm_s8_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
     return _check(lib().gemm_s8_noalloc(M, N, K, A, lda, B, ldb, C, ldc, stream))
 
 
+def gemm_f16_host(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    """gemm_f16 with host-resident A, B, C (asynchronous on `stream`; see include/ptc.h)."""
+    return _check(lib().gemm_f16_host(M, N, K, A, lda, B, ldb, C, ldc, stream))
+
+
+def gemm_s8_host(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    """gemm_s8 with host-resident A, B, C (asynchronous on `stream`)."""
+    return _check(lib().gemm_s8_host(M, N, K, A, lda, B, ldb, C, ldc, stream))
+
+
+def gemm_s4_host(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    """gemm_s4 with host-resident A, B, C (asynchronous on `stream`)."""
+    return _check(lib().gemm_s4_host(M, N, K, A, lda, B, ldb, C, ldc, stream))
+
+
 def gemm_poll_device_error() -> int:
     """Status of the device error word (read and cleared); synchronises the device."""
     return int(lib().gemm_poll_device_error())
@@ -171,34 +188,40 @@ def _rowmajor(t, name):
     return max(32, (t.shape[1] + 31) // 32 * 32)
 
 
-def _run(fn, A, B, out, out_shape, out_dtype, M, N, K, lda_scale, stream):
+_HOST_FN = {}
+
+
+def _run(fn, A, B, out, out_shape, out_dtype, M, N, K, lda_scale, stream, sync=True):
+    """Device tensors: the device entry point on `stream`.  Host tensors: the
+    host entry point (pipelined copies inside the library); the result is
+    ready on return unless sync=False, in which case `stream` must be
+    synchronised before `out` is read and A, B must be kept alive (and
+    unchanged) until then."""
     import torch
     host = A.device.type == "cpu"
     if host != (B.device.type == "cpu"):
         raise ValueError("A and B must both be on the host or both on the device")
     if host:
-        dev = torch.device("cuda", torch.cuda.current_device())
-        Ad = A.to(dev, non_blocking=True)
-        Bd = B.to(dev, non_blocking=True)
-        Cd = torch.empty(out_shape, dtype=out_dtype, device=dev)
-    else:
-        Ad, Bd = A, B
-        Cd = out if out is not None else torch.empty(out_shape, dtype=out_dtype, device=A.device)
-    lda = _rowmajor(Ad, "A") * lda_scale
-    ldb = _rowmajor(Bd, "B") * lda_scale
-    ldc = _rowmajor(Cd, "C")
-    fn(M, N, K, Ad.data_ptr(), lda, Bd.data_ptr(), ldb, Cd.data_ptr(), ldc, _stream(stream))
-    if host:
-        if out is None:
-            out = torch.empty(out_shape, dtype=out_dtype, pin_memory=True)
-        out.copy_(Cd, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-        return out
-    return Cd
+        hfn = _HOST_FN.get(fn)
+        if hfn is None:
+            raise ValueError("this product has no host-buffer entry point")
+        C = out if out is not None else torch.empty(out_shape, dtype=out_dtype, pin_memory=True)
+        if C.device.type != "cpu":
+            raise ValueError("host operands need a host result tensor")
+        st = _stream(stream)
+        hfn(M, N, K, A.data_ptr(), _rowmajor(A, "A") * lda_scale, B.data_ptr(), _rowmajor(B, "B") * lda_scale,
+            C.data_ptr(), _rowmajor(C, "C"), st)
+        if sync:
+            torch.cuda.ExternalStream(st).synchronize() if st else torch.cuda.synchronize()
+        return C
+    C = out if out is not None else torch.empty(out_shape, dtype=out_dtype, device=A.device)
+    fn(M, N, K, A.data_ptr(), _rowmajor(A, "A") * lda_scale, B.data_ptr(), _rowmajor(B, "B") * lda_scale,
+       C.data_ptr(), _rowmajor(C, "C"), _stream(stream))
+    return C
 
 
-def matmul_f16(A, B, out=None, stream=None):
-    """FP16 A (M,K) @ B (K,N) -> float32 (M,N) on the tensor cores."""
+def matmul_f16(A, B, out=None, stream=None, sync=True):
+    """FP16 A (M,K) @ B (K,N) -> float32 (M,N) on the tensor cores (device or host tensors)."""
     import torch
     if A.dtype != torch.float16 or B.dtype != torch.float16:
         raise TypeError("matmul_f16 takes float16 operands")
@@ -206,7 +229,7 @@ def matmul_f16(A, B, out=None, stream=None):
     K2, N = B.shape
     if K != K2:
         raise ValueError("inner dimensions differ")
-    return _run(gemm_f16, A, B, out, (M, N), torch.float32, M, N, K, 1, stream)
+    return _run(gemm_f16, A, B, out, (M, N), torch.float32, M, N, K, 1, stream, sync)
 
 
 def matmul_f16_f16acc(A, B, out=None, stream=None):
@@ -221,7 +244,7 @@ def matmul_f16_f16acc(A, B, out=None, stream=None):
     return _run(gemm_f16_f16acc, A, B, out, (M, N), torch.float16, M, N, K, 1, stream)
 
 
-def matmul_s8(A, Bt, out=None, stream=None):
+def matmul_s8(A, Bt, out=None, stream=None, sync=True):
     """INT8 A (M,K) @ B where B (K,N) is column-major, given as Bt (N,K) -> int32 (M,N)."""
     import torch
     if A.dtype != torch.int8 or Bt.dtype != torch.int8:
@@ -230,17 +253,17 @@ def matmul_s8(A, Bt, out=None, stream=None):
     N, K2 = Bt.shape
     if K != K2:
         raise ValueError("inner dimensions differ")
-    return _run(gemm_s8, A, Bt, out, (M, N), torch.int32, M, N, K, 1, stream)
+    return _run(gemm_s8, A, Bt, out, (M, N), torch.int32, M, N, K, 1, stream, sync)
 
 
-def matmul_s4(A, Bt, K, out=None, stream=None):
+def matmul_s4(A, Bt, K, out=None, stream=None, sync=True):
     """Packed INT4 A (M, >=K/2 bytes) @ B, B column-major given as Bt (N, >=K/2 bytes),
     two values per byte with the low nibble first -> int32 (M,N)."""
     import torch
     if A.dtype != torch.uint8 or Bt.dtype != torch.uint8:
         raise TypeError("matmul_s4 takes packed uint8 operands")
     M, N = A.shape[0], Bt.shape[0]
-    return _run(gemm_s4, A, Bt, out, (M, N), torch.int32, M, N, int(K), 2, stream)
+    return _run(gemm_s4, A, Bt, out, (M, N), torch.int32, M, N, int(K), 2, stream, sync)
 
 
 def _out_type(dtype):
@@ -285,3 +308,6 @@ def matmul_s4_scaled(A, Bt, K, scale_a=None, scale_b=None, out_dtype=None, out=N
         raise TypeError("matmul_s4_scaled takes packed uint8 operands")
     dt = out.dtype if out is not None else (out_dtype or torch.float32)
     return _scaled(gemm_s4_scaled, A, Bt, int(K), scale_a, scale_b, dt, out, stream, 2)
+
+
+_HOST_FN.update({gemm_f16: gemm_f16_host, gemm_s8: gemm_s8_host, gemm_s4: gemm_s4_host})

@@ -13,6 +13,7 @@
 
 #include <atomic>
 #include <cstdint>
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -392,6 +393,219 @@ int int_gemm(bool s4, int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     return rc;
 }
 
+// ------------------------------------------------------------ host buffers
+// Library-owned copy streams of one device (created on first use).
+struct CopyStreams {
+    std::once_flag once;
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    int ok = 0;
+};
+CopyStreams g_copy[kMaxDevices];
+
+int copy_streams(int dev, CopyStreams **out) {
+    CopyStreams &c = g_copy[dev];
+    std::call_once(c.once, [&] {
+        if (cudaStreamCreateWithFlags(&c.h2d, cudaStreamNonBlocking) == cudaSuccess &&
+            cudaStreamCreateWithFlags(&c.d2h, cudaStreamNonBlocking) == cudaSuccess)
+            c.ok = 1;
+        else
+            cudaGetLastError();
+    });
+    if (!c.ok) return fail(PTC_ERR_LAUNCH, "could not create the library's copy streams");
+    *out = &c;
+    return PTC_OK;
+}
+
+// Events of one host-buffer call; destroyed (lazily, by the driver) on return.
+struct EventSet {
+    cudaEvent_t ev[64];
+    int n = 0;
+    cudaError_t make(cudaEvent_t *e) {
+        cudaError_t r = cudaEventCreateWithFlags(e, cudaEventDisableTiming);
+        if (r == cudaSuccess) ev[n++] = *e;
+        return r;
+    }
+    ~EventSet() {
+        for (int i = 0; i < n; ++i) cudaEventDestroy(ev[i]);
+    }
+};
+
+// One GEMM with host-resident A, B and C, pipelined over row panels of A / C:
+//   copy stream 1: B, then the A panels (host -> device)
+//   caller's stream: operand conversion (integer routes) and the tensor-core
+//                    kernel of each panel as soon as its A panel has arrived
+//   copy stream 2: each C panel (device -> host) as soon as its kernel is done
+// Device buffers come from the library pool, stream-ordered on the caller's
+// stream; everything runs after the work already queued on that stream, and
+// the stream waits for the last copy.  prec: 0 FP16, 1 INT8, 2 packed INT4.
+int host_gemm(int prec, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+              int64_t ldb, void *C, int64_t ldc, void *stream) {
+    int rc = check_sizes(M, N, K);
+    if (rc) return rc;
+    if (M == 0 || N == 0) return PTC_OK;
+    const bool f16 = prec == 0, s4 = prec == 2;
+    if (!C || ldc < N) return fail(PTC_ERR_INVALID, "C is NULL or ldc < N");
+    if (K > 0 && (!A || !B)) return fail(PTC_ERR_INVALID, "A or B is NULL");
+    if (K > 0 && (lda < K || ldb < (f16 ? N : K))) return fail(PTC_ERR_INVALID, "lda or ldb below its minimum");
+    if (s4 && K > 0 && ((lda & 1) || (ldb & 1)))
+        return fail(PTC_ERR_INVALID, "lda, ldb must be even (counted in nibbles)");
+    if (!aligned16(C) || ldc % 4) return fail(PTC_ERR_ALIGN, "C must be 16-byte aligned, ldc % 4 == 0");
+    const int pitch_mult = f16 ? 8 : (s4 ? 32 : 16);
+    if (K > 0 && (!aligned16(A) || !aligned16(B) || lda % pitch_mult || ldb % pitch_mult))
+        return fail(PTC_ERR_ALIGN, "A, B must be 16-byte aligned with 16-byte row pitches");
+    // Bytes per element x 2 (nibbles count half a byte).
+    const int e2 = f16 ? 4 : (s4 ? 1 : 2);
+    const uint64_t cbytes = span_bytes(M, N, ldc, 4, 1);
+    if (K > 0 && (overlaps(C, cbytes, A, span_bytes(M, K, lda, e2, 2)) ||
+                  overlaps(C, cbytes, B, f16 ? span_bytes(K, N, ldb, 2, 1) : span_bytes(N, K, ldb, e2, 2))))
+        return fail(PTC_ERR_OVERLAP, "C overlaps A or B");
+
+    int dev;
+    DevInfo *d;
+    if ((rc = current_device(&dev, &d))) return rc;
+    if (!d->pool_ok) return fail(PTC_ERR_ALLOC, "workspace memory pool unavailable");
+    CopyStreams *cs;
+    if ((rc = copy_streams(dev, &cs))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    // Device copies with 16-byte row pitches, plus the integer routes' workspace.
+    const int64_t a_row = (K * e2 + 1) / 2, a_pitch = round_up(a_row > 0 ? a_row : 1, 16);
+    const int64_t b_rows = f16 ? K : N, b_row = f16 ? N * 2 : (K * e2 + 1) / 2;
+    const int64_t b_pitch = round_up(b_row > 0 ? b_row : 1, 16);
+    const int64_t c_pitch = round_up(N * 4, 16);
+    const int k_elems = f16 ? 64 : (s4 ? 128 : 64);
+    const int wsize = s4 ? 1 : 2;
+    const int64_t ldw = round_up(K > 0 ? K : 1, k_elems);
+    int64_t off = 0;
+    const int64_t off_a = off;
+    off += round_up(M * a_pitch, 1024);
+    const int64_t off_b = off;
+    off += round_up(b_rows * b_pitch, 1024);
+    const int64_t off_c = off;
+    off += round_up(M * c_pitch, 1024);
+    const int64_t off_wa = off;
+    if (!f16) off += round_up(M * ldw * wsize, 1024);
+    const int64_t off_wb = off;
+    if (!f16) off += round_up(N * ldw * wsize, 1024);
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, size_t(off), d->pool, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PTC_ERR_ALLOC, "device buffers for host operands could not be allocated");
+    }
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    uint8_t *Ad = base + off_a, *Bd = base + off_b, *Cd = base + off_c;
+    uint8_t *Wa = base + off_wa, *Wb = base + off_wb;
+
+    // Row panels: 2048 rows (several waves of tiles each) once M allows four.
+    const int64_t panel = (M >= 4 * 2048) ? 2048 : M;
+    const int npanels = int((M + panel - 1) / panel);
+    EventSet evs;
+    cudaEvent_t ev_start, ev_b, ev_done;
+    rc = PTC_OK;
+    auto cuda = [&](cudaError_t r, const char *what) {
+        if (rc == PTC_OK && r != cudaSuccess) rc = fail_cuda(r, what);
+        return rc == PTC_OK;
+    };
+    if (npanels > 28) rc = fail(PTC_ERR_INVALID, "too many row panels");
+    if (!cuda(evs.make(&ev_start), "event") || !cuda(evs.make(&ev_b), "event") ||
+        !cuda(evs.make(&ev_done), "event")) {
+        cudaFreeAsync(ws, s);
+        return rc;
+    }
+    cuda(cudaEventRecord(ev_start, s), "event record");
+    cuda(cudaStreamWaitEvent(cs->h2d, ev_start, 0), "stream wait");
+    cuda(cudaStreamWaitEvent(cs->d2h, ev_start, 0), "stream wait");
+
+    if (K == 0) {
+        if (rc == PTC_OK) {
+            cudaError_t r = ptc::launch_zero_fill(Cd, c_pitch / 4, int(M), int(N), 4, d->sms * 4, s);
+            if (cuda(r, "zero-fill launch")) g_launches.fetch_add(1);
+        }
+        cuda(cudaMemcpy2DAsync(C, size_t(ldc) * 4, Cd, size_t(c_pitch), size_t(N) * 4, size_t(M),
+                               cudaMemcpyDeviceToHost, s), "C copy to host");
+        cudaFreeAsync(ws, s);
+        return rc;
+    }
+
+    // B, then the A panels, host -> device.
+    cuda(cudaMemcpy2DAsync(Bd, size_t(b_pitch), B, size_t(f16 ? ldb * 2 : (ldb * e2) / 2), size_t(b_row),
+                           size_t(b_rows), cudaMemcpyHostToDevice, cs->h2d), "B copy to device");
+    cuda(cudaEventRecord(ev_b, cs->h2d), "event record");
+    cudaEvent_t ev_a[32], ev_c[32];
+    for (int p = 0; p < npanels && rc == PTC_OK; ++p) {
+        const int64_t r0 = p * panel, rows = std::min(panel, M - r0);
+        if (!cuda(evs.make(&ev_a[p]), "event") || !cuda(evs.make(&ev_c[p]), "event")) break;
+        const size_t apitch_host = size_t((lda * e2) / 2);
+        cuda(cudaMemcpy2DAsync(Ad + r0 * a_pitch, size_t(a_pitch),
+                               static_cast<const uint8_t *>(A) + r0 * apitch_host, apitch_host, size_t(a_row),
+                               size_t(rows), cudaMemcpyHostToDevice, cs->h2d), "A copy to device");
+        cuda(cudaEventRecord(ev_a[p], cs->h2d), "event record");
+    }
+
+    // Kernels on the caller's stream, panel by panel.
+    cuda(cudaStreamWaitEvent(s, ev_b, 0), "stream wait");
+    const int cgrid = d->sms * 8;
+    if (!f16 && rc == PTC_OK) {
+        cudaError_t r = s4 ? ptc::launch_s4_to_e4m3_pair(Bd, b_pitch, 0, Bd, b_pitch, int(N), int(K), Wa, Wb,
+                                                          ldw, cgrid, s)
+                           : ptc::launch_s8_to_f16_pair(reinterpret_cast<const int8_t *>(Bd), b_pitch, 0,
+                                                        reinterpret_cast<const int8_t *>(Bd), b_pitch, int(N),
+                                                        int(K), reinterpret_cast<uint16_t *>(Wa),
+                                                        reinterpret_cast<uint16_t *>(Wb), ldw, cgrid, s);
+        if (cuda(r, "operand conversion launch")) g_launches.fetch_add(1);
+    }
+    for (int p = 0; p < npanels && rc == PTC_OK; ++p) {
+        const int64_t r0 = p * panel, rows = std::min(panel, M - r0);
+        cuda(cudaStreamWaitEvent(s, ev_a[p], 0), "stream wait");
+        const int ctas = choose_ctas(rows, N, d->sms);
+        CUtensorMap ta, tb;
+        if (f16) {
+            if (rc == PTC_OK)
+                rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Ad + r0 * a_pitch, K, rows, a_pitch, 64, ptc::kBM);
+            if (rc == PTC_OK)
+                rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Bd, N, K, b_pitch, 64, 64);
+        } else {
+            uint8_t *wa = Wa + r0 * ldw * wsize;
+            cudaError_t r =
+                s4 ? ptc::launch_s4_to_e4m3_pair(Ad + r0 * a_pitch, a_pitch, int(rows), Ad, a_pitch, 0, int(K), wa,
+                                                 wa, ldw, cgrid, s)
+                   : ptc::launch_s8_to_f16_pair(reinterpret_cast<const int8_t *>(Ad + r0 * a_pitch), a_pitch,
+                                                int(rows), reinterpret_cast<const int8_t *>(Ad), a_pitch, 0, int(K),
+                                                reinterpret_cast<uint16_t *>(wa), reinterpret_cast<uint16_t *>(wa),
+                                                ldw, cgrid, s);
+            if (cuda(r, "operand conversion launch")) g_launches.fetch_add(1);
+            const CUtensorMapDataType dt = s4 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+            if (rc == PTC_OK) rc = make_tmap(&ta, dt, wa, K, rows, uint64_t(ldw) * wsize, k_elems, ptc::kBM);
+            if (rc == PTC_OK) rc = make_tmap(&tb, dt, Wb, K, N, uint64_t(ldw) * wsize, k_elems, ptc::kBN / ctas);
+        }
+        if (rc != PTC_OK) break;
+        GemmArgs args = base_args(rows, N, K, k_elems, Cd + r0 * c_pitch, c_pitch / 4, ctas);
+        if (!f16) {
+            const int ch = s4 ? g_chunk_s4.load() : g_chunk_s8.load();
+            args.kb_per_chunk = ch > 0 ? ch : 1;
+            args.out_mode = ptc::OUT_S32;
+        }
+        rc = launch_gemm_checked(s4 ? Kind::E4M3 : Kind::F16, f16, f16 ? ptc::EPI_F32 : ptc::EPI_INT, ctas, ta, tb,
+                                 args, *d, s);
+        cuda(cudaEventRecord(ev_c[p], s), "event record");
+        // C panel, device -> host, once its kernel is done.
+        cuda(cudaStreamWaitEvent(cs->d2h, ev_c[p], 0), "stream wait");
+        cuda(cudaMemcpy2DAsync(static_cast<uint8_t *>(C) + r0 * ldc * 4, size_t(ldc) * 4, Cd + r0 * c_pitch,
+                               size_t(c_pitch), size_t(N) * 4, size_t(rows), cudaMemcpyDeviceToHost, cs->d2h),
+             "C copy to host");
+    }
+    // The caller's stream waits for the last copy; the buffers go back to the pool after it.
+    cudaError_t r1 = cudaEventRecord(ev_done, cs->d2h);
+    cudaError_t r2 = cudaStreamWaitEvent(s, ev_done, 0);
+    cudaError_t r3 = cudaStreamWaitEvent(s, ev_b, 0);
+    cuda(r1, "event record");
+    cuda(r2, "stream wait");
+    cuda(r3, "stream wait");
+    cudaFreeAsync(ws, s);
+    return rc;
+}
+
 int scaled_mode(int out_type) {
     switch (out_type) {
         case PTC_OUT_F32: return ptc::OUT_F32;
@@ -433,6 +647,24 @@ int gemm_s4_scaled(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, 
     const int mode = scaled_mode(out_type);
     if (mode < 0) return fail(PTC_ERR_INVALID, "out_type must be PTC_OUT_F32, PTC_OUT_BF16 or PTC_OUT_F16");
     return int_gemm(true, M, N, K, A, lda, B, ldb, C, ldc, mode, scale_a, scale_b, stream);
+}
+
+int gemm_f16_host(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                  int64_t ldb, float *C, int64_t ldc, void *stream) {
+    g_msg[0] = 0;
+    return host_gemm(0, M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
+int gemm_s8_host(int64_t M, int64_t N, int64_t K, const int8_t *A, int64_t lda, const int8_t *B,
+                 int64_t ldb, int32_t *C, int64_t ldc, void *stream) {
+    g_msg[0] = 0;
+    return host_gemm(1, M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
+int gemm_s4_host(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                 int64_t ldb, int32_t *C, int64_t ldc, void *stream) {
+    g_msg[0] = 0;
+    return host_gemm(2, M, N, K, A, lda, B, ldb, C, ldc, stream);
 }
 
 const char *gemm_status_string(int status) {
