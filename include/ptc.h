@@ -237,6 +237,38 @@ int gemm_s4_host(int64_t M, int64_t N, int64_t K,
                  int32_t *C, int64_t ldc,
                  void *stream);
 
+/*
+ * The paper's own kernel families on GB300, as same-precision baselines for
+ * its speedup definitions (section III-A, III-B: every PTX kernel is compared
+ * with the WMMA kernel of its precision, and quantised kernels with the FP16
+ * WMMA kernel).  Eight warps per block, 16 x 16 warp tiles (block tile
+ * 32 x 64), two cp.async stages, then:
+ *   PTC_BASELINE_F16_WMMA  WMMA m16n16k16, FP16 -> FP32      (fp16_wmma)
+ *   PTC_BASELINE_F16_MMA   mma.sync m16n8k16, FP16 -> FP32   (fp16_ptx_mma)
+ *   PTC_BASELINE_S8_WMMA   WMMA m16n16k16, s8 -> s32         (int8_wmma)
+ *   PTC_BASELINE_S8_MMA    mma.sync m16n8k32, s8 -> s32      (int8_ptx_mma_k32)
+ *   PTC_BASELINE_S4_WMMA   WMMA m8n8k32, s4 -> s32           (int4_wmma)
+ *   PTC_BASELINE_S4_MMA    mma.sync m16n8k64, s4 -> s32      (int4_ptx_mma_k64)
+ * Operands and C have the layouts of gemm_f16 / gemm_s8 / gemm_s4 (C FP32 for
+ * the FP16 variants, int32 otherwise).  Restrictions of these simple kernels:
+ * M % 32 == 0, N % 64 == 0, K a positive multiple of 32 (FP16), 64 (INT8) or
+ * 128 (INT4); C 32-byte aligned with ldc % 8 == 0.  They are comparison
+ * points, not the fast path; integer results are exact, FP16 results are FP32
+ * tensor-core sums.
+ */
+#define PTC_BASELINE_F16_WMMA 0
+#define PTC_BASELINE_F16_MMA 1
+#define PTC_BASELINE_S8_WMMA 2
+#define PTC_BASELINE_S8_MMA 3
+#define PTC_BASELINE_S4_WMMA 4
+#define PTC_BASELINE_S4_MMA 5
+
+int gemm_baseline(int variant, int64_t M, int64_t N, int64_t K,
+                  const void *A, int64_t lda,
+                  const void *B, int64_t ldb,
+                  void *C, int64_t ldc,
+                  void *stream);
+
 /* Human-readable text of a status code.  For PTC_ERR_LAUNCH the text of the
  * failing CUDA call on the calling thread is appended.  Never NULL; the
  * string stays valid until the next call on the same thread. */

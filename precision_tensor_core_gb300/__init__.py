@@ -41,6 +41,13 @@ PTC_ERR_LAUNCH = 5
 PTC_ERR_TIMEOUT = 6
 PTC_ERR_ALLOC = 7
 
+PTC_BASELINE_F16_WMMA = 0
+PTC_BASELINE_F16_MMA = 1
+PTC_BASELINE_S8_WMMA = 2
+PTC_BASELINE_S8_MMA = 3
+PTC_BASELINE_S4_WMMA = 4
+PTC_BASELINE_S4_MMA = 5
+
 PTC_OUT_F32 = 0
 PTC_OUT_BF16 = 1
 PTC_OUT_F16 = 2
@@ -74,6 +81,8 @@ def lib() -> ctypes.CDLL:
             fn = getattr(L, name)
             fn.restype = ctypes.c_int
             fn.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _vp, _vp, _i64, ctypes.c_int, _vp]
+        L.gemm_baseline.restype = ctypes.c_int
+        L.gemm_baseline.argtypes = [ctypes.c_int, _i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]
         L.gemm_status_string.restype = ctypes.c_char_p
         L.gemm_status_string.argtypes = [ctypes.c_int]
         L.gemm_poll_device_error.restype = ctypes.c_int
@@ -149,6 +158,11 @@ def gemm_s8_host(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
 def gemm_s4_host(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
     """gemm_s4 with host-resident A, B, C (asynchronous on `stream`)."""
     return _check(lib().gemm_s4_host(M, N, K, A, lda, B, ldb, C, ldc, stream))
+
+
+def gemm_baseline(variant, M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    """The paper's WMMA / mma.sync kernel families on GB300 (PTC_BASELINE_*); see include/ptc.h."""
+    return _check(lib().gemm_baseline(variant, M, N, K, A, lda, B, ldb, C, ldc, stream))
 
 
 def gemm_poll_device_error() -> int:

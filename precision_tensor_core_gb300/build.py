@@ -20,7 +20,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libptc.so")
-SOURCES = ["gemm_tc.cu", "convert.cu", "api.cu", "gemm_s8_noalloc.cu"]
+SOURCES = ["gemm_tc.cu", "convert.cu", "api.cu", "gemm_s8_noalloc.cu", "baseline.cu"]
 GENCODE = "-gencode=arch=compute_103a,code=sm_103a"
 
 

@@ -667,6 +667,44 @@ int gemm_s4_host(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, co
     return host_gemm(2, M, N, K, A, lda, B, ldb, C, ldc, stream);
 }
 
+int gemm_baseline(int variant, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
+                  int64_t ldb, void *C, int64_t ldc, void *stream) {
+    g_msg[0] = 0;
+    if (variant < PTC_BASELINE_F16_WMMA || variant > PTC_BASELINE_S4_MMA)
+        return fail(PTC_ERR_INVALID, "unknown baseline variant");
+    const ptc::Variant v = static_cast<ptc::Variant>(variant);
+    int rc = check_sizes(M, N, K);
+    if (rc) return rc;
+    if (M == 0 || N == 0) return PTC_OK;
+    const bool f16 = v == ptc::BASE_F16_WMMA || v == ptc::BASE_F16_MMA;
+    const bool s4 = v == ptc::BASE_S4_WMMA || v == ptc::BASE_S4_MMA;
+    const int kmult = ptc::baseline_k_multiple(v);
+    if (M % 32 || N % 64 || K % kmult || K == 0)
+        return fail(PTC_ERR_INVALID, "baseline kernels need M % 32 == 0, N % 64 == 0 and K a positive multiple "
+                                     "of 32 (FP16), 64 (INT8) or 128 (INT4)");
+    if (!A || !B || !C) return fail(PTC_ERR_INVALID, "A, B or C is NULL");
+    if (lda < K || ldb < (f16 ? N : K) || ldc < N) return fail(PTC_ERR_INVALID, "leading dimension below its minimum");
+    if (s4 && ((lda & 1) || (ldb & 1))) return fail(PTC_ERR_INVALID, "lda, ldb must be even (counted in nibbles)");
+    const int64_t lda_b = f16 ? lda * 2 : (s4 ? lda / 2 : lda);
+    const int64_t ldb_b = f16 ? ldb * 2 : (s4 ? ldb / 2 : ldb);
+    if (!aligned16(A) || !aligned16(B) || lda_b % 16 || ldb_b % 16)
+        return fail(PTC_ERR_ALIGN, "A, B must be 16-byte aligned with 16-byte row pitches");
+    if ((reinterpret_cast<uintptr_t>(C) & 31u) || ldc % 8)
+        return fail(PTC_ERR_ALIGN, "C must be 32-byte aligned, ldc % 8 == 0");
+    const uint64_t cbytes = span_bytes(M, N, ldc, 4, 1);
+    if (overlaps(C, cbytes, A, uint64_t((M - 1) * lda_b) + uint64_t(f16 ? K * 2 : (s4 ? (K + 1) / 2 : K))) ||
+        overlaps(C, cbytes, B, uint64_t(((f16 ? K : N) - 1) * ldb_b) + uint64_t(f16 ? N * 2 : (s4 ? (K + 1) / 2 : K))))
+        return fail(PTC_ERR_OVERLAP, "C overlaps A or B");
+    int dev;
+    DevInfo *d;
+    if ((rc = current_device(&dev, &d))) return rc;
+    cudaError_t e = ptc::launch_baseline(v, A, lda_b, B, ldb_b, C, ldc, int(M), int(N), int(K),
+                                         static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail_cuda(e, "baseline kernel launch");
+    g_launches.fetch_add(1);
+    return PTC_OK;
+}
+
 const char *gemm_status_string(int status) {
     static const char *names[] = {"PTC_OK",           "PTC_ERR_INVALID: invalid argument",
                                   "PTC_ERR_ALIGN: misaligned pointer or row pitch",

@@ -85,6 +85,22 @@ cudaError_t launch_s4_to_e4m3_pair(const uint8_t *a, int64_t lda, int rows_a, co
                                    int64_t ldb, int rows_b, int cols, uint8_t *dst_a, uint8_t *dst_b,
                                    int64_t ldd, int grid, cudaStream_t stream);
 
+// The paper's kernel families on GB300 (baseline.cu): WMMA and mma.sync.
+enum Variant : int {
+    BASE_F16_WMMA = 0,
+    BASE_F16_MMA = 1,
+    BASE_S8_WMMA = 2,
+    BASE_S8_MMA = 3,
+    BASE_S4_WMMA = 4,
+    BASE_S4_MMA = 5,
+};
+// K must be a multiple of this many values for variant v (M of 32, N of 64).
+int baseline_k_multiple(Variant v);
+// A row-major, B column-major (integer) or row-major (FP16); pitches in bytes;
+// C row-major FP32 (FP16 variants) or int32, ldc in elements.
+cudaError_t launch_baseline(Variant v, const void *A, int64_t lda_b, const void *B, int64_t ldb_b, void *C,
+                            int64_t ldc, int M, int N, int K, cudaStream_t s);
+
 // Adds to the library's kernel-launch counter (ptc_kernel_launch_count).
 void note_launches(uint64_t n);
 // Sets the calling thread's detail text shown by gemm_status_string.

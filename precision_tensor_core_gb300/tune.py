@@ -3,6 +3,10 @@
     python -m precision_tensor_core_gb300.tune --mode knobs --n 8192
     python -m precision_tensor_core_gb300.tune --mode sizes --sizes 512,1024,2048,4096,8192
 
+`baselines` times the paper's kernel families on GB300 (gemm_baseline: WMMA
+and mma.sync) beside the library's tcgen05 entry points at each size, and
+prints the paper's speedup definitions: each kernel over the WMMA kernel of
+its precision, and over the FP16 WMMA kernel.
 `variants` times gemm_f16_f16acc against gemm_f16, and gemm_s8_scaled /
 gemm_s4_scaled (each output type) against gemm_s8 / gemm_s4, at one size.
 `knobs` times gemm_f16 / gemm_s8 / gemm_s4 at one size under each setting of
@@ -38,7 +42,7 @@ KNOBS = {"cta_pair": [1, 2], "group_m": [4, 16, 32], "l2_hint": [1, 2, 3],
 
 def main():
     p = argparse.ArgumentParser()
-    p.add_argument("--mode", choices=["knobs", "sizes", "variants"], default="sizes")
+    p.add_argument("--mode", choices=["knobs", "sizes", "variants", "baselines"], default="sizes")
     p.add_argument("--n", type=int, default=8192)
     p.add_argument("--sizes", default="512,1024,2048,4096,8192")
     p.add_argument("--calls", type=int, default=0, help="calls per timing (0: by size)")
@@ -116,7 +120,36 @@ def main():
         return out
 
     results = {}
-    if a.mode == "variants":
+    if a.mode == "baselines":
+        base = {"fp16_wmma": ("f16", ptc.PTC_BASELINE_F16_WMMA), "fp16_ptx_mma": ("f16", ptc.PTC_BASELINE_F16_MMA),
+                "int8_wmma": ("s8", ptc.PTC_BASELINE_S8_WMMA), "int8_ptx_mma_k32": ("s8", ptc.PTC_BASELINE_S8_MMA),
+                "int4_wmma": ("s4", ptc.PTC_BASELINE_S4_WMMA), "int4_ptx_mma_k64": ("s4", ptc.PTC_BASELINE_S4_MMA)}
+        print(f"{'N':>6} {'kernel':>18} {'ms':>10} {'TOPS':>9} {'vs same-prec WMMA':>18} {'vs FP16 WMMA':>13}")
+        for n in [int(x) for x in a.sizes.split(",")]:
+            ops = operands(n)
+            calls = a.calls or max(2, min(50, int(5e11 / (2.0 * n ** 3))))
+            row = {}
+            for name, (prec, v) in base.items():
+                A, B, C = ops[prec]
+                # the stream is read at call time, so that graph capture sees the launch
+                fn = (lambda A=A, B=B, C=C, v=v: ptc.gemm_baseline(
+                    v, n, n, n, A.data_ptr(), n, B.data_ptr(), n, C.data_ptr(), n,
+                    torch.cuda.current_stream().cuda_stream))
+                row[name] = time_ms(fn, calls)
+            for prec, name in (("f16", "tcgen05 gemm_f16"), ("s8", "tcgen05 gemm_s8"), ("s4", "tcgen05 gemm_s4")):
+                row[name] = time_ms(call(prec, ops, n), calls)
+            wmma_of = {"fp16": "fp16_wmma", "int8": "int8_wmma", "int4": "int4_wmma",
+                       "tcgen05 gemm_f16": "fp16_wmma", "tcgen05 gemm_s8": "int8_wmma", "tcgen05 gemm_s4": "int4_wmma"}
+            results[str(n)] = {}
+            for name, ms in row.items():
+                ref = wmma_of.get(name, wmma_of.get(name.split("_")[0], "fp16_wmma"))
+                sp_same = row[ref] / ms
+                sp_f16 = row["fp16_wmma"] / ms
+                results[str(n)][name] = {"ms": ms, "tops": 2.0 * n ** 3 / (ms * 1e-3) / 1e12,
+                                         "speedup_vs_same_precision_wmma": sp_same, "speedup_vs_fp16_wmma": sp_f16}
+                print(f"{n:>6} {name:>18} {ms:>10.4f} {2.0 * n ** 3 / (ms * 1e-3) / 1e12:>9.1f} {sp_same:>17.2f}x"
+                      f" {sp_f16:>12.2f}x", flush=True)
+    elif a.mode == "variants":
         n = a.n
         ops = operands(n)
         sa = torch.rand(n, device=dev) + 0.5
