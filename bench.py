@@ -46,7 +46,7 @@ METRIC = "GEMM TFLOP/s / TOPS at N=8192 (FP16, INT8, INT4); fraction of GB300 de
 # DRAM read + write bytes of one launch of the FP16 GEMM kernel at N = 8192, from
 # the ncu capture summarised in profiles/gemm_f16_n8192.md (set to None whenever
 # that kernel changes, until it is captured again).
-F16_KERNEL_DRAM_BYTES = 1.032e9 + 0.247e9
+F16_KERNEL_DRAM_BYTES = 1.060e9 + 0.252e9
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 

@@ -302,8 +302,6 @@ int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile);
  *                  exactly representable integer)
  *   "s4_chunk_kb"  INT4 route: K blocks (128 values each) per fold, default 64
  *                  (8192 values: |partial| <= 2^19)
- *   "prefetch_kb"  L2 prefetch of the operands this many K blocks ahead of
- *                  the loads; 0 (default) off (measured much slower on GB300)
  *   "l2_hint"      L2 eviction policy of operand loads: 0 (default) none;
  *                  1 A evict-last / B evict-first; 2 A evict-last; 3 both
  *                  evict-normal (all measured slower than 0 on GB300)
@@ -312,6 +310,20 @@ int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile);
  *                  256 x 256 tiles (tcgen05 cta_group::2); 1: always one CTA;
  *                  2: always CTA pairs.  Results do not depend on the choice
  *                  except through the FP16 summation order.
+ *   "tail_split"   1 (default): when K spans at least split_min_kb K
+ *                  blocks and the last wave of output tiles would occupy at
+ *                  most half of the CTAs (or CTA pairs), each tile of that
+ *                  wave runs as two units over the two halves of K on two
+ *                  CTAs (or pairs), and the epilogue adds their partial sums,
+ *                  so that the tail takes about half the time.  The exchange
+ *                  uses up to ~20 MB of stream-ordered workspace from the
+ *                  library pool.  0: never.  Integer results do not depend on
+ *                  the choice; FP16 results of split tiles differ by the
+ *                  summation order (the sum of two FP32 half sums).
+ *   "split_min_kb" K blocks (64 values FP16 / INT8, 128 INT4) below which no
+ *                  tile is split, default 64 (the split saves about half a
+ *                  tile's K loop and costs a few microseconds per call);
+ *                  2 or more.
  * Values above the defaults can make gemm_s8 / gemm_s4 inexact for adversarial
  * inputs; they exist to measure the tensor cores' accumulation width. */
 int ptc_set_tuning(const char *key, int64_t value);

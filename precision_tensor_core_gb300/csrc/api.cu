@@ -39,8 +39,9 @@ std::atomic<int> g_chunk_s8{16};  // 1024 K values: |partial| <= 1024 * 2^14 = 2
 std::atomic<int> g_chunk_s4{64};  // 8192 K values: |partial| <= 8192 * 2^6  = 2^19
 std::atomic<int> g_group_m{8};
 std::atomic<int> g_l2_hint{0};
-std::atomic<int> g_prefetch_kb{0};
-std::atomic<int> g_cta_pair{0};   // 0: by problem size, 1: one CTA per tile, 2: CTA pairs
+std::atomic<int> g_cta_pair{0};     // 0: by problem size, 1: one CTA per tile, 2: CTA pairs
+std::atomic<int> g_tail_split{1};   // 1: split a short last wave in K
+std::atomic<int> g_split_min_kb{64};
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 std::atomic<int64_t> g_stall_tile{-1};
 
@@ -210,7 +211,8 @@ GemmArgs base_args(int64_t M, int64_t N, int64_t K, int k_elems_per_block, void 
     a.group_m = g_group_m.load() > 0 ? g_group_m.load() : 1;
     a.stall_tile = int(g_stall_tile.exchange(-1));
     a.l2_hint = g_l2_hint.load();
-    a.prefetch_kb = g_prefetch_kb.load();
+    a.split_ok = g_tail_split.load();
+    a.split_min_kb = g_split_min_kb.load();
     a.wait_limit_ns = g_wait_ns.load();
     return a;
 }
@@ -218,7 +220,7 @@ GemmArgs base_args(int64_t M, int64_t N, int64_t K, int k_elems_per_block, void 
 int launch_gemm_checked(Kind kind, bool b_mn, int epi, int ctas, const CUtensorMap &ta,
                         const CUtensorMap &tb, const GemmArgs &args, const DevInfo &d,
                         cudaStream_t stream) {
-    cudaError_t e = ptc::launch_gemm(kind, b_mn, epi, ctas, ta, tb, args, d.sms, stream);
+    cudaError_t e = ptc::launch_gemm(kind, b_mn, epi, ctas, ta, tb, args, d.sms, d.pool_ok ? d.pool : nullptr, stream);
     if (e != cudaSuccess) return fail_cuda(e, "GEMM kernel launch");
     g_launches.fetch_add(1);
     return PTC_OK;
@@ -755,12 +757,16 @@ int ptc_set_tuning(const char *key, int64_t value) {
         g_group_m.store(int(value));
         return PTC_OK;
     }
-    if (std::strcmp(key, "prefetch_kb") == 0 && value >= 0 && value <= 1024) {
-        g_prefetch_kb.store(int(value));
-        return PTC_OK;
-    }
     if (std::strcmp(key, "l2_hint") == 0 && value >= 0 && value <= 3) {
         g_l2_hint.store(int(value));
+        return PTC_OK;
+    }
+    if (std::strcmp(key, "tail_split") == 0 && (value == 0 || value == 1)) {
+        g_tail_split.store(int(value));
+        return PTC_OK;
+    }
+    if (std::strcmp(key, "split_min_kb") == 0 && value >= 2 && value <= (1 << 20)) {
+        g_split_min_kb.store(int(value));
         return PTC_OK;
     }
     if (std::strcmp(key, "cta_pair") == 0 && value >= 0 && value <= 2) {

@@ -194,12 +194,11 @@ extern "C" int gemm_s8_noalloc(int64_t M, int64_t N, int64_t K, const int8_t *A,
     args.group_m = kGroupM;
     args.stall_tile = -1;
     args.l2_hint = 0;
-    args.prefetch_kb = 0;
     args.out_mode = ptc::OUT_S32;
     args.scale_a = nullptr;
     args.scale_b = nullptr;
     args.wait_limit_ns = kWaitNs;
-    if ((e = ptc::launch_gemm(ptc::Kind::F16, false, ptc::EPI_INT, 1, ta, tb, args, d->sms, s)) != cudaSuccess) {
+    if ((e = ptc::launch_gemm(ptc::Kind::F16, false, ptc::EPI_INT, 1, ta, tb, args, d->sms, nullptr, s)) != cudaSuccess) {
         cudaGetLastError();
         return reject(PTC_ERR_LAUNCH, cudaGetErrorString(e));
     }

@@ -100,6 +100,82 @@ __device__ __forceinline__ void tile_coords(int t, const GemmArgs &a, int &mb, i
     nb = r / gsz;
 }
 
+// Entry v of the launch's work list: whole tiles in raster order, then, when
+// the last wave would leave at least half of the clusters idle, each of its
+// tiles as two units over the two halves of the K range.  Both halves feed the
+// tensor cores at the rate of a whole tile; the epilogue warp that finishes
+// second adds the other half's partial sums (no waiting on either side).
+struct WorkRef {
+    int mb, nb;    // tile coordinates in units of (kBM * CTAS) x kBN
+    int kb0, kb1;  // K blocks of this unit
+    int part;      // 0: whole tile; 1, 2: first / second K half of split tile `slot`
+    int slot;
+};
+
+__device__ __forceinline__ WorkRef work_unit(int v, const GemmArgs &a) {
+    const int full = a.num_tiles - a.tail_split;
+    WorkRef r;
+    if (v < full) {
+        tile_coords(v, a, r.mb, r.nb);
+        r.kb0 = 0;
+        r.kb1 = a.num_kb;
+        r.part = 0;
+        r.slot = 0;
+    } else {
+        const int u = v - full;
+        r.slot = u >> 1;
+        tile_coords(full + r.slot, a, r.mb, r.nb);
+        const int mid = a.num_kb >> 1;
+        r.part = 1 + (u & 1);
+        r.kb0 = (u & 1) ? mid : 0;
+        r.kb1 = (u & 1) ? a.num_kb : mid;
+    }
+    return r;
+}
+
+// Partial sums of one epilogue warp's 32 x 128 slice of a split tile, stored
+// as float4 [column / 4][lane] so that each warp-wide 16-byte access covers
+// 512 contiguous bytes.  Integer partials are stored by bit pattern.
+constexpr int kSliceWords = 32 * (kBN / 2);
+
+__device__ __forceinline__ float4 *split_partial(const GemmArgs &a, int slice, int half) {
+    return reinterpret_cast<float4 *>(a.split_part + size_t(slice * 2 + half) * kSliceWords);
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
+// True when the other half of this slice has already published its partial
+// sums (then this warp completes the tile without publishing its own).
+__device__ __forceinline__ bool split_other_done(const uint32_t *cnt, int lane) {
+    uint32_t v = 0;
+    if (lane == 0) v = ld_acquire_gpu(cnt);
+    v = __shfl_sync(0xffffffffu, v, 0);
+    __threadfence();
+    return v != 0;
+}
+
+// Publish this warp's partial sums (already stored by every lane); true when
+// the other half had published first, so that this warp completes the tile.
+__device__ __forceinline__ bool split_publish(uint32_t *cnt, int lane) {
+    __threadfence();
+    __syncwarp();
+    uint32_t old = 0;
+    if (lane == 0) old = atom_add_acq_rel_gpu(cnt, 1u);
+    old = __shfl_sync(0xffffffffu, old, 0);
+    __threadfence();
+    return old != 0;
+}
+
 // Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, AbortState *ab,
                                           uint64_t limit, int lane) {
@@ -182,6 +258,79 @@ __device__ __forceinline__ void store_scaled_row(const GemmArgs &args, int row, 
     }
 }
 
+// 32 FP16 accumulators (the low half of each 32-bit tensor-memory column) to
+// dst[0 .. valid), valid capped at 32.
+__device__ __forceinline__ void store_f16acc_32(uint16_t *dst, const uint32_t (&r)[32], int valid) {
+    if (valid >= 32) {
+        uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            d[i] = make_uint4((r[8 * i] & 0xFFFFu) | (r[8 * i + 1] << 16), (r[8 * i + 2] & 0xFFFFu) | (r[8 * i + 3] << 16),
+                              (r[8 * i + 4] & 0xFFFFu) | (r[8 * i + 5] << 16), (r[8 * i + 6] & 0xFFFFu) | (r[8 * i + 7] << 16));
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            if (j < valid) dst[j] = static_cast<uint16_t>(r[j]);
+    }
+}
+
+// Epilogue of one K half of a split tile (FP32 or FP16 accumulators), for
+// this warp's 32 x 128 slice at tensor-memory address t_acc: publish the
+// partial sums (to `mine`), or, when the other half has published first, add
+// its partial sums (`other`; in FP32, the same bits whichever half adds) and
+// store C.  crow points at C[row][col0] (null when row >= M); `valid` is the
+// number of columns of the slice below N.  Scalars only, so that the call
+// keeps the kernel's parameters out of local memory.
+template <int EPI>
+__device__ __noinline__ void split_epilogue(uint32_t t_acc, uint32_t *cnt, float4 *mine, const float4 *other,
+                                            void *crow, int valid, int lane) {
+    bool finish = split_other_done(cnt, lane);
+    if (!finish) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+            uint32_t r[32];
+            tmem_ld_32cols(t_acc + uint32_t(32 * c), r);
+            tmem_ld_wait();
+            float f[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                f[j] = (EPI == EPI_F16ACC) ? __half2float(__ushort_as_half(static_cast<uint16_t>(r[j]))) : __uint_as_float(r[j]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                mine[(8 * c + i) * 32 + lane] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+        }
+        finish = split_publish(cnt, lane);
+    }
+    if (!finish) return;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tmem_ld_32cols(t_acc + uint32_t(32 * c), r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float4 o = __ldcg(other + (8 * c + i) * 32 + lane);
+            const float ov[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int j = 4 * i + e;
+                if constexpr (EPI == EPI_F16ACC)
+                    r[j] = __half_as_ushort(
+                        __float2half_rn(__fadd_rn(__half2float(__ushort_as_half(static_cast<uint16_t>(r[j]))), ov[e])));
+                else
+                    r[j] = __float_as_uint(__fadd_rn(__uint_as_float(r[j]), ov[e]));
+            }
+        }
+        const int v = valid - 32 * c;
+        if (crow != nullptr && v > 0) {
+            if constexpr (EPI == EPI_F16ACC)
+                store_f16acc_32(static_cast<uint16_t *>(crow) + 32 * c, r, v);
+            else
+                store_32(static_cast<float *>(crow) + 32 * c, r, v);
+        }
+    }
+}
+
 // CTA r of a pair owns rows 128 r .. 128 r + 127 of the 256 x 256 tile and
 // stages B rows 128 r .. 128 r + 127.  The even CTA issues the MMAs for both;
 // its full barriers collect both CTAs' copies, its commits arrive on both
@@ -237,7 +386,6 @@ __global__ void __launch_bounds__(THREADS, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = st->tmem_base;
 
-    const int nchunks = (args.num_kb + args.kb_per_chunk - 1) / args.kb_per_chunk;
     constexpr int K_ELEMS = (KIND == Kind::F16) ? kRowBytes / 2 : kRowBytes;
 
     if (warp == 0) {
@@ -255,38 +403,17 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t ph = 0;
             uint32_t outstanding = 0, out_phase = 0;  // per-stage bits of issued copies
             bool ok = true;
-            int seq = 0;  // position in this CTA's sequence of (tile, K block) loads
-            for (int t = cluster; t < args.num_tiles && ok; t += nclusters) {
-                int mb, nb;
-                tile_coords(t, args, mb, nb);
-                const int m0 = mb * (kBM * CTAS) + int(rank) * kBM;
-                const int n0 = nb * kBN + int(rank) * C_::B_ROWS;
-                for (int kb = 0; kb < args.num_kb; ++kb, ++seq) {
-                    if (args.prefetch_kb > 0) {
-                        // Warm L2 with the operands this CTA loads prefetch_kb K blocks later.
-                        const int p = seq + args.prefetch_kb;
-                        const int lt = p / args.num_kb, kbp = p - lt * args.num_kb;
-                        const int tp = cluster + lt * nclusters;
-                        if (tp < args.num_tiles) {
-                            int mbp, nbp;
-                            tile_coords(tp, args, mbp, nbp);
-                            tma_prefetch_2d(&tmA, kbp * K_ELEMS, mbp * (kBM * CTAS) + int(rank) * kBM);
-                            const int n0p = nbp * kBN + int(rank) * C_::B_ROWS;
-                            if constexpr (B_MN) {
-#pragma unroll
-                                for (int i = 0; i < C_::B_ROWS / 64; ++i)
-                                    tma_prefetch_2d(&tmB, n0p + 64 * i, kbp * K_ELEMS);
-                            } else {
-                                tma_prefetch_2d(&tmB, kbp * K_ELEMS, n0p);
-                            }
-                        }
-                    }
+            for (int t = cluster; t < args.num_vunits && ok; t += nclusters) {
+                const WorkRef wr = work_unit(t, args);
+                const int m0 = wr.mb * (kBM * CTAS) + int(rank) * kBM;
+                const int n0 = wr.nb * kBN + int(rank) * C_::B_ROWS;
+                for (int kb = wr.kb0; kb < wr.kb1; ++kb) {
                     if (!mbar_wait(&st->empty[s], ph ^ 1u, &st->abort, &g_error_word, limit)) {
                         ok = false;
                         break;
                     }
                     outstanding &= ~(1u << s);
-                    const bool stall = (t == args.stall_tile && kb == 0 && rank == 0);
+                    const bool stall = (t == args.stall_tile && kb == wr.kb0 && rank == 0);
                     if (!stall) {
                         uint8_t *a_dst = a_ring + s * C_::A_STAGE;
                         uint8_t *b_dst = b_ring + s * C_::B_STAGE;
@@ -360,7 +487,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             int abuf = 0;
             uint32_t aph = 0;
             bool ok = true;
-            for (int t = cluster; t < args.num_tiles && ok; t += nclusters) {
+            for (int t = cluster; t < args.num_vunits && ok; t += nclusters) {
+                const WorkRef wr = work_unit(t, args);
+                const int nchunks = (wr.kb1 - wr.kb0 + args.kb_per_chunk - 1) / args.kb_per_chunk;
                 for (int ch = 0; ch < nchunks && ok; ++ch) {
                     if (!mbar_wait(&st->acc_empty[abuf], aph ^ 1u, &st->abort, &g_error_word, limit)) {
                         ok = false;
@@ -368,8 +497,8 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     tc_fence_after_sync();
                     const uint32_t d_tmem = tmem_base + uint32_t(abuf * kBN);
-                    const int kb0 = ch * args.kb_per_chunk;
-                    const int kb1 = min(args.num_kb, kb0 + args.kb_per_chunk);
+                    const int kb0 = wr.kb0 + ch * args.kb_per_chunk;
+                    const int kb1 = min(wr.kb1, kb0 + args.kb_per_chunk);
                     for (int kb = kb0; kb < kb1; ++kb) {
                         if (!mbar_wait(&st->full[s], ph, &st->abort, &g_error_word, limit)) {
                             ok = false;
@@ -422,23 +551,28 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int h = (warp - 2) >> 2;      // column half of the tile
         const uint32_t t_lane = tmem_base + (uint32_t(32 * q) << 16) + uint32_t(h * (kBN / 2));
         // Accumulator buffers are released on the issuing (even) CTA's barriers.
-        uint32_t release0 = 0u, release1 = 0u;
-        if constexpr (CTAS == 2) {
-            release0 = mapa_shared(smem_u32(&st->acc_empty[0]), 0);
-            release1 = mapa_shared(smem_u32(&st->acc_empty[1]), 0);
-        }
+        auto release = [&](int b) {
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (CTAS == 1)
+                    mbar_arrive(&st->acc_empty[b]);
+                else
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&st->acc_empty[b]), 0));
+            }
+        };
         int abuf = 0;
         uint32_t aph = 0;
         bool ok = true;
-        for (int t = cluster; t < args.num_tiles && ok; t += nclusters) {
-            int mb, nb;
-            tile_coords(t, args, mb, nb);
-            const int row = mb * (kBM * CTAS) + int(rank) * kBM + 32 * q + lane;
-            const int col0 = nb * kBN + h * (kBN / 2);
+        for (int t = cluster; t < args.num_vunits && ok; t += nclusters) {
+            const WorkRef wr = work_unit(t, args);
+            const int row = wr.mb * (kBM * CTAS) + int(rank) * kBM + 32 * q + lane;
+            const int col0 = wr.nb * kBN + h * (kBN / 2);
             if constexpr (INT_OUT) {
                 int32_t acc[kBN / 2];
 #pragma unroll
                 for (int j = 0; j < kBN / 2; ++j) acc[j] = 0;
+                const int nchunks = (wr.kb1 - wr.kb0 + args.kb_per_chunk - 1) / args.kb_per_chunk;
                 for (int ch = 0; ch < nchunks; ++ch) {
                     if (!warp_wait(&st->acc_full[abuf], aph, &st->abort, limit, lane)) {
                         ok = false;
@@ -453,20 +587,37 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
                         for (int j = 0; j < 16; ++j) acc[16 * c + j] += __float2int_rn(__uint_as_float(r[j]));
                     }
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if constexpr (CTAS == 1)
-                            mbar_arrive(&st->acc_empty[abuf]);
-                        else
-                            mbar_arrive_cluster(abuf ? release1 : release0);
-                    }
+                    release(abuf);
                     if (++abuf == 2) {
                         abuf = 0;
                         aph ^= 1u;
                     }
                 }
                 if (!ok) break;
+                if (wr.part != 0) {
+                    // Sum of the two K halves, wrapping like every int32 partial sum.
+                    const int slice = ((wr.slot * CTAS + int(rank)) * 4 + q) * 2 + h;
+                    uint32_t *cnt = args.split_count + slice;
+                    bool finish = split_other_done(cnt, lane);
+                    if (!finish) {
+                        float4 *mine = split_partial(args, slice, wr.part - 1);
+#pragma unroll
+                        for (int i = 0; i < kBN / 8; ++i)
+                            mine[i * 32 + lane] = make_float4(__int_as_float(acc[4 * i]), __int_as_float(acc[4 * i + 1]),
+                                                              __int_as_float(acc[4 * i + 2]), __int_as_float(acc[4 * i + 3]));
+                        finish = split_publish(cnt, lane);
+                    }
+                    if (!finish) continue;
+                    const float4 *other = split_partial(args, slice, 2 - wr.part);
+#pragma unroll
+                    for (int i = 0; i < kBN / 8; ++i) {
+                        const float4 o = __ldcg(other + i * 32 + lane);
+                        acc[4 * i] = int32_t(uint32_t(acc[4 * i]) + uint32_t(__float_as_int(o.x)));
+                        acc[4 * i + 1] = int32_t(uint32_t(acc[4 * i + 1]) + uint32_t(__float_as_int(o.y)));
+                        acc[4 * i + 2] = int32_t(uint32_t(acc[4 * i + 2]) + uint32_t(__float_as_int(o.z)));
+                        acc[4 * i + 3] = int32_t(uint32_t(acc[4 * i + 3]) + uint32_t(__float_as_int(o.w)));
+                    }
+                }
                 if (row < args.M) {
                     if (args.out_mode == OUT_S32) {
                         int32_t *crow = reinterpret_cast<int32_t *>(args.C) + int64_t(row) * args.ldc;
@@ -488,44 +639,33 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                float *crow = reinterpret_cast<float *>(args.C) + int64_t(row) * args.ldc;
+                if (wr.part == 0) {
+                    float *crow = reinterpret_cast<float *>(args.C) + int64_t(row) * args.ldc;
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint32_t r[32];
-                    tmem_ld_32cols(t_lane + uint32_t(abuf * kBN + 32 * c), r);
-                    tmem_ld_wait();
-                    const int cc = col0 + 32 * c;
-                    if constexpr (EPI == EPI_F16ACC) {
-                        // An FP16 accumulator occupies the low half of its 32-bit column.
-                        if (row < args.M && cc < args.N) {
-                            uint16_t *dst = reinterpret_cast<uint16_t *>(args.C) + int64_t(row) * args.ldc + cc;
-                            const int valid = min(32, args.N - cc);
-                            if (valid == 32) {
-                                uint4 *d = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-                                for (int i = 0; i < 4; ++i)
-                                    d[i] = make_uint4((r[8 * i] & 0xFFFFu) | (r[8 * i + 1] << 16),
-                                                      (r[8 * i + 2] & 0xFFFFu) | (r[8 * i + 3] << 16),
-                                                      (r[8 * i + 4] & 0xFFFFu) | (r[8 * i + 5] << 16),
-                                                      (r[8 * i + 6] & 0xFFFFu) | (r[8 * i + 7] << 16));
-                            } else {
-#pragma unroll
-                                for (int j = 0; j < 32; ++j)
-                                    if (j < valid) dst[j] = static_cast<uint16_t>(r[j]);
-                            }
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t r[32];
+                        tmem_ld_32cols(t_lane + uint32_t(abuf * kBN + 32 * c), r);
+                        tmem_ld_wait();
+                        const int cc = col0 + 32 * c;
+                        if constexpr (EPI == EPI_F16ACC) {
+                            if (row < args.M && cc < args.N)
+                                store_f16acc_32(reinterpret_cast<uint16_t *>(args.C) + int64_t(row) * args.ldc + cc, r,
+                                                args.N - cc);
+                        } else {
+                            if (row < args.M && cc < args.N) store_32(crow + cc, r, args.N - cc);
                         }
-                    } else {
-                        if (row < args.M && cc < args.N) store_32(crow + cc, r, args.N - cc);
                     }
+                } else {
+                    const int slice = ((wr.slot * CTAS + int(rank)) * 4 + q) * 2 + h;
+                    void *crow = nullptr;
+                    if (row < args.M)
+                        crow = static_cast<uint8_t *>(args.C) +
+                               (int64_t(row) * args.ldc + col0) * (EPI == EPI_F16ACC ? 2 : 4);
+                    split_epilogue<EPI>(t_lane + uint32_t(abuf * kBN), args.split_count + slice,
+                                        split_partial(args, slice, wr.part - 1), split_partial(args, slice, 2 - wr.part),
+                                        crow, args.N - col0, lane);
                 }
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) {
-                    if constexpr (CTAS == 1)
-                        mbar_arrive(&st->acc_empty[abuf]);
-                    else
-                        mbar_arrive_cluster(abuf ? release1 : release0);
-                }
+                release(abuf);
                 if (++abuf == 2) {
                     abuf = 0;
                     aph ^= 1u;
@@ -560,7 +700,7 @@ struct LaunchCache {
 
 template <Kind KIND, bool B_MN, int EPI, int CTAS>
 cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args,
-                       int sms, cudaStream_t stream) {
+                       int sms, cudaMemPool_t pool, cudaStream_t stream) {
     auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS>;
     constexpr size_t SMEM = smem_bytes<CTAS>();
     static thread_local LaunchCache cache;  // per device (re-queried when it changes)
@@ -597,9 +737,44 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
         cache.max_clusters = clusters;
         cache.dev = dev;
     }
-    const int clusters = args.num_tiles < cache.max_clusters ? args.num_tiles : cache.max_clusters;
+    // Work list: split the last wave's tiles in K when they fill at most half
+    // of the clusters (a lone partial wave included).  The halves exchange
+    // partial sums through a stream-ordered workspace from `pool`: a counter
+    // per epilogue warp slice (zeroed here) and two slices of partial sums.
+    GemmArgs a = args;
+    const int maxc = cache.max_clusters;
+    const int tail = a.num_tiles < maxc ? a.num_tiles : a.num_tiles % maxc;
+    a.tail_split = 0;
+    a.split_count = nullptr;
+    a.split_part = nullptr;
+    void *ws = nullptr;
+    // The split saves about half of a tile's K loop (~0.14 us per K block);
+    // setting up the exchange costs ~6 us per call, so short K (below
+    // split_min_kb blocks, 64 by default) runs whole.
+    if (pool != nullptr && a.split_ok && a.num_kb >= 2 && a.num_kb >= a.split_min_kb && tail > 0 &&
+        2 * tail <= maxc) {
+        const size_t slices = size_t(tail) * CTAS * EPI_WARPS;
+        const size_t count_bytes = (slices * sizeof(uint32_t) + 255) / 256 * 256;
+        const size_t bytes = count_bytes + slices * 2 * kSliceWords * sizeof(float);
+        if (cudaMallocFromPoolAsync(&ws, bytes, pool, stream) == cudaSuccess) {
+            e = cudaMemsetAsync(ws, 0, count_bytes, stream);
+            if (e != cudaSuccess) {
+                cudaFreeAsync(ws, stream);
+                return e;
+            }
+            a.tail_split = tail;
+            a.split_count = static_cast<uint32_t *>(ws);
+            a.split_part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + count_bytes);
+        } else {
+            cudaGetLastError();  // no workspace: run the tail whole
+            ws = nullptr;
+        }
+    }
+    a.num_vunits = a.num_tiles + a.tail_split;
+    const int clusters = a.num_vunits < maxc ? a.num_vunits : maxc;
     cfg.gridDim = dim3(CTAS * clusters, 1, 1);
-    e = cudaLaunchKernelEx(&cfg, fn, ta, tb, args);
+    e = cudaLaunchKernelEx(&cfg, fn, ta, tb, a);
+    if (ws != nullptr) cudaFreeAsync(ws, stream);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -609,11 +784,11 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
 size_t gemm_smem_bytes(int ctas) { return ctas == 2 ? smem_bytes<2>() : smem_bytes<1>(); }
 
 cudaError_t launch_gemm(Kind kind, bool b_mn_major, int epi, int ctas, const CUtensorMap &ta,
-                        const CUtensorMap &tb, const GemmArgs &args, int sms,
+                        const CUtensorMap &tb, const GemmArgs &args, int sms, cudaMemPool_t pool,
                         cudaStream_t stream) {
-#define PTC_LAUNCH(K, BMN, E)                                              \
-    return ctas == 2 ? launch_one<K, BMN, E, 2>(ta, tb, args, sms, stream) \
-                     : launch_one<K, BMN, E, 1>(ta, tb, args, sms, stream)
+#define PTC_LAUNCH(K, BMN, E)                                                    \
+    return ctas == 2 ? launch_one<K, BMN, E, 2>(ta, tb, args, sms, pool, stream) \
+                     : launch_one<K, BMN, E, 1>(ta, tb, args, sms, pool, stream)
     if (kind == Kind::F16 && b_mn_major && epi == EPI_F32) PTC_LAUNCH(Kind::F16, true, EPI_F32);
     if (kind == Kind::F16 && b_mn_major && epi == EPI_F16ACC) PTC_LAUNCH(Kind::F16, true, EPI_F16ACC);
     if (kind == Kind::F16 && !b_mn_major && epi == EPI_INT) PTC_LAUNCH(Kind::F16, false, EPI_INT);

@@ -29,10 +29,19 @@ struct GemmArgs {
                            // epilogue folds the partial sum into int32 registers
     int group_m;           // tiles of M per raster group (L2 reuse)
     int stall_tile;        // test hook: withhold this tile's operands (-1: none)
-    int prefetch_kb;       // L2 prefetch distance in K blocks ahead of the loads (0: off)
     int l2_hint;           // L2 policy of operand loads: 0 none, 1 A evict-last and
                            // B evict-first, 2 A evict-last, 3 both evict-normal
     uint64_t wait_limit_ns;
+    // Work list of the launch (set by launch_gemm): the last tail_split tiles
+    // run as two units each over the two halves of K, num_vunits units in all;
+    // the halves exchange partial sums through split_part, ordered by the
+    // arrival counters split_count (zero at launch).
+    int split_ok;          // 1: the tail may be split (tuning knob "tail_split")
+    int split_min_kb;      // ... when K spans at least this many K blocks
+    int tail_split;
+    int num_vunits;
+    uint32_t *split_count;
+    float *split_part;
     // Integer routes only: output of the epilogue.
     int out_mode;          // OUT_S32, or OUT_F32 / OUT_BF16 / OUT_F16 (scaled)
     const float *scale_a;  // M row scales (scaled modes; NULL: 1)
@@ -61,8 +70,11 @@ enum Epi : int {
 //   E4M3 + B K-major  + EPI_INT:     gemm_s4 (operands converted s4 -> e4m3)
 // args.tiles_m counts tiles of kBM * ctas rows.  The tensor map of A has boxes
 // of kBM rows; that of B boxes of kBN / ctas rows (K-major) or 64 x 64 (MN-major).
+// With a non-null pool (and args.split_ok) a short last wave is split in K,
+// using a workspace of at most ~20 MB taken from the pool on `stream` and
+// returned after the kernel; a null pool runs every tile whole.
 cudaError_t launch_gemm(Kind kind, bool b_mn_major, int epi, int ctas, const CUtensorMap &ta,
-                        const CUtensorMap &tb, const GemmArgs &args, int sms,
+                        const CUtensorMap &tb, const GemmArgs &args, int sms, cudaMemPool_t pool,
                         cudaStream_t stream);
 
 // C[M x N] = 0 for elements of esize (2 or 4) bytes, ldc in elements.

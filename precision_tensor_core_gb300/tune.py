@@ -10,7 +10,7 @@ its precision, and over the FP16 WMMA kernel.
 `variants` times gemm_f16_f16acc against gemm_f16, and gemm_s8_scaled /
 gemm_s4_scaled (each output type) against gemm_s8 / gemm_s4, at one size.
 `knobs` times gemm_f16 / gemm_s8 / gemm_s4 at one size under each setting of
-the library's tuning knobs (ptc_set_tuning: CTA pairs, raster group, L2
+the library's tuning knobs (ptc_set_tuning: CTA pairs, tail split, raster group, L2
 eviction policy, INT fold length), one knob at a time from the defaults: the
 ablation that shows the defaults are a local optimum.  `sizes` times the three
 entry points at each size with the library defaults.
@@ -34,10 +34,10 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-DEFAULTS = {"cta_pair": 0, "group_m": 8, "l2_hint": 0, "prefetch_kb": 0, "s8_chunk_kb": 16,
-            "s4_chunk_kb": 64}
-KNOBS = {"cta_pair": [1, 2], "group_m": [4, 16, 32], "l2_hint": [1, 2, 3],
-         "prefetch_kb": [4, 8, 16, 32], "s8_chunk_kb": [4, 8], "s4_chunk_kb": [2, 8, 16, 128]}
+DEFAULTS = {"cta_pair": 0, "group_m": 8, "l2_hint": 0, "s8_chunk_kb": 16,
+            "s4_chunk_kb": 64, "tail_split": 1, "split_min_kb": 64}
+KNOBS = {"cta_pair": [1, 2], "tail_split": [0], "split_min_kb": [16, 32], "group_m": [4, 16, 32], "l2_hint": [1, 2, 3],
+         "s8_chunk_kb": [4, 8], "s4_chunk_kb": [2, 8, 16, 128]}
 
 
 def main():
