@@ -39,60 +39,6 @@ __device__ __forceinline__ uint16_t s8_to_f16_bits(int8_t v) {
     return __half_as_ushort(__int2half_rn(static_cast<int>(v)));
 }
 
-// Converts rows [0, rows_a) of A and then rows [0, rows_b) of B, cols
-// elements each, in one grid-stride pass over (row, 16-element vector) pairs.
-// Each thread takes UNROLL vectors per pass and issues all their loads before
-// converting, so that several 16-byte loads per thread are in flight.
-constexpr int UNROLL = 4;
-
-__global__ void s8_to_f16_kernel(const int8_t *__restrict__ src_a, int64_t lds_a, int rows_a,
-                                 const int8_t *__restrict__ src_b, int64_t lds_b, int rows_b,
-                                 int cols, uint16_t *__restrict__ dst_a, uint16_t *__restrict__ dst_b,
-                                 int64_t ldd) {
-    const int vpr = (cols + 15) / 16;  // 16-element vectors per row
-    const int64_t total = int64_t(rows_a + rows_b) * vpr;
-    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-    for (int64_t base = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; base < total;
-         base += stride * UNROLL) {
-        uint4 x[UNROLL];
-        const int8_t *s[UNROLL];
-        uint16_t *d[UNROLL];
-        int c0[UNROLL];
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            const int64_t i = base + u * stride;
-            s[u] = nullptr;
-            if (i >= total) continue;
-            int64_t r = i / vpr;
-            c0[u] = int(i - r * vpr) * 16;
-            if (r < rows_a) {
-                s[u] = src_a + r * lds_a + c0[u];
-                d[u] = dst_a + r * ldd + c0[u];
-            } else {
-                r -= rows_a;
-                s[u] = src_b + r * lds_b + c0[u];
-                d[u] = dst_b + r * ldd + c0[u];
-            }
-            if (c0[u] + 16 <= cols) x[u] = __ldcs(reinterpret_cast<const uint4 *>(s[u]));
-        }
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            if (s[u] == nullptr) continue;
-            if (c0[u] + 16 <= cols) {
-                uint4 o0, o1;
-                s8x4_to_f16x4(x[u].x, o0.x, o0.y);
-                s8x4_to_f16x4(x[u].y, o0.z, o0.w);
-                s8x4_to_f16x4(x[u].z, o1.x, o1.y);
-                s8x4_to_f16x4(x[u].w, o1.z, o1.w);
-                reinterpret_cast<uint4 *>(d[u])[0] = o0;
-                reinterpret_cast<uint4 *>(d[u])[1] = o1;
-            } else {
-                for (int j = 0; j < cols - c0[u]; ++j) d[u][j] = s8_to_f16_bits(s[u][j]);
-            }
-        }
-    }
-}
-
 // ---------------------------------------------------------------- s4 -> e4m3
 // E4M3 (sign, 4 exponent bits with bias 7, 3 fraction bits) encoding of a
 // small integer, from the format's definition: |v| = 2^e * (1 + f/8).
@@ -136,79 +82,127 @@ __device__ __forceinline__ uint8_t s4_to_e4m3_byte(uint32_t nib) {
     return static_cast<uint8_t>(s4x4_to_e4m3x4(nib & 0xFu) & 0xFFu);
 }
 
-// As s8_to_f16_kernel: rows of A, then rows of B, 32-element vectors.
-__global__ void s4_to_e4m3_kernel(const uint8_t *__restrict__ src_a, int64_t lds_a, int rows_a,
-                                  const uint8_t *__restrict__ src_b, int64_t lds_b, int rows_b,
-                                  int cols, uint8_t *__restrict__ dst_a, uint8_t *__restrict__ dst_b,
-                                  int64_t ldd) {
-    const int vpr = (cols + 31) / 32;  // 32-element (16-byte packed) vectors per row
-    const int64_t total = int64_t(rows_a + rows_b) * vpr;
-    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
-    for (int64_t base = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; base < total;
-         base += stride * UNROLL) {
-        uint4 x[UNROLL];
-        const uint8_t *s[UNROLL];
-        uint8_t *d[UNROLL];
-        int c0[UNROLL];
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            const int64_t i = base + u * stride;
-            s[u] = nullptr;
-            if (i >= total) continue;
-            int64_t r = i / vpr;
-            c0[u] = int(i - r * vpr) * 32;
-            if (r < rows_a) {
-                s[u] = src_a + r * lds_a + c0[u] / 2;
-                d[u] = dst_a + r * ldd + c0[u];
-            } else {
-                r -= rows_a;
-                s[u] = src_b + r * lds_b + c0[u] / 2;
-                d[u] = dst_b + r * ldd + c0[u];
-            }
-            if (c0[u] + 32 <= cols) x[u] = __ldcs(reinterpret_cast<const uint4 *>(s[u]));
+// The two conversions, as element types, 16-byte input vectors and a
+// vector / scalar conversion.
+struct S8ToF16 {
+    using In = int8_t;
+    using Out = uint16_t;
+    static constexpr int VEC = 16;  // elements per 16-byte input vector (32 output bytes)
+    __device__ static const uint8_t *row_at(const uint8_t *row, int c0) { return row + c0; }
+    __device__ static void vector(const uint4 &x, uint4 &o0, uint4 &o1) {
+        s8x4_to_f16x4(x.x, o0.x, o0.y);
+        s8x4_to_f16x4(x.y, o0.z, o0.w);
+        s8x4_to_f16x4(x.z, o1.x, o1.y);
+        s8x4_to_f16x4(x.w, o1.z, o1.w);
+    }
+    __device__ static void scalar(const uint8_t *s, Out *d, int n) {
+        for (int j = 0; j < n; ++j) d[j] = s8_to_f16_bits(static_cast<int8_t>(s[j]));
+    }
+};
+
+struct S4ToE4M3 {
+    using Out = uint8_t;
+    static constexpr int VEC = 32;  // packed: 32 elements per 16-byte input vector (32 output bytes)
+    __device__ static const uint8_t *row_at(const uint8_t *row, int c0) { return row + c0 / 2; }
+    __device__ static void vector(const uint4 &x, uint4 &o0, uint4 &o1) {
+        o0 = make_uint4(s4x4_to_e4m3x4(x.x & 0xFFFFu), s4x4_to_e4m3x4(x.x >> 16), s4x4_to_e4m3x4(x.y & 0xFFFFu),
+                        s4x4_to_e4m3x4(x.y >> 16));
+        o1 = make_uint4(s4x4_to_e4m3x4(x.z & 0xFFFFu), s4x4_to_e4m3x4(x.z >> 16), s4x4_to_e4m3x4(x.w & 0xFFFFu),
+                        s4x4_to_e4m3x4(x.w >> 16));
+    }
+    __device__ static void scalar(const uint8_t *s, Out *d, int n) {
+        for (int j = 0; j < n; ++j) {
+            const uint32_t b = s[j >> 1];
+            d[j] = s4_to_e4m3_byte((j & 1) ? (b >> 4) : b);
         }
+    }
+};
+
+// Converts rows [0, rows_a) of A and then rows [0, rows_b) of B, cols
+// elements each (source pitches in bytes, destination pitch in elements).
+// A group of 2^tpr_log2 threads covers one row; a 256-thread block covers
+// 256 >> tpr_log2 rows per pass and strides over rows by the grid, so the
+// row and vector of a thread come from a shift and a mask, not a division.
+// Each thread issues UNROLL 16-byte loads (vectors lane, lane + group, ...)
+// before converting them; the ragged end of a row is converted element by
+// element, so no byte past a row's last element is read.
+constexpr int UNROLL = 4;
+
+template <class Op>
+__global__ void __launch_bounds__(256) convert_kernel(const uint8_t *__restrict__ src_a, int64_t lds_a, int rows_a,
+                                                      const uint8_t *__restrict__ src_b, int64_t lds_b, int rows_b,
+                                                      int cols, typename Op::Out *__restrict__ dst_a,
+                                                      typename Op::Out *__restrict__ dst_b, int64_t ldd, int tpr_log2) {
+    using Out = typename Op::Out;
+    const int tpr = 1 << tpr_log2;
+    const int lane = threadIdx.x & (tpr - 1);
+    const int rpb = blockDim.x >> tpr_log2;
+    const int vpr = (cols + Op::VEC - 1) / Op::VEC;
+    const int64_t rows = int64_t(rows_a) + rows_b;
+    for (int64_t r = int64_t(blockIdx.x) * rpb + (threadIdx.x >> tpr_log2); r < rows; r += int64_t(gridDim.x) * rpb) {
+        const uint8_t *srow;
+        Out *drow;
+        if (r < rows_a) {
+            srow = src_a + r * lds_a;
+            drow = dst_a + r * ldd;
+        } else {
+            srow = src_b + (r - rows_a) * lds_b;
+            drow = dst_b + (r - rows_a) * ldd;
+        }
+        for (int v0 = lane; v0 < vpr; v0 += tpr * UNROLL) {
+            uint4 x[UNROLL];
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            if (s[u] == nullptr) continue;
-            if (c0[u] + 32 <= cols) {
-                const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
-                uint32_t o[8];
+            for (int u = 0; u < UNROLL; ++u) {
+                const int c0 = (v0 + u * tpr) * Op::VEC;
+                if (c0 + Op::VEC <= cols) x[u] = __ldcs(reinterpret_cast<const uint4 *>(Op::row_at(srow, c0)));
+            }
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    o[2 * q] = s4x4_to_e4m3x4(w[q] & 0xFFFFu);
-                    o[2 * q + 1] = s4x4_to_e4m3x4(w[q] >> 16);
-                }
-                reinterpret_cast<uint4 *>(d[u])[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                reinterpret_cast<uint4 *>(d[u])[1] = make_uint4(o[4], o[5], o[6], o[7]);
-            } else {
-                for (int j = 0; j < cols - c0[u]; ++j) {
-                    const uint32_t b = s[u][j >> 1];
-                    d[u][j] = s4_to_e4m3_byte((j & 1) ? (b >> 4) : b);
+            for (int u = 0; u < UNROLL; ++u) {
+                const int c0 = (v0 + u * tpr) * Op::VEC;
+                if (c0 + Op::VEC <= cols) {
+                    uint4 o0, o1;
+                    Op::vector(x[u], o0, o1);
+                    uint4 *d = reinterpret_cast<uint4 *>(drow + c0);
+                    d[0] = o0;
+                    d[1] = o1;
+                } else if (c0 < cols) {
+                    Op::scalar(Op::row_at(srow, c0), drow + c0, cols - c0);
                 }
             }
         }
     }
 }
 
+// log2 of the threads per row: enough for one pass of UNROLL vectors per
+// thread over a row, at most the whole block.
+int threads_per_row_log2(int cols, int vec) {
+    const int vpr = (cols + vec - 1) / vec;
+    int l = 0;
+    while (l < 8 && (1 << l) * UNROLL < vpr) ++l;
+    return l;
+}
+
 }  // namespace
 
 cudaError_t launch_s8_to_f16(const int8_t *src, int64_t lds, int rows, int cols, uint16_t *dst,
                              int64_t ldd, int grid, cudaStream_t stream) {
-    s8_to_f16_kernel<<<grid, 256, 0, stream>>>(src, lds, rows, src, lds, 0, cols, dst, dst, ldd);
-    return cudaGetLastError();
+    return launch_s8_to_f16_pair(src, lds, rows, src, lds, 0, cols, dst, dst, ldd, grid, stream);
 }
 
 cudaError_t launch_s8_to_f16_pair(const int8_t *a, int64_t lda, int rows_a, const int8_t *b,
                                   int64_t ldb, int rows_b, int cols, uint16_t *dst_a, uint16_t *dst_b,
                                   int64_t ldd, int grid, cudaStream_t stream) {
-    s8_to_f16_kernel<<<grid, 256, 0, stream>>>(a, lda, rows_a, b, ldb, rows_b, cols, dst_a, dst_b, ldd);
+    convert_kernel<S8ToF16><<<grid, 256, 0, stream>>>(reinterpret_cast<const uint8_t *>(a), lda, rows_a,
+                                                      reinterpret_cast<const uint8_t *>(b), ldb, rows_b, cols, dst_a,
+                                                      dst_b, ldd, threads_per_row_log2(cols, S8ToF16::VEC));
     return cudaGetLastError();
 }
 
 cudaError_t launch_s4_to_e4m3_pair(const uint8_t *a, int64_t lda, int rows_a, const uint8_t *b,
                                    int64_t ldb, int rows_b, int cols, uint8_t *dst_a, uint8_t *dst_b,
                                    int64_t ldd, int grid, cudaStream_t stream) {
-    s4_to_e4m3_kernel<<<grid, 256, 0, stream>>>(a, lda, rows_a, b, ldb, rows_b, cols, dst_a, dst_b, ldd);
+    convert_kernel<S4ToE4M3><<<grid, 256, 0, stream>>>(a, lda, rows_a, b, ldb, rows_b, cols, dst_a, dst_b, ldd,
+                                                       threads_per_row_log2(cols, S4ToE4M3::VEC));
     return cudaGetLastError();
 }
 
