@@ -14,6 +14,9 @@ Reported (one JSON line from rank 0):
                device time of the timed steps  [TOPS]
   per_precision  TFLOP/s (FP16) and TOPS (INT8, INT4) of each call, averaged
                over the timed steps (CUDA events on the launching stream)
+  peak_fractions  each precision against its nominal dense peak, against the
+               measured peak of the tensor-core kind it runs on, and against
+               that kind's nominal rate scaled to the run's median SM clock
   roofline     the FP16 GEMM kernel (one launch per gemm_f16 call) against the
                measured bf16 tensor-core peak (FP16 runs at the bf16 rate)
   e2e          the same metric through the public API with pinned host
@@ -22,7 +25,11 @@ Reported (one JSON line from rank 0):
   cpu_baseline the CPU oracle on a bounded row sample of the same workload
   clocks       SM clocks and throttle reasons sampled during the timed region
 
---impl reference times the CPU oracle as the reference arm.
+--impl reference times the CPU oracle as the reference arm, on row samples.
+--sweep times every precision at N = 512 ... 8192 (graph replays, median and
+min of 5 batches, an L2-flushed variant for N <= 2048) with the CPU oracle
+timed beside each configuration; it prints one JSON line per configuration
+and no bench line.
 Multi-GPU: one process per GPU under torchrun; every rank runs the full step
 on its own data (independent problems, weak scaling); only the timing
 barrier and a max-reduction of the elapsed time cross ranks.
@@ -44,9 +51,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "GEMM TFLOP/s / TOPS at N=8192 (FP16, INT8, INT4); fraction of GB300 dense peak"
 # DRAM read + write bytes of one launch of the FP16 GEMM kernel at N = 8192, from
-# the ncu capture summarised in profiles/gemm_f16_n8192.md (set to None whenever
-# that kernel changes, until it is captured again).
-F16_KERNEL_DRAM_BYTES = 1.060e9 + 0.252e9
+# an ncu capture of that kernel (`ncu --set full -k regex:gemm_kernel` on
+# `python -m precision_tensor_core_gb300.run --prec f16 --n 8192`); set to None
+# whenever that kernel changes, until it is captured again.
+F16_KERNEL_DRAM_BYTES = 1.102e9 + 0.256e9
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -60,6 +68,11 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=0, help="0: min(steps, 20)")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU-baseline budget")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--sweep", action="store_true",
+                   help="precision x size sweep with the oracle timed beside each size (no bench line)")
+    p.add_argument("--sweep-sizes", type=lambda v: [int(x) for x in v.split(",")],
+                   default=[512, 1024, 2048, 4096, 8192])
+    p.add_argument("--sweep-oracle-seconds", type=float, default=2.0)
     return p.parse_args()
 
 
@@ -254,8 +267,38 @@ def run_ours(args, rank, world, dist):
                 "traffic": traffic,
                 "int8_frac_of_f16_peak": per["int8_tops"] / peak,
                 "int4_frac_of_fp8_peak": per["int4_tops"] / (2 * peak)}
+    fractions = peak_fractions(per, peak, clocks)
     return {"value": value, "elapsed_ms": elapsed_ms, "per": per, "e2e": e2e, "roofline": roofline,
-            "clocks": clocks, "launches": int(launches)}
+            "clocks": clocks, "launches": int(launches), "fractions": fractions}
+
+
+# Nominal dense tensor-core rates of GB300 quoted with the metric (TFLOP/s or
+# TOPS): FP16 about 2.25 P, INT8 about 4.5 P; INT4 is quoted as INT8's.  The
+# FP8 (E4M3) kind is nominally twice the FP16 kind.
+NOMINAL = {"fp16": 2250.0, "int8": 4500.0, "int4": 4500.0}
+PIPE_NOMINAL = {"kind::f16": 2250.0, "kind::f8f6f4": 4500.0}
+
+
+def peak_fractions(per, measured_f16_peak, clocks):
+    """Each precision's throughput against the denominators of the metric:
+    the nominal dense peak of its precision, the tensor-core kind it actually
+    runs on (measured sustained bf16 rate for kind::f16, twice that for the
+    E4M3 kind), and that kind's nominal rate scaled by the median SM clock of
+    the run over the maximum clock (nominal rates taken at the maximum clock)."""
+    mhz, mhz_max = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    scale = (mhz / mhz_max) if (mhz and mhz_max) else None
+    rows = {"fp16": ("fp16_tflops", "kind::f16", measured_f16_peak),
+            "int8": ("int8_tops", "kind::f16", measured_f16_peak),
+            "int4": ("int4_tops", "kind::f8f6f4", 2 * measured_f16_peak)}
+    out = {}
+    for prec, (key, kind, pipe_peak) in rows.items():
+        a = per[key]
+        clock_peak = PIPE_NOMINAL[kind] * scale if scale else None
+        out[prec] = {"achieved": a, "nominal_peak": NOMINAL[prec], "frac_nominal": a / NOMINAL[prec],
+                     "pipe": kind, "pipe_peak_measured": pipe_peak, "frac_pipe_measured": a / pipe_peak,
+                     "pipe_peak_clock_adjusted": clock_peak,
+                     "frac_pipe_clock_adjusted": (a / clock_peak) if clock_peak else None}
+    return out
 
 
 # ---------------------------------------------------------------- oracle timing
@@ -283,6 +326,130 @@ def cpu_baseline(host, n, budget_s):
     return {"value": ops / secs / 1e12, "unit": "TOPS", "cores": cores, "kind": "oracle",
             "sample": f"first {rows} output rows of each of the FP16, INT8 and INT4 N={n} GEMMs "
                       f"({ops:.3g} ops, {secs:.1f} s, {cores} threads)"}
+
+
+# ---------------------------------------------------------------- size sweep
+def _oracle_rows(prec, A, B, n, rows, nthreads):
+    """Seconds the CPU oracle takes for the first `rows` output rows."""
+    import oracle
+    t0 = time.perf_counter()
+    if prec.startswith("f16"):
+        oracle.gemm_f16(A[:rows], B, nthreads=nthreads)
+    elif prec == "s8":
+        oracle.gemm_s8(A[:rows], B, nthreads=nthreads)
+    else:
+        oracle.gemm_s4(A[:rows], B, n, nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def _oracle_time(prec, A, B, n, nthreads, budget_s):
+    """Oracle time of the whole N x N product on `nthreads` threads: measured
+    when it fits the budget, else extrapolated from a timed row sample."""
+    rows = max(1, min(n, nthreads))
+    secs = _oracle_rows(prec, A, B, n, rows, nthreads)
+    while rows < n and secs < budget_s / 4:
+        rows = min(n, rows * 4)
+        secs = _oracle_rows(prec, A, B, n, rows, nthreads)
+    full = secs * n / rows
+    return {"threads": nthreads, "seconds": full, "extrapolated": rows < n, "rows_timed": rows,
+            "tops": 2.0 * n ** 3 / full / 1e12}
+
+
+def run_sweep(args):
+    """Precision x size sweep: GPU time per call (median and min over 5
+    batches of CUDA-graph replays, L2 warm; for N <= 2048 also with a 512 MiB
+    L2 flush before every call) and the CPU oracle on the same inputs (all
+    host cores; one core too for N <= 1024).  One JSON line per configuration."""
+    import torch
+    import datagen
+    import __graft_entry__
+    import precision_tensor_core_gb300 as ptc
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    cores = os.cpu_count() or 1
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream()
+    cases = [("f16u", 512)] if 512 in args.sweep_sizes else []
+    cases += [(p, n) for n in args.sweep_sizes for p in ("f16", "s8", "s4")]
+
+    def graph_of(fn, calls):
+        g = torch.cuda.CUDAGraph()
+        stream.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(calls):
+                    fn()
+        torch.cuda.current_stream().wait_stream(stream)
+        torch.cuda.synchronize()
+        return g
+
+    def batches(g, calls, min_ms=200.0, nb=5):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        reps = max(1, int(min_ms / max(e0.elapsed_time(e1), 1e-3)) + 1)
+        out = []
+        for _ in range(nb):
+            e0.record()
+            for _ in range(reps):
+                g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            out.append(e0.elapsed_time(e1) * 1e3 / (reps * calls))
+        return out, reps * calls
+
+    for prec, n in cases:
+        if prec == "f16u":
+            A, B = datagen.f16_operands(n, "uniform")
+        elif prec == "f16":
+            A, B = datagen.f16_operands(n, "normal")
+        elif prec == "s8":
+            A, B = datagen.s8_operands(n)
+        else:
+            A, B = datagen.s4_operands(n)
+        if prec.startswith("f16"):
+            Ad = torch.from_numpy(np.ascontiguousarray(A).view(np.float16)).to(dev)
+            Bd = torch.from_numpy(np.ascontiguousarray(B).view(np.float16)).to(dev)
+            C = torch.empty((n, n), dtype=torch.float32, device=dev)
+            fn = lambda: ptc.matmul_f16(Ad, Bd, out=C)  # noqa: E731
+        else:
+            Ad, Bd = torch.from_numpy(A).to(dev), torch.from_numpy(B).to(dev)
+            C = torch.empty((n, n), dtype=torch.int32, device=dev)
+            fn = ((lambda: ptc.matmul_s8(Ad, Bd, out=C)) if prec == "s8"
+                  else (lambda: ptc.matmul_s4(Ad, Bd, n, out=C)))
+        calls = int(max(20, min(200, 2e11 / (2.0 * n ** 3))))
+        us, total = batches(graph_of(fn, calls), calls)
+        ops = 2.0 * n ** 3
+        gpu = {"median_us": statistics.median(us), "min_us": min(us), "batches": len(us),
+               "calls_per_batch": total, "tops_median": ops / statistics.median(us) / 1e6,
+               "tops_best": ops / min(us) / 1e6}
+        flushed = None
+        if n <= 2048:
+            fc = 20
+            both, _ = batches(graph_of(lambda: (flush.zero_(), fn()), fc), fc)
+            alone, _ = batches(graph_of(lambda: flush.zero_(), fc), fc)
+            t = statistics.median(both) - statistics.median(alone)
+            flushed = {"median_us": t, "tops_median": ops / t / 1e6,
+                       "how": "512 MiB buffer written before every call; flush time measured alone and subtracted"}
+        assert ptc.gemm_poll_device_error() == ptc.PTC_OK
+        orc_all = _oracle_time(prec, A, B, n, cores, args.sweep_oracle_seconds)
+        orc_one = _oracle_time(prec, A, B, n, 1, args.sweep_oracle_seconds) if n <= 1024 else None
+        line = {"sweep": True, "precision": {"f16u": "fp16", "f16": "fp16", "s8": "int8", "s4": "int4"}[prec],
+                "N": n, "values": {"f16u": "uniform [-1,1]", "f16": "normal(0,1)/sqrt(K)",
+                                   "s8": "uniform [-128,127]", "s4": "uniform [-8,7], packed"}[prec],
+                "unit": "TFLOP/s" if prec.startswith("f16") else "TOPS",
+                "gpu": gpu, "gpu_l2_flushed": flushed,
+                "oracle_all_cores": orc_all, "oracle_single_thread": orc_one,
+                "gpu_over_oracle_all_cores": orc_all["seconds"] * 1e6 / gpu["median_us"]}
+        print(json.dumps(line), flush=True)
+        del Ad, Bd, C
+        torch.cuda.empty_cache()
 
 
 def run_reference(args):
@@ -322,6 +489,10 @@ def main():
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
         return
+    if args.sweep:
+        if rank == 0:
+            run_sweep(args)
+        return
     dist = None
     if world > 1:
         import torch
@@ -345,7 +516,8 @@ def main():
                                    "one step = one GEMM of each",
                        "N": args.n, "l2": "inputs larger than L2 (~1.2 GB per step), no flush",
                        "parallelism": f"replicas x{world}"},
-            "per_precision": res["per"], "roofline": res["roofline"], "cpu_baseline": cpu,
+            "per_precision": res["per"], "peak_fractions": res["fractions"], "roofline": res["roofline"],
+            "cpu_baseline": cpu,
             "e2e": res["e2e"], "gpu_launches": res["launches"], "clocks": res["clocks"],
         }
         print(json.dumps(line), flush=True)

@@ -192,12 +192,24 @@ __device__ __forceinline__ void pause_ns(uint64_t ns) {
     }
 }
 
+// One 32-byte store (a whole L2 sector) of eight 32-bit words; dst 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(uint32_t *dst, const uint32_t *w) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(w[0]), "r"(w[1]), "r"(w[2]),
+                 "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 template <typename T>
-__device__ __forceinline__ void store_32(T *dst, const uint32_t (&v)[32], int valid) {
+__device__ __forceinline__ void store_32(T *dst, const uint32_t (&v)[32], int valid, bool wide) {
     if (valid >= 32) {
-        uint4 *d = reinterpret_cast<uint4 *>(dst);
+        if (wide) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) d[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+            for (int i = 0; i < 4; ++i) st_global_v8(reinterpret_cast<uint32_t *>(dst) + 8 * i, &v[8 * i]);
+        } else {
+            uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) d[i] = make_uint4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+        }
     } else {
         uint32_t *d = reinterpret_cast<uint32_t *>(dst);
 #pragma unroll
@@ -228,7 +240,7 @@ __device__ __forceinline__ void store_scaled_row(const GemmArgs &args, int row, 
             uint32_t v[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(f[j]);
-            store_32(reinterpret_cast<float *>(args.C) + int64_t(row) * args.ldc + cc, v, valid);
+            store_32(reinterpret_cast<float *>(args.C) + int64_t(row) * args.ldc + cc, v, valid, args.c_wide);
         } else {
             // 16-bit outputs: pairs packed into 32-bit words, 64 bytes per 32 columns.
             uint32_t w[16];
@@ -245,7 +257,10 @@ __device__ __forceinline__ void store_scaled_row(const GemmArgs &args, int row, 
                 w[j] = lo | (hi << 16);
             }
             uint16_t *dst = reinterpret_cast<uint16_t *>(args.C) + int64_t(row) * args.ldc + cc;
-            if (valid == 32) {
+            if (valid == 32 && args.c_wide) {
+                st_global_v8(reinterpret_cast<uint32_t *>(dst), &w[0]);
+                st_global_v8(reinterpret_cast<uint32_t *>(dst) + 8, &w[8]);
+            } else if (valid == 32) {
                 uint4 *d = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
@@ -259,14 +274,20 @@ __device__ __forceinline__ void store_scaled_row(const GemmArgs &args, int row, 
 }
 
 // 32 FP16 accumulators (the low half of each 32-bit tensor-memory column) to
-// dst[0 .. valid), valid capped at 32.
-__device__ __forceinline__ void store_f16acc_32(uint16_t *dst, const uint32_t (&r)[32], int valid) {
+// dst[0 .. valid), valid capped at 32; `wide`: two 32-byte stores.
+__device__ __forceinline__ void store_f16acc_32(uint16_t *dst, const uint32_t (&r)[32], int valid, bool wide) {
     if (valid >= 32) {
-        uint4 *d = reinterpret_cast<uint4 *>(dst);
+        uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            d[i] = make_uint4((r[8 * i] & 0xFFFFu) | (r[8 * i + 1] << 16), (r[8 * i + 2] & 0xFFFFu) | (r[8 * i + 3] << 16),
-                              (r[8 * i + 4] & 0xFFFFu) | (r[8 * i + 5] << 16), (r[8 * i + 6] & 0xFFFFu) | (r[8 * i + 7] << 16));
+        for (int j = 0; j < 16; ++j) w[j] = (r[2 * j] & 0xFFFFu) | (r[2 * j + 1] << 16);
+        if (wide) {
+            st_global_v8(reinterpret_cast<uint32_t *>(dst), &w[0]);
+            st_global_v8(reinterpret_cast<uint32_t *>(dst) + 8, &w[8]);
+        } else {
+            uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+        }
     } else {
 #pragma unroll
         for (int j = 0; j < 32; ++j)
@@ -279,11 +300,12 @@ __device__ __forceinline__ void store_f16acc_32(uint16_t *dst, const uint32_t (&
 // partial sums (to `mine`), or, when the other half has published first, add
 // its partial sums (`other`; in FP32, the same bits whichever half adds) and
 // store C.  crow points at C[row][col0] (null when row >= M); `valid` is the
-// number of columns of the slice below N.  Scalars only, so that the call
-// keeps the kernel's parameters out of local memory.
+// number of columns of the slice below N; `wide`: 32-byte C stores.  Inlined:
+// as an out-of-line call from the CTA-pair kernel its 32-byte stores after the
+// first 32 columns were lost (caught by the split-tile parity tests).
 template <int EPI>
-__device__ __noinline__ void split_epilogue(uint32_t t_acc, uint32_t *cnt, float4 *mine, const float4 *other,
-                                            void *crow, int valid, int lane) {
+__device__ __forceinline__ void split_epilogue(uint32_t t_acc, uint32_t *cnt, float4 *mine, const float4 *other,
+                                               void *crow, int valid, bool wide, int lane) {
     bool finish = split_other_done(cnt, lane);
     if (!finish) {
 #pragma unroll 1
@@ -324,9 +346,9 @@ __device__ __noinline__ void split_epilogue(uint32_t t_acc, uint32_t *cnt, float
         const int v = valid - 32 * c;
         if (crow != nullptr && v > 0) {
             if constexpr (EPI == EPI_F16ACC)
-                store_f16acc_32(static_cast<uint16_t *>(crow) + 32 * c, r, v);
+                store_f16acc_32(static_cast<uint16_t *>(crow) + 32 * c, r, v, wide);
             else
-                store_32(static_cast<float *>(crow) + 32 * c, r, v);
+                store_32(static_cast<float *>(crow) + 32 * c, r, v, wide);
         }
     }
 }
@@ -623,11 +645,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                         int32_t *crow = reinterpret_cast<int32_t *>(args.C) + int64_t(row) * args.ldc;
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
-                            uint32_t v[32];
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) v[j] = static_cast<uint32_t>(acc[32 * c + j]);
                             const int cc = col0 + 32 * c;
-                            if (cc < args.N) store_32(crow + cc, v, args.N - cc);
+                            if (cc < args.N)
+                                store_32(crow + cc, reinterpret_cast<const uint32_t(&)[32]>(acc[32 * c]), args.N - cc,
+                                         args.c_wide);
                         }
                     } else {
                         store_scaled_row(args, row, col0, acc);
@@ -650,9 +671,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                         if constexpr (EPI == EPI_F16ACC) {
                             if (row < args.M && cc < args.N)
                                 store_f16acc_32(reinterpret_cast<uint16_t *>(args.C) + int64_t(row) * args.ldc + cc, r,
-                                                args.N - cc);
+                                                args.N - cc, args.c_wide);
                         } else {
-                            if (row < args.M && cc < args.N) store_32(crow + cc, r, args.N - cc);
+                            if (row < args.M && cc < args.N) store_32(crow + cc, r, args.N - cc, args.c_wide);
                         }
                     }
                 } else {
@@ -663,7 +684,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                (int64_t(row) * args.ldc + col0) * (EPI == EPI_F16ACC ? 2 : 4);
                     split_epilogue<EPI>(t_lane + uint32_t(abuf * kBN), args.split_count + slice,
                                         split_partial(args, slice, wr.part - 1), split_partial(args, slice, 2 - wr.part),
-                                        crow, args.N - col0, lane);
+                                        crow, args.N - col0, args.c_wide, lane);
                 }
                 release(abuf);
                 if (++abuf == 2) {
@@ -742,6 +763,9 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
     // partial sums through a stream-ordered workspace from `pool`: a counter
     // per epilogue warp slice (zeroed here) and two slices of partial sums.
     GemmArgs a = args;
+    // 32-byte C stores (whole L2 sectors) when C's base and row pitch allow them.
+    const int64_t esize = (EPI == EPI_F16ACC || (EPI == EPI_INT && (a.out_mode == OUT_BF16 || a.out_mode == OUT_F16))) ? 2 : 4;
+    a.c_wide = (reinterpret_cast<uintptr_t>(a.C) % 32 == 0 && (a.ldc * esize) % 32 == 0) ? 1 : 0;
     const int maxc = cache.max_clusters;
     const int tail = a.num_tiles < maxc ? a.num_tiles : a.num_tiles % maxc;
     a.tail_split = 0;

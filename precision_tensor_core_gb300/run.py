@@ -4,7 +4,9 @@
 
 Inputs are the seeded synthetic operands of the benchmark (FP16 normal/sqrt(K),
 INT8 and INT4 uniform).  Nothing is timed or checked here; use bench.py for
-numbers and the test suite for parity.
+numbers and the test suite for parity.  `--prec cublas_f16` runs the same FP16
+product through cuBLAS instead (torch.mm with FP32 output), as a library kernel
+to profile beside ours; it is not part of the library.
 """
 from __future__ import annotations
 
@@ -21,7 +23,7 @@ if ROOT not in sys.path:
 
 def main():
     p = argparse.ArgumentParser()
-    p.add_argument("--prec", choices=["f16", "s8", "s4", "s8_noalloc"], default="f16")
+    p.add_argument("--prec", choices=["f16", "s8", "s4", "s8_noalloc", "cublas_f16"], default="f16")
     p.add_argument("--n", type=int, default=8192)
     p.add_argument("--reps", type=int, default=2)
     a = p.parse_args()
@@ -36,7 +38,12 @@ def main():
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     n = a.n
-    if a.prec == "f16":
+    if a.prec == "cublas_f16":
+        A, B = datagen.f16_operands(n, "normal")
+        Ad = torch.from_numpy(A.view(np.float16)).to(dev)
+        Bd = torch.from_numpy(B.view(np.float16)).to(dev)
+        run = lambda: torch.mm(Ad, Bd, out_dtype=torch.float32)
+    elif a.prec == "f16":
         A, B = datagen.f16_operands(n, "normal")
         Ad = torch.from_numpy(A.view(np.float16)).to(dev)
         Bd = torch.from_numpy(B.view(np.float16)).to(dev)

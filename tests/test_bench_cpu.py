@@ -80,3 +80,28 @@ def test_reference_arm_other_ranks_exit_quietly():
     r = _run_bench(["--impl", "reference", "--n", "256", "--steps", "2", "--warmup", "1"],
                    {"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_peak_fractions_denominators():
+    per = {"fp16_tflops": 1500.0, "int8_tops": 1125.0, "int4_tops": 2250.0}
+    f = bench.peak_fractions(per, 1500.0, {"sm_mhz": 1035.0, "sm_max_mhz": 2070.0})
+    assert f["fp16"]["frac_nominal"] == pytest.approx(1500 / 2250)
+    assert f["int8"]["frac_nominal"] == pytest.approx(1125 / 4500)
+    assert f["fp16"]["frac_pipe_measured"] == pytest.approx(1.0)
+    assert f["int8"]["pipe"] == "kind::f16" and f["int8"]["frac_pipe_measured"] == pytest.approx(0.75)
+    assert f["int4"]["pipe"] == "kind::f8f6f4" and f["int4"]["pipe_peak_measured"] == pytest.approx(3000.0)
+    # half the maximum clock halves the nominal rate of the kind
+    assert f["fp16"]["pipe_peak_clock_adjusted"] == pytest.approx(1125.0)
+    assert f["int4"]["frac_pipe_clock_adjusted"] == pytest.approx(2250 / 2250)
+    g = bench.peak_fractions(per, 1500.0, {"sm_mhz": None, "sm_max_mhz": None})
+    assert g["fp16"]["pipe_peak_clock_adjusted"] is None and g["fp16"]["frac_pipe_clock_adjusted"] is None
+
+
+def test_sweep_oracle_time_measured_and_extrapolated():
+    import datagen
+    A, B = datagen.s8_operands(64)
+    full = bench._oracle_time("s8", A, B, 64, 2, budget_s=100.0)
+    assert full["rows_timed"] == 64 and not full["extrapolated"] and full["seconds"] > 0
+    part = bench._oracle_time("s8", A, B, 64, 2, budget_s=0.0)
+    assert part["rows_timed"] == 2 and part["extrapolated"]
+    assert part["tops"] == pytest.approx(2.0 * 64 ** 3 / part["seconds"] / 1e12)
