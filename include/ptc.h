@@ -302,6 +302,8 @@ int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile);
  *                  exactly representable integer)
  *   "s4_chunk_kb"  INT4 route: K blocks (128 values each) per fold, default 64
  *                  (8192 values: |partial| <= 2^19)
+ *                  Both fold lengths must be even (CTA pairs stage two K
+ *                  blocks at a time); odd values return PTC_ERR_INVALID.
  *   "l2_hint"      L2 eviction policy of operand loads: 0 (default) none;
  *                  1 A evict-last / B evict-first; 2 A evict-last; 3 both
  *                  evict-normal (all measured slower than 0 on GB300)

@@ -745,11 +745,11 @@ int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile) {
 
 int ptc_set_tuning(const char *key, int64_t value) {
     if (!key) return fail(PTC_ERR_INVALID, "key is NULL");
-    if (std::strcmp(key, "s8_chunk_kb") == 0 && value > 0 && value < (1 << 30)) {
+    if (std::strcmp(key, "s8_chunk_kb") == 0 && value > 0 && value % 2 == 0 && value < (1 << 30)) {
         g_chunk_s8.store(int(value));
         return PTC_OK;
     }
-    if (std::strcmp(key, "s4_chunk_kb") == 0 && value > 0 && value < (1 << 30)) {
+    if (std::strcmp(key, "s4_chunk_kb") == 0 && value > 0 && value % 2 == 0 && value < (1 << 30)) {
         g_chunk_s4.store(int(value));
         return PTC_OK;
     }

@@ -24,9 +24,12 @@ pytestmark = pytest.mark.gpu
 
 # (M, N, K): 2560 x 2048 is 160 one-CTA tiles / 80 pair tiles, a wave plus a
 # short tail on 148..152 CTAs / 74..76 pairs; 2560 x 1848 leaves a last tile
-# column of 56 values; 640 x 1000 is a lone partial wave; K = 200 and 136 give
-# odd numbers of 64-value K blocks; K = 40 is a single block (no split).
-SHAPES = [(2560, 2048, 192), (2560, 1848, 200), (640, 1000, 136), (2560, 2048, 40)]
+# column of 56 values; 640 x 1000 is a lone partial wave; K = 192, 136 and 320
+# give odd numbers of 64-value K blocks (3, 3, 5), K = 200 four blocks; CTA
+# pairs stage two blocks at a time, so their split point is a whole stage and
+# K = 128 (one pair stage) is not split; K = 40 is a single block (no split).
+SHAPES = [(2560, 2048, 192), (2560, 1848, 200), (640, 1000, 136), (2560, 2048, 40), (2560, 2048, 128),
+          (640, 1000, 320)]
 
 
 
