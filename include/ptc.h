@@ -121,6 +121,23 @@ int gemm_s8(int64_t M, int64_t N, int64_t K,
             void *stream);
 
 /*
+ * INT8 GEMM with B row-major: as gemm_s8, except
+ *   B  row-major (K x N), element (k,j) at B[k*ldb + j]; ldb >= N, ldb % 16 == 0
+ * The paper's ablation of a transposed B ("Hand-Written PTX Tensor-Core GEMM
+ * Kernels: A Multi-Precision Study on NVIDIA L4", section IV-D) found this
+ * orientation far slower for its cp.async / ldmatrix kernel; here B is
+ * converted into K rows of N binary16 values and read by the tensor cores as
+ * an MN-major operand (the layout gemm_f16 reads), so the orientation costs
+ * only the conversion of a differently shaped B.  Workspace: about
+ * 2*(M*K + K*N) bytes from the library pool, stream-ordered on `stream`.
+ */
+int gemm_s8_b_rowmajor(int64_t M, int64_t N, int64_t K,
+                       const int8_t *A, int64_t lda,
+                       const int8_t *B, int64_t ldb,
+                       int32_t *C, int64_t ldc,
+                       void *stream);
+
+/*
  * Packed INT4 GEMM: C[M x N] (int32) = A[M x K] (s4) . B[K x N] (s4), exact.
  * Two signed 4-bit values per byte, element 2t of a row in bits 0..3 of byte
  * t and element 2t+1 in bits 4..7 (low nibble = even k); Listing 1 addresses
@@ -322,6 +339,9 @@ int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile);
  *                  library pool.  0: never.  Integer results do not depend on
  *                  the choice; FP16 results of split tiles differ by the
  *                  summation order (the sum of two FP32 half sums).
+ *   "pair_stage_kb" CTA pairs: K blocks per shared-memory ring stage, 2
+ *                  (default: 3 stages of 64 KiB per CTA) or 1 (7 stages of
+ *                  32 KiB).  Results do not depend on the choice.
  *   "split_min_kb" K blocks (64 values FP16 / INT8, 128 INT4) below which no
  *                  tile is split, default 64 (the split saves about half a
  *                  tile's K loop and costs a few microseconds per call);

@@ -8,7 +8,7 @@ Two layers, both argument marshalling only (every arithmetic step runs in the
 library's CUDA kernels):
 
 * ``gemm_f16``, ``gemm_f16_f16acc``, ``gemm_s8``, ``gemm_s4``, ``gemm_s8_scaled``, ``gemm_s4_scaled``,
-  ``gemm_s8_noalloc``, ``gemm_status_string``,
+  ``gemm_s8_noalloc``, ``gemm_s8_b_rowmajor``, ``gemm_status_string``,
   ``gemm_poll_device_error``, ``ptc_kernel_launch_count``,
   ``ptc_debug_set_wait_limit``, ``ptc_set_tuning``: the C ABI of
   ``include/ptc.h`` under the same names, taking integers (sizes, leading
@@ -73,7 +73,7 @@ def lib() -> ctypes.CDLL:
             raise RuntimeError(f"libptc.so is not built ({LIB_PATH}); run __graft_entry__.build()")
         L = ctypes.CDLL(LIB_PATH)
         for name in ("gemm_f16", "gemm_f16_f16acc", "gemm_s8", "gemm_s4", "gemm_s8_noalloc",
-                     "gemm_f16_host", "gemm_s8_host", "gemm_s4_host"):
+                     "gemm_s8_b_rowmajor", "gemm_f16_host", "gemm_s8_host", "gemm_s4_host"):
             fn = getattr(L, name)
             fn.restype = ctypes.c_int
             fn.argtypes = [_i64, _i64, _i64, _vp, _i64, _vp, _i64, _vp, _i64, _vp]
@@ -121,6 +121,11 @@ def gemm_f16_f16acc(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
 def gemm_s8(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
     """C[MxN] s32 = A[MxK] s8 (row-major) . B[KxN] s8 (column-major); device addresses."""
     return _check(lib().gemm_s8(M, N, K, A, lda, B, ldb, C, ldc, stream))
+
+
+def gemm_s8_b_rowmajor(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:
+    """C[MxN] s32 = A[MxK] s8 (row-major) . B[KxN] s8 (row-major, ldb >= N); device addresses."""
+    return _check(lib().gemm_s8_b_rowmajor(M, N, K, A, lda, B, ldb, C, ldc, stream))
 
 
 def gemm_s4(M, N, K, A, lda, B, ldb, C, ldc, stream=0) -> int:

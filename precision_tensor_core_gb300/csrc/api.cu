@@ -42,6 +42,7 @@ std::atomic<int> g_l2_hint{0};
 std::atomic<int> g_cta_pair{0};     // 0: by problem size, 1: one CTA per tile, 2: CTA pairs
 std::atomic<int> g_tail_split{1};   // 1: split a short last wave in K
 std::atomic<int> g_split_min_kb{64};
+std::atomic<int> g_pair_stage_kb{2};  // CTA pairs: K blocks per ring stage
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 std::atomic<int64_t> g_stall_tile{-1};
 
@@ -213,6 +214,7 @@ GemmArgs base_args(int64_t M, int64_t N, int64_t K, int k_elems_per_block, void 
     a.l2_hint = g_l2_hint.load();
     a.split_ok = g_tail_split.load();
     a.split_min_kb = g_split_min_kb.load();
+    a.stage_kb = g_pair_stage_kb.load();
     a.wait_limit_ns = g_wait_ns.load();
     return a;
 }
@@ -390,6 +392,69 @@ int int_gemm(bool s4, int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
         args.scale_a = sa;
         args.scale_b = sb;
         rc = launch_gemm_checked(s4 ? Kind::E4M3 : Kind::F16, false, ptc::EPI_INT, ctas, ta, tb, args, *d, s);
+    }
+    cudaFreeAsync(ws, s);
+    return rc;
+}
+
+// INT8 with B row-major (K x N): A converted as for gemm_s8, B converted into
+// K rows of N binary16 values, read by the MMAs as an MN-major operand (the
+// same layout as gemm_f16's B).
+int s8_rowb_gemm(int64_t M, int64_t N, int64_t K, const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
+                 int32_t *C, int64_t ldc, void *stream) {
+    int rc = check_sizes(M, N, K);
+    if (rc) return rc;
+    if (M == 0 || N == 0) return PTC_OK;
+    if (!C || ldc < N) return fail(PTC_ERR_INVALID, "C is NULL or ldc < N");
+    if (K > 0 && (!A || !B)) return fail(PTC_ERR_INVALID, "A or B is NULL");
+    if (K > 0 && (lda < K || ldb < N)) return fail(PTC_ERR_INVALID, "lda < K or ldb < N");
+    if (!aligned16(C) || (ldc * 4) % 16)
+        return fail(PTC_ERR_ALIGN, "C must be 16-byte aligned with a row pitch that is a multiple of 16 bytes");
+    if (K > 0 && (!aligned16(A) || !aligned16(B) || lda % 16 || ldb % 16))
+        return fail(PTC_ERR_ALIGN, "A, B must be 16-byte aligned, lda % 16 == 0, ldb % 16 == 0");
+    const uint64_t cbytes = span_bytes(M, N, ldc, 4, 1);
+    if (K > 0 && (overlaps(C, cbytes, A, span_bytes(M, K, lda, 1, 1)) ||
+                  overlaps(C, cbytes, B, span_bytes(K, N, ldb, 1, 1))))
+        return fail(PTC_ERR_OVERLAP, "C overlaps A or B");
+
+    int dev;
+    DevInfo *d;
+    if ((rc = current_device(&dev, &d))) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (K == 0) return zero_c(C, ldc, M, N, 4, *d, s);
+    if (!d->pool_ok) return fail(PTC_ERR_ALLOC, "workspace memory pool unavailable");
+
+    const int64_t ldw_a = round_up(K, 64);  // binary16 elements per A row (128-byte multiple)
+    const int64_t ldw_b = round_up(N, 64);  // binary16 elements per B row
+    const int64_t a_bytes = round_up(M * ldw_a * 2, 1024);
+    const int64_t b_bytes = round_up(K * ldw_b * 2, 1024);
+    void *ws = nullptr;
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, size_t(a_bytes + b_bytes), d->pool, s);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PTC_ERR_ALLOC, "workspace allocation failed");
+    }
+    uint16_t *aw = static_cast<uint16_t *>(ws);
+    uint16_t *bw = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + a_bytes);
+    const int cgrid = d->sms * 8;
+    rc = PTC_OK;
+    e = ptc::launch_s8_to_f16(A, lda, int(M), int(K), aw, ldw_a, cgrid, s);
+    if (e == cudaSuccess) {
+        g_launches.fetch_add(1);
+        e = ptc::launch_s8_to_f16(B, ldb, int(K), int(N), bw, ldw_b, cgrid, s);
+        if (e == cudaSuccess) g_launches.fetch_add(1);
+    }
+    if (e != cudaSuccess) rc = fail_cuda(e, "operand conversion launch");
+    const int ctas = choose_ctas(M, N, d->sms);
+    CUtensorMap ta, tb;
+    if (!rc) rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, aw, K, M, uint64_t(ldw_a) * 2, 64, ptc::kBM);
+    if (!rc) rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bw, N, K, uint64_t(ldw_b) * 2, 64, 64);
+    if (!rc) {
+        GemmArgs args = base_args(M, N, K, 64, C, ldc, ctas);
+        const int ch = g_chunk_s8.load();
+        args.kb_per_chunk = ch > 0 ? ch : 1;
+        args.out_mode = ptc::OUT_S32;
+        rc = launch_gemm_checked(Kind::F16, true, ptc::EPI_INT, ctas, ta, tb, args, *d, s);
     }
     cudaFreeAsync(ws, s);
     return rc;
@@ -627,6 +692,12 @@ int gemm_s8(int64_t M, int64_t N, int64_t K, const int8_t *A, int64_t lda, const
     return int_gemm(false, M, N, K, A, lda, B, ldb, C, ldc, ptc::OUT_S32, nullptr, nullptr, stream);
 }
 
+int gemm_s8_b_rowmajor(int64_t M, int64_t N, int64_t K, const int8_t *A, int64_t lda, const int8_t *B,
+                       int64_t ldb, int32_t *C, int64_t ldc, void *stream) {
+    g_msg[0] = 0;
+    return s8_rowb_gemm(M, N, K, A, lda, B, ldb, C, ldc, stream);
+}
+
 int gemm_s4(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
             int64_t ldb, int32_t *C, int64_t ldc, void *stream) {
     g_msg[0] = 0;
@@ -763,6 +834,10 @@ int ptc_set_tuning(const char *key, int64_t value) {
     }
     if (std::strcmp(key, "tail_split") == 0 && (value == 0 || value == 1)) {
         g_tail_split.store(int(value));
+        return PTC_OK;
+    }
+    if (std::strcmp(key, "pair_stage_kb") == 0 && (value == 1 || value == 2)) {
+        g_pair_stage_kb.store(int(value));
         return PTC_OK;
     }
     if (std::strcmp(key, "split_min_kb") == 0 && value >= 2 && value <= (1 << 20)) {

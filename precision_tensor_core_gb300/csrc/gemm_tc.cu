@@ -60,15 +60,17 @@ constexpr int TMEM_COLS = 512;                  // two accumulators of kBN colum
 constexpr int KSTEP_BYTES = 32;                 // K bytes per tcgen05.mma (16 f16 / 32 e4m3)
 constexpr int KSTEPS = kRowBytes / KSTEP_BYTES; // MMAs per stage
 
-// Per-CTA shapes of the two variants.  A CTA stages 128 rows of A; alone it
+// Per-CTA shapes of the variants.  A CTA stages 128 rows of A; alone it
 // stages all 256 rows of B (4 stages of one K block, 48 KiB each), in a pair
-// it stages half of B (the pair's MMAs read B from both CTAs) in 3 stages of
-// two K blocks (64 KiB each): half as many barrier round trips per byte as
-// one-block stages, measured 3-6% faster than 7 stages of one block.
-template <int CTAS>
+// it stages half of B (the pair's MMAs read B from both CTAs), in 3 stages of
+// two K blocks (64 KiB each) by default or 7 stages of one K block (32 KiB
+// each): two-block stages take half as many barrier round trips per byte and
+// measured 3-6% faster.
+template <int CTAS, int SUBK>
 struct Cfg {
-    static constexpr int STAGES = CTAS == 1 ? 4 : 3;
-    static constexpr int SUB = CTAS == 1 ? 1 : 2;  // K blocks per stage
+    static_assert(CTAS == 2 || SUBK == 1, "one CTA stages one K block at a time");
+    static constexpr int STAGES = CTAS == 1 ? 4 : (SUBK == 1 ? 7 : 3);
+    static constexpr int SUB = SUBK;  // K blocks per stage
     static constexpr int B_ROWS = kBN / CTAS;
     static constexpr int A_BLOCK = kBM * kRowBytes;     // one K block of A
     static constexpr int B_BLOCK = B_ROWS * kRowBytes;  // one K block of B
@@ -88,12 +90,13 @@ struct SharedTail {
     AbortState abort;
 };
 
-template <int CTAS>
+template <int CTAS, int SUBK>
 constexpr size_t smem_bytes() {
-    return 1024 + size_t(Cfg<CTAS>::STAGES) * Cfg<CTAS>::STAGE +
-           sizeof(SharedTail<Cfg<CTAS>::STAGES>);
+    return 1024 + size_t(Cfg<CTAS, SUBK>::STAGES) * Cfg<CTAS, SUBK>::STAGE +
+           sizeof(SharedTail<Cfg<CTAS, SUBK>::STAGES>);
 }
-static_assert(smem_bytes<1>() <= 232448 && smem_bytes<2>() <= 232448, "shared memory budget");
+static_assert(smem_bytes<1, 1>() <= 232448 && smem_bytes<2, 1>() <= 232448 && smem_bytes<2, 2>() <= 232448,
+              "shared memory budget");
 
 __device__ __forceinline__ void tile_coords(int t, const GemmArgs &a, int &mb, int &nb) {
     const int per_group = a.group_m * a.tiles_n;
@@ -366,13 +369,13 @@ __device__ __forceinline__ void split_epilogue(uint32_t t_acc, uint32_t *cnt, fl
 // its full barriers collect both CTAs' copies, its commits arrive on both
 // CTAs' empty / accumulator-full barriers, and both CTAs' epilogues release
 // accumulator buffers on its acc_empty barriers.
-template <Kind KIND, bool B_MN, int EPI, int CTAS>
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const GemmArgs args) {
     static_assert(!(B_MN && KIND == Kind::E4M3), "MN-major B is used by the FP16 path only");
     constexpr bool INT_OUT = EPI == EPI_INT;
-    using C_ = Cfg<CTAS>;
+    using C_ = Cfg<CTAS, SUBK>;
     constexpr int STAGES = C_::STAGES;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzle atoms must sit on 1024-byte boundaries.
@@ -735,11 +738,11 @@ struct LaunchCache {
     int max_clusters = 0;
 };
 
-template <Kind KIND, bool B_MN, int EPI, int CTAS>
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK>
 cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args,
                        int sms, cudaMemPool_t pool, cudaStream_t stream) {
-    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS>;
-    constexpr size_t SMEM = smem_bytes<CTAS>();
+    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS, SUBK>;
+    constexpr size_t SMEM = smem_bytes<CTAS, SUBK>();
     static thread_local LaunchCache cache;  // per device (re-queried when it changes)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -791,7 +794,7 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
     // The split saves about half of a tile's K loop (~0.14 us per K block);
     // setting up the exchange costs ~6 us per call, so short K (below
     // split_min_kb blocks, 64 by default) runs whole.
-    if (pool != nullptr && a.split_ok && a.num_kb > Cfg<CTAS>::SUB && a.num_kb >= a.split_min_kb && tail > 0 &&
+    if (pool != nullptr && a.split_ok && a.num_kb > SUBK && a.num_kb >= a.split_min_kb && tail > 0 &&
         2 * tail <= maxc) {
         const size_t slices = size_t(tail) * CTAS * EPI_WARPS;
         const size_t count_bytes = (slices * sizeof(uint32_t) + 255) / 256 * 256;
@@ -821,17 +824,19 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
 
 }  // namespace
 
-size_t gemm_smem_bytes(int ctas) { return ctas == 2 ? smem_bytes<2>() : smem_bytes<1>(); }
+size_t gemm_smem_bytes(int ctas) { return ctas == 2 ? smem_bytes<2, 2>() : smem_bytes<1, 1>(); }
 
 cudaError_t launch_gemm(Kind kind, bool b_mn_major, int epi, int ctas, const CUtensorMap &ta,
                         const CUtensorMap &tb, const GemmArgs &args, int sms, cudaMemPool_t pool,
                         cudaStream_t stream) {
 #define PTC_LAUNCH(K, BMN, E)                                                    \
-    return ctas == 2 ? launch_one<K, BMN, E, 2>(ta, tb, args, sms, pool, stream) \
-                     : launch_one<K, BMN, E, 1>(ta, tb, args, sms, pool, stream)
+    return ctas == 1 ? launch_one<K, BMN, E, 1, 1>(ta, tb, args, sms, pool, stream)          \
+           : args.stage_kb == 1 ? launch_one<K, BMN, E, 2, 1>(ta, tb, args, sms, pool, stream) \
+                                : launch_one<K, BMN, E, 2, 2>(ta, tb, args, sms, pool, stream)
     if (kind == Kind::F16 && b_mn_major && epi == EPI_F32) PTC_LAUNCH(Kind::F16, true, EPI_F32);
     if (kind == Kind::F16 && b_mn_major && epi == EPI_F16ACC) PTC_LAUNCH(Kind::F16, true, EPI_F16ACC);
     if (kind == Kind::F16 && !b_mn_major && epi == EPI_INT) PTC_LAUNCH(Kind::F16, false, EPI_INT);
+    if (kind == Kind::F16 && b_mn_major && epi == EPI_INT) PTC_LAUNCH(Kind::F16, true, EPI_INT);
     if (kind == Kind::E4M3 && !b_mn_major && epi == EPI_INT) PTC_LAUNCH(Kind::E4M3, false, EPI_INT);
 #undef PTC_LAUNCH
     return cudaErrorInvalidValue;

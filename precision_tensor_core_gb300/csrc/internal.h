@@ -36,6 +36,7 @@ struct GemmArgs {
     // run as two units each over the two halves of K, num_vunits units in all;
     // the halves exchange partial sums through split_part, ordered by the
     // arrival counters split_count (zero at launch).
+    int stage_kb;          // CTA pairs: K blocks per ring stage, 1 or 2 (0: 2)
     int c_wide;            // 1: C's base and pitch allow 32-byte stores (set by launch_gemm)
     int split_ok;          // 1: the tail may be split (tuning knob "tail_split")
     int split_min_kb;      // ... when K spans at least this many K blocks

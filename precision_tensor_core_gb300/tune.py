@@ -7,10 +7,12 @@
 and mma.sync) beside the library's tcgen05 entry points at each size, and
 prints the paper's speedup definitions: each kernel over the WMMA kernel of
 its precision, and over the FP16 WMMA kernel.
-`variants` times gemm_f16_f16acc against gemm_f16, and gemm_s8_scaled /
-gemm_s4_scaled (each output type) against gemm_s8 / gemm_s4, at one size.
+`variants` times gemm_f16_f16acc against gemm_f16, gemm_s8_b_rowmajor (B
+row-major, read MN-major) against gemm_s8 (B column-major), and
+gemm_s8_scaled / gemm_s4_scaled (each output type) against gemm_s8 / gemm_s4,
+at one size.
 `knobs` times gemm_f16 / gemm_s8 / gemm_s4 at one size under each setting of
-the library's tuning knobs (ptc_set_tuning: CTA pairs, tail split, raster group, L2
+the library's tuning knobs (ptc_set_tuning: CTA pairs, pair ring stage depth, tail split, raster group, L2
 eviction policy, INT fold length), one knob at a time from the defaults: the
 ablation that shows the defaults are a local optimum.  `sizes` times the three
 entry points at each size with the library defaults.  `cublas` times gemm_f16
@@ -39,8 +41,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 DEFAULTS = {"cta_pair": 0, "group_m": 8, "l2_hint": 0, "s8_chunk_kb": 16,
-            "s4_chunk_kb": 64, "tail_split": 1, "split_min_kb": 64}
-KNOBS = {"cta_pair": [1, 2], "tail_split": [0], "split_min_kb": [16, 32], "group_m": [4, 16, 32], "l2_hint": [1, 2, 3],
+            "s4_chunk_kb": 64, "tail_split": 1, "split_min_kb": 64, "pair_stage_kb": 2}
+KNOBS = {"cta_pair": [1, 2], "pair_stage_kb": [1], "tail_split": [0], "split_min_kb": [16, 32], "group_m": [4, 16, 32], "l2_hint": [1, 2, 3],
          "s8_chunk_kb": [4, 8], "s4_chunk_kb": [2, 8, 16, 128]}
 
 
@@ -208,6 +210,15 @@ def main():
         Ch = torch.empty((n, n), dtype=torch.float16, device=dev)
         for key, fn in (("gemm_f16 -> f32", call("f16", ops, n)),
                         ("gemm_f16_f16acc -> f16", lambda: ptc.matmul_f16_f16acc(A, B, out=Ch))):
+            ms = time_ms(fn, calls)
+            results[key] = {"ms": ms, "tops": 2.0 * n ** 3 / (ms * 1e-3) / 1e12}
+            print(f"{key:>24} {results[key]['tops']:>8.1f} {ms:>8.4f}", flush=True)
+        A8, B8, C8 = ops["s8"]
+        B8_kn = B8.t().contiguous()  # the same B, row-major (K x N)
+        for key, fn in (("gemm_s8 (B col-major)", call("s8", ops, n)),
+                        ("gemm_s8_b_rowmajor", lambda: ptc.gemm_s8_b_rowmajor(
+                            n, n, n, A8.data_ptr(), n, B8_kn.data_ptr(), n, C8.data_ptr(), n,
+                            torch.cuda.current_stream().cuda_stream))):
             ms = time_ms(fn, calls)
             results[key] = {"ms": ms, "tops": 2.0 * n ** 3 / (ms * 1e-3) / 1e12}
             print(f"{key:>24} {results[key]['tops']:>8.1f} {ms:>8.4f}", flush=True)

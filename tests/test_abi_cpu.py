@@ -57,12 +57,12 @@ def good_args(name, M=64, N=64, K=64):
     A = BASE
     B = BASE + (1 << 30)
     C = BASE + (1 << 31)
-    if name == "gemm_f16":
+    if name in ("gemm_f16", "gemm_s8_b_rowmajor"):
         return dict(M=M, N=N, K=K, A=A, lda=K, B=B, ldb=N, C=C, ldc=N)
     return dict(M=M, N=N, K=K, A=A, lda=K, B=B, ldb=K, C=C, ldc=N)
 
 
-NAMES = ["gemm_f16", "gemm_s8", "gemm_s4"]
+NAMES = ["gemm_f16", "gemm_s8", "gemm_s4", "gemm_s8_b_rowmajor"]
 
 
 @pytest.mark.parametrize("name", NAMES)
@@ -75,7 +75,7 @@ def test_invalid_sizes_and_pointers(L, name):
     assert call(L, name, **{**g, "B": None}) == ptc.PTC_ERR_INVALID
     assert call(L, name, **{**g, "lda": g["K"] - 1}) == ptc.PTC_ERR_INVALID
     assert call(L, name, **{**g, "ldc": g["N"] - 4}) == ptc.PTC_ERR_INVALID
-    bad_ldb = g["N"] - 1 if name == "gemm_f16" else g["K"] - 1
+    bad_ldb = g["N"] - 1 if name in ("gemm_f16", "gemm_s8_b_rowmajor") else g["K"] - 1
     assert call(L, name, **{**g, "ldb": bad_ldb}) == ptc.PTC_ERR_INVALID
 
 
@@ -94,7 +94,7 @@ def test_alignment(L, name):
     assert call(L, name, **{**g, "B": g["B"] + 4}) == ptc.PTC_ERR_ALIGN
     assert call(L, name, **{**g, "C": g["C"] + 4}) == ptc.PTC_ERR_ALIGN
     assert call(L, name, **{**g, "ldc": 66}) == ptc.PTC_ERR_ALIGN
-    pitch_bad = {"gemm_f16": 68, "gemm_s8": 72, "gemm_s4": 80}[name]
+    pitch_bad = {"gemm_f16": 68, "gemm_s8": 72, "gemm_s4": 80, "gemm_s8_b_rowmajor": 72}[name]
     assert call(L, name, **{**g, "lda": pitch_bad}) == ptc.PTC_ERR_ALIGN
 
 
@@ -110,7 +110,7 @@ def test_overlap(L, name):
     assert call(L, name, **{**g, "C": g["A"]}) == ptc.PTC_ERR_OVERLAP
     assert call(L, name, **{**g, "C": g["B"] + 64}) == ptc.PTC_ERR_OVERLAP
     # adjacent but disjoint is fine up to the device check
-    esize = {"gemm_f16": 2, "gemm_s8": 1, "gemm_s4": 0.5}[name]
+    esize = {"gemm_f16": 2, "gemm_s8": 1, "gemm_s4": 0.5, "gemm_s8_b_rowmajor": 1}[name]
     a_end = g["A"] + int(((g["M"] - 1) * g["lda"] + g["K"]) * esize)
     r = call(L, name, **{**g, "C": (a_end + 15) // 16 * 16})
     assert r != ptc.PTC_ERR_OVERLAP
@@ -137,7 +137,7 @@ def test_status_strings_and_tuning(L):
     assert ptc.ptc_set_tuning("group_m", 16) == 0
     assert ptc.ptc_set_tuning("group_m", 8) == 0
     for key, bad, good in (("split_min_kb", 1, 64), ("tail_split", 2, 1), ("cta_pair", 3, 0),
-                           ("s8_chunk_kb", 3, 16), ("s4_chunk_kb", 7, 64)):
+                           ("s8_chunk_kb", 3, 16), ("s4_chunk_kb", 7, 64), ("pair_stage_kb", 3, 2)):
         with pytest.raises(ptc.PtcError):
             ptc.ptc_set_tuning(key, bad)
         assert ptc.ptc_set_tuning(key, good) == 0

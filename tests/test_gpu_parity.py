@@ -420,3 +420,37 @@ def test_wait_timeout_is_reported_and_context_survives(cta_mode):
     torch.cuda.synchronize()
     check_f16(C.cpu().numpy(), A, B)
     assert ptc.gemm_poll_device_error() == ptc.PTC_OK
+
+
+@pytest.mark.parametrize("stage_kb", [1, 2])
+@pytest.mark.parametrize("M,N,K", [(300, 520, 200), (257, 513, 1000), (512, 1024, 4160), (136, 264, 129)])
+def test_pair_ring_stage_depths(M, N, K, stage_kb):
+    """CTA pairs with one- or two-block ring stages (odd K block counts leave a
+    zero-filled block in the last two-block stage)."""
+    ptc.ptc_set_tuning("cta_pair", 2)
+    ptc.ptc_set_tuning("pair_stage_kb", stage_kb)
+    try:
+        A, B = datagen.f16_operands(N, "normal", seed=M + K, m=M, k=K)
+        A, B = pad_cols(A, 8), pad_cols(B, 8)
+        Cd = torch.empty((M, (N + 3) // 4 * 4), dtype=torch.float32, device=DEV)
+        Ad, Bd = f16_dev(A), f16_dev(B)
+        ptc.gemm_f16(M, N, K, Ad.data_ptr(), Ad.shape[1], Bd.data_ptr(), Bd.shape[1], Cd.data_ptr(), Cd.shape[1], 0)
+        torch.cuda.synchronize()
+        check_f16(Cd.cpu().numpy()[:, :N], A[:, :K], B[:K, :N])
+        A8, Bt8 = datagen.s8_operands(N, seed=M + K + 1, m=M, k=K)
+        A8, Bt8 = pad_cols(A8, 16), pad_cols(Bt8, 16)
+        Ci = torch.empty((M, (N + 3) // 4 * 4), dtype=torch.int32, device=DEV)
+        Ad, Bd = int_dev(A8), int_dev(Bt8)
+        ptc.gemm_s8(M, N, K, Ad.data_ptr(), A8.shape[1], Bd.data_ptr(), Bt8.shape[1], Ci.data_ptr(), Ci.shape[1], 0)
+        torch.cuda.synchronize()
+        assert np.array_equal(Ci.cpu().numpy()[:, :N], oracle.wrap_s32(oracle.gemm_s8(A8[:, :K], Bt8[:, :K])))
+        Ap = s4_packed_padded(datagen.uniform_s4_values(M + K + 2, M, K))
+        Bp = s4_packed_padded(datagen.uniform_s4_values(M + K + 3, N, K))
+        Ad, Bd = int_dev(Ap), int_dev(Bp)
+        ptc.gemm_s4(M, N, K, Ad.data_ptr(), 2 * Ap.shape[1], Bd.data_ptr(), 2 * Bp.shape[1], Ci.data_ptr(),
+                    Ci.shape[1], 0)
+        torch.cuda.synchronize()
+        assert np.array_equal(Ci.cpu().numpy()[:, :N], oracle.wrap_s32(oracle.gemm_s4(Ap, Bp, K)))
+    finally:
+        ptc.ptc_set_tuning("pair_stage_kb", 2)
+        ptc.ptc_set_tuning("cta_pair", 0)
