@@ -242,6 +242,9 @@ int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 namespace ptc {
 void note_launches(uint64_t n) { g_launches.fetch_add(n); }
 void set_message(const char *text) { std::snprintf(g_msg, sizeof(g_msg), "%s", text); }
+int encode_tmap_c32(CUtensorMap *map, const void *C, uint64_t n, uint64_t m, uint64_t ldc) {
+    return make_tmap(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, C, n, m, ldc * 4, 32, 32);
+}
 int encode_tmap_2d(CUtensorMap *map, bool one_byte, const void *base, uint64_t inner, uint64_t outer,
                    uint64_t pitch, uint32_t box_inner, uint32_t box_outer) {
     return make_tmap(map, one_byte ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,

@@ -90,6 +90,12 @@ struct SharedTail {
     AbortState abort;
 };
 
+// A single-wave launch stages C for TMA stores in the ring, which is idle once
+// a CTA's only tile has been multiplied: 32 x 128 four-byte values per
+// epilogue warp (four 32 x 32 blocks of 4 KiB).
+constexpr int kStageC = 32 * 32 * 4;
+constexpr int kStageWarp = 4 * kStageC;
+
 template <int CTAS, int SUBK>
 constexpr size_t smem_bytes() {
     return 1024 + size_t(Cfg<CTAS, SUBK>::STAGES) * Cfg<CTAS, SUBK>::STAGE +
@@ -97,6 +103,10 @@ constexpr size_t smem_bytes() {
 }
 static_assert(smem_bytes<1, 1>() <= 232448 && smem_bytes<2, 1>() <= 232448 && smem_bytes<2, 2>() <= 232448,
               "shared memory budget");
+static_assert(Cfg<1, 1>::STAGES * Cfg<1, 1>::STAGE >= EPI_WARPS * kStageWarp &&
+                  Cfg<2, 1>::STAGES * Cfg<2, 1>::STAGE >= EPI_WARPS * kStageWarp &&
+                  Cfg<2, 2>::STAGES * Cfg<2, 2>::STAGE >= EPI_WARPS * kStageWarp,
+              "the ring holds the C staging of a single-wave launch");
 
 __device__ __forceinline__ void tile_coords(int t, const GemmArgs &a, int &mb, int &nb) {
     const int per_group = a.group_m * a.tiles_n;
@@ -229,18 +239,75 @@ __device__ __forceinline__ void store_32(T *dst, const uint32_t (&v)[32], int va
     }
 }
 
+// A 32 x 32 block of 4-byte C through a staging buffer `stg` (1024-byte
+// aligned; row `lane` holds the lane's 32 values in 128 bytes with the
+// 128-byte swizzle, so that the warp's writes do not conflict), then to C at
+// (col, row0) by one TMA store that clips at M and N:
+//   stage_begin, stage_put for each 16-byte piece j = 0..7, stage_end.
+// A store reads its buffer asynchronously; stage_begin with `wait` first
+// waits until every earlier store of this warp has read its buffer.
+__device__ __forceinline__ void stage_begin(int lane, bool wait) {
+    if (wait) {
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+    }
+}
+
+__device__ __forceinline__ void stage_put(uint32_t stg, int lane, int j, uint32_t a, uint32_t b, uint32_t c,
+                                          uint32_t d) {
+    st_shared_v4(stg + uint32_t(lane) * 128u + (uint32_t(j ^ (lane & 7)) << 4), a, b, c, d);
+}
+
+__device__ __forceinline__ void stage_end(const CUtensorMap *tmC, uint32_t stg, int lane, int col, int row0) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        tma_store_2d(tmC, stg, col, row0);
+        bulk_commit_group();
+    }
+}
+
+__device__ __forceinline__ void tma_store_block(const CUtensorMap *tmC, uint32_t stg, const uint32_t (&v)[32],
+                                                int lane, int col, int row0, bool wait) {
+    stage_begin(lane, wait);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) stage_put(stg, lane, j, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    stage_end(tmC, stg, lane, col, row0);
+}
+
 // Scaled integer epilogue (dequantisation): for the 128 columns col0 .. of
 // `row`, value = rn(rn(rn(float(acc)) * sa) * sb) in FP32, in that order and
 // without contraction, then rounded to nearest-even in the output type.
 // Columns at or beyond N are not written.
 __device__ __forceinline__ void store_scaled_row(const GemmArgs &args, int row, int col0,
-                                                 const int32_t (&acc)[kBN / 2]) {
-    const float sa = args.scale_a ? __ldg(args.scale_a + row) : 1.0f;
+                                                 const int32_t (&acc)[kBN / 2], const CUtensorMap *tmC,
+                                                 uint32_t stg, int lane, int row0, bool pending) {
+    const float sa = (args.scale_a && row < args.M) ? __ldg(args.scale_a + row) : 1.0f;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         const int cc = col0 + 32 * c;
         if (cc >= args.N) break;
         const int valid = min(32, args.N - cc);
+        if (args.c_tma) {
+            // FP32 output through the staging buffer (the whole warp takes part).
+            const uint32_t blk = stg + uint32_t(c * kStageC);
+            stage_begin(lane, pending && c == 0);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                float f4[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int jj = 4 * j + e;
+                    const float sb = (args.scale_b && jj < valid) ? __ldg(args.scale_b + cc + jj) : 1.0f;
+                    f4[e] = __fmul_rn(__fmul_rn(__int2float_rn(acc[32 * c + jj]), sa), sb);
+                }
+                stage_put(blk, lane, j, __float_as_uint(f4[0]), __float_as_uint(f4[1]), __float_as_uint(f4[2]),
+                          __float_as_uint(f4[3]));
+            }
+            stage_end(tmC, blk, lane, cc, row0);
+            continue;
+        }
+        if (row >= args.M) continue;
         float f[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
@@ -372,7 +439,7 @@ __device__ __forceinline__ void split_epilogue(uint32_t t_acc, uint32_t *cnt, fl
 template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const GemmArgs args) {
+                const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
     static_assert(!(B_MN && KIND == Kind::E4M3), "MN-major B is used by the FP16 path only");
     constexpr bool INT_OUT = EPI == EPI_INT;
     using C_ = Cfg<CTAS, SUBK>;
@@ -406,6 +473,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if (args.c_tma) tma_prefetch_desc(&tmC);
     }
     if (warp == 1) {
         tmem_alloc<CTAS>(&st->tmem_base, TMEM_COLS);
@@ -590,6 +658,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------ epilogue
         const int q = warp & 3;             // tensor-memory lane quarter
         const int h = (warp - 2) >> 2;      // column half of the tile
+        // Single-wave launches: this warp's four C staging blocks in the idle ring.
+        const uint32_t stg = smem_u32(smem) + uint32_t(warp - 2) * uint32_t(kStageWarp);
+        bool stg_pending = false;           // TMA stores may still be reading the blocks
         const uint32_t t_lane = tmem_base + (uint32_t(32 * q) << 16) + uint32_t(h * (kBN / 2));
         // Accumulator buffers are released on the issuing (even) CTA's barriers.
         auto release = [&](int b) {
@@ -659,8 +730,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                         acc[4 * i + 3] = int32_t(uint32_t(acc[4 * i + 3]) + uint32_t(__float_as_int(o.w)));
                     }
                 }
-                if (row < args.M) {
-                    if (args.out_mode == OUT_S32) {
+                const int row0 = row - lane;  // first row of this warp's 32
+                if (args.out_mode == OUT_S32 && args.c_tma) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int cc = col0 + 32 * c;
+                        if (cc < args.N)
+                            tma_store_block(&tmC, stg + uint32_t(c * kStageC),
+                                            reinterpret_cast<const uint32_t(&)[32]>(acc[32 * c]), lane, cc, row0,
+                                            stg_pending && c == 0);
+                    }
+                    stg_pending = true;
+                } else if (args.out_mode == OUT_S32) {
+                    if (row < args.M) {
                         int32_t *crow = reinterpret_cast<int32_t *>(args.C) + int64_t(row) * args.ldc;
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
@@ -669,9 +751,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 store_32(crow + cc, reinterpret_cast<const uint32_t(&)[32]>(acc[32 * c]), args.N - cc,
                                          args.c_wide);
                         }
-                    } else {
-                        store_scaled_row(args, row, col0, acc);
                     }
+                } else {
+                    store_scaled_row(args, row, col0, acc, &tmC, stg, lane, row0, stg_pending);
+                    stg_pending = stg_pending || args.c_tma;
                 }
             } else {
                 if (!warp_wait(&st->acc_full[abuf], aph, &st->abort, limit, lane)) {
@@ -679,7 +762,19 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                if (wr.part == 0) {
+                if (wr.part == 0 && EPI == EPI_F32 && args.c_tma) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        uint32_t r[32];
+                        tmem_ld_32cols(t_lane + uint32_t(abuf * kBN + 32 * c), r);
+                        tmem_ld_wait();
+                        const int cc = col0 + 32 * c;
+                        if (cc < args.N)
+                            tma_store_block(&tmC, stg + uint32_t(c * kStageC), r, lane, cc, row - lane,
+                                            stg_pending && c == 0);
+                    }
+                    stg_pending = true;
+                } else if (wr.part == 0) {
                     float *crow = reinterpret_cast<float *>(args.C) + int64_t(row) * args.ldc;
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
@@ -712,6 +807,10 @@ __global__ void __launch_bounds__(THREADS, 1)
                 }
             }
         }
+        // Every TMA store of C has read its staging block before the CTA exits
+        // (the writes themselves complete with the grid).
+        if (stg_pending && lane == 0) bulk_wait_group_read0();
+        __syncwarp();
     }
 
     tc_fence_before_sync();
@@ -785,6 +884,12 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
     // 32-byte C stores (whole L2 sectors) when C's base and row pitch allow them.
     const int64_t esize = (EPI == EPI_F16ACC || (EPI == EPI_INT && (a.out_mode == OUT_BF16 || a.out_mode == OUT_F16))) ? 2 : 4;
     a.c_wide = (reinterpret_cast<uintptr_t>(a.C) % 32 == 0 && (a.ldc * esize) % 32 == 0) ? 1 : 0;
+    // 4-byte C (FP32, int32, scaled FP32) is written by TMA stores of 32 x 32
+    // blocks staged in shared memory; 16-bit C by 16/32-byte stores per lane.
+    CUtensorMap tc;
+    std::memset(&tc, 0, sizeof(tc));
+    a.c_tma = 0;
+    const bool tma_c = esize == 4;
     const int maxc = cache.max_clusters;
     const int tail = a.num_tiles < maxc ? a.num_tiles : a.num_tiles % maxc;
     a.tail_split = 0;
@@ -815,8 +920,14 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
     }
     a.num_vunits = a.num_tiles + a.tail_split;
     const int clusters = a.num_vunits < maxc ? a.num_vunits : maxc;
+    // Single wave (at most one unit per cluster): the epilogue is not hidden
+    // behind a next tile, so C goes out by TMA stores staged in the idle ring;
+    // otherwise by 32-byte stores, which keep the TMA engine to the operand loads.
+    if (tma_c && a.num_vunits <= maxc &&
+        encode_tmap_c32(&tc, a.C, uint64_t(a.N), uint64_t(a.M), uint64_t(a.ldc)) == 0)
+        a.c_tma = 1;
     cfg.gridDim = dim3(CTAS * clusters, 1, 1);
-    e = cudaLaunchKernelEx(&cfg, fn, ta, tb, a);
+    e = cudaLaunchKernelEx(&cfg, fn, ta, tb, tc, a);
     if (ws != nullptr) cudaFreeAsync(ws, stream);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

@@ -38,6 +38,7 @@ struct GemmArgs {
     // arrival counters split_count (zero at launch).
     int stage_kb;          // CTA pairs: K blocks per ring stage, 1 or 2 (0: 2)
     int c_wide;            // 1: C's base and pitch allow 32-byte stores (set by launch_gemm)
+    int c_tma;             // 1: 4-byte C written by TMA stores through shared memory (set by launch_gemm)
     int split_ok;          // 1: the tail may be split (tuning knob "tail_split")
     int split_min_kb;      // ... when K spans at least this many K blocks
     int tail_split;
@@ -121,6 +122,9 @@ void note_launches(uint64_t n);
 void set_message(const char *text);
 // TMA tensor map of a row-major matrix (2-byte elements, or 1-byte when
 // one_byte), 128-byte swizzle, zero fill outside; returns a PTC_* status.
+// C as 4-byte elements: N x M (ldc elements between rows), boxes of 32 x 32
+// with the 128-byte swizzle, for the epilogue's TMA stores.
+int encode_tmap_c32(CUtensorMap *map, const void *C, uint64_t n, uint64_t m, uint64_t ldc);
 int encode_tmap_2d(CUtensorMap *map, bool one_byte, const void *base, uint64_t inner, uint64_t outer,
                    uint64_t pitch, uint32_t box_inner, uint32_t box_outer);
 
