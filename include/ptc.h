@@ -324,9 +324,10 @@ int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile);
  *   "l2_hint"      L2 eviction policy of operand loads: 0 (default) none;
  *                  1 A evict-last / B evict-first; 2 A evict-last; 3 both
  *                  evict-normal (all measured slower than 0 on GB300)
- *   "cta_pair"     0 (default): one CTA per 128 x 256 output tile while such
- *                  tiles leave SMs idle, else clusters of two CTAs sharing
- *                  256 x 256 tiles (tcgen05 cta_group::2); 1: always one CTA;
+ *   "cta_pair"     0 (default): clusters of two CTAs sharing 256 x 256
+ *                  tiles (tcgen05 cta_group::2) once 128 x 256 one-CTA tiles
+ *                  would fill the SMs, and for FP16 from 32 one-CTA tiles up;
+ *                  otherwise one CTA per 128 x 256 tile; 1: always one CTA;
  *                  2: always CTA pairs.  Results do not depend on the choice
  *                  except through the FP16 summation order.
  *   "tail_split"   1 (default): when K spans at least split_min_kb K

@@ -187,11 +187,18 @@ int fail(int code, const char *text) {
 // One CTA per 128 x 256 tile while that leaves SMs idle; CTA pairs on
 // 256 x 256 tiles (half the B traffic per CTA, deeper ring) once the one-CTA
 // tiles cover every SM.
-int choose_ctas(int64_t M, int64_t N, int sms) {
+// One CTA per 128 x 256 tile, or CTA pairs on 256 x 256 tiles.  Pairs move a
+// third fewer operand bytes per output, and once one-CTA tiles fill the GPU
+// they are faster for every route; below that, measured per route: FP16
+// pairs were faster from 32 one-CTA tiles up (N = 1024 .. 2048: 4-10%), the
+// integer routes (binary16 / E4M3 operands from a conversion pass) were
+// faster with one CTA per tile.
+int choose_ctas(int64_t M, int64_t N, int sms, bool f16) {
     const int forced = g_cta_pair.load();
     if (forced == 1 || forced == 2) return forced;
     const int64_t tiles1 = ((M + ptc::kBM - 1) / ptc::kBM) * ((N + ptc::kBN - 1) / ptc::kBN);
-    return tiles1 >= sms ? 2 : 1;
+    if (tiles1 >= sms) return 2;
+    return (f16 && tiles1 >= 32) ? 2 : 1;
 }
 
 GemmArgs base_args(int64_t M, int64_t N, int64_t K, int k_elems_per_block, void *C, int64_t ldc,
@@ -280,7 +287,7 @@ int f16_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0) return zero_c(C, ldc, M, N, eb, *d, s);
 
-    const int ctas = choose_ctas(M, N, d->sms);
+    const int ctas = choose_ctas(M, N, d->sms, true);
     CUtensorMap ta, tb;
     if ((rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, uint64_t(lda) * 2, 64, ptc::kBM)))
         return rc;
@@ -382,7 +389,7 @@ int int_gemm(bool s4, int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
         rc = fail_cuda(e, "operand conversion launch");
     else
         g_launches.fetch_add(1);
-    const int ctas = choose_ctas(M, N, d->sms);
+    const int ctas = choose_ctas(M, N, d->sms, false);
     const CUtensorMapDataType dt = s4 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap ta, tb;
     if (!rc) rc = make_tmap(&ta, dt, aw, K, M, uint64_t(ldw) * wsize, k_elems, ptc::kBM);
@@ -448,7 +455,7 @@ int s8_rowb_gemm(int64_t M, int64_t N, int64_t K, const int8_t *A, int64_t lda, 
         if (e == cudaSuccess) g_launches.fetch_add(1);
     }
     if (e != cudaSuccess) rc = fail_cuda(e, "operand conversion launch");
-    const int ctas = choose_ctas(M, N, d->sms);
+    const int ctas = choose_ctas(M, N, d->sms, false);
     CUtensorMap ta, tb;
     if (!rc) rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, aw, K, M, uint64_t(ldw_a) * 2, 64, ptc::kBM);
     if (!rc) rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bw, N, K, uint64_t(ldw_b) * 2, 64, 64);
@@ -628,7 +635,7 @@ int host_gemm(int prec, int64_t M, int64_t N, int64_t K, const void *A, int64_t 
     for (int p = 0; p < npanels && rc == PTC_OK; ++p) {
         const int64_t r0 = p * panel, rows = std::min(panel, M - r0);
         cuda(cudaStreamWaitEvent(s, ev_a[p], 0), "stream wait");
-        const int ctas = choose_ctas(rows, N, d->sms);
+        const int ctas = choose_ctas(rows, N, d->sms, f16);
         CUtensorMap ta, tb;
         if (f16) {
             if (rc == PTC_OK)

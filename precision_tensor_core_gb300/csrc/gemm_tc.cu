@@ -281,14 +281,14 @@ __device__ __forceinline__ void tma_store_block(const CUtensorMap *tmC, uint32_t
 // Columns at or beyond N are not written.
 __device__ __forceinline__ void store_scaled_row(const GemmArgs &args, int row, int col0,
                                                  const int32_t (&acc)[kBN / 2], const CUtensorMap *tmC,
-                                                 uint32_t stg, int lane, int row0, bool pending) {
+                                                 bool use_tma, uint32_t stg, int lane, int row0, bool pending) {
     const float sa = (args.scale_a && row < args.M) ? __ldg(args.scale_a + row) : 1.0f;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         const int cc = col0 + 32 * c;
         if (cc >= args.N) break;
         const int valid = min(32, args.N - cc);
-        if (args.c_tma) {
+        if (use_tma) {
             // FP32 output through the staging buffer (the whole warp takes part).
             const uint32_t blk = stg + uint32_t(c * kStageC);
             stage_begin(lane, pending && c == 0);
@@ -658,7 +658,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         // ------------------------------------------------------ epilogue
         const int q = warp & 3;             // tensor-memory lane quarter
         const int h = (warp - 2) >> 2;      // column half of the tile
-        // Single-wave launches: this warp's four C staging blocks in the idle ring.
+        // The unit whose 4-byte C goes out by TMA stores (this cluster's last, or
+        // none), and this warp's four C staging blocks in the idle ring.
+        const int tma_t = (EPI == EPI_F32 && args.c_tma && cluster < args.num_vunits)
+                              ? cluster + (args.num_vunits - 1 - cluster) / nclusters * nclusters
+                              : -1;
         const uint32_t stg = smem_u32(smem) + uint32_t(warp - 2) * uint32_t(kStageWarp);
         bool stg_pending = false;           // TMA stores may still be reading the blocks
         const uint32_t t_lane = tmem_base + (uint32_t(32 * q) << 16) + uint32_t(h * (kBN / 2));
@@ -731,7 +735,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
                 const int row0 = row - lane;  // first row of this warp's 32
-                if (args.out_mode == OUT_S32 && args.c_tma) {
+                // Integer routes: TMA stores in single-wave launches (every unit
+                // is its cluster's last); a per-unit choice, as the FP32 path
+                // makes, costs this register-bound epilogue spills.
+                const bool use_tma = args.c_tma && args.num_vunits <= nclusters;
+                if (args.out_mode == OUT_S32 && use_tma) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         const int cc = col0 + 32 * c;
@@ -753,8 +761,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                         }
                     }
                 } else {
-                    store_scaled_row(args, row, col0, acc, &tmC, stg, lane, row0, stg_pending);
-                    stg_pending = stg_pending || args.c_tma;
+                    const bool tma_f32 = use_tma && args.out_mode == OUT_F32;
+                    store_scaled_row(args, row, col0, acc, &tmC, tma_f32, stg, lane, row0, stg_pending);
+                    stg_pending = stg_pending || tma_f32;
                 }
             } else {
                 if (!warp_wait(&st->acc_full[abuf], aph, &st->abort, limit, lane)) {
@@ -762,7 +771,11 @@ __global__ void __launch_bounds__(THREADS, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                if (wr.part == 0 && EPI == EPI_F32 && args.c_tma) {
+                // This cluster's last unit: its epilogue is not hidden behind a
+                // next tile, and the ring is idle once the unit has been
+                // multiplied, so 4-byte C goes out by TMA stores staged there.
+                const bool use_tma = t == tma_t;
+                if (wr.part == 0 && EPI == EPI_F32 && use_tma) {
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t r[32];
@@ -920,12 +933,10 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
     }
     a.num_vunits = a.num_tiles + a.tail_split;
     const int clusters = a.num_vunits < maxc ? a.num_vunits : maxc;
-    // Single wave (at most one unit per cluster): the epilogue is not hidden
-    // behind a next tile, so C goes out by TMA stores staged in the idle ring;
-    // otherwise by 32-byte stores, which keep the TMA engine to the operand loads.
-    if (tma_c && a.num_vunits <= maxc &&
-        encode_tmap_c32(&tc, a.C, uint64_t(a.N), uint64_t(a.M), uint64_t(a.ldc)) == 0)
-        a.c_tma = 1;
+    // Each cluster's last unit writes 4-byte C by TMA stores staged in the idle
+    // ring (its epilogue is exposed); earlier units use 32-byte stores, which
+    // leave the TMA engine to the operand loads while the next tile runs.
+    if (tma_c && encode_tmap_c32(&tc, a.C, uint64_t(a.N), uint64_t(a.M), uint64_t(a.ldc)) == 0) a.c_tma = 1;
     cfg.gridDim = dim3(CTAS * clusters, 1, 1);
     e = cudaLaunchKernelEx(&cfg, fn, ta, tb, tc, a);
     if (ws != nullptr) cudaFreeAsync(ws, stream);

@@ -38,7 +38,8 @@ struct GemmArgs {
     // arrival counters split_count (zero at launch).
     int stage_kb;          // CTA pairs: K blocks per ring stage, 1 or 2 (0: 2)
     int c_wide;            // 1: C's base and pitch allow 32-byte stores (set by launch_gemm)
-    int c_tma;             // 1: 4-byte C written by TMA stores through shared memory (set by launch_gemm)
+    int c_tma;             // 1: a TMA map of 4-byte C is passed; each cluster's last unit stores
+                           // through it (set by launch_gemm)
     int split_ok;          // 1: the tail may be split (tuning knob "tail_split")
     int split_min_kb;      // ... when K spans at least this many K blocks
     int tail_split;
