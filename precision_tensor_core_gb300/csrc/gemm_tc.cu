@@ -16,15 +16,24 @@
 //               ldmatrix + mma.sync and register accumulators).
 //   warps 2-9   epilogue: tcgen05.ld tensor memory -> registers -> global C,
 //               overlapped with the next tile's MMAs through the second
-//               accumulator buffer.
+//               accumulator buffer; 32-byte stores per lane, or 32 x 32
+//               blocks staged in the then idle ring and written by TMA stores
+//               where nothing hides the epilogue (4-byte C of a single-wave
+//               launch, and the last tile of each cluster in FP32 C).
 //
 // Two shapes of the same kernel:
-//   CTAS = 1    one CTA per 128 x 256 output tile (M = 128 MMAs), 4 stages.
+//   CTAS = 1    one CTA per 128 x 256 output tile (M = 128 MMAs), 4 stages of
+//               one K block.
 //   CTAS = 2    a cluster of two CTAs per 256 x 256 output tile
 //               (tcgen05 cta_group::2, M = 256 MMAs issued by the even CTA):
 //               each CTA stages its own 128 rows of A and half of B, so a CTA
-//               moves 32 KiB per stage instead of 48 KiB and the ring holds 7
-//               stages.
+//               moves 32 KiB per K block instead of 48 KiB; the ring holds 3
+//               stages of two K blocks (or, as a tuning choice, 7 of one).
+//
+// The work list: output tiles in grouped raster order, strided over the
+// clusters; when the last wave would leave at least half of the clusters idle,
+// its tiles run as two K halves whose epilogue warps add partial sums through
+// a workspace (see work_unit).
 //
 // Integer routes: sm_103a has no integer tcgen05 MMA, so INT8 runs on the
 // FP16 kind (every s8 value is an exact binary16) and INT4 on the E4M3 kind
