@@ -88,10 +88,10 @@ struct Cfg {
     static constexpr int STAGE = A_STAGE + B_STAGE;
 };
 
-template <int STAGES>
+template <int STAGES, int SUB>
 struct SharedTail {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
+    uint64_t full[STAGES * SUB];  // per K block of a stage: its operands have landed
+    uint64_t empty[STAGES];       // per stage: its MMAs have read it
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
@@ -108,7 +108,7 @@ constexpr int kStageWarp = 4 * kStageC;
 template <int CTAS, int SUBK>
 constexpr size_t smem_bytes() {
     return 1024 + size_t(Cfg<CTAS, SUBK>::STAGES) * Cfg<CTAS, SUBK>::STAGE +
-           sizeof(SharedTail<Cfg<CTAS, SUBK>::STAGES>);
+           sizeof(SharedTail<Cfg<CTAS, SUBK>::STAGES, SUBK>);
 }
 static_assert(smem_bytes<1, 1>() <= 232448 && smem_bytes<2, 1>() <= 232448 && smem_bytes<2, 2>() <= 232448,
               "shared memory budget");
@@ -459,7 +459,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     uint8_t *a_ring = smem;
     uint8_t *b_ring = smem + STAGES * C_::A_STAGE;
-    SharedTail<STAGES> *st = reinterpret_cast<SharedTail<STAGES> *>(smem + STAGES * C_::STAGE);
+    using Tail = SharedTail<STAGES, C_::SUB>;
+    Tail *st = reinterpret_cast<Tail *>(smem + STAGES * C_::STAGE);
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -470,7 +471,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&st->full[s], 1);
+            for (int sb = 0; sb < C_::SUB; ++sb) mbar_init(&st->full[s * C_::SUB + sb], 1);
             mbar_init(&st->empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -546,19 +547,22 @@ __global__ void __launch_bounds__(THREADS, 1)
                             outstanding |= 1u << s;
                             out_phase = (out_phase & ~(1u << s)) | (ph << s);
                         } else {
-                            // Both CTAs' copies complete on the even CTA's full barrier,
-                            // which alone expects the pair's bytes.
-                            const uint32_t bar = mapa_shared(smem_u32(&st->full[s]), 0);
-                            if (rank == 0) mbar_arrive_expect_tx(&st->full[s], CTAS * C_::STAGE);
-                            auto load = [&](void *dst, const CUtensorMap *map, int x, int y, uint64_t pol) {
-                                if (hint)
-                                    tma_load_2d_pair_hint(dst, map, bar, x, y, pol);
-                                else
-                                    tma_load_2d_pair(dst, map, bar, x, y);
-                            };
-                            // Two K blocks per stage; a block past K reads as zeros.
+                            // Both CTAs' copies of a K block complete on the even CTA's
+                            // full barrier of that block, which alone expects the pair's
+                            // bytes; each block has its own barrier, so that the MMAs
+                            // start on the first block of a stage while the second lands.
+                            // A block past K reads as zeros.
 #pragma unroll
                             for (int sb = 0; sb < C_::SUB; ++sb) {
+                                uint64_t *fb = &st->full[s * C_::SUB + sb];
+                                if (rank == 0) mbar_arrive_expect_tx(fb, CTAS * (C_::A_BLOCK + C_::B_BLOCK));
+                                const uint32_t bar = mapa_shared(smem_u32(fb), 0);
+                                auto load = [&](void *dst, const CUtensorMap *map, int x, int y, uint64_t pol) {
+                                    if (hint)
+                                        tma_load_2d_pair_hint(dst, map, bar, x, y, pol);
+                                    else
+                                        tma_load_2d_pair(dst, map, bar, x, y);
+                                };
                                 load(a_dst + sb * C_::A_BLOCK, &tmA, (kb + sb) * K_ELEMS, m0, pol_a);
                                 if constexpr (B_MN) {
 #pragma unroll
@@ -614,17 +618,21 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const uint32_t d_tmem = tmem_base + uint32_t(abuf * kBN);
                     const int kb0 = wr.kb0 + ch * args.kb_per_chunk;
                     const int kb1 = min(wr.kb1, kb0 + args.kb_per_chunk);
-                    for (int kb = kb0; kb < kb1; kb += C_::SUB) {
-                        if (!mbar_wait(&st->full[s], ph, &st->abort, &g_error_word, limit)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after_sync();
+                    for (int kb = kb0; kb < kb1 && ok; kb += C_::SUB) {
                         const uint32_t a_addr = a_base + s * C_::A_STAGE;
                         const uint32_t b_addr = b_base + s * C_::B_STAGE;
 #pragma unroll
                         for (int kk = 0; kk < KSTEPS * C_::SUB; ++kk) {
                             const int k = kk % KSTEPS;
+                            if (k == 0) {
+                                // The next K block of the stage has landed.
+                                if (!mbar_wait(&st->full[s * C_::SUB + kk / KSTEPS], ph, &st->abort, &g_error_word,
+                                               limit)) {
+                                    ok = false;
+                                    break;
+                                }
+                                tc_fence_after_sync();
+                            }
                             const uint32_t a_blk = a_addr + (kk / KSTEPS) * C_::A_BLOCK;
                             const uint32_t b_blk = b_addr + (kk / KSTEPS) * C_::B_BLOCK;
                             const uint64_t adesc = smem_desc_sw128(a_blk + k * KSTEP_BYTES, 16, 1024);
@@ -636,6 +644,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
                             mma<CTAS, KIND == Kind::E4M3>(d_tmem, adesc, bdesc, IDESC, acc);
                         }
+                        if (!ok) break;
                         if constexpr (CTAS == 1)
                             mma_commit<1>(&st->empty[s]);
                         else
