@@ -309,6 +309,14 @@ uint64_t ptc_kernel_launch_count(void);
  * launch only.  Returns PTC_OK. */
 int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile);
 
+/* Launch shape of the last GEMM kernel the calling thread launched through
+ * this library: *grid = CTAs launched, *cluster = CTAs per thread-block
+ * cluster (1; 2 for CTA pairs; KS for K-split clusters), *ksplit = CTAs that
+ * share one output tile's K range (1 when the tiles are not split that way).
+ * All zero before the first launch.  Host-side only (no device work).
+ * Returns PTC_OK, or PTC_ERR_INVALID when a pointer is NULL. */
+int ptc_last_launch(int *grid, int *cluster, int *ksplit);
+
 /* Tuning and test knobs, process-wide.  Returns PTC_OK, or PTC_ERR_INVALID for
  * an unknown key or a value out of range.  Keys:
  *   "group_m"      output-tile rows per raster group of the persistent
@@ -347,6 +355,24 @@ int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile);
  *                  tile is split, default 64 (the split saves about half a
  *                  tile's K loop and costs a few microseconds per call);
  *                  2 or more.
+ *   "ksplit"       small problems: when 128 x 256 one-CTA tiles would fill at
+ *                  most half of the SMs in one wave, each tile runs on a
+ *                  thread-block cluster of KS CTAs that share its K blocks
+ *                  (about 1/KS each) and add their partial sums through
+ *                  distributed shared memory, in rank order.  0 (default):
+ *                  the largest KS of 8, 4, 2 whose clusters fit one wave with
+ *                  at least one K block per CTA; 2, 4 or 8: only that KS
+ *                  (one CTA per tile when it does not fit); 1: never (the
+ *                  "cta_pair" rule decides alone).  Integer results do not
+ *                  depend on the choice; FP16 results differ by the summation
+ *                  order (a rank-ordered sum of KS FP32 partial sums), and
+ *                  FP16-accumulator results are rounded to binary16 once,
+ *                  from that FP32 sum.  No workspace is used.
+ *   "pdl"          1 (default): kernels are launched with programmatic
+ *                  stream serialization, so that a kernel can start (set up
+ *                  barriers and tensor memory) while the previous kernel of
+ *                  the stream finishes; it waits for that kernel before its
+ *                  first global-memory access.  0: plain stream order.
  * Values above the defaults can make gemm_s8 / gemm_s4 inexact for adversarial
  * inputs; they exist to measure the tensor cores' accumulation width. */
 int ptc_set_tuning(const char *key, int64_t value);

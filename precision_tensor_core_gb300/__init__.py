@@ -9,7 +9,7 @@ library's CUDA kernels):
 
 * ``gemm_f16``, ``gemm_f16_f16acc``, ``gemm_s8``, ``gemm_s4``, ``gemm_s8_scaled``, ``gemm_s4_scaled``,
   ``gemm_s8_noalloc``, ``gemm_s8_b_rowmajor``, ``gemm_status_string``,
-  ``gemm_poll_device_error``, ``ptc_kernel_launch_count``,
+  ``gemm_poll_device_error``, ``ptc_kernel_launch_count``, ``ptc_last_launch``,
   ``ptc_debug_set_wait_limit``, ``ptc_set_tuning``: the C ABI of
   ``include/ptc.h`` under the same names, taking integers (sizes, leading
   dimensions, device addresses, a cudaStream_t handle).  A nonzero status
@@ -93,6 +93,9 @@ def lib() -> ctypes.CDLL:
         L.ptc_debug_set_wait_limit.argtypes = [ctypes.c_uint64, _i64]
         L.ptc_set_tuning.restype = ctypes.c_int
         L.ptc_set_tuning.argtypes = [ctypes.c_char_p, _i64]
+        _ip = ctypes.POINTER(ctypes.c_int)
+        L.ptc_last_launch.restype = ctypes.c_int
+        L.ptc_last_launch.argtypes = [_ip, _ip, _ip]
         _lib = L
     return _lib
 
@@ -185,6 +188,14 @@ def ptc_debug_set_wait_limit(timeout_ns: int, stall_tile: int = -1) -> int:
 
 def ptc_set_tuning(key: str, value: int) -> int:
     return _check(lib().ptc_set_tuning(key.encode(), int(value)))
+
+
+def ptc_last_launch() -> tuple[int, int, int]:
+    """(grid CTAs, CTAs per cluster, CTAs sharing a tile's K range) of the
+    calling thread's last GEMM kernel launch."""
+    g, c, k = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().ptc_last_launch(ctypes.byref(g), ctypes.byref(c), ctypes.byref(k)))
+    return g.value, c.value, k.value
 
 
 # ---------------------------------------------------------------- torch layer

@@ -43,6 +43,8 @@ std::atomic<int> g_cta_pair{0};     // 0: by problem size, 1: one CTA per tile, 
 std::atomic<int> g_tail_split{1};   // 1: split a short last wave in K
 std::atomic<int> g_split_min_kb{64};
 std::atomic<int> g_pair_stage_kb{2};  // CTA pairs: K blocks per ring stage
+std::atomic<int> g_ksplit{0};         // K-split clusters: 0 by size, 1 never, 2 / 4 / 8 that size
+std::atomic<int> g_pdl{1};            // programmatic stream serialization of the library's kernels
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 std::atomic<int64_t> g_stall_tile{-1};
 
@@ -184,19 +186,19 @@ int fail(int code, const char *text) {
 }
 
 // ------------------------------------------------------------ launches
-// One CTA per 128 x 256 tile while that leaves SMs idle; CTA pairs on
-// 256 x 256 tiles (half the B traffic per CTA, deeper ring) once the one-CTA
-// tiles cover every SM.
-// One CTA per 128 x 256 tile, or CTA pairs on 256 x 256 tiles.  Pairs move a
-// third fewer operand bytes per output, and once one-CTA tiles fill the GPU
-// they are faster for every route; below that, measured per route: FP16
+// One CTA per 128 x 256 tile, or CTA pairs on 256 x 256 tiles.  One-CTA tiles
+// that fill at most half of the SMs run in K-split clusters (2-8 CTAs share
+// each tile's K blocks) when pick_ksplit takes them.  Otherwise pairs, which
+// move a third fewer operand bytes per output: once one-CTA tiles fill the
+// GPU they are faster for every route; below that, measured per route, FP16
 // pairs were faster from 32 one-CTA tiles up (N = 1024 .. 2048: 4-10%), the
-// integer routes (binary16 / E4M3 operands from a conversion pass) were
-// faster with one CTA per tile.
-int choose_ctas(int64_t M, int64_t N, int sms, bool f16) {
+// integer routes (binary16 / E4M3 operands from a conversion pass) with one
+// CTA per tile.
+int choose_ctas(int64_t M, int64_t N, int64_t num_kb, int sms, bool f16) {
     const int forced = g_cta_pair.load();
     if (forced == 1 || forced == 2) return forced;
     const int64_t tiles1 = ((M + ptc::kBM - 1) / ptc::kBM) * ((N + ptc::kBN - 1) / ptc::kBN);
+    if (2 * tiles1 <= sms && ptc::pick_ksplit(int(tiles1), int(num_kb), g_ksplit.load(), sms) > 1) return 1;
     if (tiles1 >= sms) return 2;
     return (f16 && tiles1 >= 32) ? 2 : 1;
 }
@@ -222,6 +224,8 @@ GemmArgs base_args(int64_t M, int64_t N, int64_t K, int k_elems_per_block, void 
     a.split_ok = g_tail_split.load();
     a.split_min_kb = g_split_min_kb.load();
     a.stage_kb = g_pair_stage_kb.load();
+    a.ksplit = g_ksplit.load();
+    a.pdl = g_pdl.load();
     a.wait_limit_ns = g_wait_ns.load();
     return a;
 }
@@ -287,7 +291,7 @@ int f16_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0) return zero_c(C, ldc, M, N, eb, *d, s);
 
-    const int ctas = choose_ctas(M, N, d->sms, true);
+    const int ctas = choose_ctas(M, N, (K + 63) / 64, d->sms, true);
     CUtensorMap ta, tb;
     if ((rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, uint64_t(lda) * 2, 64, ptc::kBM)))
         return rc;
@@ -379,17 +383,17 @@ int int_gemm(bool s4, int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     if (s4)
         e = ptc::launch_s4_to_e4m3_pair(static_cast<const uint8_t *>(A), lda / 2, int(M),
                                         static_cast<const uint8_t *>(B), ldb / 2, int(N), int(K), aw, bw,
-                                        ldw, cgrid, s);
+                                        ldw, cgrid, s, g_pdl.load() != 0);
     else
         e = ptc::launch_s8_to_f16_pair(static_cast<const int8_t *>(A), lda, int(M),
                                        static_cast<const int8_t *>(B), ldb, int(N), int(K),
                                        reinterpret_cast<uint16_t *>(aw), reinterpret_cast<uint16_t *>(bw),
-                                       ldw, cgrid, s);
+                                       ldw, cgrid, s, g_pdl.load() != 0);
     if (e != cudaSuccess)
         rc = fail_cuda(e, "operand conversion launch");
     else
         g_launches.fetch_add(1);
-    const int ctas = choose_ctas(M, N, d->sms, false);
+    const int ctas = choose_ctas(M, N, ldw / k_elems, d->sms, false);
     const CUtensorMapDataType dt = s4 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap ta, tb;
     if (!rc) rc = make_tmap(&ta, dt, aw, K, M, uint64_t(ldw) * wsize, k_elems, ptc::kBM);
@@ -448,14 +452,14 @@ int s8_rowb_gemm(int64_t M, int64_t N, int64_t K, const int8_t *A, int64_t lda, 
     uint16_t *bw = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws) + a_bytes);
     const int cgrid = d->sms * 8;
     rc = PTC_OK;
-    e = ptc::launch_s8_to_f16(A, lda, int(M), int(K), aw, ldw_a, cgrid, s);
+    e = ptc::launch_s8_to_f16(A, lda, int(M), int(K), aw, ldw_a, cgrid, s, g_pdl.load() != 0);
     if (e == cudaSuccess) {
         g_launches.fetch_add(1);
-        e = ptc::launch_s8_to_f16(B, ldb, int(K), int(N), bw, ldw_b, cgrid, s);
+        e = ptc::launch_s8_to_f16(B, ldb, int(K), int(N), bw, ldw_b, cgrid, s, g_pdl.load() != 0);
         if (e == cudaSuccess) g_launches.fetch_add(1);
     }
     if (e != cudaSuccess) rc = fail_cuda(e, "operand conversion launch");
-    const int ctas = choose_ctas(M, N, d->sms, false);
+    const int ctas = choose_ctas(M, N, (K + 63) / 64, d->sms, false);
     CUtensorMap ta, tb;
     if (!rc) rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, aw, K, M, uint64_t(ldw_a) * 2, 64, ptc::kBM);
     if (!rc) rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bw, N, K, uint64_t(ldw_b) * 2, 64, 64);
@@ -625,17 +629,17 @@ int host_gemm(int prec, int64_t M, int64_t N, int64_t K, const void *A, int64_t 
     const int cgrid = d->sms * 8;
     if (!f16 && rc == PTC_OK) {
         cudaError_t r = s4 ? ptc::launch_s4_to_e4m3_pair(Bd, b_pitch, 0, Bd, b_pitch, int(N), int(K), Wa, Wb,
-                                                          ldw, cgrid, s)
+                                                          ldw, cgrid, s, g_pdl.load() != 0)
                            : ptc::launch_s8_to_f16_pair(reinterpret_cast<const int8_t *>(Bd), b_pitch, 0,
                                                         reinterpret_cast<const int8_t *>(Bd), b_pitch, int(N),
                                                         int(K), reinterpret_cast<uint16_t *>(Wa),
-                                                        reinterpret_cast<uint16_t *>(Wb), ldw, cgrid, s);
+                                                        reinterpret_cast<uint16_t *>(Wb), ldw, cgrid, s, g_pdl.load() != 0);
         if (cuda(r, "operand conversion launch")) g_launches.fetch_add(1);
     }
     for (int p = 0; p < npanels && rc == PTC_OK; ++p) {
         const int64_t r0 = p * panel, rows = std::min(panel, M - r0);
         cuda(cudaStreamWaitEvent(s, ev_a[p], 0), "stream wait");
-        const int ctas = choose_ctas(rows, N, d->sms, f16);
+        const int ctas = choose_ctas(rows, N, (K + k_elems - 1) / k_elems, d->sms, f16);
         CUtensorMap ta, tb;
         if (f16) {
             if (rc == PTC_OK)
@@ -646,11 +650,11 @@ int host_gemm(int prec, int64_t M, int64_t N, int64_t K, const void *A, int64_t 
             uint8_t *wa = Wa + r0 * ldw * wsize;
             cudaError_t r =
                 s4 ? ptc::launch_s4_to_e4m3_pair(Ad + r0 * a_pitch, a_pitch, int(rows), Ad, a_pitch, 0, int(K), wa,
-                                                 wa, ldw, cgrid, s)
+                                                 wa, ldw, cgrid, s, g_pdl.load() != 0)
                    : ptc::launch_s8_to_f16_pair(reinterpret_cast<const int8_t *>(Ad + r0 * a_pitch), a_pitch,
                                                 int(rows), reinterpret_cast<const int8_t *>(Ad), a_pitch, 0, int(K),
                                                 reinterpret_cast<uint16_t *>(wa), reinterpret_cast<uint16_t *>(wa),
-                                                ldw, cgrid, s);
+                                                ldw, cgrid, s, g_pdl.load() != 0);
             if (cuda(r, "operand conversion launch")) g_launches.fetch_add(1);
             const CUtensorMapDataType dt = s4 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
             if (rc == PTC_OK) rc = make_tmap(&ta, dt, wa, K, rows, uint64_t(ldw) * wsize, k_elems, ptc::kBM);
@@ -824,6 +828,12 @@ int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile) {
     return PTC_OK;
 }
 
+int ptc_last_launch(int *grid, int *cluster, int *ksplit) {
+    if (!grid || !cluster || !ksplit) return fail(PTC_ERR_INVALID, "NULL pointer");
+    ptc::last_launch(grid, cluster, ksplit);
+    return PTC_OK;
+}
+
 int ptc_set_tuning(const char *key, int64_t value) {
     if (!key) return fail(PTC_ERR_INVALID, "key is NULL");
     if (std::strcmp(key, "s8_chunk_kb") == 0 && value > 0 && value % 2 == 0 && value < (1 << 30)) {
@@ -852,6 +862,14 @@ int ptc_set_tuning(const char *key, int64_t value) {
     }
     if (std::strcmp(key, "split_min_kb") == 0 && value >= 2 && value <= (1 << 20)) {
         g_split_min_kb.store(int(value));
+        return PTC_OK;
+    }
+    if (std::strcmp(key, "ksplit") == 0 && (value == 0 || value == 1 || value == 2 || value == 4 || value == 8)) {
+        g_ksplit.store(int(value));
+        return PTC_OK;
+    }
+    if (std::strcmp(key, "pdl") == 0 && (value == 0 || value == 1)) {
+        g_pdl.store(int(value));
         return PTC_OK;
     }
     if (std::strcmp(key, "cta_pair") == 0 && value >= 0 && value <= 2) {

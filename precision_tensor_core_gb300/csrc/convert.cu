@@ -11,10 +11,13 @@
 // streaming, HBM-bound kernels: 16-byte loads and stores, a grid-stride loop
 // over (row, 16-byte vector) pairs, and scalar code only for the ragged end
 // of a row, so no byte past a row's last element is read.
+#include <cstring>
+
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace ptc {
 namespace {
@@ -149,6 +152,11 @@ __global__ void __launch_bounds__(256) convert_kernel(const uint8_t *__restrict_
                                                       typename Op::Out *__restrict__ dst_b, int64_t ldd, int tpr_log2) {
     using Out = typename Op::Out;
     constexpr int V = W32 ? 2 * Op::VEC : Op::VEC;  // elements per input vector
+    // Launched after a kernel that may still run (programmatic serialization):
+    // its writes (and its reads of this workspace) are complete past here.  The
+    // GEMM that follows may launch at once and set up while this pass runs.
+    griddep_wait();
+    griddep_launch_dependents();
     const int tpr = 1 << tpr_log2;
     const int lane = threadIdx.x & (tpr - 1);
     const int rpb = blockDim.x >> tpr_log2;
@@ -212,8 +220,8 @@ int threads_per_row_log2(int cols, int vec) {
 }  // namespace
 
 cudaError_t launch_s8_to_f16(const int8_t *src, int64_t lds, int rows, int cols, uint16_t *dst,
-                             int64_t ldd, int grid, cudaStream_t stream) {
-    return launch_s8_to_f16_pair(src, lds, rows, src, lds, 0, cols, dst, dst, ldd, grid, stream);
+                             int64_t ldd, int grid, cudaStream_t stream, bool pdl) {
+    return launch_s8_to_f16_pair(src, lds, rows, src, lds, 0, cols, dst, dst, ldd, grid, stream, pdl);
 }
 
 // 32-byte vectors when both sources start on 32-byte boundaries and their
@@ -226,28 +234,40 @@ static bool aligned32(const void *a, int64_t lda, const void *b, int64_t ldb) {
 template <class Op>
 cudaError_t launch_convert(const uint8_t *a, int64_t lda, int rows_a, const uint8_t *b, int64_t ldb, int rows_b,
                            int cols, typename Op::Out *dst_a, typename Op::Out *dst_b, int64_t ldd, int grid,
-                           cudaStream_t stream) {
-    if (aligned32(a, lda, b, ldb))
-        convert_kernel<Op, true><<<grid, 256, 0, stream>>>(a, lda, rows_a, b, ldb, rows_b, cols, dst_a, dst_b, ldd,
-                                                           threads_per_row_log2(cols, 2 * Op::VEC));
-    else
-        convert_kernel<Op, false><<<grid, 256, 0, stream>>>(a, lda, rows_a, b, ldb, rows_b, cols, dst_a, dst_b, ldd,
-                                                            threads_per_row_log2(cols, Op::VEC));
+                           cudaStream_t stream, bool pdl) {
+    const bool w32 = aligned32(a, lda, b, ldb);
+    auto *fn = w32 ? convert_kernel<Op, true> : convert_kernel<Op, false>;
+    const int tpr_log2 = threads_per_row_log2(cols, w32 ? 2 * Op::VEC : Op::VEC);
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute attr[1];
+    std::memset(attr, 0, sizeof(attr));
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    if (pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    cudaError_t e = cudaLaunchKernelEx(&cfg, fn, a, lda, rows_a, b, ldb, rows_b, cols, dst_a, dst_b, ldd, tpr_log2);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 cudaError_t launch_s8_to_f16_pair(const int8_t *a, int64_t lda, int rows_a, const int8_t *b,
                                   int64_t ldb, int rows_b, int cols, uint16_t *dst_a, uint16_t *dst_b,
-                                  int64_t ldd, int grid, cudaStream_t stream) {
+                                  int64_t ldd, int grid, cudaStream_t stream, bool pdl) {
     return launch_convert<S8ToF16>(reinterpret_cast<const uint8_t *>(a), lda, rows_a,
                                    reinterpret_cast<const uint8_t *>(b), ldb, rows_b, cols, dst_a, dst_b, ldd, grid,
-                                   stream);
+                                   stream, pdl);
 }
 
 cudaError_t launch_s4_to_e4m3_pair(const uint8_t *a, int64_t lda, int rows_a, const uint8_t *b,
                                    int64_t ldb, int rows_b, int cols, uint8_t *dst_a, uint8_t *dst_b,
-                                   int64_t ldd, int grid, cudaStream_t stream) {
-    return launch_convert<S4ToE4M3>(a, lda, rows_a, b, ldb, rows_b, cols, dst_a, dst_b, ldd, grid, stream);
+                                   int64_t ldd, int grid, cudaStream_t stream, bool pdl) {
+    return launch_convert<S4ToE4M3>(a, lda, rows_a, b, ldb, rows_b, cols, dst_a, dst_b, ldd, grid, stream, pdl);
 }
 
 }  // namespace ptc

@@ -29,6 +29,14 @@
 //               each CTA stages its own 128 rows of A and half of B, so a CTA
 //               moves 32 KiB per K block instead of 48 KiB; the ring holds 3
 //               stages of two K blocks (or, as a tuning choice, 7 of one).
+//   KS = 2/4/8  one-CTA tiles in clusters of KS CTAs that share a tile's K
+//               range (split-K inside a cluster), for single-wave launches
+//               whose tiles would leave most SMs idle: each CTA multiplies
+//               about 1/KS of the K blocks, writes its 128 x 256 partial sums
+//               into its idle ring, and after a cluster barrier completes
+//               128/KS rows of the tile by adding the KS partials in rank
+//               order, read from the peers' shared memory (distributed shared
+//               memory).  No workspace, no atomics, the same sums every run.
 //
 // The work list: output tiles in grouped raster order, strided over the
 // clusters; when the last wave would leave at least half of the clusters idle,
@@ -44,7 +52,10 @@
 // in registers.  The int32 result is therefore the exact sum modulo 2^32.
 //
 // Tiles are spread over a persistent grid of at most one CTA per SM with no
-// dependency between clusters (no grid-wide spin barrier).  Every wait is
+// dependency between clusters (no grid-wide spin barrier).  The kernel may be
+// launched while the previous kernel of the stream still runs (programmatic
+// serialization): it sets up barriers and tensor memory, then waits for that
+// kernel before its first global-memory access.  Every wait is
 // bounded by a %globaltimer limit: on expiry the CTA raises an abort flag,
 // records PTC_ERR_TIMEOUT in a device error word, lets its in-flight copies
 // and MMAs land, frees tensor memory and exits.
@@ -112,6 +123,11 @@ constexpr size_t smem_bytes() {
 }
 static_assert(smem_bytes<1, 1>() <= 232448 && smem_bytes<2, 1>() <= 232448 && smem_bytes<2, 2>() <= 232448,
               "shared memory budget");
+// A K-split cluster's partial sums: 128 rows of 256 four-byte values, row r
+// at r * 1024 bytes, its 16-byte piece j at piece j ^ (r & 7) (the writers,
+// one row per lane, and the readers, one piece per lane, do not conflict).
+constexpr int kPartialRow = kBN * 4;
+static_assert(Cfg<1, 1>::STAGES * Cfg<1, 1>::STAGE >= kBM * kPartialRow, "the ring holds a tile's partial sums");
 static_assert(Cfg<1, 1>::STAGES * Cfg<1, 1>::STAGE >= EPI_WARPS * kStageWarp &&
                   Cfg<2, 1>::STAGES * Cfg<2, 1>::STAGE >= EPI_WARPS * kStageWarp &&
                   Cfg<2, 2>::STAGES * Cfg<2, 2>::STAGE >= EPI_WARPS * kStageWarp,
@@ -440,16 +456,136 @@ __device__ __forceinline__ void split_epilogue(uint32_t t_acc, uint32_t *cnt, fl
     }
 }
 
+// K-split clusters: CTA `krank` of `ks` multiplies K blocks [kb0, kb1) of the
+// unit, an even share (the first num_kb % ks CTAs take one block more).
+__device__ __forceinline__ void ksplit_range(WorkRef &w, int krank, int ks) {
+    const int n = w.kb1 - w.kb0, q = n / ks, r = n % ks;
+    const int b = w.kb0 + krank * q + min(krank, r);
+    w.kb0 = b;
+    w.kb1 = b + q + (krank < r ? 1 : 0);
+}
+
+// 32 four-byte partial sums of local row `row`, columns 4 * piece0 .., into
+// the partial-sum layout at shared address `base`.
+__device__ __forceinline__ void put_partial(uint32_t base, int row, int piece0, const uint32_t (&v)[32]) {
+    const uint32_t rb = base + uint32_t(row) * kPartialRow;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        st_shared_v4(rb + (uint32_t((piece0 + i) ^ (row & 7)) << 4), v[4 * i], v[4 * i + 1], v[4 * i + 2],
+                     v[4 * i + 3]);
+}
+
+// Four consecutive results of one row to C (row-major, ldc elements) at
+// column `col`; `valid` of them lie below N.  16-byte (4-byte C) or 8-byte
+// (2-byte C) stores, aligned because C rows start on 16-byte boundaries.
+template <typename T>
+__device__ __forceinline__ void store_4(T *dst, const T (&v)[4], int valid) {
+    if (valid >= 4) {
+        if constexpr (sizeof(T) == 4) {
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(reinterpret_cast<const uint32_t &>(v[0]),
+                                                         reinterpret_cast<const uint32_t &>(v[1]),
+                                                         reinterpret_cast<const uint32_t &>(v[2]),
+                                                         reinterpret_cast<const uint32_t &>(v[3]));
+        } else {
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(uint32_t(v[0]) | (uint32_t(v[1]) << 16),
+                                                         uint32_t(v[2]) | (uint32_t(v[3]) << 16));
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (e < valid) dst[e] = v[e];
+    }
+}
+
+// Completion of a K-split tile: this CTA (`krank` of KS) owns local rows
+// krank * 128/KS .. of the tile (mb, nb); epilogue warp `ew` takes every
+// eighth of them, each lane 4 columns in each half of the row (pieces lane
+// and lane + 32).  The KS partials are added in rank order: FP32 sums with
+// round-to-nearest additions (FP16 accumulators were widened exactly to FP32
+// and the sum is rounded to binary16 once), int32 sums wrapping mod 2^32.
+template <int EPI, int KS>
+__device__ __forceinline__ void ksplit_complete(const GemmArgs &args, int mb, int nb, int krank, uint32_t base,
+                                                int ew, int lane) {
+    constexpr int R = kBM / KS;
+#pragma unroll 1
+    for (int i = ew; i < R; i += EPI_WARPS) {
+        const int lr = krank * R + i;
+        const int row = mb * kBM + lr;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int piece = lane + 32 * half;
+            const uint32_t addr = base + uint32_t(lr) * kPartialRow + (uint32_t(piece ^ (lr & 7)) << 4);
+            uint4 p[KS];
+#pragma unroll
+            for (int k = 0; k < KS; ++k) p[k] = ld_shared_cluster_v4(mapa_shared(addr, uint32_t(k)));
+            const int col = nb * kBN + 4 * piece;
+            if (row >= args.M || col >= args.N) continue;
+            const int valid = args.N - col;
+            if constexpr (EPI == EPI_INT) {
+                uint32_t s[4] = {p[0].x, p[0].y, p[0].z, p[0].w};
+#pragma unroll
+                for (int k = 1; k < KS; ++k) {
+                    s[0] += p[k].x;
+                    s[1] += p[k].y;
+                    s[2] += p[k].z;
+                    s[3] += p[k].w;
+                }
+                if (args.out_mode == OUT_S32) {
+                    const int32_t v[4] = {int32_t(s[0]), int32_t(s[1]), int32_t(s[2]), int32_t(s[3])};
+                    store_4(reinterpret_cast<int32_t *>(args.C) + int64_t(row) * args.ldc + col, v, valid);
+                    continue;
+                }
+                const float sa = args.scale_a ? __ldg(args.scale_a + row) : 1.0f;
+                float f[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float sb = (args.scale_b && e < valid) ? __ldg(args.scale_b + col + e) : 1.0f;
+                    f[e] = __fmul_rn(__fmul_rn(__int2float_rn(int32_t(s[e])), sa), sb);
+                }
+                if (args.out_mode == OUT_F32) {
+                    store_4(reinterpret_cast<float *>(args.C) + int64_t(row) * args.ldc + col, f, valid);
+                } else {
+                    uint16_t h[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        h[e] = args.out_mode == OUT_BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(f[e]))
+                                                         : __half_as_ushort(__float2half_rn(f[e]));
+                    store_4(reinterpret_cast<uint16_t *>(args.C) + int64_t(row) * args.ldc + col, h, valid);
+                }
+            } else {
+                float f[4] = {__uint_as_float(p[0].x), __uint_as_float(p[0].y), __uint_as_float(p[0].z),
+                              __uint_as_float(p[0].w)};
+#pragma unroll
+                for (int k = 1; k < KS; ++k) {
+                    f[0] = __fadd_rn(f[0], __uint_as_float(p[k].x));
+                    f[1] = __fadd_rn(f[1], __uint_as_float(p[k].y));
+                    f[2] = __fadd_rn(f[2], __uint_as_float(p[k].z));
+                    f[3] = __fadd_rn(f[3], __uint_as_float(p[k].w));
+                }
+                if constexpr (EPI == EPI_F16ACC) {
+                    uint16_t h[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) h[e] = __half_as_ushort(__float2half_rn(f[e]));
+                    store_4(reinterpret_cast<uint16_t *>(args.C) + int64_t(row) * args.ldc + col, h, valid);
+                } else {
+                    store_4(reinterpret_cast<float *>(args.C) + int64_t(row) * args.ldc + col, f, valid);
+                }
+            }
+        }
+    }
+}
+
 // CTA r of a pair owns rows 128 r .. 128 r + 127 of the 256 x 256 tile and
 // stages B rows 128 r .. 128 r + 127.  The even CTA issues the MMAs for both;
 // its full barriers collect both CTAs' copies, its commits arrive on both
 // CTAs' empty / accumulator-full barriers, and both CTAs' epilogues release
 // accumulator buffers on its acc_empty barriers.
-template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK>
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
     static_assert(!(B_MN && KIND == Kind::E4M3), "MN-major B is used by the FP16 path only");
+    static_assert(KS == 1 || (CTAS == 1 && kBM % (KS * EPI_WARPS) == 0), "K-split clusters of one-CTA tiles");
     constexpr bool INT_OUT = EPI == EPI_INT;
     using C_ = Cfg<CTAS, SUBK>;
     constexpr int STAGES = C_::STAGES;
@@ -465,9 +601,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const uint64_t limit = args.wait_limit_ns;
-    const uint32_t rank = (CTAS == 1) ? 0u : cluster_ctarank();
-    const int cluster = blockIdx.x / CTAS;
-    const int nclusters = gridDim.x / CTAS;
+    constexpr int CL = CTAS * KS;  // CTAs per cluster
+    const uint32_t crank = (CL == 1) ? 0u : cluster_ctarank();
+    const uint32_t rank = (CTAS == 1) ? 0u : crank;  // CTA of a pair
+    const int krank = (KS == 1) ? 0 : int(crank);    // K share of a K-split cluster
+    const int cluster = blockIdx.x / CL;
+    const int nclusters = gridDim.x / CL;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -496,6 +635,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         cluster_sync();
     tc_fence_after_sync();
     const uint32_t tmem_base = st->tmem_base;
+    // Global memory from here on: after the previous kernel of the stream.
+    griddep_wait();
+    griddep_launch_dependents();
 
     constexpr int K_ELEMS = (KIND == Kind::F16) ? kRowBytes / 2 : kRowBytes;
 
@@ -515,7 +657,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t outstanding = 0, out_phase = 0;  // per-stage bits of issued copies
             bool ok = true;
             for (int t = cluster; t < args.num_vunits && ok; t += nclusters) {
-                const WorkRef wr = work_unit(t, args, C_::SUB);
+                WorkRef wr = work_unit(t, args, C_::SUB);
+                if constexpr (KS > 1) ksplit_range(wr, krank, KS);
                 const int m0 = wr.mb * (kBM * CTAS) + int(rank) * kBM;
                 const int n0 = wr.nb * kBN + int(rank) * C_::B_ROWS;
                 for (int kb = wr.kb0; kb < wr.kb1; kb += C_::SUB) {
@@ -607,7 +750,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             uint32_t aph = 0;
             bool ok = true;
             for (int t = cluster; t < args.num_vunits && ok; t += nclusters) {
-                const WorkRef wr = work_unit(t, args, C_::SUB);
+                WorkRef wr = work_unit(t, args, C_::SUB);
+                if constexpr (KS > 1) ksplit_range(wr, krank, KS);
                 const int nchunks = (wr.kb1 - wr.kb0 + args.kb_per_chunk - 1) / args.kb_per_chunk;
                 for (int ch = 0; ch < nchunks && ok; ++ch) {
                     if (!mbar_wait(&st->acc_empty[abuf], aph ^ 1u, &st->abort, &g_error_word, limit)) {
@@ -699,7 +843,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t aph = 0;
         bool ok = true;
         for (int t = cluster; t < args.num_vunits && ok; t += nclusters) {
-            const WorkRef wr = work_unit(t, args, C_::SUB);
+            WorkRef wr = work_unit(t, args, C_::SUB);
+            if constexpr (KS > 1) ksplit_range(wr, krank, KS);
             const int row = wr.mb * (kBM * CTAS) + int(rank) * kBM + 32 * q + lane;
             const int col0 = wr.nb * kBN + h * (kBN / 2);
             if constexpr (INT_OUT) {
@@ -728,6 +873,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 }
                 if (!ok) break;
+                if constexpr (KS > 1) {
+                    // K-split cluster: the partial sums wait in the ring for the
+                    // cluster's completion pass.
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        put_partial(smem_u32(smem), 32 * q + lane, h * (kBN / 8) + 8 * c,
+                                    reinterpret_cast<const uint32_t(&)[32]>(acc[32 * c]));
+                    continue;
+                }
                 if (wr.part != 0) {
                     // Sum of the two K halves, wrapping like every int32 partial sum.
                     const int slice = ((wr.slot * CTAS + int(rank)) * 4 + q) * 2 + h;
@@ -793,43 +947,60 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // next tile, and the ring is idle once the unit has been
                 // multiplied, so 4-byte C goes out by TMA stores staged there.
                 const bool use_tma = t == tma_t;
-                if (wr.part == 0 && EPI == EPI_F32 && use_tma) {
+                if constexpr (KS > 1) {
+                    // K-split cluster: the partial sums (FP16 accumulators widened
+                    // exactly to FP32) wait in the ring for the completion pass.
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         uint32_t r[32];
                         tmem_ld_32cols(t_lane + uint32_t(abuf * kBN + 32 * c), r);
                         tmem_ld_wait();
-                        const int cc = col0 + 32 * c;
-                        if (cc < args.N)
-                            tma_store_block(&tmC, stg + uint32_t(c * kStageC), r, lane, cc, row - lane,
-                                            stg_pending && c == 0);
-                    }
-                    stg_pending = true;
-                } else if (wr.part == 0) {
-                    float *crow = reinterpret_cast<float *>(args.C) + int64_t(row) * args.ldc;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t r[32];
-                        tmem_ld_32cols(t_lane + uint32_t(abuf * kBN + 32 * c), r);
-                        tmem_ld_wait();
-                        const int cc = col0 + 32 * c;
                         if constexpr (EPI == EPI_F16ACC) {
-                            if (row < args.M && cc < args.N)
-                                store_f16acc_32(reinterpret_cast<uint16_t *>(args.C) + int64_t(row) * args.ldc + cc, r,
-                                                args.N - cc, args.c_wide);
-                        } else {
-                            if (row < args.M && cc < args.N) store_32(crow + cc, r, args.N - cc, args.c_wide);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e)
+                                r[e] = __float_as_uint(__half2float(__ushort_as_half(static_cast<uint16_t>(r[e]))));
                         }
+                        put_partial(smem_u32(smem), 32 * q + lane, h * (kBN / 8) + 8 * c, r);
                     }
                 } else {
-                    const int slice = ((wr.slot * CTAS + int(rank)) * 4 + q) * 2 + h;
-                    void *crow = nullptr;
-                    if (row < args.M)
-                        crow = static_cast<uint8_t *>(args.C) +
-                               (int64_t(row) * args.ldc + col0) * (EPI == EPI_F16ACC ? 2 : 4);
-                    split_epilogue<EPI>(t_lane + uint32_t(abuf * kBN), args.split_count + slice,
-                                        split_partial(args, slice, wr.part - 1), split_partial(args, slice, 2 - wr.part),
-                                        crow, args.N - col0, args.c_wide, lane);
+                    if (wr.part == 0 && EPI == EPI_F32 && use_tma) {
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t r[32];
+                            tmem_ld_32cols(t_lane + uint32_t(abuf * kBN + 32 * c), r);
+                            tmem_ld_wait();
+                            const int cc = col0 + 32 * c;
+                            if (cc < args.N)
+                                tma_store_block(&tmC, stg + uint32_t(c * kStageC), r, lane, cc, row - lane,
+                                                stg_pending && c == 0);
+                        }
+                        stg_pending = true;
+                    } else if (wr.part == 0) {
+                        float *crow = reinterpret_cast<float *>(args.C) + int64_t(row) * args.ldc;
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            uint32_t r[32];
+                            tmem_ld_32cols(t_lane + uint32_t(abuf * kBN + 32 * c), r);
+                            tmem_ld_wait();
+                            const int cc = col0 + 32 * c;
+                            if constexpr (EPI == EPI_F16ACC) {
+                                if (row < args.M && cc < args.N)
+                                    store_f16acc_32(reinterpret_cast<uint16_t *>(args.C) + int64_t(row) * args.ldc + cc, r,
+                                                    args.N - cc, args.c_wide);
+                            } else {
+                                if (row < args.M && cc < args.N) store_32(crow + cc, r, args.N - cc, args.c_wide);
+                            }
+                        }
+                    } else {
+                        const int slice = ((wr.slot * CTAS + int(rank)) * 4 + q) * 2 + h;
+                        void *crow = nullptr;
+                        if (row < args.M)
+                            crow = static_cast<uint8_t *>(args.C) +
+                                   (int64_t(row) * args.ldc + col0) * (EPI == EPI_F16ACC ? 2 : 4);
+                        split_epilogue<EPI>(t_lane + uint32_t(abuf * kBN), args.split_count + slice,
+                                            split_partial(args, slice, wr.part - 1), split_partial(args, slice, 2 - wr.part),
+                                            crow, args.N - col0, args.c_wide, lane);
+                    }
                 }
                 release(abuf);
                 if (++abuf == 2) {
@@ -844,8 +1015,18 @@ __global__ void __launch_bounds__(THREADS, 1)
         __syncwarp();
     }
 
+    if constexpr (KS > 1) {
+        // Every CTA's partial sums are in its ring (barrier release / acquire at
+        // cluster scope); each completes its rows of the tile from all of them.
+        cluster_sync();
+        if (warp >= 2 && cluster < args.num_vunits) {
+            const WorkRef wr = work_unit(cluster, args, C_::SUB);
+            ksplit_complete<EPI, KS>(args, wr.mb, wr.nb, krank, smem_u32(smem), warp - 2, lane);
+        }
+    }
+    // A K-split cluster's peers read this CTA's ring until this barrier.
     tc_fence_before_sync();
-    if constexpr (CTAS == 1)
+    if constexpr (CL == 1)
         __syncthreads();
     else
         cluster_sync();
@@ -868,36 +1049,56 @@ struct LaunchCache {
     int max_clusters = 0;
 };
 
-template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK>
-cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args,
-                       int sms, cudaMemPool_t pool, cudaStream_t stream) {
-    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS, SUBK>;
-    constexpr size_t SMEM = smem_bytes<CTAS, SUBK>();
+struct LastLaunch {
+    int grid = 0, cluster = 0, ksplit = 0;
+};
+thread_local LastLaunch g_last;
+
+// Launch shape of one variant: dynamic shared memory, cluster dimension and
+// (optionally) programmatic stream serialization.
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS>
+void launch_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[2], bool pdl, cudaStream_t stream) {
+    std::memset(&cfg, 0, sizeof(cfg));
+    std::memset(attr, 0, sizeof(attr));
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = smem_bytes<CTAS, SUBK>();
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    int n = 0;
+    if constexpr (CTAS * KS > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = CTAS * KS;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.numAttrs = n;
+}
+
+// Clusters of the variant that can be resident at once on the current device
+// (cached per device; the shared-memory opt-in is set on first use).
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS>
+cudaError_t cluster_capacity(int sms, int *out) {
+    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS, SUBK, KS>;
+    constexpr int CL = CTAS * KS;
     static thread_local LaunchCache cache;  // per device (re-queried when it changes)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof(cfg));
-    cudaLaunchAttribute attr[1];
-    std::memset(attr, 0, sizeof(attr));
-    cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = SMEM;
-    cfg.stream = stream;
-    if constexpr (CTAS == 2) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
     if (dev != cache.dev) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM));
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes<CTAS, SUBK>()));
         if (e != cudaSuccess) return e;
-        int clusters = sms / CTAS;
-        if constexpr (CTAS == 2) {
-            cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+        int clusters = sms / CL;
+        if constexpr (CL > 1) {
+            cudaLaunchConfig_t cfg;
+            cudaLaunchAttribute attr[2];
+            launch_config<KIND, B_MN, EPI, CTAS, SUBK, KS>(cfg, attr, false, nullptr);
+            cfg.gridDim = dim3(CL * (sms / CL), 1, 1);
             int n = 0;
             e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
             if (e != cudaSuccess) return e;
@@ -907,6 +1108,21 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
         cache.max_clusters = clusters;
         cache.dev = dev;
     }
+    *out = cache.max_clusters;
+    return cudaSuccess;
+}
+
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS>
+cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args,
+                       int sms, cudaMemPool_t pool, cudaStream_t stream) {
+    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS, SUBK, KS>;
+    int maxc = 0;
+    cudaError_t e = cluster_capacity<KIND, B_MN, EPI, CTAS, SUBK, KS>(sms, &maxc);
+    if (e != cudaSuccess) return e;
+    if (KS > 1 && args.num_tiles > maxc) return cudaErrorInvalidConfiguration;  // one wave of clusters
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    launch_config<KIND, B_MN, EPI, CTAS, SUBK, KS>(cfg, attr, args.pdl != 0, stream);
     // Work list: split the last wave's tiles in K when they fill at most half
     // of the clusters (a lone partial wave included).  The halves exchange
     // partial sums through a stream-ordered workspace from `pool`: a counter
@@ -921,7 +1137,6 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
     std::memset(&tc, 0, sizeof(tc));
     a.c_tma = 0;
     const bool tma_c = esize == 4;
-    const int maxc = cache.max_clusters;
     const int tail = a.num_tiles < maxc ? a.num_tiles : a.num_tiles % maxc;
     a.tail_split = 0;
     a.split_count = nullptr;
@@ -930,7 +1145,7 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
     // The split saves about half of a tile's K loop (~0.14 us per K block);
     // setting up the exchange costs ~6 us per call, so short K (below
     // split_min_kb blocks, 64 by default) runs whole.
-    if (pool != nullptr && a.split_ok && a.num_kb > SUBK && a.num_kb >= a.split_min_kb && tail > 0 &&
+    if (KS == 1 && pool != nullptr && a.split_ok && a.num_kb > SUBK && a.num_kb >= a.split_min_kb && tail > 0 &&
         2 * tail <= maxc) {
         const size_t slices = size_t(tail) * CTAS * EPI_WARPS;
         const size_t count_bytes = (slices * sizeof(uint32_t) + 255) / 256 * 256;
@@ -954,25 +1169,75 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
     // Each cluster's last unit writes 4-byte C by TMA stores staged in the idle
     // ring (its epilogue is exposed); earlier units use 32-byte stores, which
     // leave the TMA engine to the operand loads while the next tile runs.
-    if (tma_c && encode_tmap_c32(&tc, a.C, uint64_t(a.N), uint64_t(a.M), uint64_t(a.ldc)) == 0) a.c_tma = 1;
-    cfg.gridDim = dim3(CTAS * clusters, 1, 1);
+    // (A K-split cluster writes C from its completion pass, without TMA.)
+    if (KS == 1 && tma_c && encode_tmap_c32(&tc, a.C, uint64_t(a.N), uint64_t(a.M), uint64_t(a.ldc)) == 0)
+        a.c_tma = 1;
+    cfg.gridDim = dim3(CTAS * KS * clusters, 1, 1);
     e = cudaLaunchKernelEx(&cfg, fn, ta, tb, tc, a);
+    if (e == cudaSuccess) {
+        g_last.grid = CTAS * KS * clusters;
+        g_last.cluster = CTAS * KS;
+        g_last.ksplit = KS;
+    }
     if (ws != nullptr) cudaFreeAsync(ws, stream);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
+// Clusters of KS one-CTA tiles that fit one wave (the same for every variant:
+// one 320-thread CTA with ~197 KB of shared memory per SM); 0 when that
+// cluster shape cannot run.
+int ksplit_capacity(int ks, int sms) {
+    int cap = 0;
+    cudaError_t e = cudaSuccess;
+    if (ks == 8) e = cluster_capacity<Kind::F16, true, EPI_F32, 1, 1, 8>(sms, &cap);
+    if (ks == 4) e = cluster_capacity<Kind::F16, true, EPI_F32, 1, 1, 4>(sms, &cap);
+    if (ks == 2) e = cluster_capacity<Kind::F16, true, EPI_F32, 1, 1, 2>(sms, &cap);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return cap;
+}
+
 }  // namespace
+
+void last_launch(int *grid, int *cluster, int *ksplit) {
+    *grid = g_last.grid;
+    *cluster = g_last.cluster;
+    *ksplit = g_last.ksplit;
+}
+
+int pick_ksplit(int tiles, int num_kb, int knob, int sms) {
+    if (knob == 1 || 2 * tiles > sms) return 1;
+    for (int ks = 8; ks >= 2; ks /= 2) {
+        if ((knob != 0 && knob != ks) || num_kb < ks) continue;
+        // The split costs ~1-1.5 us per call (partial sums to shared memory,
+        // two cluster barriers, the reduction); a one-CTA K block takes
+        // ~0.15 us, so by size it is taken when each CTA sheds 8 or more.
+        const int shed = num_kb - (num_kb + ks - 1) / ks;
+        if (knob == 0 && shed < 8) continue;
+        if (tiles <= ksplit_capacity(ks, sms)) return ks;
+    }
+    return 1;
+}
 
 size_t gemm_smem_bytes(int ctas) { return ctas == 2 ? smem_bytes<2, 2>() : smem_bytes<1, 1>(); }
 
+// One-CTA launches run as K-split clusters when pick_ksplit says so.
 cudaError_t launch_gemm(Kind kind, bool b_mn_major, int epi, int ctas, const CUtensorMap &ta,
                         const CUtensorMap &tb, const GemmArgs &args, int sms, cudaMemPool_t pool,
                         cudaStream_t stream) {
-#define PTC_LAUNCH(K, BMN, E)                                                    \
-    return ctas == 1 ? launch_one<K, BMN, E, 1, 1>(ta, tb, args, sms, pool, stream)          \
-           : args.stage_kb == 1 ? launch_one<K, BMN, E, 2, 1>(ta, tb, args, sms, pool, stream) \
-                                : launch_one<K, BMN, E, 2, 2>(ta, tb, args, sms, pool, stream)
+    const int ks = ctas == 1 ? pick_ksplit(args.num_tiles, args.num_kb, args.ksplit, sms) : 1;
+#define PTC_LAUNCH(K, BMN, E)                                                                       \
+    do {                                                                                            \
+        if (ks == 8) return launch_one<K, BMN, E, 1, 1, 8>(ta, tb, args, sms, pool, stream);        \
+        if (ks == 4) return launch_one<K, BMN, E, 1, 1, 4>(ta, tb, args, sms, pool, stream);        \
+        if (ks == 2) return launch_one<K, BMN, E, 1, 1, 2>(ta, tb, args, sms, pool, stream);        \
+        return ctas == 1 ? launch_one<K, BMN, E, 1, 1, 1>(ta, tb, args, sms, pool, stream)          \
+               : args.stage_kb == 1 ? launch_one<K, BMN, E, 2, 1, 1>(ta, tb, args, sms, pool, stream) \
+                                    : launch_one<K, BMN, E, 2, 2, 1>(ta, tb, args, sms, pool, stream); \
+    } while (0)
     if (kind == Kind::F16 && b_mn_major && epi == EPI_F32) PTC_LAUNCH(Kind::F16, true, EPI_F32);
     if (kind == Kind::F16 && b_mn_major && epi == EPI_F16ACC) PTC_LAUNCH(Kind::F16, true, EPI_F16ACC);
     if (kind == Kind::F16 && !b_mn_major && epi == EPI_INT) PTC_LAUNCH(Kind::F16, false, EPI_INT);

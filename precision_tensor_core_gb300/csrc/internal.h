@@ -40,6 +40,10 @@ struct GemmArgs {
     int c_wide;            // 1: C's base and pitch allow 32-byte stores (set by launch_gemm)
     int c_tma;             // 1: a TMA map of 4-byte C is passed; each cluster's last unit stores
                            // through it (set by launch_gemm)
+    int ksplit;            // single-wave one-CTA launches: CTAs per tile sharing its K range
+                           // in a cluster (0: chosen by size, 1: none, 2 / 4 / 8: that many
+                           // when the launch allows it; tuning knob "ksplit")
+    int pdl;               // 1: launched with programmatic stream serialization (knob "pdl")
     int split_ok;          // 1: the tail may be split (tuning knob "tail_split")
     int split_min_kb;      // ... when K spans at least this many K blocks
     int tail_split;
@@ -81,6 +85,16 @@ cudaError_t launch_gemm(Kind kind, bool b_mn_major, int epi, int ctas, const CUt
                         const CUtensorMap &tb, const GemmArgs &args, int sms, cudaMemPool_t pool,
                         cudaStream_t stream);
 
+// CTAs per K-split cluster for a one-CTA launch of `tiles` output tiles of
+// num_kb K blocks each: 1 (no split), 2, 4 or 8.  knob: 0 chooses by size
+// (the largest KS whose clusters fit one wave and that sheds each CTA at
+// least 8 K blocks), 1 never, 2 / 4 / 8 that KS when it fits.
+int pick_ksplit(int tiles, int num_kb, int knob, int sms);
+
+// Launch shape of the calling thread's last GEMM kernel launch (grid CTAs,
+// CTAs per cluster, CTAs sharing a tile's K range); zeros before the first.
+void last_launch(int *grid, int *cluster, int *ksplit);
+
 // C[M x N] = 0 for elements of esize (2 or 4) bytes, ldc in elements.
 cudaError_t launch_zero_fill(void *C, int64_t ldc, int M, int N, int esize, int grid, cudaStream_t stream);
 
@@ -91,15 +105,17 @@ cudaError_t read_and_clear_error_word(uint32_t *out);
 // dense, 128-byte-pitched workspace matrices of `cols` columns.
 //   s8 -> binary16: source pitches in bytes, destination pitch ldd elements
 cudaError_t launch_s8_to_f16(const int8_t *src, int64_t lds, int rows, int cols, uint16_t *dst,
-                             int64_t ldd, int grid, cudaStream_t stream);
+                             int64_t ldd, int grid, cudaStream_t stream, bool pdl = false);
 //   both operands in one launch: rows_a rows of A, then rows_b rows of B
 cudaError_t launch_s8_to_f16_pair(const int8_t *a, int64_t lda, int rows_a, const int8_t *b,
                                   int64_t ldb, int rows_b, int cols, uint16_t *dst_a, uint16_t *dst_b,
-                                  int64_t ldd, int grid, cudaStream_t stream);
+                                  int64_t ldd, int grid, cudaStream_t stream, bool pdl = false);
 //   packed s4 -> E4M3, both operands: source pitches in BYTES, ldd in elements
 cudaError_t launch_s4_to_e4m3_pair(const uint8_t *a, int64_t lda, int rows_a, const uint8_t *b,
                                    int64_t ldb, int rows_b, int cols, uint8_t *dst_a, uint8_t *dst_b,
-                                   int64_t ldd, int grid, cudaStream_t stream);
+                                   int64_t ldd, int grid, cudaStream_t stream, bool pdl = false);
+// pdl: launched with programmatic stream serialization (it may start before the
+// previous kernel in the stream ends; it waits for it before touching memory).
 
 // The paper's kernel families on GB300 (baseline.cu): WMMA and mma.sync.
 enum Variant : int {

@@ -160,6 +160,16 @@ __device__ __forceinline__ void cluster_sync() {
                      "memory");
 }
 
+// 16 bytes from shared::cluster address `addr` (this CTA's or a peer's).
+__device__ __forceinline__ uint4 ld_shared_cluster_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 // Arrive on an mbarrier given by its shared::cluster address (own or peer CTA).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
@@ -175,6 +185,21 @@ __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorM
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster_addr)
         : "memory");
+}
+
+// ---------------------------------------------------------------- dependent launches
+// A kernel launched with programmatic stream serialization may start while
+// the kernel before it in the stream is still running: griddep_wait blocks
+// until that kernel has completed and its memory operations are visible, so
+// every global-memory access of the kernel comes after it.  Without a
+// programmatic predecessor it returns at once.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Lets the next kernel in the stream (if launched programmatically) start
+// once every CTA of this grid has called this or exited; it still waits for
+// this grid's completion before touching memory.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ---------------------------------------------------------------- L2 policies

@@ -12,9 +12,13 @@ row-major, read MN-major) against gemm_s8 (B column-major), and
 gemm_s8_scaled / gemm_s4_scaled (each output type) against gemm_s8 / gemm_s4,
 at one size.
 `knobs` times gemm_f16 / gemm_s8 / gemm_s4 at one size under each setting of
-the library's tuning knobs (ptc_set_tuning: CTA pairs, pair ring stage depth, tail split, raster group, L2
-eviction policy, INT fold length), one knob at a time from the defaults: the
-ablation that shows the defaults are a local optimum.  `sizes` times the three
+the library's tuning knobs (ptc_set_tuning: CTA pairs, pair ring stage depth,
+tail split, K-split clusters, programmatic launches, raster group, L2 eviction
+policy, INT fold length), one knob at a time from the defaults: the ablation
+that shows the defaults are a local optimum.  `launch` compares launch shapes
+at small sizes (K-split clusters of 2, 4, 8 CTAs, programmatic launches on
+and off), reporting the median of 7 graph replays and the launch record
+(grid CTAs, CTAs per tile's K range) of each.  `sizes` times the three
 entry points at each size with the library defaults.  `cublas` times gemm_f16
 against cuBLAS on the same FP16 operands (torch.mm with FP32 output, and with
 FP16 output), interleaved in one process so that both see the same clocks and
@@ -41,14 +45,22 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 DEFAULTS = {"cta_pair": 0, "group_m": 8, "l2_hint": 0, "s8_chunk_kb": 16,
-            "s4_chunk_kb": 64, "tail_split": 1, "split_min_kb": 64, "pair_stage_kb": 2}
-KNOBS = {"cta_pair": [1, 2], "pair_stage_kb": [1], "tail_split": [0], "split_min_kb": [16, 32], "group_m": [4, 16, 32], "l2_hint": [1, 2, 3],
-         "s8_chunk_kb": [4, 8], "s4_chunk_kb": [2, 8, 16, 128]}
+            "s4_chunk_kb": 64, "tail_split": 1, "split_min_kb": 64, "pair_stage_kb": 2, "ksplit": 0, "pdl": 1}
+KNOBS = {"cta_pair": [1, 2], "pair_stage_kb": [1], "tail_split": [0], "split_min_kb": [16, 32],
+         "group_m": [4, 16, 32], "l2_hint": [1, 2, 3], "s8_chunk_kb": [4, 8], "s4_chunk_kb": [2, 8, 16, 128],
+         "ksplit": [1, 2, 4, 8], "pdl": [0]}
+# `launch` mode: launch-shape settings compared at small sizes, each timed as
+# the median of 7 replays of a CUDA graph of back-to-back calls.
+LAUNCH_SETTINGS = [("plain launches, no K-split", {"ksplit": 1, "pdl": 0}),
+                   ("programmatic launches, no K-split", {"ksplit": 1, "pdl": 1}),
+                   ("defaults (K-split by size, programmatic)", {"ksplit": 0, "pdl": 1}),
+                   ("K-split 2", {"ksplit": 2, "pdl": 1}), ("K-split 4", {"ksplit": 4, "pdl": 1}),
+                   ("K-split 8", {"ksplit": 8, "pdl": 1})]
 
 
 def main():
     p = argparse.ArgumentParser()
-    p.add_argument("--mode", choices=["knobs", "sizes", "variants", "baselines", "cublas"], default="sizes")
+    p.add_argument("--mode", choices=["knobs", "sizes", "variants", "baselines", "cublas", "launch"], default="sizes")
     p.add_argument("--n", type=int, default=8192)
     p.add_argument("--sizes", default="512,1024,2048,4096,8192")
     p.add_argument("--calls", type=int, default=0, help="calls per timing (0: by size)")
@@ -126,7 +138,51 @@ def main():
         return out
 
     results = {}
-    if a.mode == "cublas":
+    if a.mode == "launch":
+        import statistics
+
+        def graph_median_us(fn, calls):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(s):
+                with torch.cuda.graph(g, stream=s):
+                    for _ in range(calls):
+                        fn()
+            torch.cuda.current_stream().wait_stream(s)
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            v = []
+            for _ in range(7):
+                e0.record()
+                g.replay()
+                e1.record()
+                torch.cuda.synchronize()
+                v.append(e0.elapsed_time(e1) / calls * 1000.0)
+            return statistics.median(v)
+
+        print(f"{'N':>6} {'prec':>4} " + " ".join(f"{name:>42}" for name, _ in LAUNCH_SETTINGS))
+        for n in [int(x) for x in a.sizes.split(",")]:
+            ops = operands(n)
+            calls = a.calls or max(20, min(200, int(2e11 / (2.0 * n ** 3))))
+            results[str(n)] = {}
+            for prec in ("f16", "s8", "s4"):
+                row = {}
+                for name, kv in LAUNCH_SETTINGS:
+                    for k, v in kv.items():
+                        ptc.ptc_set_tuning(k, v)
+                    us = graph_median_us(call(prec, ops, n), calls)
+                    grid, _, ks = ptc.ptc_last_launch()
+                    row[name] = {"us": us, "grid": grid, "ksplit": ks}
+                for k, v in DEFAULTS.items():
+                    ptc.ptc_set_tuning(k, v)
+                results[str(n)][prec] = row
+                print(f"{n:>6} {prec:>4} " + " ".join(
+                    f"{r['us']:>29.2f} us ({r['grid']:>3}/{r['ksplit']})" for r in row.values()), flush=True)
+    elif a.mode == "cublas":
         import statistics
         n = a.n
         A, B, C = operands(n)["f16"]

@@ -55,7 +55,9 @@ def mode(request):
     ptc.ptc_set_tuning("cta_pair", ctas)
     ptc.ptc_set_tuning("tail_split", split)
     ptc.ptc_set_tuning("split_min_kb", 2)
+    ptc.ptc_set_tuning("ksplit", 1)  # the lone partial wave would otherwise run as K-split clusters
     yield request.param
+    ptc.ptc_set_tuning("ksplit", 0)
     ptc.ptc_set_tuning("split_min_kb", 64)
     ptc.ptc_set_tuning("tail_split", 1)
     ptc.ptc_set_tuning("cta_pair", 0)
