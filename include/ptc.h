@@ -312,10 +312,11 @@ int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile);
 /* Launch shape of the last GEMM kernel the calling thread launched through
  * this library: *grid = CTAs launched, *cluster = CTAs per thread-block
  * cluster (1; 2 for CTA pairs; KS for K-split clusters), *ksplit = CTAs that
- * share one output tile's K range (1 when the tiles are not split that way).
- * All zero before the first launch.  Host-side only (no device work).
- * Returns PTC_OK, or PTC_ERR_INVALID when a pointer is NULL. */
-int ptc_last_launch(int *grid, int *cluster, int *ksplit);
+ * share one output tile's K range (1 when the tiles are not split that way),
+ * *tile_n = output columns per tile (256, or 128 / 64 for narrow one-CTA
+ * tiles).  All zero before the first launch.  Host-side only (no device
+ * work).  Returns PTC_OK, or PTC_ERR_INVALID when a pointer is NULL. */
+int ptc_last_launch(int *grid, int *cluster, int *ksplit, int *tile_n);
 
 /* Tuning and test knobs, process-wide.  Returns PTC_OK, or PTC_ERR_INVALID for
  * an unknown key or a value out of range.  Keys:
@@ -368,6 +369,17 @@ int ptc_last_launch(int *grid, int *cluster, int *ksplit);
  *                  order (a rank-ordered sum of KS FP32 partial sums), and
  *                  FP16-accumulator results are rounded to binary16 once,
  *                  from that FP32 sum.  No workspace is used.
+ *   "tile_n"       output tile width: 0 (default) chooses by size; 64 or
+ *                  128: one CTA per 128 x 64 / 128 x 128 tile; 256: only
+ *                  128 x 256 one-CTA tiles (with or without K-split
+ *                  clusters) and 256 x 256 CTA-pair tiles.
+ *                  By size, a product whose 128 x 256 tiles would occupy
+ *                  fewer CTAs than there are SMs (one wave) takes, among
+ *                  narrow tiles that still fit one wave, K-split clusters and
+ *                  whole 128 x 256 tiles, the shape with the least estimated
+ *                  time: each SM writes C to L2 at ~32 bytes per clock, so
+ *                  narrow tiles spread a small product's output over more
+ *                  SMs.  Results do not depend on the choice.
  *   "pdl"          1 (default): kernels are launched with programmatic
  *                  stream serialization, so that a kernel can start (set up
  *                  barriers and tensor memory) while the previous kernel of

@@ -95,7 +95,7 @@ def lib() -> ctypes.CDLL:
         L.ptc_set_tuning.argtypes = [ctypes.c_char_p, _i64]
         _ip = ctypes.POINTER(ctypes.c_int)
         L.ptc_last_launch.restype = ctypes.c_int
-        L.ptc_last_launch.argtypes = [_ip, _ip, _ip]
+        L.ptc_last_launch.argtypes = [_ip, _ip, _ip, _ip]
         _lib = L
     return _lib
 
@@ -190,12 +190,12 @@ def ptc_set_tuning(key: str, value: int) -> int:
     return _check(lib().ptc_set_tuning(key.encode(), int(value)))
 
 
-def ptc_last_launch() -> tuple[int, int, int]:
-    """(grid CTAs, CTAs per cluster, CTAs sharing a tile's K range) of the
-    calling thread's last GEMM kernel launch."""
-    g, c, k = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
-    _check(lib().ptc_last_launch(ctypes.byref(g), ctypes.byref(c), ctypes.byref(k)))
-    return g.value, c.value, k.value
+def ptc_last_launch() -> tuple[int, int, int, int]:
+    """(grid CTAs, CTAs per cluster, CTAs sharing a tile's K range, tile
+    width) of the calling thread's last GEMM kernel launch."""
+    g, c, k, n = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().ptc_last_launch(ctypes.byref(g), ctypes.byref(c), ctypes.byref(k), ctypes.byref(n)))
+    return g.value, c.value, k.value, n.value
 
 
 # ---------------------------------------------------------------- torch layer

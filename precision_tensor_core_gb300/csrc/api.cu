@@ -44,6 +44,7 @@ std::atomic<int> g_tail_split{1};   // 1: split a short last wave in K
 std::atomic<int> g_split_min_kb{64};
 std::atomic<int> g_pair_stage_kb{2};  // CTA pairs: K blocks per ring stage
 std::atomic<int> g_ksplit{0};         // K-split clusters: 0 by size, 1 never, 2 / 4 / 8 that size
+std::atomic<int> g_tile_n{0};         // one-CTA tile width: 0 by size, 64 / 128 / 256 that width
 std::atomic<int> g_pdl{1};            // programmatic stream serialization of the library's kernels
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 std::atomic<int64_t> g_stall_tile{-1};
@@ -186,25 +187,75 @@ int fail(int code, const char *text) {
 }
 
 // ------------------------------------------------------------ launches
-// One CTA per 128 x 256 tile, or CTA pairs on 256 x 256 tiles.  One-CTA tiles
-// that fill at most half of the SMs run in K-split clusters (2-8 CTAs share
-// each tile's K blocks) when pick_ksplit takes them.  Otherwise pairs, which
-// move a third fewer operand bytes per output: once one-CTA tiles fill the
-// GPU they are faster for every route; below that, measured per route, FP16
-// pairs were faster from 32 one-CTA tiles up (N = 1024 .. 2048: 4-10%), the
-// integer routes (binary16 / E4M3 operands from a conversion pass) with one
-// CTA per tile.
-int choose_ctas(int64_t M, int64_t N, int64_t num_kb, int sms, bool f16) {
-    const int forced = g_cta_pair.load();
-    if (forced == 1 || forced == 2) return forced;
-    const int64_t tiles1 = ((M + ptc::kBM - 1) / ptc::kBM) * ((N + ptc::kBN - 1) / ptc::kBN);
-    if (2 * tiles1 <= sms && ptc::pick_ksplit(int(tiles1), int(num_kb), g_ksplit.load(), sms) > 1) return 1;
-    if (tiles1 >= sms) return 2;
-    return (f16 && tiles1 >= 32) ? 2 : 1;
+// Launch shape: CTAs per output tile (1, or a pair on 256 x 256 tiles), the
+// tile width of one-CTA tiles (256, 128 or 64 columns of 128 rows), and the
+// K-split knob passed to the kernel launcher (1: no split; 2 / 4 / 8 that
+// cluster size; 0 its size rule).
+struct Shape {
+    int ctas, bn, ks;
+};
+
+// Estimated SM clocks of one CTA's work in a single-wave launch, the quantity
+// the automatic shape choice minimises.  Per 128-byte K block: the larger of
+// the MMAs (2 * bn clocks for 128 rows; the E4M3 kind does twice the values
+// per block at twice the rate) and the operand copies (16 KiB of A plus bn
+// rows of B at ~128 bytes per clock); then the C tile leaving the SM at ~32
+// bytes per clock (the per-SM write path to L2, measured with ncu), which is
+// what makes 256-wide tiles slow when few SMs share a small product; a
+// K-split cluster also writes its partial sums to shared memory (~128 bytes
+// per clock) and passes two cluster barriers (~2000 clocks, measured).
+int64_t est_clocks(int64_t num_kb, int bn, int ks, int esize) {
+    const int64_t per_block = std::max<int64_t>(2 * bn, 128 + bn);
+    int64_t c = (num_kb + ks - 1) / ks * per_block + int64_t(4) * bn * esize;
+    if (ks > 1) c += int64_t(4) * bn + 2000;
+    return c;
+}
+
+int64_t tile_count(int64_t M, int64_t N, int rows, int cols) {
+    return ((M + rows - 1) / rows) * ((N + cols - 1) / cols);
+}
+
+// Multi-wave products run on CTA pairs (256 x 256 tiles: a third fewer
+// operand bytes per output).  A product whose 128 x 256 tiles fit one wave
+// takes the shape of least estimated time among: narrow one-CTA tiles
+// (128 x 128, 128 x 64) that still fit one wave, K-split clusters of
+// 128 x 256 tiles (pick_ksplit), and whole 128 x 256 tiles; whole tiles go to
+// pairs for FP16 from 32 one-CTA tiles up (measured 4-10% faster at N = 1024
+// .. 2048 before narrow tiles existed; the integer routes were faster with
+// one CTA per tile).  esize: bytes per C element.  The knobs cta_pair,
+// tile_n and ksplit force parts of the choice.
+Shape choose_shape(int64_t M, int64_t N, int64_t num_kb, int sms, bool f16, int esize) {
+    const int fpair = g_cta_pair.load(), ftile = g_tile_n.load(), fks = g_ksplit.load();
+    if (fpair == 2) return {2, ptc::kBN, 1};
+    if ((ftile == 64 || ftile == 128) && tile_count(M, N, ptc::kBM, ftile) <= (int64_t(1) << 20))
+        return {1, ftile, 1};
+    if (fpair == 1) return {1, ptc::kBN, fks};
+    const int64_t t256 = tile_count(M, N, ptc::kBM, ptc::kBN);
+    if (t256 >= sms) return {2, ptc::kBN, 1};
+    Shape best{1, ptc::kBN, 1};
+    int64_t best_c = est_clocks(num_kb, ptc::kBN, 1, esize);
+    if (fks != 1) {
+        const int ks = ptc::pick_ksplit(int(t256), int(num_kb), fks, sms);
+        if (ks > 1 && (fks != 0 || est_clocks(num_kb, ptc::kBN, ks, esize) < best_c)) {
+            best = {1, ptc::kBN, ks};
+            best_c = fks != 0 ? 0 : est_clocks(num_kb, ptc::kBN, ks, esize);
+        }
+    }
+    for (int bn : {128, 64}) {
+        if (ftile != 0 || tile_count(M, N, ptc::kBM, bn) > sms) continue;
+        const int64_t c = est_clocks(num_kb, bn, 1, esize);
+        if (c < best_c) {
+            best = {1, bn, 1};
+            best_c = c;
+        }
+    }
+    if (best.bn == ptc::kBN && best.ks == 1 && f16 && t256 >= 32) return {2, ptc::kBN, 1};
+    return best;
 }
 
 GemmArgs base_args(int64_t M, int64_t N, int64_t K, int k_elems_per_block, void *C, int64_t ldc,
-                   int ctas) {
+                   const Shape &sh) {
+    const int ctas = sh.ctas;
     GemmArgs a;
     std::memset(&a, 0, sizeof(a));
     a.C = C;
@@ -214,7 +265,8 @@ GemmArgs base_args(int64_t M, int64_t N, int64_t K, int k_elems_per_block, void 
     a.K = int(K);
     const int64_t tile_m = int64_t(ptc::kBM) * ctas;
     a.tiles_m = int((M + tile_m - 1) / tile_m);
-    a.tiles_n = int((N + ptc::kBN - 1) / ptc::kBN);
+    a.bn = sh.ctas == 1 ? sh.bn : ptc::kBN;
+    a.tiles_n = int((N + a.bn - 1) / a.bn);
     a.num_tiles = a.tiles_m * a.tiles_n;
     a.num_kb = int((K + k_elems_per_block - 1) / k_elems_per_block);
     a.kb_per_chunk = a.num_kb;
@@ -224,7 +276,7 @@ GemmArgs base_args(int64_t M, int64_t N, int64_t K, int k_elems_per_block, void 
     a.split_ok = g_tail_split.load();
     a.split_min_kb = g_split_min_kb.load();
     a.stage_kb = g_pair_stage_kb.load();
-    a.ksplit = g_ksplit.load();
+    a.ksplit = sh.ks;
     a.pdl = g_pdl.load();
     a.wait_limit_ns = g_wait_ns.load();
     return a;
@@ -291,14 +343,14 @@ int f16_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0) return zero_c(C, ldc, M, N, eb, *d, s);
 
-    const int ctas = choose_ctas(M, N, (K + 63) / 64, d->sms, true);
+    const Shape sh = choose_shape(M, N, (K + 63) / 64, d->sms, true, eb);
     CUtensorMap ta, tb;
     if ((rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, uint64_t(lda) * 2, 64, ptc::kBM)))
         return rc;
     if ((rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, N, K, uint64_t(ldb) * 2, 64, 64)))
         return rc;
-    GemmArgs args = base_args(M, N, K, 64, C, ldc, ctas);
-    return launch_gemm_checked(Kind::F16, true, epi, ctas, ta, tb, args, *d, s);
+    GemmArgs args = base_args(M, N, K, 64, C, ldc, sh);
+    return launch_gemm_checked(Kind::F16, true, epi, sh.ctas, ta, tb, args, *d, s);
 }
 
 }  // namespace
@@ -393,19 +445,19 @@ int int_gemm(bool s4, int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
         rc = fail_cuda(e, "operand conversion launch");
     else
         g_launches.fetch_add(1);
-    const int ctas = choose_ctas(M, N, ldw / k_elems, d->sms, false);
+    const Shape sh = choose_shape(M, N, ldw / k_elems, d->sms, false, eb);
     const CUtensorMapDataType dt = s4 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap ta, tb;
     if (!rc) rc = make_tmap(&ta, dt, aw, K, M, uint64_t(ldw) * wsize, k_elems, ptc::kBM);
-    if (!rc) rc = make_tmap(&tb, dt, bw, K, N, uint64_t(ldw) * wsize, k_elems, ptc::kBN / ctas);
+    if (!rc) rc = make_tmap(&tb, dt, bw, K, N, uint64_t(ldw) * wsize, k_elems, sh.bn / sh.ctas);
     if (!rc) {
-        GemmArgs args = base_args(M, N, K, k_elems, C, ldc, ctas);
+        GemmArgs args = base_args(M, N, K, k_elems, C, ldc, sh);
         const int ch = s4 ? g_chunk_s4.load() : g_chunk_s8.load();
         args.kb_per_chunk = ch > 0 ? ch : 1;
         args.out_mode = mode;
         args.scale_a = sa;
         args.scale_b = sb;
-        rc = launch_gemm_checked(s4 ? Kind::E4M3 : Kind::F16, false, ptc::EPI_INT, ctas, ta, tb, args, *d, s);
+        rc = launch_gemm_checked(s4 ? Kind::E4M3 : Kind::F16, false, ptc::EPI_INT, sh.ctas, ta, tb, args, *d, s);
     }
     cudaFreeAsync(ws, s);
     return rc;
@@ -459,16 +511,16 @@ int s8_rowb_gemm(int64_t M, int64_t N, int64_t K, const int8_t *A, int64_t lda, 
         if (e == cudaSuccess) g_launches.fetch_add(1);
     }
     if (e != cudaSuccess) rc = fail_cuda(e, "operand conversion launch");
-    const int ctas = choose_ctas(M, N, (K + 63) / 64, d->sms, false);
+    const Shape sh = choose_shape(M, N, (K + 63) / 64, d->sms, false, 4);
     CUtensorMap ta, tb;
     if (!rc) rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, aw, K, M, uint64_t(ldw_a) * 2, 64, ptc::kBM);
     if (!rc) rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, bw, N, K, uint64_t(ldw_b) * 2, 64, 64);
     if (!rc) {
-        GemmArgs args = base_args(M, N, K, 64, C, ldc, ctas);
+        GemmArgs args = base_args(M, N, K, 64, C, ldc, sh);
         const int ch = g_chunk_s8.load();
         args.kb_per_chunk = ch > 0 ? ch : 1;
         args.out_mode = ptc::OUT_S32;
-        rc = launch_gemm_checked(Kind::F16, true, ptc::EPI_INT, ctas, ta, tb, args, *d, s);
+        rc = launch_gemm_checked(Kind::F16, true, ptc::EPI_INT, sh.ctas, ta, tb, args, *d, s);
     }
     cudaFreeAsync(ws, s);
     return rc;
@@ -639,7 +691,7 @@ int host_gemm(int prec, int64_t M, int64_t N, int64_t K, const void *A, int64_t 
     for (int p = 0; p < npanels && rc == PTC_OK; ++p) {
         const int64_t r0 = p * panel, rows = std::min(panel, M - r0);
         cuda(cudaStreamWaitEvent(s, ev_a[p], 0), "stream wait");
-        const int ctas = choose_ctas(rows, N, (K + k_elems - 1) / k_elems, d->sms, f16);
+        const Shape sh = choose_shape(rows, N, (K + k_elems - 1) / k_elems, d->sms, f16, 4);
         CUtensorMap ta, tb;
         if (f16) {
             if (rc == PTC_OK)
@@ -658,16 +710,16 @@ int host_gemm(int prec, int64_t M, int64_t N, int64_t K, const void *A, int64_t 
             if (cuda(r, "operand conversion launch")) g_launches.fetch_add(1);
             const CUtensorMapDataType dt = s4 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
             if (rc == PTC_OK) rc = make_tmap(&ta, dt, wa, K, rows, uint64_t(ldw) * wsize, k_elems, ptc::kBM);
-            if (rc == PTC_OK) rc = make_tmap(&tb, dt, Wb, K, N, uint64_t(ldw) * wsize, k_elems, ptc::kBN / ctas);
+            if (rc == PTC_OK) rc = make_tmap(&tb, dt, Wb, K, N, uint64_t(ldw) * wsize, k_elems, sh.bn / sh.ctas);
         }
         if (rc != PTC_OK) break;
-        GemmArgs args = base_args(rows, N, K, k_elems, Cd + r0 * c_pitch, c_pitch / 4, ctas);
+        GemmArgs args = base_args(rows, N, K, k_elems, Cd + r0 * c_pitch, c_pitch / 4, sh);
         if (!f16) {
             const int ch = s4 ? g_chunk_s4.load() : g_chunk_s8.load();
             args.kb_per_chunk = ch > 0 ? ch : 1;
             args.out_mode = ptc::OUT_S32;
         }
-        rc = launch_gemm_checked(s4 ? Kind::E4M3 : Kind::F16, f16, f16 ? ptc::EPI_F32 : ptc::EPI_INT, ctas, ta, tb,
+        rc = launch_gemm_checked(s4 ? Kind::E4M3 : Kind::F16, f16, f16 ? ptc::EPI_F32 : ptc::EPI_INT, sh.ctas, ta, tb,
                                  args, *d, s);
         cuda(cudaEventRecord(ev_c[p], s), "event record");
         // C panel, device -> host, once its kernel is done.
@@ -828,9 +880,9 @@ int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile) {
     return PTC_OK;
 }
 
-int ptc_last_launch(int *grid, int *cluster, int *ksplit) {
-    if (!grid || !cluster || !ksplit) return fail(PTC_ERR_INVALID, "NULL pointer");
-    ptc::last_launch(grid, cluster, ksplit);
+int ptc_last_launch(int *grid, int *cluster, int *ksplit, int *tile_n) {
+    if (!grid || !cluster || !ksplit || !tile_n) return fail(PTC_ERR_INVALID, "NULL pointer");
+    ptc::last_launch(grid, cluster, ksplit, tile_n);
     return PTC_OK;
 }
 
@@ -866,6 +918,10 @@ int ptc_set_tuning(const char *key, int64_t value) {
     }
     if (std::strcmp(key, "ksplit") == 0 && (value == 0 || value == 1 || value == 2 || value == 4 || value == 8)) {
         g_ksplit.store(int(value));
+        return PTC_OK;
+    }
+    if (std::strcmp(key, "tile_n") == 0 && (value == 0 || value == 64 || value == 128 || value == 256)) {
+        g_tile_n.store(int(value));
         return PTC_OK;
     }
     if (std::strcmp(key, "pdl") == 0 && (value == 0 || value == 1)) {

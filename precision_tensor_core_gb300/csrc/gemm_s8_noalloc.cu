@@ -187,6 +187,7 @@ extern "C" int gemm_s8_noalloc(int64_t M, int64_t N, int64_t K, const int8_t *A,
     args.N = int(N);
     args.K = int(K);
     args.tiles_m = int((M + ptc::kBM - 1) / ptc::kBM);
+    args.bn = ptc::kBN;
     args.tiles_n = int((N + ptc::kBN - 1) / ptc::kBN);
     args.num_tiles = args.tiles_m * args.tiles_n;
     args.num_kb = int((K + 63) / 64);

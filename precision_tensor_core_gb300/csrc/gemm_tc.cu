@@ -76,27 +76,30 @@ namespace {
 
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;
-constexpr int TMEM_COLS = 512;                  // two accumulators of kBN columns
 constexpr int KSTEP_BYTES = 32;                 // K bytes per tcgen05.mma (16 f16 / 32 e4m3)
 constexpr int KSTEPS = kRowBytes / KSTEP_BYTES; // MMAs per stage
 
 // Per-CTA shapes of the variants.  A CTA stages 128 rows of A; alone it
-// stages all 256 rows of B (4 stages of one K block, 48 KiB each), in a pair
-// it stages half of B (the pair's MMAs read B from both CTAs), in 3 stages of
-// two K blocks (64 KiB each) by default or 7 stages of one K block (32 KiB
-// each): two-block stages take half as many barrier round trips per byte and
-// measured 3-6% faster.
-template <int CTAS, int SUBK>
+// stages all BN rows of B (a 192 KiB ring of one-K-block stages: 4 of 48 KiB
+// for 256-wide tiles, 6 of 32 KiB for 128-wide, 8 of 24 KiB for 64-wide), in
+// a pair it stages half of B (the pair's MMAs read B from both CTAs), in 3
+// stages of two K blocks (64 KiB each) by default or 7 stages of one K block
+// (32 KiB each): two-block stages take half as many barrier round trips per
+// byte and measured 3-6% faster.
+constexpr int kRing1 = 4 * (kBM + kBN) * kRowBytes;  // one-CTA ring bytes
+template <int CTAS, int SUBK, int BN>
 struct Cfg {
     static_assert(CTAS == 2 || SUBK == 1, "one CTA stages one K block at a time");
-    static constexpr int STAGES = CTAS == 1 ? 4 : (SUBK == 1 ? 7 : 3);
+    static_assert(BN == kBN || (CTAS == 1 && (BN == 64 || BN == 128)), "narrow tiles are one-CTA tiles");
     static constexpr int SUB = SUBK;  // K blocks per stage
-    static constexpr int B_ROWS = kBN / CTAS;
+    static constexpr int B_ROWS = BN / CTAS;
     static constexpr int A_BLOCK = kBM * kRowBytes;     // one K block of A
     static constexpr int B_BLOCK = B_ROWS * kRowBytes;  // one K block of B
     static constexpr int A_STAGE = SUB * A_BLOCK;
     static constexpr int B_STAGE = SUB * B_BLOCK;
     static constexpr int STAGE = A_STAGE + B_STAGE;
+    static constexpr int STAGES = CTAS == 1 ? kRing1 / STAGE : (SUBK == 1 ? 7 : 3);
+    static constexpr int TMEM_COLS = 2 * BN;  // two accumulators of BN columns
 };
 
 template <int STAGES, int SUB>
@@ -116,21 +119,25 @@ struct SharedTail {
 constexpr int kStageC = 32 * 32 * 4;
 constexpr int kStageWarp = 4 * kStageC;
 
-template <int CTAS, int SUBK>
+template <int CTAS, int SUBK, int BN = kBN>
 constexpr size_t smem_bytes() {
-    return 1024 + size_t(Cfg<CTAS, SUBK>::STAGES) * Cfg<CTAS, SUBK>::STAGE +
-           sizeof(SharedTail<Cfg<CTAS, SUBK>::STAGES, SUBK>);
+    return 1024 + size_t(Cfg<CTAS, SUBK, BN>::STAGES) * Cfg<CTAS, SUBK, BN>::STAGE +
+           sizeof(SharedTail<Cfg<CTAS, SUBK, BN>::STAGES, SUBK>);
 }
-static_assert(smem_bytes<1, 1>() <= 232448 && smem_bytes<2, 1>() <= 232448 && smem_bytes<2, 2>() <= 232448,
+static_assert(smem_bytes<1, 1>() <= 232448 && smem_bytes<2, 1>() <= 232448 && smem_bytes<2, 2>() <= 232448 &&
+                  smem_bytes<1, 1, 128>() <= 232448 && smem_bytes<1, 1, 64>() <= 232448,
               "shared memory budget");
 // A K-split cluster's partial sums: 128 rows of 256 four-byte values, row r
 // at r * 1024 bytes, its 16-byte piece j at piece j ^ (r & 7) (the writers,
 // one row per lane, and the readers, one piece per lane, do not conflict).
 constexpr int kPartialRow = kBN * 4;
-static_assert(Cfg<1, 1>::STAGES * Cfg<1, 1>::STAGE >= kBM * kPartialRow, "the ring holds a tile's partial sums");
-static_assert(Cfg<1, 1>::STAGES * Cfg<1, 1>::STAGE >= EPI_WARPS * kStageWarp &&
-                  Cfg<2, 1>::STAGES * Cfg<2, 1>::STAGE >= EPI_WARPS * kStageWarp &&
-                  Cfg<2, 2>::STAGES * Cfg<2, 2>::STAGE >= EPI_WARPS * kStageWarp,
+static_assert(Cfg<1, 1, kBN>::STAGES * Cfg<1, 1, kBN>::STAGE >= kBM * kPartialRow,
+              "the ring holds a tile's partial sums");
+static_assert(Cfg<1, 1, kBN>::STAGES * Cfg<1, 1, kBN>::STAGE >= EPI_WARPS * kStageWarp &&
+                  Cfg<1, 1, 128>::STAGES * Cfg<1, 1, 128>::STAGE >= EPI_WARPS * kStageWarp &&
+                  Cfg<1, 1, 64>::STAGES * Cfg<1, 1, 64>::STAGE >= EPI_WARPS * kStageWarp &&
+                  Cfg<2, 1, kBN>::STAGES * Cfg<2, 1, kBN>::STAGE >= EPI_WARPS * kStageWarp &&
+                  Cfg<2, 2, kBN>::STAGES * Cfg<2, 2, kBN>::STAGE >= EPI_WARPS * kStageWarp,
               "the ring holds the C staging of a single-wave launch");
 
 __device__ __forceinline__ void tile_coords(int t, const GemmArgs &a, int &mb, int &nb) {
@@ -149,7 +156,7 @@ __device__ __forceinline__ void tile_coords(int t, const GemmArgs &a, int &mb, i
 // tensor cores at the rate of a whole tile; the epilogue warp that finishes
 // second adds the other half's partial sums (no waiting on either side).
 struct WorkRef {
-    int mb, nb;    // tile coordinates in units of (kBM * CTAS) x kBN
+    int mb, nb;    // tile coordinates in units of (kBM * CTAS) x BN
     int kb0, kb1;  // K blocks of this unit
     int part;      // 0: whole tile; 1, 2: first / second K half of split tile `slot`
     int slot;
@@ -300,16 +307,17 @@ __device__ __forceinline__ void tma_store_block(const CUtensorMap *tmC, uint32_t
     stage_end(tmC, stg, lane, col, row0);
 }
 
-// Scaled integer epilogue (dequantisation): for the 128 columns col0 .. of
+// Scaled integer epilogue (dequantisation): for the HALF columns col0 .. of
 // `row`, value = rn(rn(rn(float(acc)) * sa) * sb) in FP32, in that order and
 // without contraction, then rounded to nearest-even in the output type.
 // Columns at or beyond N are not written.
+template <int HALF>
 __device__ __forceinline__ void store_scaled_row(const GemmArgs &args, int row, int col0,
-                                                 const int32_t (&acc)[kBN / 2], const CUtensorMap *tmC,
+                                                 const int32_t (&acc)[HALF], const CUtensorMap *tmC,
                                                  bool use_tma, uint32_t stg, int lane, int row0, bool pending) {
     const float sa = (args.scale_a && row < args.M) ? __ldg(args.scale_a + row) : 1.0f;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < HALF / 32; ++c) {
         const int cc = col0 + 32 * c;
         if (cc >= args.N) break;
         const int valid = min(32, args.N - cc);
@@ -580,14 +588,18 @@ __device__ __forceinline__ void ksplit_complete(const GemmArgs &args, int mb, in
 // its full barriers collect both CTAs' copies, its commits arrive on both
 // CTAs' empty / accumulator-full barriers, and both CTAs' epilogues release
 // accumulator buffers on its acc_empty barriers.
-template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS>
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
     static_assert(!(B_MN && KIND == Kind::E4M3), "MN-major B is used by the FP16 path only");
-    static_assert(KS == 1 || (CTAS == 1 && kBM % (KS * EPI_WARPS) == 0), "K-split clusters of one-CTA tiles");
+    static_assert(KS == 1 || (CTAS == 1 && BN == kBN && kBM % (KS * EPI_WARPS) == 0),
+                  "K-split clusters of 256-wide one-CTA tiles");
     constexpr bool INT_OUT = EPI == EPI_INT;
-    using C_ = Cfg<CTAS, SUBK>;
+    constexpr int HALF = BN / 2;      // columns of an epilogue warp's slice
+    constexpr int NCH = HALF / 32;    // 32-column chunks of a slice
+    using C_ = Cfg<CTAS, SUBK, BN>;
+    constexpr int TMEM_COLS = C_::TMEM_COLS;
     constexpr int STAGES = C_::STAGES;
     extern __shared__ uint8_t smem_raw[];
     // 128-byte swizzle atoms must sit on 1024-byte boundaries.
@@ -660,7 +672,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 WorkRef wr = work_unit(t, args, C_::SUB);
                 if constexpr (KS > 1) ksplit_range(wr, krank, KS);
                 const int m0 = wr.mb * (kBM * CTAS) + int(rank) * kBM;
-                const int n0 = wr.nb * kBN + int(rank) * C_::B_ROWS;
+                const int n0 = wr.nb * BN + int(rank) * C_::B_ROWS;
                 for (int kb = wr.kb0; kb < wr.kb1; kb += C_::SUB) {
                     if (!mbar_wait(&st->empty[s], ph ^ 1u, &st->abort, &g_error_word, limit)) {
                         ok = false;
@@ -741,7 +753,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0 && rank == 0) {
             constexpr uint32_t IDESC =
                 instr_desc(EPI == EPI_F16ACC ? 0u : 1u, 0u, 0u, B_MN, kBM * CTAS,
-                           kBN);  // F16 x F16 or E4M3 x E4M3 -> F32 (or F16 accumulators)
+                           BN);  // F16 x F16 or E4M3 x E4M3 -> F32 (or F16 accumulators)
             const uint32_t a_base = smem_u32(a_ring);
             const uint32_t b_base = smem_u32(b_ring);
             int s = 0;
@@ -759,7 +771,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         break;
                     }
                     tc_fence_after_sync();
-                    const uint32_t d_tmem = tmem_base + uint32_t(abuf * kBN);
+                    const uint32_t d_tmem = tmem_base + uint32_t(abuf * BN);
                     const int kb0 = wr.kb0 + ch * args.kb_per_chunk;
                     const int kb1 = min(wr.kb1, kb0 + args.kb_per_chunk);
                     for (int kb = kb0; kb < kb1 && ok; kb += C_::SUB) {
@@ -827,7 +839,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                               : -1;
         const uint32_t stg = smem_u32(smem) + uint32_t(warp - 2) * uint32_t(kStageWarp);
         bool stg_pending = false;           // TMA stores may still be reading the blocks
-        const uint32_t t_lane = tmem_base + (uint32_t(32 * q) << 16) + uint32_t(h * (kBN / 2));
+        const uint32_t t_lane = tmem_base + (uint32_t(32 * q) << 16) + uint32_t(h * HALF);
         // Accumulator buffers are released on the issuing (even) CTA's barriers.
         auto release = [&](int b) {
             tc_fence_before_sync();
@@ -846,11 +858,11 @@ __global__ void __launch_bounds__(THREADS, 1)
             WorkRef wr = work_unit(t, args, C_::SUB);
             if constexpr (KS > 1) ksplit_range(wr, krank, KS);
             const int row = wr.mb * (kBM * CTAS) + int(rank) * kBM + 32 * q + lane;
-            const int col0 = wr.nb * kBN + h * (kBN / 2);
+            const int col0 = wr.nb * BN + h * HALF;
             if constexpr (INT_OUT) {
-                int32_t acc[kBN / 2];
+                int32_t acc[HALF];
 #pragma unroll
-                for (int j = 0; j < kBN / 2; ++j) acc[j] = 0;
+                for (int j = 0; j < HALF; ++j) acc[j] = 0;
                 const int nchunks = (wr.kb1 - wr.kb0 + args.kb_per_chunk - 1) / args.kb_per_chunk;
                 for (int ch = 0; ch < nchunks; ++ch) {
                     if (!warp_wait(&st->acc_full[abuf], aph, &st->abort, limit, lane)) {
@@ -859,9 +871,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                     tc_fence_after_sync();
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
+                    for (int c = 0; c < HALF / 16; ++c) {
                         uint32_t r[16];
-                        tmem_ld_16cols(t_lane + uint32_t(abuf * kBN + 16 * c), r);
+                        tmem_ld_16cols(t_lane + uint32_t(abuf * BN + 16 * c), r);
                         tmem_ld_wait();
 #pragma unroll
                         for (int j = 0; j < 16; ++j) acc[16 * c + j] += __float2int_rn(__uint_as_float(r[j]));
@@ -877,12 +889,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // K-split cluster: the partial sums wait in the ring for the
                     // cluster's completion pass.
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        put_partial(smem_u32(smem), 32 * q + lane, h * (kBN / 8) + 8 * c,
+                    for (int c = 0; c < NCH; ++c)
+                        put_partial(smem_u32(smem), 32 * q + lane, h * (HALF / 4) + 8 * c,
                                     reinterpret_cast<const uint32_t(&)[32]>(acc[32 * c]));
                     continue;
                 }
-                if (wr.part != 0) {
+                if (BN == kBN && wr.part != 0) {
                     // Sum of the two K halves, wrapping like every int32 partial sum.
                     const int slice = ((wr.slot * CTAS + int(rank)) * 4 + q) * 2 + h;
                     uint32_t *cnt = args.split_count + slice;
@@ -890,7 +902,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (!finish) {
                         float4 *mine = split_partial(args, slice, wr.part - 1);
 #pragma unroll
-                        for (int i = 0; i < kBN / 8; ++i)
+                        for (int i = 0; i < HALF / 4; ++i)
                             mine[i * 32 + lane] = make_float4(__int_as_float(acc[4 * i]), __int_as_float(acc[4 * i + 1]),
                                                               __int_as_float(acc[4 * i + 2]), __int_as_float(acc[4 * i + 3]));
                         finish = split_publish(cnt, lane);
@@ -898,7 +910,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (!finish) continue;
                     const float4 *other = split_partial(args, slice, 2 - wr.part);
 #pragma unroll
-                    for (int i = 0; i < kBN / 8; ++i) {
+                    for (int i = 0; i < HALF / 4; ++i) {
                         const float4 o = __ldcg(other + i * 32 + lane);
                         acc[4 * i] = int32_t(uint32_t(acc[4 * i]) + uint32_t(__float_as_int(o.x)));
                         acc[4 * i + 1] = int32_t(uint32_t(acc[4 * i + 1]) + uint32_t(__float_as_int(o.y)));
@@ -913,7 +925,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const bool use_tma = args.c_tma && args.num_vunits <= nclusters;
                 if (args.out_mode == OUT_S32 && use_tma) {
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < NCH; ++c) {
                         const int cc = col0 + 32 * c;
                         if (cc < args.N)
                             tma_store_block(&tmC, stg + uint32_t(c * kStageC),
@@ -925,7 +937,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (row < args.M) {
                         int32_t *crow = reinterpret_cast<int32_t *>(args.C) + int64_t(row) * args.ldc;
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
+                        for (int c = 0; c < NCH; ++c) {
                             const int cc = col0 + 32 * c;
                             if (cc < args.N)
                                 store_32(crow + cc, reinterpret_cast<const uint32_t(&)[32]>(acc[32 * c]), args.N - cc,
@@ -934,7 +946,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     }
                 } else {
                     const bool tma_f32 = use_tma && args.out_mode == OUT_F32;
-                    store_scaled_row(args, row, col0, acc, &tmC, tma_f32, stg, lane, row0, stg_pending);
+                    store_scaled_row<HALF>(args, row, col0, acc, &tmC, tma_f32, stg, lane, row0, stg_pending);
                     stg_pending = stg_pending || tma_f32;
                 }
             } else {
@@ -951,23 +963,23 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // K-split cluster: the partial sums (FP16 accumulators widened
                     // exactly to FP32) wait in the ring for the completion pass.
 #pragma unroll
-                    for (int c = 0; c < 4; ++c) {
+                    for (int c = 0; c < NCH; ++c) {
                         uint32_t r[32];
-                        tmem_ld_32cols(t_lane + uint32_t(abuf * kBN + 32 * c), r);
+                        tmem_ld_32cols(t_lane + uint32_t(abuf * BN + 32 * c), r);
                         tmem_ld_wait();
                         if constexpr (EPI == EPI_F16ACC) {
 #pragma unroll
                             for (int e = 0; e < 32; ++e)
                                 r[e] = __float_as_uint(__half2float(__ushort_as_half(static_cast<uint16_t>(r[e]))));
                         }
-                        put_partial(smem_u32(smem), 32 * q + lane, h * (kBN / 8) + 8 * c, r);
+                        put_partial(smem_u32(smem), 32 * q + lane, h * (HALF / 4) + 8 * c, r);
                     }
                 } else {
                     if (wr.part == 0 && EPI == EPI_F32 && use_tma) {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
+                        for (int c = 0; c < NCH; ++c) {
                             uint32_t r[32];
-                            tmem_ld_32cols(t_lane + uint32_t(abuf * kBN + 32 * c), r);
+                            tmem_ld_32cols(t_lane + uint32_t(abuf * BN + 32 * c), r);
                             tmem_ld_wait();
                             const int cc = col0 + 32 * c;
                             if (cc < args.N)
@@ -978,9 +990,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                     } else if (wr.part == 0) {
                         float *crow = reinterpret_cast<float *>(args.C) + int64_t(row) * args.ldc;
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) {
+                        for (int c = 0; c < NCH; ++c) {
                             uint32_t r[32];
-                            tmem_ld_32cols(t_lane + uint32_t(abuf * kBN + 32 * c), r);
+                            tmem_ld_32cols(t_lane + uint32_t(abuf * BN + 32 * c), r);
                             tmem_ld_wait();
                             const int cc = col0 + 32 * c;
                             if constexpr (EPI == EPI_F16ACC) {
@@ -991,13 +1003,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                                 if (row < args.M && cc < args.N) store_32(crow + cc, r, args.N - cc, args.c_wide);
                             }
                         }
-                    } else {
+                    } else if constexpr (BN == kBN) {
+                        // (Only 256-wide tiles are split in halves of K.)
                         const int slice = ((wr.slot * CTAS + int(rank)) * 4 + q) * 2 + h;
                         void *crow = nullptr;
                         if (row < args.M)
                             crow = static_cast<uint8_t *>(args.C) +
                                    (int64_t(row) * args.ldc + col0) * (EPI == EPI_F16ACC ? 2 : 4);
-                        split_epilogue<EPI>(t_lane + uint32_t(abuf * kBN), args.split_count + slice,
+                        split_epilogue<EPI>(t_lane + uint32_t(abuf * BN), args.split_count + slice,
                                             split_partial(args, slice, wr.part - 1), split_partial(args, slice, 2 - wr.part),
                                             crow, args.N - col0, args.c_wide, lane);
                     }
@@ -1050,18 +1063,18 @@ struct LaunchCache {
 };
 
 struct LastLaunch {
-    int grid = 0, cluster = 0, ksplit = 0;
+    int grid = 0, cluster = 0, ksplit = 0, bn = 0;
 };
 thread_local LastLaunch g_last;
 
 // Launch shape of one variant: dynamic shared memory, cluster dimension and
 // (optionally) programmatic stream serialization.
-template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS>
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN>
 void launch_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[2], bool pdl, cudaStream_t stream) {
     std::memset(&cfg, 0, sizeof(cfg));
     std::memset(attr, 0, sizeof(attr));
     cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = smem_bytes<CTAS, SUBK>();
+    cfg.dynamicSmemBytes = smem_bytes<CTAS, SUBK, BN>();
     cfg.stream = stream;
     cfg.attrs = attr;
     int n = 0;
@@ -1082,22 +1095,22 @@ void launch_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[2], bool
 
 // Clusters of the variant that can be resident at once on the current device
 // (cached per device; the shared-memory opt-in is set on first use).
-template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS>
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN>
 cudaError_t cluster_capacity(int sms, int *out) {
-    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS, SUBK, KS>;
+    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS, SUBK, KS, BN>;
     constexpr int CL = CTAS * KS;
     static thread_local LaunchCache cache;  // per device (re-queried when it changes)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev != cache.dev) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes<CTAS, SUBK>()));
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes<CTAS, SUBK, BN>()));
         if (e != cudaSuccess) return e;
         int clusters = sms / CL;
         if constexpr (CL > 1) {
             cudaLaunchConfig_t cfg;
             cudaLaunchAttribute attr[2];
-            launch_config<KIND, B_MN, EPI, CTAS, SUBK, KS>(cfg, attr, false, nullptr);
+            launch_config<KIND, B_MN, EPI, CTAS, SUBK, KS, BN>(cfg, attr, false, nullptr);
             cfg.gridDim = dim3(CL * (sms / CL), 1, 1);
             int n = 0;
             e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
@@ -1112,17 +1125,17 @@ cudaError_t cluster_capacity(int sms, int *out) {
     return cudaSuccess;
 }
 
-template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS>
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN>
 cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args,
                        int sms, cudaMemPool_t pool, cudaStream_t stream) {
-    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS, SUBK, KS>;
+    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS, SUBK, KS, BN>;
     int maxc = 0;
-    cudaError_t e = cluster_capacity<KIND, B_MN, EPI, CTAS, SUBK, KS>(sms, &maxc);
+    cudaError_t e = cluster_capacity<KIND, B_MN, EPI, CTAS, SUBK, KS, BN>(sms, &maxc);
     if (e != cudaSuccess) return e;
     if (KS > 1 && args.num_tiles > maxc) return cudaErrorInvalidConfiguration;  // one wave of clusters
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    launch_config<KIND, B_MN, EPI, CTAS, SUBK, KS>(cfg, attr, args.pdl != 0, stream);
+    launch_config<KIND, B_MN, EPI, CTAS, SUBK, KS, BN>(cfg, attr, args.pdl != 0, stream);
     // Work list: split the last wave's tiles in K when they fill at most half
     // of the clusters (a lone partial wave included).  The halves exchange
     // partial sums through a stream-ordered workspace from `pool`: a counter
@@ -1145,8 +1158,8 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
     // The split saves about half of a tile's K loop (~0.14 us per K block);
     // setting up the exchange costs ~6 us per call, so short K (below
     // split_min_kb blocks, 64 by default) runs whole.
-    if (KS == 1 && pool != nullptr && a.split_ok && a.num_kb > SUBK && a.num_kb >= a.split_min_kb && tail > 0 &&
-        2 * tail <= maxc) {
+    if (KS == 1 && BN == kBN && pool != nullptr && a.split_ok && a.num_kb > SUBK && a.num_kb >= a.split_min_kb &&
+        tail > 0 && 2 * tail <= maxc) {
         const size_t slices = size_t(tail) * CTAS * EPI_WARPS;
         const size_t count_bytes = (slices * sizeof(uint32_t) + 255) / 256 * 256;
         const size_t bytes = count_bytes + slices * 2 * kSliceWords * sizeof(float);
@@ -1178,6 +1191,7 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
         g_last.grid = CTAS * KS * clusters;
         g_last.cluster = CTAS * KS;
         g_last.ksplit = KS;
+        g_last.bn = BN;
     }
     if (ws != nullptr) cudaFreeAsync(ws, stream);
     if (e != cudaSuccess) return e;
@@ -1190,9 +1204,9 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
 int ksplit_capacity(int ks, int sms) {
     int cap = 0;
     cudaError_t e = cudaSuccess;
-    if (ks == 8) e = cluster_capacity<Kind::F16, true, EPI_F32, 1, 1, 8>(sms, &cap);
-    if (ks == 4) e = cluster_capacity<Kind::F16, true, EPI_F32, 1, 1, 4>(sms, &cap);
-    if (ks == 2) e = cluster_capacity<Kind::F16, true, EPI_F32, 1, 1, 2>(sms, &cap);
+    if (ks == 8) e = cluster_capacity<Kind::F16, true, EPI_F32, 1, 1, 8, kBN>(sms, &cap);
+    if (ks == 4) e = cluster_capacity<Kind::F16, true, EPI_F32, 1, 1, 4, kBN>(sms, &cap);
+    if (ks == 2) e = cluster_capacity<Kind::F16, true, EPI_F32, 1, 1, 2, kBN>(sms, &cap);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return 0;
@@ -1202,10 +1216,11 @@ int ksplit_capacity(int ks, int sms) {
 
 }  // namespace
 
-void last_launch(int *grid, int *cluster, int *ksplit) {
+void last_launch(int *grid, int *cluster, int *ksplit, int *tile_n) {
     *grid = g_last.grid;
     *cluster = g_last.cluster;
     *ksplit = g_last.ksplit;
+    *tile_n = g_last.bn;
 }
 
 int pick_ksplit(int tiles, int num_kb, int knob, int sms) {
@@ -1224,19 +1239,24 @@ int pick_ksplit(int tiles, int num_kb, int knob, int sms) {
 
 size_t gemm_smem_bytes(int ctas) { return ctas == 2 ? smem_bytes<2, 2>() : smem_bytes<1, 1>(); }
 
-// One-CTA launches run as K-split clusters when pick_ksplit says so.
+// One-CTA launches of 256-wide tiles run as K-split clusters when pick_ksplit
+// says so; args.bn = 64 / 128 selects the narrow one-CTA tiles.
 cudaError_t launch_gemm(Kind kind, bool b_mn_major, int epi, int ctas, const CUtensorMap &ta,
                         const CUtensorMap &tb, const GemmArgs &args, int sms, cudaMemPool_t pool,
                         cudaStream_t stream) {
-    const int ks = ctas == 1 ? pick_ksplit(args.num_tiles, args.num_kb, args.ksplit, sms) : 1;
+    const int bn = (ctas == 1 && args.bn != 0) ? args.bn : kBN;
+    if (bn != kBN && bn != 64 && bn != 128) return cudaErrorInvalidValue;
+    const int ks = (ctas == 1 && bn == kBN) ? pick_ksplit(args.num_tiles, args.num_kb, args.ksplit, sms) : 1;
 #define PTC_LAUNCH(K, BMN, E)                                                                       \
     do {                                                                                            \
-        if (ks == 8) return launch_one<K, BMN, E, 1, 1, 8>(ta, tb, args, sms, pool, stream);        \
-        if (ks == 4) return launch_one<K, BMN, E, 1, 1, 4>(ta, tb, args, sms, pool, stream);        \
-        if (ks == 2) return launch_one<K, BMN, E, 1, 1, 2>(ta, tb, args, sms, pool, stream);        \
-        return ctas == 1 ? launch_one<K, BMN, E, 1, 1, 1>(ta, tb, args, sms, pool, stream)          \
-               : args.stage_kb == 1 ? launch_one<K, BMN, E, 2, 1, 1>(ta, tb, args, sms, pool, stream) \
-                                    : launch_one<K, BMN, E, 2, 2, 1>(ta, tb, args, sms, pool, stream); \
+        if (bn == 64) return launch_one<K, BMN, E, 1, 1, 1, 64>(ta, tb, args, sms, pool, stream);   \
+        if (bn == 128) return launch_one<K, BMN, E, 1, 1, 1, 128>(ta, tb, args, sms, pool, stream); \
+        if (ks == 8) return launch_one<K, BMN, E, 1, 1, 8, kBN>(ta, tb, args, sms, pool, stream);   \
+        if (ks == 4) return launch_one<K, BMN, E, 1, 1, 4, kBN>(ta, tb, args, sms, pool, stream);   \
+        if (ks == 2) return launch_one<K, BMN, E, 1, 1, 2, kBN>(ta, tb, args, sms, pool, stream);   \
+        return ctas == 1 ? launch_one<K, BMN, E, 1, 1, 1, kBN>(ta, tb, args, sms, pool, stream)     \
+               : args.stage_kb == 1 ? launch_one<K, BMN, E, 2, 1, 1, kBN>(ta, tb, args, sms, pool, stream) \
+                                    : launch_one<K, BMN, E, 2, 2, 1, kBN>(ta, tb, args, sms, pool, stream); \
     } while (0)
     if (kind == Kind::F16 && b_mn_major && epi == EPI_F32) PTC_LAUNCH(Kind::F16, true, EPI_F32);
     if (kind == Kind::F16 && b_mn_major && epi == EPI_F16ACC) PTC_LAUNCH(Kind::F16, true, EPI_F16ACC);

@@ -22,7 +22,8 @@ struct GemmArgs {
     void *C;               // float (FP16 path) or int32 (integer paths), row-major
     int64_t ldc;           // elements
     int M, N, K;           // K in operand elements
-    int tiles_m, tiles_n;  // output tiles of kBM x kBN
+    int tiles_m, tiles_n;  // output tiles of (kBM * ctas) x bn
+    int bn;                // one-CTA launches: tile width 256 (0 means 256), 128 or 64
     int num_tiles;
     int num_kb;            // K blocks of kRowBytes bytes
     int kb_per_chunk;      // K blocks summed in one accumulator buffer before the
@@ -76,8 +77,9 @@ enum Epi : int {
 //   F16  + B MN-major + EPI_F16ACC:  gemm_f16_f16acc
 //   F16  + B K-major  + EPI_INT:     gemm_s8 (operands converted s8 -> f16)
 //   E4M3 + B K-major  + EPI_INT:     gemm_s4 (operands converted s4 -> e4m3)
-// args.tiles_m counts tiles of kBM * ctas rows.  The tensor map of A has boxes
-// of kBM rows; that of B boxes of kBN / ctas rows (K-major) or 64 x 64 (MN-major).
+// args.tiles_m counts tiles of kBM * ctas rows, args.tiles_n tiles of args.bn
+// columns (kBN for CTA pairs).  The tensor map of A has boxes of kBM rows;
+// that of B boxes of bn / ctas rows (K-major) or 64 x 64 (MN-major).
 // With a non-null pool (and args.split_ok) a short last wave is split in K,
 // using a workspace of at most ~20 MB taken from the pool on `stream` and
 // returned after the kernel; a null pool runs every tile whole.
@@ -92,8 +94,9 @@ cudaError_t launch_gemm(Kind kind, bool b_mn_major, int epi, int ctas, const CUt
 int pick_ksplit(int tiles, int num_kb, int knob, int sms);
 
 // Launch shape of the calling thread's last GEMM kernel launch (grid CTAs,
-// CTAs per cluster, CTAs sharing a tile's K range); zeros before the first.
-void last_launch(int *grid, int *cluster, int *ksplit);
+// CTAs per cluster, CTAs sharing a tile's K range, tile width); zeros before
+// the first.
+void last_launch(int *grid, int *cluster, int *ksplit, int *tile_n);
 
 // C[M x N] = 0 for elements of esize (2 or 4) bytes, ldc in elements.
 cudaError_t launch_zero_fill(void *C, int64_t ldc, int M, int N, int esize, int grid, cudaStream_t stream);

@@ -44,18 +44,22 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-DEFAULTS = {"cta_pair": 0, "group_m": 8, "l2_hint": 0, "s8_chunk_kb": 16,
-            "s4_chunk_kb": 64, "tail_split": 1, "split_min_kb": 64, "pair_stage_kb": 2, "ksplit": 0, "pdl": 1}
+DEFAULTS = {"cta_pair": 0, "group_m": 8, "l2_hint": 0, "s8_chunk_kb": 16, "s4_chunk_kb": 64, "tail_split": 1,
+            "split_min_kb": 64, "pair_stage_kb": 2, "ksplit": 0, "pdl": 1, "tile_n": 0}
 KNOBS = {"cta_pair": [1, 2], "pair_stage_kb": [1], "tail_split": [0], "split_min_kb": [16, 32],
          "group_m": [4, 16, 32], "l2_hint": [1, 2, 3], "s8_chunk_kb": [4, 8], "s4_chunk_kb": [2, 8, 16, 128],
-         "ksplit": [1, 2, 4, 8], "pdl": [0]}
+         "ksplit": [1, 2, 4, 8], "pdl": [0], "tile_n": [64, 128, 256]}
 # `launch` mode: launch-shape settings compared at small sizes, each timed as
 # the median of 7 replays of a CUDA graph of back-to-back calls.
-LAUNCH_SETTINGS = [("plain launches, no K-split", {"ksplit": 1, "pdl": 0}),
-                   ("programmatic launches, no K-split", {"ksplit": 1, "pdl": 1}),
-                   ("defaults (K-split by size, programmatic)", {"ksplit": 0, "pdl": 1}),
-                   ("K-split 2", {"ksplit": 2, "pdl": 1}), ("K-split 4", {"ksplit": 4, "pdl": 1}),
-                   ("K-split 8", {"ksplit": 8, "pdl": 1})]
+LAUNCH_SETTINGS = [("256-wide, plain launches", {"tile_n": 256, "ksplit": 1, "pdl": 0}),
+                   ("256-wide", {"tile_n": 256, "ksplit": 1, "pdl": 1}),
+                   ("256-wide, K-split by size", {"tile_n": 256, "ksplit": 0, "pdl": 1}),
+                   ("K-split 2", {"tile_n": 256, "ksplit": 2, "pdl": 1}),
+                   ("K-split 4", {"tile_n": 256, "ksplit": 4, "pdl": 1}),
+                   ("K-split 8", {"tile_n": 256, "ksplit": 8, "pdl": 1}),
+                   ("128-wide", {"tile_n": 128, "ksplit": 1, "pdl": 1}),
+                   ("64-wide", {"tile_n": 64, "ksplit": 1, "pdl": 1}),
+                   ("defaults", {"tile_n": 0, "ksplit": 0, "pdl": 1})]
 
 
 def main():
@@ -164,7 +168,8 @@ def main():
                 v.append(e0.elapsed_time(e1) / calls * 1000.0)
             return statistics.median(v)
 
-        print(f"{'N':>6} {'prec':>4} " + " ".join(f"{name:>42}" for name, _ in LAUNCH_SETTINGS))
+        print("each entry: microseconds per call (grid CTAs / CTAs per K range / tile width)")
+        print(f"{'N':>6} {'prec':>4} " + " ".join(f"{name:>26}" for name, _ in LAUNCH_SETTINGS))
         for n in [int(x) for x in a.sizes.split(",")]:
             ops = operands(n)
             calls = a.calls or max(20, min(200, int(2e11 / (2.0 * n ** 3))))
@@ -175,13 +180,14 @@ def main():
                     for k, v in kv.items():
                         ptc.ptc_set_tuning(k, v)
                     us = graph_median_us(call(prec, ops, n), calls)
-                    grid, _, ks = ptc.ptc_last_launch()
-                    row[name] = {"us": us, "grid": grid, "ksplit": ks}
+                    grid, _, ks, bn = ptc.ptc_last_launch()
+                    row[name] = {"us": us, "grid": grid, "ksplit": ks, "tile_n": bn}
                 for k, v in DEFAULTS.items():
                     ptc.ptc_set_tuning(k, v)
                 results[str(n)][prec] = row
                 print(f"{n:>6} {prec:>4} " + " ".join(
-                    f"{r['us']:>29.2f} us ({r['grid']:>3}/{r['ksplit']})" for r in row.values()), flush=True)
+                    f"{r['us']:>10.2f} ({r['grid']:>3}/{r['ksplit']}/{r['tile_n']:>3})" for r in row.values()),
+                    flush=True)
     elif a.mode == "cublas":
         import statistics
         n = a.n

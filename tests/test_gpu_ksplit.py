@@ -83,9 +83,9 @@ def _check_launch(ks, M, N, num_kb):
     """The recorded launch is a K-split cluster launch when it must be: a
     forced KS with at most 8 tiles (clusters of 8 then always fit one wave)
     and at least KS K blocks; by size, only when each CTA sheds 8 or more K
-    blocks, and always with clusters of 8 for at most 8 tiles of 16+ blocks."""
-    grid, cluster, used = ptc.ptc_last_launch()
-    assert used in (1, 2, 4, 8) and grid > 0
+    blocks."""
+    grid, cluster, used, tile_n = ptc.ptc_last_launch()
+    assert used in (1, 2, 4, 8) and grid > 0 and tile_n in (64, 128, 256)
     tiles = _tiles(M, N)
     if ks == 1:
         assert used == 1
@@ -93,11 +93,8 @@ def _check_launch(ks, M, N, num_kb):
         assert used in (1, ks)
         if tiles <= 8 and num_kb >= ks:
             assert used == ks
-    else:
-        if used > 1:
-            assert num_kb - (num_kb + used - 1) // used >= 8
-        if tiles <= 8 and num_kb >= 16:
-            assert used == 8
+    elif used > 1:
+        assert num_kb - (num_kb + used - 1) // used >= 8
     if used > 1:
         assert num_kb >= used and cluster == used and grid == used * tiles
 
@@ -223,7 +220,7 @@ def test_ksplit_noalloc():
     Cd = torch.empty((M, (N + 3) // 4 * 4), dtype=torch.int32, device=DEV)
     ptc.gemm_s8_noalloc(M, N, K, Ad.data_ptr(), Ad.stride(0), Bd.data_ptr(), Bd.stride(0), Cd.data_ptr(),
                         Cd.shape[1], torch.cuda.current_stream().cuda_stream)
-    grid, cluster, used = ptc.ptc_last_launch()
+    grid, cluster, used, _ = ptc.ptc_last_launch()
     assert used > 1 and grid == used * _tiles(M, N)
     torch.cuda.synchronize()
     assert np.array_equal(Cd.cpu().numpy()[:, :N], oracle.wrap_s32(oracle.gemm_s8(A, Bt)))
