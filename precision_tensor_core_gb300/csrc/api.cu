@@ -196,19 +196,20 @@ struct Shape {
 };
 
 // Estimated SM clocks of one CTA's work in a single-wave launch, the quantity
-// the automatic shape choice minimises.  Per 128-byte K block: the larger of
-// the MMAs (2 * bn clocks for 128 rows; the E4M3 kind does twice the values
-// per block at twice the rate) and the operand copies (16 KiB of A plus bn
-// rows of B at ~128 bytes per clock); then the C tile leaving the SM at ~32
-// bytes per clock (the per-SM write path to L2, measured with ncu), which is
-// what makes 256-wide tiles slow when few SMs share a small product; a
-// K-split cluster also writes its partial sums to shared memory (~128 bytes
-// per clock) and passes two cluster barriers (~2000 clocks, measured).
+// the automatic shape choice minimises (constants measured on GB300 with
+// global-timer stamps per CTA).  Per 128-byte K block: issuing its MMAs
+// (~512 clocks for 128 rows whatever the tile width: four K-steps of ~128) or
+// copying its operands (16 KiB of A plus bn rows of B at ~128 bytes per
+// clock), whichever is longer; then the C tile leaving the SM (measured ~21
+// bytes per clock end to end; the per-SM write path to L2 peaks at ~32),
+// which is what makes 256-wide tiles slow when few SMs share a small
+// product.  A K-split cluster instead writes its partial sums to shared
+// memory, passes two cluster barriers and moves the partials and C between
+// SMs: ~45 clocks per tile column.
 int64_t est_clocks(int64_t num_kb, int bn, int ks, int esize) {
-    const int64_t per_block = std::max<int64_t>(2 * bn, 128 + bn);
-    int64_t c = (num_kb + ks - 1) / ks * per_block + int64_t(4) * bn * esize;
-    if (ks > 1) c += int64_t(4) * bn + 2000;
-    return c;
+    const int64_t per_block = std::max<int64_t>(512, 128 + bn);
+    const int64_t k_loop = (num_kb + ks - 1) / ks * per_block;
+    return k_loop + (ks > 1 ? int64_t(45) * bn : int64_t(6) * bn * esize);
 }
 
 int64_t tile_count(int64_t M, int64_t N, int rows, int cols) {

@@ -173,3 +173,12 @@ def test_auto_shapes_of_the_study_sizes():
     torch.cuda.synchronize()
     assert shapes[512][3] == 64 and shapes[1024][3] == 64 and shapes[1536][3] == 128
     assert shapes[2048][1] == 2 and shapes[4096][1] == 2
+    # long K over few tiles: K-split clusters of 8 (16 or 32 K blocks per CTA
+    # against 256 or 32 on a narrow tile)
+    for (M, N, K) in ((512, 512, 16384), (128, 2048, 2048)):
+        A = torch.zeros((M, K), dtype=torch.float16, device=DEV)
+        B = torch.zeros((K, N), dtype=torch.float16, device=DEV)
+        ptc.matmul_f16(A, B)
+        grid, cluster, ks, bn = ptc.ptc_last_launch()
+        assert ks == 8 and bn == 256 and cluster == 8, (M, N, K, grid, cluster, ks, bn)
+    torch.cuda.synchronize()
