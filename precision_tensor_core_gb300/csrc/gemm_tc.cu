@@ -9,8 +9,8 @@
 //               and B into a STAGES-deep shared-memory ring (128-byte swizzle),
 //               completing on per-stage "full" mbarriers (replaces cp.async +
 //               commit_group / wait_group + __syncthreads buffer rotation).
-//   warp 1      allocates all 512 tensor-memory columns, then one thread
-//               issues tcgen05.mma (N = 256, K = 32 bytes per instruction)
+//   warp 1      allocates 2 x BN tensor-memory columns, then one thread
+//               issues tcgen05.mma (N = BN, K = 32 bytes per instruction)
 //               into a double-buffered tensor-memory accumulator and frees
 //               ring stages with tcgen05.commit -> "empty" barriers (replaces
 //               ldmatrix + mma.sync and register accumulators).
@@ -21,9 +21,13 @@
 //               where nothing hides the epilogue (4-byte C of a single-wave
 //               launch, and the last tile of each cluster in FP32 C).
 //
-// Two shapes of the same kernel:
-//   CTAS = 1    one CTA per 128 x 256 output tile (M = 128 MMAs), 4 stages of
-//               one K block.
+// Shapes of the same kernel:
+//   CTAS = 1    one CTA per 128 x BN output tile (M = 128 MMAs): BN = 256 with
+//               4 ring stages of one K block, or, for products too small to
+//               occupy the SMs with 256-wide tiles, BN = 128 / 64 (6 / 8
+//               stages), which spreads C over more SMs (each SM writes to L2
+//               at ~32 bytes per clock, so a 128 x 256 FP32 tile takes ~2 us
+//               to leave its SM).
 //   CTAS = 2    a cluster of two CTAs per 256 x 256 output tile
 //               (tcgen05 cta_group::2, M = 256 MMAs issued by the even CTA):
 //               each CTA stages its own 128 rows of A and half of B, so a CTA

@@ -80,9 +80,12 @@ enum Epi : int {
 // args.tiles_m counts tiles of kBM * ctas rows, args.tiles_n tiles of args.bn
 // columns (kBN for CTA pairs).  The tensor map of A has boxes of kBM rows;
 // that of B boxes of bn / ctas rows (K-major) or 64 x 64 (MN-major).
-// With a non-null pool (and args.split_ok) a short last wave is split in K,
-// using a workspace of at most ~20 MB taken from the pool on `stream` and
-// returned after the kernel; a null pool runs every tile whole.
+// With a non-null pool (and args.split_ok) a short last wave of 256-wide tiles
+// is split in K, using a workspace of at most ~20 MB taken from the pool on
+// `stream` and returned after the kernel; a null pool runs every tile whole.
+// One-CTA 256-wide launches run as K-split clusters when pick_ksplit(...,
+// args.ksplit, ...) returns more than 1 (no workspace).  args.pdl launches
+// with programmatic stream serialization.
 cudaError_t launch_gemm(Kind kind, bool b_mn_major, int epi, int ctas, const CUtensorMap &ta,
                         const CUtensorMap &tb, const GemmArgs &args, int sms, cudaMemPool_t pool,
                         cudaStream_t stream);
