@@ -353,9 +353,10 @@ int ptc_last_launch(int *grid, int *cluster, int *ksplit, int *tile_n);
  *                  (default: 3 stages of 64 KiB per CTA) or 1 (7 stages of
  *                  32 KiB).  Results do not depend on the choice.
  *   "split_min_kb" K blocks (64 values FP16 / INT8, 128 INT4) below which no
- *                  tile is split, default 64 (the split saves about half a
- *                  tile's K loop and costs a few microseconds per call);
- *                  2 or more.
+ *                  tile is split, default 128 (the split saves about half a
+ *                  tile's K loop and its exchange costs ~10 us per call:
+ *                  measured faster for 128 K blocks, slower for 64); 2 or
+ *                  more.
  *   "ksplit"       small problems: when 128 x 256 one-CTA tiles would fill at
  *                  most half of the SMs in one wave, each tile runs on a
  *                  thread-block cluster of KS CTAs that share its K blocks

@@ -41,7 +41,7 @@ std::atomic<int> g_group_m{8};
 std::atomic<int> g_l2_hint{0};
 std::atomic<int> g_cta_pair{0};     // 0: by problem size, 1: one CTA per tile, 2: CTA pairs
 std::atomic<int> g_tail_split{1};   // 1: split a short last wave in K
-std::atomic<int> g_split_min_kb{64};
+std::atomic<int> g_split_min_kb{128};
 std::atomic<int> g_pair_stage_kb{2};  // CTA pairs: K blocks per ring stage
 std::atomic<int> g_ksplit{0};         // K-split clusters: 0 by size, 1 never, 2 / 4 / 8 that size
 std::atomic<int> g_tile_n{0};         // one-CTA tile width: 0 by size, 64 / 128 / 256 that width

@@ -1159,9 +1159,11 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
     a.split_count = nullptr;
     a.split_part = nullptr;
     void *ws = nullptr;
-    // The split saves about half of a tile's K loop (~0.14 us per K block);
-    // setting up the exchange costs ~6 us per call, so short K (below
-    // split_min_kb blocks, 64 by default) runs whole.
+    // The split saves about half of a tile's K loop (~0.35 us per K block
+    // under the power cap); the exchange of partial sums through L2 costs
+    // ~8-12 us after the last MMA (128 KiB out of each SM at its write rate),
+    // so tiles of fewer than split_min_kb K blocks (128 by default) run whole:
+    // at 64 K blocks the split measured 7% slower for FP16 (N = 4096).
     if (KS == 1 && BN == kBN && pool != nullptr && a.split_ok && a.num_kb > SUBK && a.num_kb >= a.split_min_kb &&
         tail > 0 && 2 * tail <= maxc) {
         const size_t slices = size_t(tail) * CTAS * EPI_WARPS;

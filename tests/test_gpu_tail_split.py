@@ -40,7 +40,7 @@ def built():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
     torch.cuda.set_device(DEV)
     yield
-    ptc.ptc_set_tuning("split_min_kb", 64)
+    ptc.ptc_set_tuning("split_min_kb", 128)
     ptc.ptc_set_tuning("tail_split", 1)
     ptc.ptc_set_tuning("cta_pair", 0)
     assert ptc.gemm_poll_device_error() == ptc.PTC_OK
@@ -58,7 +58,7 @@ def mode(request):
     ptc.ptc_set_tuning("ksplit", 1)  # the lone partial wave would otherwise run as K-split clusters
     yield request.param
     ptc.ptc_set_tuning("ksplit", 0)
-    ptc.ptc_set_tuning("split_min_kb", 64)
+    ptc.ptc_set_tuning("split_min_kb", 128)
     ptc.ptc_set_tuning("tail_split", 1)
     ptc.ptc_set_tuning("cta_pair", 0)
 
@@ -126,9 +126,9 @@ def test_tail_f16acc_permutation(mode):
 
 def test_tail_int_identical_with_and_without_split():
     """Integer sums do not depend on the split, at the default threshold
-    (K = 4160 is 65 K blocks; the INT8 route folds its FP32 partial sums every
+    (K = 8256 is 129 K blocks; the INT8 route folds its FP32 partial sums every
     1024 values, so each half spans several folds)."""
-    M, N, K = 2560, 1848, 4160
+    M, N, K = 2560, 1848, 8256
     A, Bt = datagen.s8_operands(N, seed=21, m=M, k=K)
     Ad, Bd = int_dev(A), int_dev(Bt)
     out = []
