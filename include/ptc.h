@@ -349,14 +349,23 @@ int ptc_last_launch(int *grid, int *cluster, int *ksplit, int *tile_n);
  *                  library pool.  0: never.  Integer results do not depend on
  *                  the choice; FP16 results of split tiles differ by the
  *                  summation order (the sum of two FP32 half sums).
+ *   "split_reduce" 1 (default): a split tile of FP32 or int32 C is zeroed
+ *                  by its first half's CTAs when the kernel starts and both
+ *                  halves add their partial sums into it by TMA reductions
+ *                  (in FP32, 0 + a + b: the same bits in either order); only
+ *                  a flag per epilogue warp slice is kept in the workspace.
+ *                  0: the halves exchange partial sums through the
+ *                  workspace and one of them writes C (always the case for
+ *                  FP16 C and the scaled outputs).
  *   "pair_stage_kb" CTA pairs: K blocks per shared-memory ring stage, 2
  *                  (default: 3 stages of 64 KiB per CTA) or 1 (7 stages of
  *                  32 KiB).  Results do not depend on the choice.
  *   "split_min_kb" K blocks (64 values FP16 / INT8, 128 INT4) below which no
- *                  tile is split, default 128 (the split saves about half a
- *                  tile's K loop and its exchange costs ~10 us per call:
- *                  measured faster for 128 K blocks, slower for 64); 2 or
- *                  more.
+ *                  tile is split, default 64; doubled for INT4 and for
+ *                  tiles whose halves exchange partial sums (split_reduce 0,
+ *                  FP16 C, scaled outputs), as measured: the split saves
+ *                  about half a tile's K loop and costs ~4 us per call with
+ *                  TMA reductions, ~10 us with the exchange; 2 or more.
  *   "ksplit"       small problems: when 128 x 256 one-CTA tiles would fill at
  *                  most half of the SMs in one wave, each tile runs on a
  *                  thread-block cluster of KS CTAs that share its K blocks

@@ -41,10 +41,11 @@ std::atomic<int> g_group_m{8};
 std::atomic<int> g_l2_hint{0};
 std::atomic<int> g_cta_pair{0};     // 0: by problem size, 1: one CTA per tile, 2: CTA pairs
 std::atomic<int> g_tail_split{1};   // 1: split a short last wave in K
-std::atomic<int> g_split_min_kb{128};
+std::atomic<int> g_split_min_kb{64};
 std::atomic<int> g_pair_stage_kb{2};  // CTA pairs: K blocks per ring stage
 std::atomic<int> g_ksplit{0};         // K-split clusters: 0 by size, 1 never, 2 / 4 / 8 that size
-std::atomic<int> g_tile_n{0};         // one-CTA tile width: 0 by size, 64 / 128 / 256 that width
+std::atomic<int> g_tile_n{0};
+std::atomic<int> g_split_reduce{1};   // split tiles of FP32 / int32 C: halves added by TMA reductions         // one-CTA tile width: 0 by size, 64 / 128 / 256 that width
 std::atomic<int> g_pdl{1};            // programmatic stream serialization of the library's kernels
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 std::atomic<int64_t> g_stall_tile{-1};
@@ -278,6 +279,7 @@ GemmArgs base_args(int64_t M, int64_t N, int64_t K, int k_elems_per_block, void 
     a.split_min_kb = g_split_min_kb.load();
     a.stage_kb = g_pair_stage_kb.load();
     a.ksplit = sh.ks;
+    a.split_reduce = g_split_reduce.load();
     a.pdl = g_pdl.load();
     a.wait_limit_ns = g_wait_ns.load();
     return a;
@@ -306,8 +308,10 @@ int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 namespace ptc {
 void note_launches(uint64_t n) { g_launches.fetch_add(n); }
 void set_message(const char *text) { std::snprintf(g_msg, sizeof(g_msg), "%s", text); }
-int encode_tmap_c32(CUtensorMap *map, const void *C, uint64_t n, uint64_t m, uint64_t ldc) {
-    return make_tmap(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, C, n, m, ldc * 4, 32, 32);
+int encode_tmap_c32(CUtensorMap *map, const void *C, uint64_t n, uint64_t m, uint64_t ldc, bool fp32) {
+    // The element type matters to TMA reductions only (stores copy bits).
+    return make_tmap(map, fp32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_INT32, C, n, m, ldc * 4,
+                     32, 32);
 }
 int encode_tmap_2d(CUtensorMap *map, bool one_byte, const void *base, uint64_t inner, uint64_t outer,
                    uint64_t pitch, uint32_t box_inner, uint32_t box_outer) {
@@ -919,6 +923,10 @@ int ptc_set_tuning(const char *key, int64_t value) {
     }
     if (std::strcmp(key, "ksplit") == 0 && (value == 0 || value == 1 || value == 2 || value == 4 || value == 8)) {
         g_ksplit.store(int(value));
+        return PTC_OK;
+    }
+    if (std::strcmp(key, "split_reduce") == 0 && (value == 0 || value == 1)) {
+        g_split_reduce.store(int(value));
         return PTC_OK;
     }
     if (std::strcmp(key, "tile_n") == 0 && (value == 0 || value == 64 || value == 128 || value == 256)) {

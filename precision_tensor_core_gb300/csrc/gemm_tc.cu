@@ -233,6 +233,36 @@ __device__ __forceinline__ bool split_publish(uint32_t *cnt, int lane) {
     return old != 0;
 }
 
+__device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Split tiles added into C by TMA reductions: the first half's cluster zeroes
+// the tile's C at its start and sets one flag per epilogue warp slice.  Before
+// its reductions a warp waits (bounded; the zeroing happened long before in
+// practice) until its slice's flag is set, then fences so that its TMA
+// reductions come after the zeros.  False on timeout or abort.
+__device__ __forceinline__ bool split_zeroed_wait(const uint32_t *flag, AbortState *ab, uint64_t limit, int lane) {
+    uint32_t ok = 1;
+    if (lane == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_gpu(flag) == 0) {
+            if (ab->flag) {
+                ok = 0;
+                break;
+            }
+            if (globaltimer_ns() - t0 > limit) {
+                ab->flag = 1;
+                atomicCAS(&g_error_word, 0u, kErrTimeout);
+                ok = 0;
+                break;
+            }
+        }
+        if (ok) fence_proxy_async_global();
+    }
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 // Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, AbortState *ab,
                                           uint64_t limit, int lane) {
@@ -303,12 +333,22 @@ __device__ __forceinline__ void stage_end(const CUtensorMap *tmC, uint32_t stg, 
     }
 }
 
+// `add`: the block is added into C (FP32 or int32, by the tensor map's type)
+// by a TMA reduction instead of stored.
 __device__ __forceinline__ void tma_store_block(const CUtensorMap *tmC, uint32_t stg, const uint32_t (&v)[32],
-                                                int lane, int col, int row0, bool wait) {
+                                                int lane, int col, int row0, bool wait, bool add = false) {
     stage_begin(lane, wait);
 #pragma unroll
     for (int j = 0; j < 8; ++j) stage_put(stg, lane, j, v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-    stage_end(tmC, stg, lane, col, row0);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        if (add)
+            tma_reduce_add_2d(tmC, stg, col, row0);
+        else
+            tma_store_2d(tmC, stg, col, row0);
+        bulk_commit_group();
+    }
 }
 
 // Scaled integer epilogue (dequantisation): for the HALF columns col0 .. of
@@ -858,6 +898,31 @@ __global__ void __launch_bounds__(THREADS, 1)
         int abuf = 0;
         uint32_t aph = 0;
         bool ok = true;
+        if (CTAS == 2 && args.split_reduce && cluster < args.num_vunits) {
+            // This cluster's last unit is the first K half of a split tile: zero
+            // the tile's C (each warp its 32 x 128 slice) before the K loops run,
+            // for both halves to add into.
+            const int last = cluster + (args.num_vunits - 1 - cluster) / nclusters * nclusters;
+            const WorkRef lw = work_unit(last, args, C_::SUB);
+            if (lw.part == 1) {
+                const int zrow = lw.mb * (kBM * CTAS) + int(rank) * kBM + 32 * q + lane;
+                const int zcol = lw.nb * BN + h * HALF;
+                if (zrow < args.M) {
+                    uint32_t z[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) z[j] = 0u;
+                    uint32_t *crow = reinterpret_cast<uint32_t *>(args.C) + int64_t(zrow) * args.ldc;
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) {
+                        const int cc = zcol + 32 * c;
+                        if (cc < args.N) store_32(crow + cc, z, args.N - cc, args.c_wide);
+                    }
+                }
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) st_release_gpu(args.split_count + ((lw.slot * CTAS + int(rank)) * 4 + q) * 2 + h, 1u);
+            }
+        }
         for (int t = cluster; t < args.num_vunits && ok; t += nclusters) {
             WorkRef wr = work_unit(t, args, C_::SUB);
             if constexpr (KS > 1) ksplit_range(wr, krank, KS);
@@ -898,7 +963,16 @@ __global__ void __launch_bounds__(THREADS, 1)
                                     reinterpret_cast<const uint32_t(&)[32]>(acc[32 * c]));
                     continue;
                 }
-                if (BN == kBN && wr.part != 0) {
+                // A split tile of int32 C: both K halves add into the zeroed C
+                // by int32 TMA reductions (modulo 2^32, like every partial sum).
+                const bool add = CTAS == 2 && wr.part != 0 && args.split_reduce;
+                if (add) {
+                    const int slice = ((wr.slot * CTAS + int(rank)) * 4 + q) * 2 + h;
+                    if (!split_zeroed_wait(args.split_count + slice, &st->abort, limit, lane)) {
+                        ok = false;
+                        break;
+                    }
+                } else if (BN == kBN && wr.part != 0) {
                     // Sum of the two K halves, wrapping like every int32 partial sum.
                     const int slice = ((wr.slot * CTAS + int(rank)) * 4 + q) * 2 + h;
                     uint32_t *cnt = args.split_count + slice;
@@ -926,7 +1000,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 // Integer routes: TMA stores in single-wave launches (every unit
                 // is its cluster's last); a per-unit choice, as the FP32 path
                 // makes, costs this register-bound epilogue spills.
-                const bool use_tma = args.c_tma && args.num_vunits <= nclusters;
+                const bool use_tma = add || (args.c_tma && args.num_vunits <= nclusters);
                 if (args.out_mode == OUT_S32 && use_tma) {
 #pragma unroll
                     for (int c = 0; c < NCH; ++c) {
@@ -934,7 +1008,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         if (cc < args.N)
                             tma_store_block(&tmC, stg + uint32_t(c * kStageC),
                                             reinterpret_cast<const uint32_t(&)[32]>(acc[32 * c]), lane, cc, row0,
-                                            stg_pending && c == 0);
+                                            stg_pending && c == 0, add);
                     }
                     stg_pending = true;
                 } else if (args.out_mode == OUT_S32) {
@@ -979,18 +1053,28 @@ __global__ void __launch_bounds__(THREADS, 1)
                         put_partial(smem_u32(smem), 32 * q + lane, h * (HALF / 4) + 8 * c, r);
                     }
                 } else {
-                    if (wr.part == 0 && EPI == EPI_F32 && use_tma) {
+                    // A split tile of FP32 C: both K halves add into the zeroed C
+                    // by FP32 TMA reductions (0 + a + b: the same bits in either
+                    // order).
+                    const bool add = CTAS == 2 && EPI == EPI_F32 && wr.part != 0 && args.split_reduce;
+                    if (add) {
+                        const int slice = ((wr.slot * CTAS + int(rank)) * 4 + q) * 2 + h;
+                        ok = split_zeroed_wait(args.split_count + slice, &st->abort, limit, lane);
+                    }
+                    if (EPI == EPI_F32 && ((wr.part == 0 && use_tma) || add)) {
+                        if (ok) {
 #pragma unroll
-                        for (int c = 0; c < NCH; ++c) {
-                            uint32_t r[32];
-                            tmem_ld_32cols(t_lane + uint32_t(abuf * BN + 32 * c), r);
-                            tmem_ld_wait();
-                            const int cc = col0 + 32 * c;
-                            if (cc < args.N)
-                                tma_store_block(&tmC, stg + uint32_t(c * kStageC), r, lane, cc, row - lane,
-                                                stg_pending && c == 0);
+                            for (int c = 0; c < NCH; ++c) {
+                                uint32_t r[32];
+                                tmem_ld_32cols(t_lane + uint32_t(abuf * BN + 32 * c), r);
+                                tmem_ld_wait();
+                                const int cc = col0 + 32 * c;
+                                if (cc < args.N)
+                                    tma_store_block(&tmC, stg + uint32_t(c * kStageC), r, lane, cc, row - lane,
+                                                    stg_pending && c == 0, add);
+                            }
+                            stg_pending = true;
                         }
-                        stg_pending = true;
                     } else if (wr.part == 0) {
                         float *crow = reinterpret_cast<float *>(args.C) + int64_t(row) * args.ldc;
 #pragma unroll
@@ -1154,21 +1238,35 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
     std::memset(&tc, 0, sizeof(tc));
     a.c_tma = 0;
     const bool tma_c = esize == 4;
+    const bool int_c = EPI == EPI_INT && a.out_mode == OUT_S32;
+    // (A K-split cluster writes C from its completion pass, without TMA.)
+    if (KS == 1 && tma_c && encode_tmap_c32(&tc, a.C, uint64_t(a.N), uint64_t(a.M), uint64_t(a.ldc), !int_c) == 0)
+        a.c_tma = 1;
+    // Split pair tiles of FP32 or int32 C add their halves into C by TMA
+    // reductions (one-CTA tiles, split only when forced, exchange partials).
+    const bool reduce = CTAS == 2 && a.split_reduce && a.c_tma && (EPI == EPI_F32 || int_c);
+    a.split_reduce = 0;
     const int tail = a.num_tiles < maxc ? a.num_tiles : a.num_tiles % maxc;
     a.tail_split = 0;
     a.split_count = nullptr;
     a.split_part = nullptr;
     void *ws = nullptr;
     // The split saves about half of a tile's K loop (~0.35 us per K block
-    // under the power cap); the exchange of partial sums through L2 costs
-    // ~8-12 us after the last MMA (128 KiB out of each SM at its write rate),
-    // so tiles of fewer than split_min_kb K blocks (128 by default) run whole:
-    // at 64 K blocks the split measured 7% slower for FP16 (N = 4096).
-    if (KS == 1 && BN == kBN && pool != nullptr && a.split_ok && a.num_kb > SUBK && a.num_kb >= a.split_min_kb &&
+    // under the power cap).  Adding the halves into C by TMA reductions costs
+    // ~4 us after the last MMA; exchanging partial sums through the workspace
+    // ~8-12 us (128 KiB in and out of each SM at its L2 write rate).  Measured
+    // (interleaved A/B): with reductions the split gains from 64 K blocks for
+    // the FP16 kind (FP16, INT8: N = 4096 -1% / -3.5%, N = 8192 -1.5% /
+    // -2.2%) but loses at 64 blocks of the E4M3 kind (INT4, N = 8192: +1.2%);
+    // with the exchange it loses at 64 blocks (FP16 N = 4096: +7%).  So the
+    // threshold is split_min_kb K blocks (64 by default) with reductions on
+    // the FP16 kind, twice that on the E4M3 kind or with the exchange.
+    const int min_kb = a.split_min_kb * (reduce ? 1 : 2) * (KIND == Kind::E4M3 ? 2 : 1);
+    if (KS == 1 && BN == kBN && pool != nullptr && a.split_ok && a.num_kb > SUBK && a.num_kb >= min_kb &&
         tail > 0 && 2 * tail <= maxc) {
         const size_t slices = size_t(tail) * CTAS * EPI_WARPS;
         const size_t count_bytes = (slices * sizeof(uint32_t) + 255) / 256 * 256;
-        const size_t bytes = count_bytes + slices * 2 * kSliceWords * sizeof(float);
+        const size_t bytes = count_bytes + (reduce ? 0 : slices * 2 * kSliceWords * sizeof(float));
         if (cudaMallocFromPoolAsync(&ws, bytes, pool, stream) == cudaSuccess) {
             e = cudaMemsetAsync(ws, 0, count_bytes, stream);
             if (e != cudaSuccess) {
@@ -1176,8 +1274,9 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
                 return e;
             }
             a.tail_split = tail;
+            a.split_reduce = reduce ? 1 : 0;
             a.split_count = static_cast<uint32_t *>(ws);
-            a.split_part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + count_bytes);
+            a.split_part = reduce ? nullptr : reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + count_bytes);
         } else {
             cudaGetLastError();  // no workspace: run the tail whole
             ws = nullptr;
@@ -1185,12 +1284,10 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
     }
     a.num_vunits = a.num_tiles + a.tail_split;
     const int clusters = a.num_vunits < maxc ? a.num_vunits : maxc;
-    // Each cluster's last unit writes 4-byte C by TMA stores staged in the idle
-    // ring (its epilogue is exposed); earlier units use 32-byte stores, which
-    // leave the TMA engine to the operand loads while the next tile runs.
-    // (A K-split cluster writes C from its completion pass, without TMA.)
-    if (KS == 1 && tma_c && encode_tmap_c32(&tc, a.C, uint64_t(a.N), uint64_t(a.M), uint64_t(a.ldc)) == 0)
-        a.c_tma = 1;
+    // Each cluster's last unit writes 4-byte C by TMA stores (or reductions)
+    // staged in the idle ring (its epilogue is exposed); earlier units use
+    // 32-byte stores, which leave the TMA engine to the operand loads while the
+    // next tile runs.
     cfg.gridDim = dim3(CTAS * KS * clusters, 1, 1);
     e = cudaLaunchKernelEx(&cfg, fn, ta, tb, tc, a);
     if (e == cudaSuccess) {

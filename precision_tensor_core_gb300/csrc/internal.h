@@ -49,6 +49,10 @@ struct GemmArgs {
     int split_min_kb;      // ... when K spans at least this many K blocks
     int tail_split;
     int num_vunits;
+    int split_reduce;      // 1: both halves of a split tile add their partial sums into C by TMA
+                           // reductions (FP32 C, int32 C); the first half's cluster zeroes the
+                           // tile's C at its start and sets split_count[slice] (one flag per
+                           // epilogue warp slice); no partial-sum workspace
     uint32_t *split_count;
     float *split_part;
     // Integer routes only: output of the epilogue.
@@ -147,7 +151,7 @@ void set_message(const char *text);
 // one_byte), 128-byte swizzle, zero fill outside; returns a PTC_* status.
 // C as 4-byte elements: N x M (ldc elements between rows), boxes of 32 x 32
 // with the 128-byte swizzle, for the epilogue's TMA stores.
-int encode_tmap_c32(CUtensorMap *map, const void *C, uint64_t n, uint64_t m, uint64_t ldc);
+int encode_tmap_c32(CUtensorMap *map, const void *C, uint64_t n, uint64_t m, uint64_t ldc, bool fp32);
 int encode_tmap_2d(CUtensorMap *map, bool one_byte, const void *base, uint64_t inner, uint64_t outer,
                    uint64_t pitch, uint32_t box_inner, uint32_t box_outer);
 

@@ -129,6 +129,23 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t sm
                  : "memory");
 }
 
+// TMA reduction of a 2-D box from shared memory into global memory: each
+// element of the box is added (in the tensor map's element type: FP32 with
+// round-to-nearest-even, or 32-bit integers modulo 2^32) to the global
+// element at (x + i, y + j); elements outside the tensor are skipped.
+__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *map, uint32_t smem_src, int32_t x, int32_t y) {
+    asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_src), "r"(x), "r"(y)
+                 : "memory");
+}
+
+// Orders this thread's view of global memory written through the generic
+// proxy (ordinary stores, here made visible to it by an acquire) before its
+// later asynchronous-proxy (TMA) accesses of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // Wait until the source shared memory of every committed bulk store has been read.

@@ -136,9 +136,9 @@ def test_status_strings_and_tuning(L):
         ptc.ptc_set_tuning("s8_chunk_kb", 0)
     assert ptc.ptc_set_tuning("group_m", 16) == 0
     assert ptc.ptc_set_tuning("group_m", 8) == 0
-    for key, bad, good in (("split_min_kb", 1, 128), ("tail_split", 2, 1), ("cta_pair", 3, 0),
+    for key, bad, good in (("split_min_kb", 1, 64), ("tail_split", 2, 1), ("cta_pair", 3, 0),
                            ("s8_chunk_kb", 3, 16), ("s4_chunk_kb", 7, 64), ("pair_stage_kb", 3, 2),
-                           ("ksplit", 3, 0), ("ksplit", 16, 0), ("pdl", 2, 1), ("tile_n", 32, 0),
+                           ("ksplit", 3, 0), ("ksplit", 16, 0), ("pdl", 2, 1), ("split_reduce", 2, 1), ("tile_n", 32, 0),
                            ("tile_n", 192, 0)):
         with pytest.raises(ptc.PtcError):
             ptc.ptc_set_tuning(key, bad)

@@ -40,25 +40,29 @@ def built():
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
     torch.cuda.set_device(DEV)
     yield
-    ptc.ptc_set_tuning("split_min_kb", 128)
+    ptc.ptc_set_tuning("split_min_kb", 64)
     ptc.ptc_set_tuning("tail_split", 1)
     ptc.ptc_set_tuning("cta_pair", 0)
     assert ptc.gemm_poll_device_error() == ptc.PTC_OK
 
 
-@pytest.fixture(params=[(1, 1), (1, 0), (2, 1), (2, 0)], ids=["cta1-split", "cta1-nosplit", "cta2-split",
-                                                             "cta2-nosplit"])
+@pytest.fixture(params=[(1, 1, 1), (1, 0, 1), (2, 1, 1), (2, 1, 0), (2, 0, 1)],
+                ids=["cta1-split", "cta1-nosplit", "cta2-split-reduce", "cta2-split-exchange", "cta2-nosplit"])
 def mode(request):
-    """Launch mode and split setting; the split threshold is lowered to two K
-    blocks so that the oracle-sized shapes below are split."""
-    ctas, split = request.param
+    """Launch mode and split setting (CTA pairs add the halves of FP32 / int32
+    tiles into C by TMA reductions, or exchange partial sums through the
+    workspace); the split threshold is lowered to two K blocks so that the
+    oracle-sized shapes below are split."""
+    ctas, split, reduce = request.param
     ptc.ptc_set_tuning("cta_pair", ctas)
     ptc.ptc_set_tuning("tail_split", split)
+    ptc.ptc_set_tuning("split_reduce", reduce)
     ptc.ptc_set_tuning("split_min_kb", 2)
     ptc.ptc_set_tuning("ksplit", 1)  # the lone partial wave would otherwise run as K-split clusters
     yield request.param
+    ptc.ptc_set_tuning("split_reduce", 1)
     ptc.ptc_set_tuning("ksplit", 0)
-    ptc.ptc_set_tuning("split_min_kb", 128)
+    ptc.ptc_set_tuning("split_min_kb", 64)
     ptc.ptc_set_tuning("tail_split", 1)
     ptc.ptc_set_tuning("cta_pair", 0)
 
@@ -66,9 +70,14 @@ def mode(request):
 @pytest.mark.parametrize("M,N,K", SHAPES)
 def test_tail_f16(M, N, K, mode):
     A, B = datagen.f16_operands(N, "normal", seed=M + N + K, m=M, k=K)
-    C = ptc.matmul_f16(f16_dev(A), f16_dev(B))
+    Ad, Bd = f16_dev(A), f16_dev(B)
+    C = ptc.matmul_f16(Ad, Bd)
     torch.cuda.synchronize()
     check_f16(C.cpu().numpy(), A, B)
+    # the split halves may add in either order: the same bits every run
+    C2 = ptc.matmul_f16(Ad, Bd)
+    torch.cuda.synchronize()
+    assert torch.equal(C.view(torch.int32), C2.view(torch.int32))
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
