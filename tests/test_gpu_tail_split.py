@@ -150,3 +150,20 @@ def test_tail_int_identical_with_and_without_split():
     ii = np.random.default_rng(22).integers(0, M, 3000)
     jj = np.random.default_rng(23).integers(0, N, 3000)
     assert np.array_equal(out[0][ii, jj], oracle.wrap_s32(oracle.gemm_s8_at(A, Bt, ii, jj)))
+
+
+def test_split_region_exact_at_default_settings():
+    """N = 4096 with the default settings: the last wave of CTA-pair tiles (the
+    bottom-right tiles of the grouped raster order) runs as K halves added
+    into C by TMA reductions.  The whole lower-right quarter of C, which holds
+    those tiles, matches the oracle: INT8 bit-exact, FP16 within the bound."""
+    N = 4096
+    A, Bt = datagen.s8_operands(N, seed=41)
+    C = ptc.matmul_s8(int_dev(A), int_dev(Bt)).cpu().numpy()
+    r, c = slice(N // 2, N), slice(N // 2, N)
+    assert np.array_equal(C[r, c], oracle.wrap_s32(oracle.gemm_s8(A[r], Bt[c])))
+    A16, B16 = datagen.f16_operands(N, "normal", seed=42)
+    C16 = ptc.matmul_f16(f16_dev(A16), f16_dev(B16)).cpu().numpy()
+    r, c = slice(N - 512, N), slice(N // 2, N)
+    check_f16(C16[r, c], np.ascontiguousarray(A16[r]), np.ascontiguousarray(B16[:, c]))
+    assert ptc.gemm_poll_device_error() == ptc.PTC_OK
