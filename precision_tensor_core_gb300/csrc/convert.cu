@@ -238,6 +238,10 @@ cudaError_t launch_convert(const uint8_t *a, int64_t lda, int rows_a, const uint
     const bool w32 = aligned32(a, lda, b, ldb);
     auto *fn = w32 ? convert_kernel<Op, true> : convert_kernel<Op, false>;
     const int tpr_log2 = threads_per_row_log2(cols, w32 ? 2 * Op::VEC : Op::VEC);
+    // No more CTAs than there are row groups to convert (small operands).
+    const int64_t rows_per_block = 256 >> tpr_log2;
+    const int64_t needed = (int64_t(rows_a) + rows_b + rows_per_block - 1) / rows_per_block;
+    if (needed < grid) grid = int(needed > 0 ? needed : 1);
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cudaLaunchAttribute attr[1];
