@@ -335,20 +335,23 @@ int ptc_last_launch(int *grid, int *cluster, int *ksplit, int *tile_n);
  *                  evict-normal (all measured slower than 0 on GB300)
  *   "cta_pair"     0 (default): clusters of two CTAs sharing 256 x 256
  *                  tiles (tcgen05 cta_group::2) once 128 x 256 one-CTA tiles
- *                  would fill the SMs, and for FP16 from 32 one-CTA tiles up;
- *                  otherwise one CTA per 128 x 256 tile; 1: always one CTA;
- *                  2: always CTA pairs.  Results do not depend on the choice
- *                  except through the FP16 summation order.
- *   "tail_split"   1 (default): when K spans at least split_min_kb K
- *                  blocks and the last wave of output tiles would occupy at
- *                  most half of the CTAs (or CTA pairs), each tile of that
- *                  wave runs as two units over the two halves of K on two
- *                  CTAs (or pairs), and the epilogue adds their partial sums,
- *                  so that the tail takes about half the time.  The exchange
- *                  uses up to ~20 MB of stream-ordered workspace from the
- *                  library pool.  0: never.  Integer results do not depend on
- *                  the choice; FP16 results of split tiles differ by the
- *                  summation order (the sum of two FP32 half sums).
+ *                  would fill the SMs, and for FP16 whole 128 x 256 tiles
+ *                  from 32 one-CTA tiles up; otherwise one CTA per tile (see
+ *                  "tile_n" and "ksplit" for the shapes of small products);
+ *                  1: always one CTA per 128 x 256 tile; 2: always CTA
+ *                  pairs.  Results do not depend on the choice except
+ *                  through the FP16 summation order.
+ *   "tail_split"   1 (default): when K spans enough K blocks (see
+ *                  "split_min_kb") and the last wave of output tiles would
+ *                  occupy at most half of the CTAs (or CTA pairs), each tile
+ *                  of that wave runs as two units over the two halves of K on
+ *                  two CTAs (or pairs), whose partial sums are added (see
+ *                  "split_reduce"), so that the tail takes about half the
+ *                  time.  The workspace (flags, or up to ~20 MB of partial
+ *                  sums) is stream-ordered from the library pool.  0: never.
+ *                  Integer results do not depend on the choice; FP16 results
+ *                  of split tiles differ by the summation order (the sum of
+ *                  two FP32 half sums).
  *   "split_reduce" 1 (default): a split tile of FP32 or int32 C is zeroed
  *                  by its first half's CTAs when the kernel starts and both
  *                  halves add their partial sums into it by TMA reductions
