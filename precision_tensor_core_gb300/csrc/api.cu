@@ -198,17 +198,19 @@ struct Shape {
 
 // Estimated SM clocks of one CTA's work in a single-wave launch, the quantity
 // the automatic shape choice minimises (constants measured on GB300 with
-// global-timer stamps per CTA).  Per 128-byte K block: issuing its MMAs
-// (~512 clocks for 128 rows whatever the tile width: four K-steps of ~128) or
-// copying its operands (16 KiB of A plus bn rows of B at ~128 bytes per
-// clock), whichever is longer; then the C tile leaving the SM (measured ~21
+// global-timer stamps per CTA, and fitted to the measured times of every
+// shape at N = 512 .. 1536).  Per 128-byte K block: issuing its MMAs (~600
+// clocks for 128 rows whatever the tile width: four K-steps, and the block's
+// barrier round trip) or copying its operands (16 KiB of A plus bn rows of B
+// at ~128 bytes per clock), whichever is longer; then the C tile leaving the
+// SM (measured ~21
 // bytes per clock end to end; the per-SM write path to L2 peaks at ~32),
 // which is what makes 256-wide tiles slow when few SMs share a small
 // product.  A K-split cluster instead writes its partial sums to shared
 // memory, passes two cluster barriers and moves the partials and C between
 // SMs: ~45 clocks per tile column.
 int64_t est_clocks(int64_t num_kb, int bn, int ks, int esize) {
-    const int64_t per_block = std::max<int64_t>(512, 128 + bn);
+    const int64_t per_block = std::max<int64_t>(600, 128 + bn);
     const int64_t k_loop = (num_kb + ks - 1) / ks * per_block;
     return k_loop + (ks > 1 ? int64_t(45) * bn : int64_t(6) * bn * esize);
 }
@@ -230,7 +232,7 @@ Shape choose_shape(int64_t M, int64_t N, int64_t num_kb, int sms, bool f16, int 
     const int fpair = g_cta_pair.load(), ftile = g_tile_n.load(), fks = g_ksplit.load();
     if (fpair == 2) return {2, ptc::kBN, 1};
     if ((ftile == 64 || ftile == 128) && tile_count(M, N, ptc::kBM, ftile) <= (int64_t(1) << 20))
-        return {1, ftile, 1};
+        return {1, ftile, (fks == 2 || fks == 4) ? fks : 1};
     if (fpair == 1) return {1, ptc::kBN, fks};
     const int64_t t256 = tile_count(M, N, ptc::kBM, ptc::kBN);
     if (t256 >= sms) return {2, ptc::kBN, 1};
@@ -244,11 +246,18 @@ Shape choose_shape(int64_t M, int64_t N, int64_t num_kb, int sms, bool f16, int 
         }
     }
     for (int bn : {128, 64}) {
-        if (ftile != 0 || tile_count(M, N, ptc::kBM, bn) > sms) continue;
-        const int64_t c = est_clocks(num_kb, bn, 1, esize);
-        if (c < best_c) {
-            best = {1, bn, 1};
-            best_c = c;
+        const int64_t tiles = tile_count(M, N, ptc::kBM, bn);
+        if (ftile != 0 || tiles > sms) continue;
+        // whole narrow tiles, or K-split clusters of 2 / 4 of them
+        for (int ks : {1, 2, 4}) {
+            if (ks > 1 && (fks == 1 || (fks != 0 && fks != ks) || num_kb < 2 * ks ||
+                           tiles > ptc::ksplit_clusters(ks, sms)))
+                continue;
+            const int64_t c = est_clocks(num_kb, bn, ks, esize);
+            if (c < best_c) {
+                best = {1, bn, ks};
+                best_c = c;
+            }
         }
     }
     if (best.bn == ptc::kBN && best.ks == 1 && f16 && t256 >= 32) return {2, ptc::kBN, 1};

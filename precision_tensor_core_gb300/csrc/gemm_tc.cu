@@ -131,11 +131,10 @@ constexpr size_t smem_bytes() {
 static_assert(smem_bytes<1, 1>() <= 232448 && smem_bytes<2, 1>() <= 232448 && smem_bytes<2, 2>() <= 232448 &&
                   smem_bytes<1, 1, 128>() <= 232448 && smem_bytes<1, 1, 64>() <= 232448,
               "shared memory budget");
-// A K-split cluster's partial sums: 128 rows of 256 four-byte values, row r
-// at r * 1024 bytes, its 16-byte piece j at piece j ^ (r & 7) (the writers,
-// one row per lane, and the readers, one piece per lane, do not conflict).
-constexpr int kPartialRow = kBN * 4;
-static_assert(Cfg<1, 1, kBN>::STAGES * Cfg<1, 1, kBN>::STAGE >= kBM * kPartialRow,
+// A K-split cluster's partial sums: 128 rows of BN four-byte values, row r at
+// r * 4 BN bytes, its 16-byte piece j at piece j ^ (r & 7) (the writers, one
+// row per lane, and the readers, one piece per lane, do not conflict).
+static_assert(Cfg<1, 1, kBN>::STAGES * Cfg<1, 1, kBN>::STAGE >= kBM * kBN * 4,
               "the ring holds a tile's partial sums");
 static_assert(Cfg<1, 1, kBN>::STAGES * Cfg<1, 1, kBN>::STAGE >= EPI_WARPS * kStageWarp &&
                   Cfg<1, 1, 128>::STAGES * Cfg<1, 1, 128>::STAGE >= EPI_WARPS * kStageWarp &&
@@ -518,9 +517,10 @@ __device__ __forceinline__ void ksplit_range(WorkRef &w, int krank, int ks) {
 }
 
 // 32 four-byte partial sums of local row `row`, columns 4 * piece0 .., into
-// the partial-sum layout at shared address `base`.
+// the partial-sum layout (rows of PROW bytes) at shared address `base`.
+template <int PROW>
 __device__ __forceinline__ void put_partial(uint32_t base, int row, int piece0, const uint32_t (&v)[32]) {
-    const uint32_t rb = base + uint32_t(row) * kPartialRow;
+    const uint32_t rb = base + uint32_t(row) * PROW;
 #pragma unroll
     for (int i = 0; i < 8; ++i)
         st_shared_v4(rb + (uint32_t((piece0 + i) ^ (row & 7)) << 4), v[4 * i], v[4 * i + 1], v[4 * i + 2],
@@ -549,80 +549,96 @@ __device__ __forceinline__ void store_4(T *dst, const T (&v)[4], int valid) {
     }
 }
 
-// Completion of a K-split tile: this CTA (`krank` of KS) owns local rows
-// krank * 128/KS .. of the tile (mb, nb); epilogue warp `ew` takes every
-// eighth of them, each lane 4 columns in each half of the row (pieces lane
-// and lane + 32).  The KS partials are added in rank order: FP32 sums with
-// round-to-nearest additions (FP16 accumulators were widened exactly to FP32
-// and the sum is rounded to binary16 once), int32 sums wrapping mod 2^32.
+// Sum of the KS partials of four consecutive outputs (row, col ..), in rank
+// order, stored to C: FP32 sums with round-to-nearest additions (FP16
+// accumulators were widened exactly to FP32 and the sum is rounded to binary16
+// once), int32 sums wrapping mod 2^32, then the output conversion.
 template <int EPI, int KS>
+__device__ __forceinline__ void ksplit_finish(const GemmArgs &args, int row, int col, const uint4 (&p)[KS]) {
+    const int valid = args.N - col;
+    if constexpr (EPI == EPI_INT) {
+        uint32_t s[4] = {p[0].x, p[0].y, p[0].z, p[0].w};
+#pragma unroll
+        for (int k = 1; k < KS; ++k) {
+            s[0] += p[k].x;
+            s[1] += p[k].y;
+            s[2] += p[k].z;
+            s[3] += p[k].w;
+        }
+        if (args.out_mode == OUT_S32) {
+            const int32_t v[4] = {int32_t(s[0]), int32_t(s[1]), int32_t(s[2]), int32_t(s[3])};
+            store_4(reinterpret_cast<int32_t *>(args.C) + int64_t(row) * args.ldc + col, v, valid);
+            return;
+        }
+        const float sa = args.scale_a ? __ldg(args.scale_a + row) : 1.0f;
+        float f[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float sb = (args.scale_b && e < valid) ? __ldg(args.scale_b + col + e) : 1.0f;
+            f[e] = __fmul_rn(__fmul_rn(__int2float_rn(int32_t(s[e])), sa), sb);
+        }
+        if (args.out_mode == OUT_F32) {
+            store_4(reinterpret_cast<float *>(args.C) + int64_t(row) * args.ldc + col, f, valid);
+        } else {
+            uint16_t h[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                h[e] = args.out_mode == OUT_BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(f[e]))
+                                                 : __half_as_ushort(__float2half_rn(f[e]));
+            store_4(reinterpret_cast<uint16_t *>(args.C) + int64_t(row) * args.ldc + col, h, valid);
+        }
+    } else {
+        float f[4] = {__uint_as_float(p[0].x), __uint_as_float(p[0].y), __uint_as_float(p[0].z),
+                      __uint_as_float(p[0].w)};
+#pragma unroll
+        for (int k = 1; k < KS; ++k) {
+            f[0] = __fadd_rn(f[0], __uint_as_float(p[k].x));
+            f[1] = __fadd_rn(f[1], __uint_as_float(p[k].y));
+            f[2] = __fadd_rn(f[2], __uint_as_float(p[k].z));
+            f[3] = __fadd_rn(f[3], __uint_as_float(p[k].w));
+        }
+        if constexpr (EPI == EPI_F16ACC) {
+            uint16_t h[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) h[e] = __half_as_ushort(__float2half_rn(f[e]));
+            store_4(reinterpret_cast<uint16_t *>(args.C) + int64_t(row) * args.ldc + col, h, valid);
+        } else {
+            store_4(reinterpret_cast<float *>(args.C) + int64_t(row) * args.ldc + col, f, valid);
+        }
+    }
+}
+
+// Completion of a K-split tile of BN columns: this CTA (`krank` of KS) owns
+// local rows krank * 128/KS .. of the tile (mb, nb), BN / 4 16-byte pieces per
+// row.  The 256 epilogue threads take consecutive pieces (a warp covers 512
+// contiguous bytes of C per store), two at a time with all 2 x KS peer loads
+// in flight before the sums (distributed shared memory is latency-bound).
+template <int EPI, int KS, int BN>
 __device__ __forceinline__ void ksplit_complete(const GemmArgs &args, int mb, int nb, int krank, uint32_t base,
                                                 int ew, int lane) {
     constexpr int R = kBM / KS;
+    constexpr int PPR = BN / 4;     // pieces per row
+    constexpr int PROW = BN * 4;    // partial-sum row bytes
+    constexpr int NT = EPI_WARPS * 32;
+    static_assert((R * PPR) % (2 * NT) == 0, "whole passes of two pieces per thread");
 #pragma unroll 1
-    for (int i = ew; i < R; i += EPI_WARPS) {
-        const int lr = krank * R + i;
-        const int row = mb * kBM + lr;
+    for (int i0 = ew * 32 + lane; i0 < R * PPR; i0 += 2 * NT) {
+        uint4 p[2][KS];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int piece = lane + 32 * half;
-            const uint32_t addr = base + uint32_t(lr) * kPartialRow + (uint32_t(piece ^ (lr & 7)) << 4);
-            uint4 p[KS];
+        for (int u = 0; u < 2; ++u) {
+            const int idx = i0 + u * NT;
+            const int lr = krank * R + idx / PPR;
+            const int piece = idx % PPR;
+            const uint32_t addr = base + uint32_t(lr) * PROW + (uint32_t(piece ^ (lr & 7)) << 4);
 #pragma unroll
-            for (int k = 0; k < KS; ++k) p[k] = ld_shared_cluster_v4(mapa_shared(addr, uint32_t(k)));
-            const int col = nb * kBN + 4 * piece;
-            if (row >= args.M || col >= args.N) continue;
-            const int valid = args.N - col;
-            if constexpr (EPI == EPI_INT) {
-                uint32_t s[4] = {p[0].x, p[0].y, p[0].z, p[0].w};
+            for (int k = 0; k < KS; ++k) p[u][k] = ld_shared_cluster_v4(mapa_shared(addr, uint32_t(k)));
+        }
 #pragma unroll
-                for (int k = 1; k < KS; ++k) {
-                    s[0] += p[k].x;
-                    s[1] += p[k].y;
-                    s[2] += p[k].z;
-                    s[3] += p[k].w;
-                }
-                if (args.out_mode == OUT_S32) {
-                    const int32_t v[4] = {int32_t(s[0]), int32_t(s[1]), int32_t(s[2]), int32_t(s[3])};
-                    store_4(reinterpret_cast<int32_t *>(args.C) + int64_t(row) * args.ldc + col, v, valid);
-                    continue;
-                }
-                const float sa = args.scale_a ? __ldg(args.scale_a + row) : 1.0f;
-                float f[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float sb = (args.scale_b && e < valid) ? __ldg(args.scale_b + col + e) : 1.0f;
-                    f[e] = __fmul_rn(__fmul_rn(__int2float_rn(int32_t(s[e])), sa), sb);
-                }
-                if (args.out_mode == OUT_F32) {
-                    store_4(reinterpret_cast<float *>(args.C) + int64_t(row) * args.ldc + col, f, valid);
-                } else {
-                    uint16_t h[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        h[e] = args.out_mode == OUT_BF16 ? __bfloat16_as_ushort(__float2bfloat16_rn(f[e]))
-                                                         : __half_as_ushort(__float2half_rn(f[e]));
-                    store_4(reinterpret_cast<uint16_t *>(args.C) + int64_t(row) * args.ldc + col, h, valid);
-                }
-            } else {
-                float f[4] = {__uint_as_float(p[0].x), __uint_as_float(p[0].y), __uint_as_float(p[0].z),
-                              __uint_as_float(p[0].w)};
-#pragma unroll
-                for (int k = 1; k < KS; ++k) {
-                    f[0] = __fadd_rn(f[0], __uint_as_float(p[k].x));
-                    f[1] = __fadd_rn(f[1], __uint_as_float(p[k].y));
-                    f[2] = __fadd_rn(f[2], __uint_as_float(p[k].z));
-                    f[3] = __fadd_rn(f[3], __uint_as_float(p[k].w));
-                }
-                if constexpr (EPI == EPI_F16ACC) {
-                    uint16_t h[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) h[e] = __half_as_ushort(__float2half_rn(f[e]));
-                    store_4(reinterpret_cast<uint16_t *>(args.C) + int64_t(row) * args.ldc + col, h, valid);
-                } else {
-                    store_4(reinterpret_cast<float *>(args.C) + int64_t(row) * args.ldc + col, f, valid);
-                }
-            }
+        for (int u = 0; u < 2; ++u) {
+            const int idx = i0 + u * NT;
+            const int row = mb * kBM + krank * R + idx / PPR;
+            const int col = nb * BN + 4 * (idx % PPR);
+            if (row < args.M && col < args.N) ksplit_finish<EPI, KS>(args, row, col, p[u]);
         }
     }
 }
@@ -637,8 +653,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
     static_assert(!(B_MN && KIND == Kind::E4M3), "MN-major B is used by the FP16 path only");
-    static_assert(KS == 1 || (CTAS == 1 && BN == kBN && kBM % (KS * EPI_WARPS) == 0),
-                  "K-split clusters of 256-wide one-CTA tiles");
+    static_assert(KS == 1 || CTAS == 1, "K-split clusters of one-CTA tiles");
     constexpr bool INT_OUT = EPI == EPI_INT;
     constexpr int HALF = BN / 2;      // columns of an epilogue warp's slice
     constexpr int NCH = HALF / 32;    // 32-column chunks of a slice
@@ -959,7 +974,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // cluster's completion pass.
 #pragma unroll
                     for (int c = 0; c < NCH; ++c)
-                        put_partial(smem_u32(smem), 32 * q + lane, h * (HALF / 4) + 8 * c,
+                        put_partial<BN * 4>(smem_u32(smem), 32 * q + lane, h * (HALF / 4) + 8 * c,
                                     reinterpret_cast<const uint32_t(&)[32]>(acc[32 * c]));
                     continue;
                 }
@@ -1050,7 +1065,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                             for (int e = 0; e < 32; ++e)
                                 r[e] = __float_as_uint(__half2float(__ushort_as_half(static_cast<uint16_t>(r[e]))));
                         }
-                        put_partial(smem_u32(smem), 32 * q + lane, h * (HALF / 4) + 8 * c, r);
+                        put_partial<BN * 4>(smem_u32(smem), 32 * q + lane, h * (HALF / 4) + 8 * c, r);
                     }
                 } else {
                     // A split tile of FP32 C: both K halves add into the zeroed C
@@ -1122,7 +1137,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         cluster_sync();
         if (warp >= 2 && cluster < args.num_vunits) {
             const WorkRef wr = work_unit(cluster, args, C_::SUB);
-            ksplit_complete<EPI, KS>(args, wr.mb, wr.nb, krank, smem_u32(smem), warp - 2, lane);
+            ksplit_complete<EPI, KS, BN>(args, wr.mb, wr.nb, krank, smem_u32(smem), warp - 2, lane);
         }
     }
     // A K-split cluster's peers read this CTA's ring until this barrier.
@@ -1319,6 +1334,8 @@ int ksplit_capacity(int ks, int sms) {
 
 }  // namespace
 
+int ksplit_clusters(int ks, int sms) { return ksplit_capacity(ks, sms); }
+
 void last_launch(int *grid, int *cluster, int *ksplit, int *tile_n) {
     *grid = g_last.grid;
     *cluster = g_last.cluster;
@@ -1349,9 +1366,19 @@ cudaError_t launch_gemm(Kind kind, bool b_mn_major, int epi, int ctas, const CUt
                         cudaStream_t stream) {
     const int bn = (ctas == 1 && args.bn != 0) ? args.bn : kBN;
     if (bn != kBN && bn != 64 && bn != 128) return cudaErrorInvalidValue;
-    const int ks = (ctas == 1 && bn == kBN) ? pick_ksplit(args.num_tiles, args.num_kb, args.ksplit, sms) : 1;
+    int ks = 1;
+    if (ctas == 1 && bn == kBN) {
+        ks = pick_ksplit(args.num_tiles, args.num_kb, args.ksplit, sms);
+    } else if (ctas == 1 && (args.ksplit == 2 || args.ksplit == 4) && args.num_kb >= args.ksplit &&
+               args.num_tiles <= ksplit_capacity(args.ksplit, sms)) {
+        ks = args.ksplit;  // narrow tiles: the size (2 or 4) the caller chose
+    }
 #define PTC_LAUNCH(K, BMN, E)                                                                       \
     do {                                                                                            \
+        if (bn == 64 && ks == 4) return launch_one<K, BMN, E, 1, 1, 4, 64>(ta, tb, args, sms, pool, stream); \
+        if (bn == 64 && ks == 2) return launch_one<K, BMN, E, 1, 1, 2, 64>(ta, tb, args, sms, pool, stream); \
+        if (bn == 128 && ks == 4) return launch_one<K, BMN, E, 1, 1, 4, 128>(ta, tb, args, sms, pool, stream); \
+        if (bn == 128 && ks == 2) return launch_one<K, BMN, E, 1, 1, 2, 128>(ta, tb, args, sms, pool, stream); \
         if (bn == 64) return launch_one<K, BMN, E, 1, 1, 1, 64>(ta, tb, args, sms, pool, stream);   \
         if (bn == 128) return launch_one<K, BMN, E, 1, 1, 1, 128>(ta, tb, args, sms, pool, stream); \
         if (ks == 8) return launch_one<K, BMN, E, 1, 1, 8, kBN>(ta, tb, args, sms, pool, stream);   \

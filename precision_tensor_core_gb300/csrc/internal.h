@@ -100,6 +100,10 @@ cudaError_t launch_gemm(Kind kind, bool b_mn_major, int epi, int ctas, const CUt
 // least 8 K blocks), 1 never, 2 / 4 / 8 that KS when it fits.
 int pick_ksplit(int tiles, int num_kb, int knob, int sms);
 
+// Clusters of ks one-CTA tiles (2, 4 or 8) that fit one wave on this device
+// (0 when that cluster shape cannot run).
+int ksplit_clusters(int ks, int sms);
+
 // Launch shape of the calling thread's last GEMM kernel launch (grid CTAs,
 // CTAs per cluster, CTAs sharing a tile's K range, tile width); zeros before
 // the first.

@@ -58,7 +58,11 @@ LAUNCH_SETTINGS = [("256-wide, plain launches", {"tile_n": 256, "ksplit": 1, "pd
                    ("K-split 4", {"tile_n": 256, "ksplit": 4, "pdl": 1}),
                    ("K-split 8", {"tile_n": 256, "ksplit": 8, "pdl": 1}),
                    ("128-wide", {"tile_n": 128, "ksplit": 1, "pdl": 1}),
+                   ("128-wide, K-split 2", {"tile_n": 128, "ksplit": 2, "pdl": 1}),
+                   ("128-wide, K-split 4", {"tile_n": 128, "ksplit": 4, "pdl": 1}),
                    ("64-wide", {"tile_n": 64, "ksplit": 1, "pdl": 1}),
+                   ("64-wide, K-split 2", {"tile_n": 64, "ksplit": 2, "pdl": 1}),
+                   ("64-wide, K-split 4", {"tile_n": 64, "ksplit": 4, "pdl": 1}),
                    ("defaults", {"tile_n": 0, "ksplit": 0, "pdl": 1})]
 
 

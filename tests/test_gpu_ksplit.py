@@ -82,8 +82,8 @@ def _tiles(M, N):
 def _check_launch(ks, M, N, num_kb):
     """The recorded launch is a K-split cluster launch when it must be: a
     forced KS with at most 8 tiles (clusters of 8 then always fit one wave)
-    and at least KS K blocks; by size, only when each CTA sheds 8 or more K
-    blocks."""
+    and at least KS K blocks; by size, 256-wide tiles only when each CTA sheds
+    8 or more K blocks, narrow tiles with at least two K blocks per CTA."""
     grid, cluster, used, tile_n = ptc.ptc_last_launch()
     assert used in (1, 2, 4, 8) and grid > 0 and tile_n in (64, 128, 256)
     tiles = _tiles(M, N)
@@ -93,10 +93,13 @@ def _check_launch(ks, M, N, num_kb):
         assert used in (1, ks)
         if tiles <= 8 and num_kb >= ks:
             assert used == ks
-    elif used > 1:
+    elif used > 1 and tile_n == 256:
         assert num_kb - (num_kb + used - 1) // used >= 8
+    elif used > 1:
+        assert num_kb >= 2 * used  # narrow tiles: at least two K blocks per CTA
     if used > 1:
-        assert num_kb >= used and cluster == used and grid == used * tiles
+        tiles_bn = ((M + 127) // 128) * ((N + tile_n - 1) // tile_n)
+        assert num_kb >= used and cluster == used and grid == used * tiles_bn
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)

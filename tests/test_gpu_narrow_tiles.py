@@ -71,9 +71,9 @@ def _check_launch(tile_n, M, N):
         assert 1 <= grid <= tiles
     elif bn != 256:
         # by size, narrow tiles only when the 128 x 256 tiles fit one wave and
-        # the narrow ones too (no more tiles than CTAs launched)
+        # the narrow ones too (one CTA, or one K-split cluster, per tile)
         tiles = ((M + 127) // 128) * ((N + bn - 1) // bn)
-        assert grid == tiles
+        assert grid == tiles * ks and cluster == ks
 
 
 @pytest.mark.parametrize("M,N,K", SHAPES)
@@ -171,14 +171,96 @@ def test_auto_shapes_of_the_study_sizes():
         ptc.matmul_f16(A, A)
         shapes[n] = ptc.ptc_last_launch()
     torch.cuda.synchronize()
-    assert shapes[512][3] == 64 and shapes[1024][3] == 64 and shapes[1536][3] == 128
+    assert shapes[512][3] == 64 and shapes[1024][3] in (64, 128) and shapes[1536][3] == 128
     assert shapes[2048][1] == 2 and shapes[4096][1] == 2
-    # long K over few tiles: K-split clusters of 8 (16 or 32 K blocks per CTA
-    # against 256 or 32 on a narrow tile)
+    # long K over few tiles: K-split clusters (a tile's 256 or 32 K blocks
+    # shared by 2-8 CTAs), of 256-wide or narrow tiles
     for (M, N, K) in ((512, 512, 16384), (128, 2048, 2048)):
         A = torch.zeros((M, K), dtype=torch.float16, device=DEV)
         B = torch.zeros((K, N), dtype=torch.float16, device=DEV)
         ptc.matmul_f16(A, B)
         grid, cluster, ks, bn = ptc.ptc_last_launch()
-        assert ks == 8 and bn == 256 and cluster == 8, (M, N, K, grid, cluster, ks, bn)
+        assert ks > 1 and cluster == ks, (M, N, K, grid, cluster, ks, bn)
     torch.cuda.synchronize()
+
+
+@pytest.fixture(params=[(64, 2), (64, 4), (128, 2), (128, 4)], ids=["n64-ks2", "n64-ks4", "n128-ks2", "n128-ks4"])
+def narrow_ks(request):
+    """Narrow tiles in K-split clusters (forced)."""
+    bn, ks = request.param
+    ptc.ptc_set_tuning("tile_n", bn)
+    ptc.ptc_set_tuning("ksplit", ks)
+    yield request.param
+    ptc.ptc_set_tuning("ksplit", 0)
+    ptc.ptc_set_tuning("tile_n", 0)
+
+
+def _check_narrow_ks(bn, ks, M, N, num_kb):
+    grid, cluster, used, tile_n = ptc.ptc_last_launch()
+    assert tile_n == bn and used in (1, ks)
+    tiles = ((M + 127) // 128) * ((N + bn - 1) // bn)
+    if tiles <= 16 and num_kb >= ks:
+        assert used == ks and cluster == ks and grid == ks * tiles
+
+
+# (M, N, K): 512^3 (32 / 16 narrow tiles, 8 K blocks); 300 x 700 x 200 (ragged
+# tiles, 4 ragged K blocks, shares 2+2 or 1+1+1+1); 100 x 40 x 1000 (one tile);
+# 256 x 384 x 576 (9 K blocks: shares 5+4, 3+2+2+2).
+KS_SHAPES = [(512, 512, 512), (300, 700, 200), (100, 40, 1000), (256, 384, 576)]
+
+
+@pytest.mark.parametrize("M,N,K", KS_SHAPES)
+def test_narrow_ksplit_f16(M, N, K, narrow_ks):
+    A, B = datagen.f16_operands(N, "normal", seed=M + 5 * N + K, m=M, k=K)
+    C = ptc.matmul_f16(padded_f16_dev(A), padded_f16_dev(B), out=out_padded(M, N, torch.float32))
+    _check_narrow_ks(*narrow_ks, M, N, (K + 63) // 64)
+    check_f16(C.cpu().numpy(), A, B)
+
+
+@pytest.mark.parametrize("M,N,K", KS_SHAPES)
+def test_narrow_ksplit_s8(M, N, K, narrow_ks):
+    A, Bt = datagen.s8_operands(N, seed=M + 5 * N + K, m=M, k=K)
+    C = ptc.matmul_s8(padded_dev(A), padded_dev(Bt), out=out_padded(M, N, torch.int32))
+    _check_narrow_ks(*narrow_ks, M, N, (K + 63) // 64)
+    torch.cuda.synchronize()
+    assert np.array_equal(C.cpu().numpy(), oracle.wrap_s32(oracle.gemm_s8(A, Bt)))
+
+
+@pytest.mark.parametrize("M,N,K", KS_SHAPES)
+def test_narrow_ksplit_s4(M, N, K, narrow_ks):
+    A, Bt = datagen.s4_operands(N, seed=M + 5 * N + K, m=M, k=K)
+    C = ptc.matmul_s4(padded_dev(A), padded_dev(Bt), K, out=out_padded(M, N, torch.int32))
+    _check_narrow_ks(*narrow_ks, M, N, (K + 127) // 128)
+    torch.cuda.synchronize()
+    assert np.array_equal(C.cpu().numpy(), oracle.wrap_s32(oracle.gemm_s4(A, Bt, K)))
+
+
+@pytest.mark.parametrize("out", [torch.bfloat16, torch.float32], ids=["bf16", "f32"])
+def test_narrow_ksplit_scaled(out, narrow_ks):
+    M, N, K = 300, 700, 576
+    A, Bt = datagen.s8_operands(N, seed=71, m=M, k=K)
+    rng = np.random.default_rng(72)
+    sa = (rng.standard_normal(M) * 0.01).astype(np.float32)
+    sb = (rng.standard_normal(N) * 0.01).astype(np.float32)
+    C = ptc.matmul_s8_scaled(padded_dev(A), padded_dev(Bt), torch.from_numpy(sa).to(DEV),
+                             torch.from_numpy(sb).to(DEV), out_dtype=out, out=out_padded(M, N, out))
+    torch.cuda.synchronize()
+    code = {torch.bfloat16: oracle.OUT_BF16, torch.float32: oracle.OUT_F32}[out]
+    ref = oracle.dequant(oracle.gemm_s8(A, Bt), sa, sb, code)
+    if out == torch.float32:
+        got = C.cpu().view(torch.int32).numpy().view(np.uint32)
+    else:
+        got = C.cpu().view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_narrow_ksplit_f16acc_permutation(narrow_ks):
+    M, K, N = 300, 576, 700
+    perm = np.random.default_rng(73).integers(0, K, size=M)
+    A = np.zeros((M, K), np.float16)
+    A[np.arange(M), perm] = 1
+    B = np.random.default_rng(74).uniform(-100, 100, size=(K, N)).astype(np.float16)
+    C = ptc.matmul_f16_f16acc(padded_f16_dev(A.view(np.uint16)), padded_f16_dev(B.view(np.uint16)),
+                              out=out_padded(M, N, torch.float16))
+    torch.cuda.synchronize()
+    assert np.array_equal(C.cpu().numpy().astype(np.float64), B.astype(np.float64)[perm])
