@@ -309,6 +309,18 @@ uint64_t ptc_kernel_launch_count(void);
  * launch only.  Returns PTC_OK. */
 int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile);
 
+/* The launch shape the library would choose for an M x N x K product of
+ * precision `prec` (0 FP16, 1 INT8, 2 INT4; 4-byte C) on a device with `sms`
+ * SMs on which cap2 / cap4 / cap8 thread-block clusters of 2 / 4 / 8 one-CTA
+ * tiles fit at once, under the current tuning knobs: *ctas = 1 or 2 (CTA
+ * pairs on 256 x 256 tiles), *tile_n = output columns per tile (256, 128,
+ * 64), *ksplit = CTAs sharing one tile's K range (1 = none).  Host-only
+ * arithmetic (no device is touched), for inspecting and testing the
+ * automatic choice.  Returns PTC_OK, or PTC_ERR_INVALID for a NULL pointer or
+ * an argument out of range (sizes must be positive). */
+int ptc_plan_shape(int64_t M, int64_t N, int64_t K, int prec, int sms, int cap2, int cap4, int cap8, int *ctas,
+                   int *tile_n, int *ksplit);
+
 /* Launch shape of the last GEMM kernel the calling thread launched through
  * this library: *grid = CTAs launched, *cluster = CTAs per thread-block
  * cluster (1; 2 for CTA pairs; KS for K-split clusters), *ksplit = CTAs that

@@ -9,7 +9,7 @@ library's CUDA kernels):
 
 * ``gemm_f16``, ``gemm_f16_f16acc``, ``gemm_s8``, ``gemm_s4``, ``gemm_s8_scaled``, ``gemm_s4_scaled``,
   ``gemm_s8_noalloc``, ``gemm_s8_b_rowmajor``, ``gemm_status_string``,
-  ``gemm_poll_device_error``, ``ptc_kernel_launch_count``, ``ptc_last_launch``,
+  ``gemm_poll_device_error``, ``ptc_kernel_launch_count``, ``ptc_last_launch``, ``ptc_plan_shape``,
   ``ptc_debug_set_wait_limit``, ``ptc_set_tuning``: the C ABI of
   ``include/ptc.h`` under the same names, taking integers (sizes, leading
   dimensions, device addresses, a cudaStream_t handle).  A nonzero status
@@ -96,6 +96,9 @@ def lib() -> ctypes.CDLL:
         _ip = ctypes.POINTER(ctypes.c_int)
         L.ptc_last_launch.restype = ctypes.c_int
         L.ptc_last_launch.argtypes = [_ip, _ip, _ip, _ip]
+        L.ptc_plan_shape.restype = ctypes.c_int
+        L.ptc_plan_shape.argtypes = [_i64, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, _ip, _ip, _ip]
         _lib = L
     return _lib
 
@@ -188,6 +191,19 @@ def ptc_debug_set_wait_limit(timeout_ns: int, stall_tile: int = -1) -> int:
 
 def ptc_set_tuning(key: str, value: int) -> int:
     return _check(lib().ptc_set_tuning(key.encode(), int(value)))
+
+
+def ptc_plan_shape(M: int, N: int, K: int, prec: int, sms: int = 152,
+                   caps: tuple[int, int, int] = (76, 36, 15)) -> tuple[int, int, int]:
+    """(CTAs per tile, tile width, CTAs per tile's K range) the library would
+    launch for an M x N x K product of precision `prec` (0 FP16, 1 INT8,
+    2 INT4) on a device of `sms` SMs with cluster capacities `caps` (clusters
+    of 2, 4, 8 one-CTA tiles that fit at once), under the current knobs.
+    Host arithmetic only; the defaults are a GB300's figures."""
+    c, n, k = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().ptc_plan_shape(int(M), int(N), int(K), int(prec), int(sms), int(caps[0]), int(caps[1]),
+                                int(caps[2]), ctypes.byref(c), ctypes.byref(n), ctypes.byref(k)))
+    return c.value, n.value, k.value
 
 
 def ptc_last_launch() -> tuple[int, int, int, int]:

@@ -219,17 +219,39 @@ int64_t tile_count(int64_t M, int64_t N, int rows, int cols) {
     return ((M + rows - 1) / rows) * ((N + cols - 1) / cols);
 }
 
+}  // namespace
+
+namespace ptc {
+int pick_ksplit_pure(int tiles, int num_kb, int knob, int sms, const ClusterCaps &caps) {
+    if (knob == 1 || 2 * tiles > sms) return 1;
+    for (int ks = 8; ks >= 2; ks /= 2) {
+        if ((knob != 0 && knob != ks) || num_kb < ks) continue;
+        // The split costs ~1-1.5 us per call (partial sums to shared memory,
+        // two cluster barriers, the reduction); a one-CTA K block takes
+        // ~0.15 us, so by size it is taken when each CTA sheds 8 or more.
+        const int shed = num_kb - (num_kb + ks - 1) / ks;
+        if (knob == 0 && shed < 8) continue;
+        if (tiles <= caps.of(ks)) return ks;
+    }
+    return 1;
+}
+}  // namespace ptc
+
+namespace {
+
 // Multi-wave products run on CTA pairs (256 x 256 tiles: a third fewer
 // operand bytes per output).  A product whose 128 x 256 tiles fit one wave
 // takes the shape of least estimated time among: narrow one-CTA tiles
-// (128 x 128, 128 x 64) that still fit one wave, K-split clusters of
-// 128 x 256 tiles (pick_ksplit), and whole 128 x 256 tiles; whole tiles go to
-// pairs for FP16 from 32 one-CTA tiles up (measured 4-10% faster at N = 1024
-// .. 2048 before narrow tiles existed; the integer routes were faster with
-// one CTA per tile).  esize: bytes per C element.  The knobs cta_pair,
-// tile_n and ksplit force parts of the choice.
-Shape choose_shape(int64_t M, int64_t N, int64_t num_kb, int sms, bool f16, int esize) {
-    const int fpair = g_cta_pair.load(), ftile = g_tile_n.load(), fks = g_ksplit.load();
+// (128 x 128, 128 x 64) that still fit one wave, whole or in K-split
+// clusters of 2 or 4; K-split clusters of 128 x 256 tiles (pick_ksplit_pure);
+// and whole 128 x 256 tiles, which go to pairs for FP16 from 32 one-CTA tiles
+// up (measured 4-10% faster at N = 1024 .. 2048 before narrow tiles existed;
+// the integer routes were faster with one CTA per tile).  esize: bytes per C
+// element; fpair / ftile / fks: the knobs cta_pair, tile_n and ksplit, which
+// force parts of the choice; caps: the device's K-split cluster capacities.
+// Pure (host arithmetic only).
+Shape plan_shape(int64_t M, int64_t N, int64_t num_kb, int sms, bool f16, int esize, int fpair, int ftile,
+                 int fks, const ptc::ClusterCaps &caps) {
     if (fpair == 2) return {2, ptc::kBN, 1};
     if ((ftile == 64 || ftile == 128) && tile_count(M, N, ptc::kBM, ftile) <= (int64_t(1) << 20))
         return {1, ftile, (fks == 2 || fks == 4) ? fks : 1};
@@ -239,7 +261,7 @@ Shape choose_shape(int64_t M, int64_t N, int64_t num_kb, int sms, bool f16, int 
     Shape best{1, ptc::kBN, 1};
     int64_t best_c = est_clocks(num_kb, ptc::kBN, 1, esize);
     if (fks != 1) {
-        const int ks = ptc::pick_ksplit(int(t256), int(num_kb), fks, sms);
+        const int ks = ptc::pick_ksplit_pure(int(t256), int(num_kb), fks, sms, caps);
         if (ks > 1 && (fks != 0 || est_clocks(num_kb, ptc::kBN, ks, esize) < best_c)) {
             best = {1, ptc::kBN, ks};
             best_c = fks != 0 ? 0 : est_clocks(num_kb, ptc::kBN, ks, esize);
@@ -250,8 +272,7 @@ Shape choose_shape(int64_t M, int64_t N, int64_t num_kb, int sms, bool f16, int 
         if (ftile != 0 || tiles > sms) continue;
         // whole narrow tiles, or K-split clusters of 2 / 4 of them
         for (int ks : {1, 2, 4}) {
-            if (ks > 1 && (fks == 1 || (fks != 0 && fks != ks) || num_kb < 2 * ks ||
-                           tiles > ptc::ksplit_clusters(ks, sms)))
+            if (ks > 1 && (fks == 1 || (fks != 0 && fks != ks) || num_kb < 2 * ks || tiles > caps.of(ks)))
                 continue;
             const int64_t c = est_clocks(num_kb, bn, ks, esize);
             if (c < best_c) {
@@ -262,6 +283,11 @@ Shape choose_shape(int64_t M, int64_t N, int64_t num_kb, int sms, bool f16, int 
     }
     if (best.bn == ptc::kBN && best.ks == 1 && f16 && t256 >= 32) return {2, ptc::kBN, 1};
     return best;
+}
+
+Shape choose_shape(int64_t M, int64_t N, int64_t num_kb, int sms, bool f16, int esize) {
+    return plan_shape(M, N, num_kb, sms, f16, esize, g_cta_pair.load(), g_tile_n.load(), g_ksplit.load(),
+                      ptc::cluster_caps(sms));
 }
 
 GemmArgs base_args(int64_t M, int64_t N, int64_t K, int k_elems_per_block, void *C, int64_t ldc,
@@ -891,6 +917,33 @@ uint64_t ptc_kernel_launch_count(void) { return g_launches.load(); }
 int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile) {
     g_wait_ns.store(timeout_ns ? timeout_ns : kDefaultWaitNs);
     g_stall_tile.store(stall_tile);
+    return PTC_OK;
+}
+
+int ptc_plan_shape(int64_t M, int64_t N, int64_t K, int prec, int sms, int cap2, int cap4, int cap8, int *ctas,
+                   int *tile_n, int *ksplit) {
+    if (!ctas || !tile_n || !ksplit) return fail(PTC_ERR_INVALID, "NULL pointer");
+    if (prec < 0 || prec > 2 || sms <= 0 || cap2 < 0 || cap4 < 0 || cap8 < 0 || M <= 0 || N <= 0 || K <= 0)
+        return fail(PTC_ERR_INVALID, "precision, SM count, capacities or sizes out of range");
+    int rc = check_sizes(M, N, K);
+    if (rc) return rc;
+    ptc::ClusterCaps caps;
+    caps.c2 = cap2;
+    caps.c4 = cap4;
+    caps.c8 = cap8;
+    const int64_t num_kb = (K + (prec == 2 ? 127 : 63)) / (prec == 2 ? 128 : 64);
+    Shape sh = plan_shape(M, N, num_kb, sms, prec == 0, 4, g_cta_pair.load(), g_tile_n.load(), g_ksplit.load(),
+                          caps);
+    // what the launcher then runs for one-CTA tiles
+    if (sh.ctas == 1 && sh.bn == ptc::kBN) {
+        sh.ks = ptc::pick_ksplit_pure(int(tile_count(M, N, ptc::kBM, ptc::kBN)), int(num_kb), sh.ks, sms, caps);
+    } else if (sh.ctas == 1 && sh.ks > 1 &&
+               (num_kb < sh.ks || tile_count(M, N, ptc::kBM, sh.bn) > caps.of(sh.ks))) {
+        sh.ks = 1;
+    }
+    *ctas = sh.ctas;
+    *tile_n = sh.bn;
+    *ksplit = sh.ks < 1 ? 1 : sh.ks;
     return PTC_OK;
 }
 

@@ -1334,7 +1334,13 @@ int ksplit_capacity(int ks, int sms) {
 
 }  // namespace
 
-int ksplit_clusters(int ks, int sms) { return ksplit_capacity(ks, sms); }
+ClusterCaps cluster_caps(int sms) {
+    ClusterCaps c;
+    c.c2 = ksplit_capacity(2, sms);
+    c.c4 = ksplit_capacity(4, sms);
+    c.c8 = ksplit_capacity(8, sms);
+    return c;
+}
 
 void last_launch(int *grid, int *cluster, int *ksplit, int *tile_n) {
     *grid = g_last.grid;
@@ -1345,16 +1351,7 @@ void last_launch(int *grid, int *cluster, int *ksplit, int *tile_n) {
 
 int pick_ksplit(int tiles, int num_kb, int knob, int sms) {
     if (knob == 1 || 2 * tiles > sms) return 1;
-    for (int ks = 8; ks >= 2; ks /= 2) {
-        if ((knob != 0 && knob != ks) || num_kb < ks) continue;
-        // The split costs ~1-1.5 us per call (partial sums to shared memory,
-        // two cluster barriers, the reduction); a one-CTA K block takes
-        // ~0.15 us, so by size it is taken when each CTA sheds 8 or more.
-        const int shed = num_kb - (num_kb + ks - 1) / ks;
-        if (knob == 0 && shed < 8) continue;
-        if (tiles <= ksplit_capacity(ks, sms)) return ks;
-    }
-    return 1;
+    return pick_ksplit_pure(tiles, num_kb, knob, sms, cluster_caps(sms));
 }
 
 size_t gemm_smem_bytes(int ctas) { return ctas == 2 ? smem_bytes<2, 2>() : smem_bytes<1, 1>(); }

@@ -94,15 +94,23 @@ cudaError_t launch_gemm(Kind kind, bool b_mn_major, int epi, int ctas, const CUt
                         const CUtensorMap &tb, const GemmArgs &args, int sms, cudaMemPool_t pool,
                         cudaStream_t stream);
 
-// CTAs per K-split cluster for a one-CTA launch of `tiles` output tiles of
-// num_kb K blocks each: 1 (no split), 2, 4 or 8.  knob: 0 chooses by size
-// (the largest KS whose clusters fit one wave and that sheds each CTA at
-// least 8 K blocks), 1 never, 2 / 4 / 8 that KS when it fits.
-int pick_ksplit(int tiles, int num_kb, int knob, int sms);
+// Clusters of 2, 4 and 8 one-CTA tiles that fit one wave on a device (0 when
+// that cluster shape cannot run).
+struct ClusterCaps {
+    int c2 = 0, c4 = 0, c8 = 0;
+    int of(int ks) const { return ks == 2 ? c2 : ks == 4 ? c4 : ks == 8 ? c8 : 0; }
+};
 
-// Clusters of ks one-CTA tiles (2, 4 or 8) that fit one wave on this device
-// (0 when that cluster shape cannot run).
-int ksplit_clusters(int ks, int sms);
+// The current device's capacities (queried once per device and thread).
+ClusterCaps cluster_caps(int sms);
+
+// CTAs per K-split cluster for a one-CTA launch of `tiles` 256-wide output
+// tiles of num_kb K blocks each: 1 (no split), 2, 4 or 8.  knob: 0 chooses by
+// size (the largest KS whose clusters fit one wave and that sheds each CTA at
+// least 8 K blocks), 1 never, 2 / 4 / 8 that KS when it fits.  Host-only and
+// pure given the capacities.
+int pick_ksplit_pure(int tiles, int num_kb, int knob, int sms, const ClusterCaps &caps);
+int pick_ksplit(int tiles, int num_kb, int knob, int sms);
 
 // Launch shape of the calling thread's last GEMM kernel launch (grid CTAs,
 // CTAs per cluster, CTAs sharing a tile's K range, tile width); zeros before
