@@ -35,17 +35,18 @@
 //               stages of two K blocks (or, as a tuning choice, 7 of one).
 //   KS = 2/4/8  one-CTA tiles in clusters of KS CTAs that share a tile's K
 //               range (split-K inside a cluster), for single-wave launches
-//               whose tiles would leave most SMs idle: each CTA multiplies
-//               about 1/KS of the K blocks, writes its 128 x 256 partial sums
-//               into its idle ring, and after a cluster barrier completes
-//               128/KS rows of the tile by adding the KS partials in rank
-//               order, read from the peers' shared memory (distributed shared
-//               memory).  No workspace, no atomics, the same sums every run.
+//               whose tiles would leave most SMs idle (8 only for 256-wide
+//               tiles): each CTA multiplies about 1/KS of the K blocks,
+//               writes its 128 x BN partial sums into its idle ring, and
+//               after a cluster barrier completes 128/KS rows of the tile by
+//               adding the KS partials in rank order, read from the peers'
+//               shared memory (distributed shared memory).  No workspace, no
+//               atomics, the same sums every run.
 //
 // The work list: output tiles in grouped raster order, strided over the
 // clusters; when the last wave would leave at least half of the clusters idle,
-// its tiles run as two K halves whose epilogue warps add partial sums through
-// a workspace (see work_unit).
+// its tiles run as two K halves (see work_unit), added into C by TMA
+// reductions (FP32 / int32 C of CTA pairs) or through a partial-sum exchange.
 //
 // Integer routes: sm_103a has no integer tcgen05 MMA, so INT8 runs on the
 // FP16 kind (every s8 value is an exact binary16) and INT4 on the E4M3 kind
