@@ -111,8 +111,11 @@ int gemm_f16_f16acc(int64_t M, int64_t N, int64_t K,
  *   C  row-major, element (i,j) at C[i*ldc + j];    ldc >= N, ldc % 4 == 0
  * Result: bit-exact sum_k A_ik B_kj, wrapped modulo 2^32 if it leaves the
  * int32 range (unreachable for K <= 131072).
- * Uses a stream-ordered device workspace of about 2*(M+N)*K bytes, taken
- * from and returned to a library-owned memory pool on `stream`.
+ * A and B are first converted into a stream-ordered device workspace of about
+ * 2*(M+N)*K bytes, taken from and returned to a library-owned memory pool on
+ * `stream`; small products (one wave of one-CTA tiles with few K blocks each)
+ * instead convert each K block inside the GEMM kernel's shared memory and use
+ * no workspace (tuning key "in_ring").
  */
 int gemm_s8(int64_t M, int64_t N, int64_t K,
             const int8_t *A, int64_t lda,
@@ -149,7 +152,8 @@ int gemm_s8_b_rowmajor(int64_t M, int64_t N, int64_t K,
  *   C  row-major int32, ldc >= N, ldc % 4 == 0
  * Odd K is allowed: the high nibble of a row's last byte is then ignored.
  * Result: bit-exact sum_k A_ik B_kj (|C| <= 64*K, no overflow for K < 2^25).
- * Uses a stream-ordered device workspace of about (M+N)*K bytes, as gemm_s8.
+ * Uses a stream-ordered device workspace of about (M+N)*K bytes, or converts
+ * inside the GEMM kernel, as gemm_s8 (in-kernel conversion needs an even K).
  */
 int gemm_s4(int64_t M, int64_t N, int64_t K,
             const void *A, int64_t lda,
@@ -314,12 +318,14 @@ int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile);
  * SMs on which cap2 / cap4 / cap8 thread-block clusters of 2 / 4 / 8 one-CTA
  * tiles fit at once, under the current tuning knobs: *ctas = 1 or 2 (CTA
  * pairs on 256 x 256 tiles), *tile_n = output columns per tile (256, 128,
- * 64), *ksplit = CTAs sharing one tile's K range (1 = none).  Host-only
+ * 64), *ksplit = CTAs sharing one tile's K range (1 = none), and, when
+ * in_ring is not NULL, *in_ring = 1 if the integer operands would be
+ * converted inside the GEMM kernel (0: a separate pass, or FP16).  Host-only
  * arithmetic (no device is touched), for inspecting and testing the
- * automatic choice.  Returns PTC_OK, or PTC_ERR_INVALID for a NULL pointer or
- * an argument out of range (sizes must be positive). */
+ * automatic choice.  Returns PTC_OK, or PTC_ERR_INVALID for a NULL pointer
+ * (other than in_ring) or an argument out of range (sizes must be positive). */
 int ptc_plan_shape(int64_t M, int64_t N, int64_t K, int prec, int sms, int cap2, int cap4, int cap8, int *ctas,
-                   int *tile_n, int *ksplit);
+                   int *tile_n, int *ksplit, int *in_ring);
 
 /* Launch shape of the last GEMM kernel the calling thread launched through
  * this library: *grid = CTAs launched, *cluster = CTAs per thread-block
@@ -329,6 +335,13 @@ int ptc_plan_shape(int64_t M, int64_t N, int64_t K, int prec, int sms, int cap2,
  * tiles).  All zero before the first launch.  Host-side only (no device
  * work).  Returns PTC_OK, or PTC_ERR_INVALID when a pointer is NULL. */
 int ptc_last_launch(int *grid, int *cluster, int *ksplit, int *tile_n);
+
+/* Operand conversion of the calling thread's last GEMM call through this
+ * library: *mode = 0 none (FP16 operands, a call that launched nothing, or no
+ * call yet), 1 a separate conversion pass into a workspace, 2 conversion
+ * inside the GEMM kernel's shared memory.  Host-side only.  Returns PTC_OK,
+ * or PTC_ERR_INVALID when the pointer is NULL. */
+int ptc_last_conversion(int *mode);
 
 /* Tuning and test knobs, process-wide.  Returns PTC_OK, or PTC_ERR_INVALID for
  * an unknown key or a value out of range.  Keys:
@@ -410,6 +423,15 @@ int ptc_last_launch(int *grid, int *cluster, int *ksplit, int *tile_n);
  *                  barriers and tensor memory) while the previous kernel of
  *                  the stream finishes; it waits for that kernel before its
  *                  first global-memory access.  0: plain stream order.
+ *   "in_ring"      gemm_s8 / gemm_s4 (and their scaled forms) on one-CTA
+ *                  shapes may load K blocks of the raw operands and convert
+ *                  them to the MMA input type in the GEMM kernel's shared
+ *                  memory (the epilogue warps, idle during the K loop, do
+ *                  it), with no workspace and no separate kernel.  1
+ *                  (default): where estimated faster than a separate pass
+ *                  (single-wave launches with few K blocks per CTA: small
+ *                  products such as N = 512); 0: never; 2: on every one-CTA
+ *                  shape.  Results do not depend on the choice.
  * Values above the defaults can make gemm_s8 / gemm_s4 inexact for adversarial
  * inputs; they exist to measure the tensor cores' accumulation width. */
 int ptc_set_tuning(const char *key, int64_t value);

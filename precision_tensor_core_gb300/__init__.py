@@ -9,7 +9,7 @@ library's CUDA kernels):
 
 * ``gemm_f16``, ``gemm_f16_f16acc``, ``gemm_s8``, ``gemm_s4``, ``gemm_s8_scaled``, ``gemm_s4_scaled``,
   ``gemm_s8_noalloc``, ``gemm_s8_b_rowmajor``, ``gemm_status_string``,
-  ``gemm_poll_device_error``, ``ptc_kernel_launch_count``, ``ptc_last_launch``, ``ptc_plan_shape``,
+  ``gemm_poll_device_error``, ``ptc_kernel_launch_count``, ``ptc_last_launch``, ``ptc_last_conversion``, ``ptc_plan_shape``,
   ``ptc_debug_set_wait_limit``, ``ptc_set_tuning``: the C ABI of
   ``include/ptc.h`` under the same names, taking integers (sizes, leading
   dimensions, device addresses, a cudaStream_t handle).  A nonzero status
@@ -96,9 +96,11 @@ def lib() -> ctypes.CDLL:
         _ip = ctypes.POINTER(ctypes.c_int)
         L.ptc_last_launch.restype = ctypes.c_int
         L.ptc_last_launch.argtypes = [_ip, _ip, _ip, _ip]
+        L.ptc_last_conversion.restype = ctypes.c_int
+        L.ptc_last_conversion.argtypes = [_ip]
         L.ptc_plan_shape.restype = ctypes.c_int
         L.ptc_plan_shape.argtypes = [_i64, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                     ctypes.c_int, _ip, _ip, _ip]
+                                     ctypes.c_int, _ip, _ip, _ip, _ip]
         _lib = L
     return _lib
 
@@ -194,15 +196,19 @@ def ptc_set_tuning(key: str, value: int) -> int:
 
 
 def ptc_plan_shape(M: int, N: int, K: int, prec: int, sms: int = 152,
-                   caps: tuple[int, int, int] = (76, 36, 15)) -> tuple[int, int, int]:
+                   caps: tuple[int, int, int] = (76, 36, 15), with_ring: bool = False):
     """(CTAs per tile, tile width, CTAs per tile's K range) the library would
     launch for an M x N x K product of precision `prec` (0 FP16, 1 INT8,
     2 INT4) on a device of `sms` SMs with cluster capacities `caps` (clusters
-    of 2, 4, 8 one-CTA tiles that fit at once), under the current knobs.
-    Host arithmetic only; the defaults are a GB300's figures."""
-    c, n, k = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    of 2, 4, 8 one-CTA tiles that fit at once), under the current knobs; with
+    `with_ring`, a fourth item: whether the integer operands are converted
+    inside the GEMM kernel.  Host arithmetic only; the defaults are a GB300's
+    figures."""
+    c, n, k, r = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
     _check(lib().ptc_plan_shape(int(M), int(N), int(K), int(prec), int(sms), int(caps[0]), int(caps[1]),
-                                int(caps[2]), ctypes.byref(c), ctypes.byref(n), ctypes.byref(k)))
+                                int(caps[2]), ctypes.byref(c), ctypes.byref(n), ctypes.byref(k), ctypes.byref(r)))
+    if with_ring:
+        return c.value, n.value, k.value, bool(r.value)
     return c.value, n.value, k.value
 
 
@@ -212,6 +218,14 @@ def ptc_last_launch() -> tuple[int, int, int, int]:
     g, c, k, n = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
     _check(lib().ptc_last_launch(ctypes.byref(g), ctypes.byref(c), ctypes.byref(k), ctypes.byref(n)))
     return g.value, c.value, k.value, n.value
+
+
+def ptc_last_conversion() -> int:
+    """Operand conversion of the calling thread's last GEMM call: 0 none, 1 a
+    separate pass into a workspace, 2 inside the GEMM kernel."""
+    m = ctypes.c_int(0)
+    _check(lib().ptc_last_conversion(ctypes.byref(m)))
+    return m.value
 
 
 # ---------------------------------------------------------------- torch layer

@@ -44,9 +44,12 @@ std::atomic<int> g_tail_split{1};   // 1: split a short last wave in K
 std::atomic<int> g_split_min_kb{64};
 std::atomic<int> g_pair_stage_kb{2};  // CTA pairs: K blocks per ring stage
 std::atomic<int> g_ksplit{0};         // K-split clusters: 0 by size, 1 never, 2 / 4 / 8 that size
-std::atomic<int> g_tile_n{0};
-std::atomic<int> g_split_reduce{1};   // split tiles of FP32 / int32 C: halves added by TMA reductions         // one-CTA tile width: 0 by size, 64 / 128 / 256 that width
+std::atomic<int> g_tile_n{0};         // one-CTA tile width: 0 by size, 64 / 128 / 256 that width
+std::atomic<int> g_split_reduce{1};   // split tiles of FP32 / int32 C: halves added by TMA reductions
 std::atomic<int> g_pdl{1};            // programmatic stream serialization of the library's kernels
+std::atomic<int> g_in_ring{1};        // integer routes: operands converted in the GEMM kernel's shared
+                                      // memory where estimated faster (0: never, 2: on every one-CTA shape)
+thread_local int g_last_conv = 0;     // operand conversion of this thread's last GEMM call
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 std::atomic<int64_t> g_stall_tile{-1};
 
@@ -132,9 +135,10 @@ EncodeTiledFn encode_fn() {
 
 // 2-D row-major view: `inner` contiguous elements per row, `outer` rows,
 // `pitch` bytes between rows; boxes of box_inner x box_outer elements with the
-// 128-byte swizzle; out-of-range elements of a box read as zero.
+// 128-byte swizzle (or `swizzle`); out-of-range elements of a box read as zero.
 int make_tmap(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t inner,
-              uint64_t outer, uint64_t pitch, uint32_t box_inner, uint32_t box_outer) {
+              uint64_t outer, uint64_t pitch, uint32_t box_inner, uint32_t box_outer,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) {
         std::snprintf(g_msg, sizeof(g_msg), "cuTensorMapEncodeTiled unavailable");
@@ -145,7 +149,7 @@ int make_tmap(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64
     cuuint32_t box[2] = {box_inner, box_outer};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         std::snprintf(g_msg, sizeof(g_msg), "cuTensorMapEncodeTiled failed (CUresult %d)", int(r));
@@ -194,6 +198,7 @@ int fail(int code, const char *text) {
 // cluster size; 0 its size rule).
 struct Shape {
     int ctas, bn, ks;
+    bool ring = false;  // integer routes: operands converted inside the GEMM kernel
 };
 
 // Estimated SM clocks of one CTA's work in a single-wave launch, the quantity
@@ -217,6 +222,26 @@ int64_t est_clocks(int64_t num_kb, int bn, int ks, int esize) {
 
 int64_t tile_count(int64_t M, int64_t N, int rows, int cols) {
     return ((M + rows - 1) / rows) * ((N + cols - 1) / cols);
+}
+
+// Operand conversion of the integer routes (conv 1: s8 -> binary16, 2: packed
+// s4 -> E4M3), in the same SM clocks, fitted to the launch-shape sweep of
+// both paths at N = 512 .. 2048 (CUDA-graph replays; the fit orders the two
+// paths correctly for 70 of 72 single-wave shapes).  A separate pass costs
+// ~2.7 us (its launch, its ramp, the GEMM's wait for it) plus its traffic
+// (64 bytes read and 128 written per row and K block) at ~12 bytes per clock
+// from L2.  In-ring conversion costs ~1.35 us before the first MMA plus, per
+// K block of a CTA, what the eight converting warps add to the K loop (two
+// per scheduler, latency-bound: ncu counts ~2400 instructions per K block of
+// a 256-wide tile issued in 36% of the cycles): ~0.14 / 0.23 / 0.32 us for s8
+// on 64 / 128 / 256-wide tiles, ~2.7 times that for s4, whose lookup takes
+// more instructions per byte.  In ring only in single-wave launches.
+int64_t pass_clocks(int64_t M, int64_t N, int64_t num_kb) { return 5100 + (M + N) * num_kb * 192 / 6300; }
+
+int64_t ring_clocks(int64_t num_kb, int bn, int ks, int conv) {
+    static const int64_t per_kb[2][3] = {{270, 440, 610}, {720, 1240, 1630}};
+    const int w = bn == 64 ? 0 : bn == 128 ? 1 : 2;
+    return 2560 + (num_kb + ks - 1) / ks * per_kb[conv == 2 ? 1 : 0][w];
 }
 
 }  // namespace
@@ -249,34 +274,72 @@ namespace {
 // the integer routes were faster with one CTA per tile).  esize: bytes per C
 // element; fpair / ftile / fks: the knobs cta_pair, tile_n and ksplit, which
 // force parts of the choice; caps: the device's K-split cluster capacities.
-// Pure (host arithmetic only).
+// conv (integer routes that may convert in the ring: 1 s8, 2 packed s4; 0
+// otherwise) adds to each one-CTA candidate the cheaper of the two operand
+// conversions (a separate pass, or in-ring conversion in a single-wave
+// launch); fring is the in_ring knob (0 never in ring, 1 by that estimate,
+// 2 always on one-CTA shapes).  Pure (host arithmetic only).
 Shape plan_shape(int64_t M, int64_t N, int64_t num_kb, int sms, bool f16, int esize, int fpair, int ftile,
-                 int fks, const ptc::ClusterCaps &caps) {
+                 int fks, const ptc::ClusterCaps &caps, int conv = 0, int fring = 0) {
+    const int64_t pass = conv != 0 ? pass_clocks(M, N, num_kb) : 0;
+    // Marks `sh` in-ring when that is allowed and estimated cheaper; returns
+    // the conversion's estimated clocks.
+    auto conversion = [&](Shape &sh, int64_t tiles) -> int64_t {
+        sh.ring = false;
+        if (conv == 0 || fring == 0 || sh.ctas != 1) return pass;
+        if (fring == 2) {
+            sh.ring = true;
+            return 0;
+        }
+        if (tiles * sh.ks > sms) return pass;  // several tiles per CTA: the pass
+        const int64_t r = ring_clocks(num_kb, sh.bn, sh.ks, conv);
+        sh.ring = r < pass;
+        return sh.ring ? r : pass;
+    };
     if (fpair == 2) return {2, ptc::kBN, 1};
-    if ((ftile == 64 || ftile == 128) && tile_count(M, N, ptc::kBM, ftile) <= (int64_t(1) << 20))
-        return {1, ftile, (fks == 2 || fks == 4) ? fks : 1};
-    if (fpair == 1) return {1, ptc::kBN, fks};
+    if ((ftile == 64 || ftile == 128) && tile_count(M, N, ptc::kBM, ftile) <= (int64_t(1) << 20)) {
+        Shape sh{1, ftile, (fks == 2 || fks == 4) ? fks : 1};
+        conversion(sh, tile_count(M, N, ptc::kBM, ftile));
+        return sh;
+    }
     const int64_t t256 = tile_count(M, N, ptc::kBM, ptc::kBN);
+    if (fpair == 1) {
+        Shape sh{1, ptc::kBN, fks};
+        Shape est = sh;  // the K-split the launcher will pick, for the estimate
+        est.ks = (fks == 1 || 2 * t256 > sms) ? 1 : ptc::pick_ksplit_pure(int(t256), int(num_kb), fks, sms, caps);
+        conversion(est, t256);
+        sh.ring = est.ring;
+        return sh;
+    }
     if (t256 >= sms) return {2, ptc::kBN, 1};
     Shape best{1, ptc::kBN, 1};
-    int64_t best_c = est_clocks(num_kb, ptc::kBN, 1, esize);
+    int64_t best_c = est_clocks(num_kb, ptc::kBN, 1, esize) + conversion(best, t256);
     if (fks != 1) {
         const int ks = ptc::pick_ksplit_pure(int(t256), int(num_kb), fks, sms, caps);
-        if (ks > 1 && (fks != 0 || est_clocks(num_kb, ptc::kBN, ks, esize) < best_c)) {
-            best = {1, ptc::kBN, ks};
-            best_c = fks != 0 ? 0 : est_clocks(num_kb, ptc::kBN, ks, esize);
+        if (ks > 1) {
+            Shape sh{1, ptc::kBN, ks};
+            const int64_t c = est_clocks(num_kb, ptc::kBN, ks, esize) + conversion(sh, t256);
+            if (fks != 0 || c < best_c) {
+                best = sh;
+                best_c = fks != 0 ? 0 : c;
+            }
         }
     }
     for (int bn : {128, 64}) {
         const int64_t tiles = tile_count(M, N, ptc::kBM, bn);
         if (ftile != 0 || tiles > sms) continue;
-        // whole narrow tiles, or K-split clusters of 2 / 4 of them
+        // whole narrow tiles, or K-split clusters of 2 / 4 of them (at least
+        // two K blocks per CTA; one with in-ring conversion, where the split
+        // shortens the conversion too: measured fastest for INT4 at N = 512)
         for (int ks : {1, 2, 4}) {
-            if (ks > 1 && (fks == 1 || (fks != 0 && fks != ks) || num_kb < 2 * ks || tiles > caps.of(ks)))
+            if (ks > 1 && (fks == 1 || (fks != 0 && fks != ks) || num_kb < ks || tiles > caps.of(ks)))
                 continue;
-            const int64_t c = est_clocks(num_kb, bn, ks, esize);
+            Shape sh{1, bn, ks};
+            const int64_t conv_c = conversion(sh, tiles);
+            if (ks > 1 && num_kb < 2 * ks && !sh.ring) continue;
+            const int64_t c = est_clocks(num_kb, bn, ks, esize) + conv_c;
             if (c < best_c) {
-                best = {1, bn, ks};
+                best = sh;
                 best_c = c;
             }
         }
@@ -285,9 +348,9 @@ Shape plan_shape(int64_t M, int64_t N, int64_t num_kb, int sms, bool f16, int es
     return best;
 }
 
-Shape choose_shape(int64_t M, int64_t N, int64_t num_kb, int sms, bool f16, int esize) {
+Shape choose_shape(int64_t M, int64_t N, int64_t num_kb, int sms, bool f16, int esize, int conv = 0) {
     return plan_shape(M, N, num_kb, sms, f16, esize, g_cta_pair.load(), g_tile_n.load(), g_ksplit.load(),
-                      ptc::cluster_caps(sms));
+                      ptc::cluster_caps(sms), conv, g_in_ring.load());
 }
 
 GemmArgs base_args(int64_t M, int64_t N, int64_t K, int k_elems_per_block, void *C, int64_t ldc,
@@ -361,6 +424,7 @@ namespace {
 // EPI_F32 (FP32 accumulators, FP32 C) or EPI_F16ACC (FP16 accumulators, FP16 C).
 int f16_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B, int64_t ldb,
              void *C, int64_t ldc, int epi, void *stream) {
+    g_last_conv = 0;
     int rc = check_sizes(M, N, K);
     if (rc) return rc;
     if (M == 0 || N == 0) return PTC_OK;
@@ -423,6 +487,7 @@ int out_bytes(int mode) { return (mode == ptc::OUT_BF16 || mode == ptc::OUT_F16)
 int int_gemm(bool s4, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
              int64_t ldb, void *C, int64_t ldc, int mode, const float *sa, const float *sb,
              void *stream) {
+    g_last_conv = 0;
     int rc = check_sizes(M, N, K);
     if (rc) return rc;
     if (M == 0 || N == 0) return PTC_OK;
@@ -453,13 +518,41 @@ int int_gemm(bool s4, int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     if ((rc = current_device(&dev, &d))) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (K == 0) return zero_c(C, ldc, M, N, eb, *d, s);
+
+    const int k_elems = s4 ? 128 : 64;  // elements per 128-byte K block
+    const int wsize = s4 ? 1 : 2;       // workspace bytes per element
+    const int64_t ldw = round_up(K, k_elems);
+    // In-ring conversion (chosen with the shape, for one-CTA shapes): the
+    // kernel loads K blocks of the raw operands (64 bytes per row: 64 s8 or
+    // 128 packed s4; zeros past K) and converts them in shared memory, with no
+    // workspace and no separate pass.  Packed s4 needs an even K (no stray
+    // high nibble).
+    const int conv = s4 ? (K % 2 == 0 ? 2 : 0) : 1;
+    const Shape sh = choose_shape(M, N, ldw / k_elems, d->sms, false, eb, conv);
+    const int chunk = s4 ? g_chunk_s4.load() : g_chunk_s8.load();
+    if (sh.ring) {
+        const uint64_t kbytes = uint64_t(s4 ? K / 2 : K);
+        CUtensorMap ta, tb;
+        rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, A, kbytes, uint64_t(M), uint64_t(s4 ? lda / 2 : lda), 64,
+                       ptc::kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (!rc)
+            rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, kbytes, uint64_t(N), uint64_t(s4 ? ldb / 2 : ldb),
+                           64, uint32_t(sh.bn), CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (rc) return rc;
+        GemmArgs args = base_args(M, N, K, k_elems, C, ldc, sh);
+        args.kb_per_chunk = chunk > 0 ? chunk : 1;
+        args.out_mode = mode;
+        args.scale_a = sa;
+        args.scale_b = sb;
+        args.in_ring = 1;
+        rc = launch_gemm_checked(s4 ? Kind::E4M3 : Kind::F16, false, ptc::EPI_INT, 1, ta, tb, args, *d, s);
+        if (!rc) g_last_conv = 2;
+        return rc;
+    }
     if (!d->pool_ok) return fail(PTC_ERR_ALLOC, "workspace memory pool unavailable");
 
     // Workspace: A and B as rows of K in the MMA input type (binary16 for
     // INT8, E4M3 for INT4), pitch rounded to 128 bytes, blocks 1024-aligned.
-    const int k_elems = s4 ? 128 : 64;  // elements per 128-byte K block
-    const int wsize = s4 ? 1 : 2;       // workspace bytes per element
-    const int64_t ldw = round_up(K, k_elems);
     const int64_t a_bytes = round_up(M * ldw * wsize, 1024);
     const int64_t b_bytes = round_up(N * ldw * wsize, 1024);
     void *ws = nullptr;
@@ -485,19 +578,18 @@ int int_gemm(bool s4, int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
         rc = fail_cuda(e, "operand conversion launch");
     else
         g_launches.fetch_add(1);
-    const Shape sh = choose_shape(M, N, ldw / k_elems, d->sms, false, eb);
     const CUtensorMapDataType dt = s4 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     CUtensorMap ta, tb;
     if (!rc) rc = make_tmap(&ta, dt, aw, K, M, uint64_t(ldw) * wsize, k_elems, ptc::kBM);
     if (!rc) rc = make_tmap(&tb, dt, bw, K, N, uint64_t(ldw) * wsize, k_elems, sh.bn / sh.ctas);
     if (!rc) {
         GemmArgs args = base_args(M, N, K, k_elems, C, ldc, sh);
-        const int ch = s4 ? g_chunk_s4.load() : g_chunk_s8.load();
-        args.kb_per_chunk = ch > 0 ? ch : 1;
+        args.kb_per_chunk = chunk > 0 ? chunk : 1;
         args.out_mode = mode;
         args.scale_a = sa;
         args.scale_b = sb;
         rc = launch_gemm_checked(s4 ? Kind::E4M3 : Kind::F16, false, ptc::EPI_INT, sh.ctas, ta, tb, args, *d, s);
+        if (!rc) g_last_conv = 1;
     }
     cudaFreeAsync(ws, s);
     return rc;
@@ -508,6 +600,7 @@ int int_gemm(bool s4, int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
 // same layout as gemm_f16's B).
 int s8_rowb_gemm(int64_t M, int64_t N, int64_t K, const int8_t *A, int64_t lda, const int8_t *B, int64_t ldb,
                  int32_t *C, int64_t ldc, void *stream) {
+    g_last_conv = 0;
     int rc = check_sizes(M, N, K);
     if (rc) return rc;
     if (M == 0 || N == 0) return PTC_OK;
@@ -561,6 +654,7 @@ int s8_rowb_gemm(int64_t M, int64_t N, int64_t K, const int8_t *A, int64_t lda, 
         args.kb_per_chunk = ch > 0 ? ch : 1;
         args.out_mode = ptc::OUT_S32;
         rc = launch_gemm_checked(Kind::F16, true, ptc::EPI_INT, sh.ctas, ta, tb, args, *d, s);
+        if (!rc) g_last_conv = 1;
     }
     cudaFreeAsync(ws, s);
     return rc;
@@ -613,6 +707,7 @@ struct EventSet {
 // the stream waits for the last copy.  prec: 0 FP16, 1 INT8, 2 packed INT4.
 int host_gemm(int prec, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
               int64_t ldb, void *C, int64_t ldc, void *stream) {
+    g_last_conv = 0;
     int rc = check_sizes(M, N, K);
     if (rc) return rc;
     if (M == 0 || N == 0) return PTC_OK;
@@ -921,7 +1016,7 @@ int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile) {
 }
 
 int ptc_plan_shape(int64_t M, int64_t N, int64_t K, int prec, int sms, int cap2, int cap4, int cap8, int *ctas,
-                   int *tile_n, int *ksplit) {
+                   int *tile_n, int *ksplit, int *in_ring) {
     if (!ctas || !tile_n || !ksplit) return fail(PTC_ERR_INVALID, "NULL pointer");
     if (prec < 0 || prec > 2 || sms <= 0 || cap2 < 0 || cap4 < 0 || cap8 < 0 || M <= 0 || N <= 0 || K <= 0)
         return fail(PTC_ERR_INVALID, "precision, SM count, capacities or sizes out of range");
@@ -932,8 +1027,9 @@ int ptc_plan_shape(int64_t M, int64_t N, int64_t K, int prec, int sms, int cap2,
     caps.c4 = cap4;
     caps.c8 = cap8;
     const int64_t num_kb = (K + (prec == 2 ? 127 : 63)) / (prec == 2 ? 128 : 64);
+    const int conv = prec == 1 ? 1 : (prec == 2 && K % 2 == 0) ? 2 : 0;
     Shape sh = plan_shape(M, N, num_kb, sms, prec == 0, 4, g_cta_pair.load(), g_tile_n.load(), g_ksplit.load(),
-                          caps);
+                          caps, conv, g_in_ring.load());
     // what the launcher then runs for one-CTA tiles
     if (sh.ctas == 1 && sh.bn == ptc::kBN) {
         sh.ks = ptc::pick_ksplit_pure(int(tile_count(M, N, ptc::kBM, ptc::kBN)), int(num_kb), sh.ks, sms, caps);
@@ -944,12 +1040,19 @@ int ptc_plan_shape(int64_t M, int64_t N, int64_t K, int prec, int sms, int cap2,
     *ctas = sh.ctas;
     *tile_n = sh.bn;
     *ksplit = sh.ks < 1 ? 1 : sh.ks;
+    if (in_ring) *in_ring = sh.ring ? 1 : 0;
     return PTC_OK;
 }
 
 int ptc_last_launch(int *grid, int *cluster, int *ksplit, int *tile_n) {
     if (!grid || !cluster || !ksplit || !tile_n) return fail(PTC_ERR_INVALID, "NULL pointer");
     ptc::last_launch(grid, cluster, ksplit, tile_n);
+    return PTC_OK;
+}
+
+int ptc_last_conversion(int *mode) {
+    if (!mode) return fail(PTC_ERR_INVALID, "NULL pointer");
+    *mode = g_last_conv;
     return PTC_OK;
 }
 
@@ -997,6 +1100,10 @@ int ptc_set_tuning(const char *key, int64_t value) {
     }
     if (std::strcmp(key, "pdl") == 0 && (value == 0 || value == 1)) {
         g_pdl.store(int(value));
+        return PTC_OK;
+    }
+    if (std::strcmp(key, "in_ring") == 0 && value >= 0 && value <= 2) {
+        g_in_ring.store(int(value));
         return PTC_OK;
     }
     if (std::strcmp(key, "cta_pair") == 0 && value >= 0 && value <= 2) {

@@ -17,73 +17,11 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "convert.cuh"
 #include "ptx.cuh"
 
 namespace ptc {
 namespace {
-
-// ---------------------------------------------------------------- s8 -> f16
-// Four int8 lanes -> four binary16 lanes without a conversion per element:
-// flipping the sign bit maps v to u = v + 128 in [0, 255]; the binary16 with
-// bit pattern 0x6400 | u is exactly 1024 + u (exponent 2^10, unit spacing);
-// subtracting 1152 = 1024 + 128 leaves v exactly.
-__device__ __forceinline__ void s8x4_to_f16x4(uint32_t x, uint32_t &lo, uint32_t &hi) {
-    const uint32_t u = x ^ 0x80808080u;
-    const uint32_t p01 = __byte_perm(u, 0x64646464u, 0x4140);
-    const uint32_t p23 = __byte_perm(u, 0x64646464u, 0x4342);
-    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
-    const __half2 r01 = __hsub2(*reinterpret_cast<const __half2 *>(&p01), bias);
-    const __half2 r23 = __hsub2(*reinterpret_cast<const __half2 *>(&p23), bias);
-    lo = *reinterpret_cast<const uint32_t *>(&r01);
-    hi = *reinterpret_cast<const uint32_t *>(&r23);
-}
-
-__device__ __forceinline__ uint16_t s8_to_f16_bits(int8_t v) {
-    return __half_as_ushort(__int2half_rn(static_cast<int>(v)));
-}
-
-// ---------------------------------------------------------------- s4 -> e4m3
-// E4M3 (sign, 4 exponent bits with bias 7, 3 fraction bits) encoding of a
-// small integer, from the format's definition: |v| = 2^e * (1 + f/8).
-__host__ __device__ constexpr uint32_t e4m3_of_int(int v) {
-    const uint32_t sign = v < 0 ? 0x80u : 0u;
-    const int a = v < 0 ? -v : v;
-    if (a == 0) return sign;
-    int e = 0;
-    while ((a >> (e + 1)) != 0) ++e;            // e = floor(log2 a)
-    const uint32_t frac = uint32_t((a << 3) >> e) - 8u;  // exact for a <= 15
-    return sign | (uint32_t(e + 7) << 3) | frac;
-}
-
-// Byte i of the four lookup words is the E4M3 encoding of the two's-complement
-// nibble i (0..7 -> 0..7, 8..15 -> -8..-1).
-__host__ __device__ constexpr uint32_t lut_word(int first) {
-    uint32_t w = 0;
-    for (int i = 0; i < 4; ++i) {
-        const int nib = first + i;
-        w |= e4m3_of_int(nib >= 8 ? nib - 16 : nib) << (8 * i);
-    }
-    return w;
-}
-constexpr uint32_t LUT0 = lut_word(0), LUT1 = lut_word(4), LUT2 = lut_word(8), LUT3 = lut_word(12);
-static_assert(e4m3_of_int(1) == 0x38 && e4m3_of_int(7) == 0x4E && e4m3_of_int(-8) == 0xD0,
-              "E4M3 encoding");
-
-// Four packed s4 (16 bits, element j in bits 4j..4j+3) -> four E4M3 bytes.
-// The nibbles are exactly the byte selectors of PRMT: the low three bits pick
-// a byte of the 8-entry half-table, bit 3 picks the half.
-__device__ __forceinline__ uint32_t s4x4_to_e4m3x4(uint32_t sel16) {
-    const uint32_t idx = sel16 & 0x7777u;
-    const uint32_t pos = __byte_perm(LUT0, LUT1, idx);
-    const uint32_t neg = __byte_perm(LUT2, LUT3, idx);
-    const uint32_t t = (sel16 >> 3) & 0x1111u;  // bit 3 of each nibble at bit 4j
-    const uint32_t m = ((t & 1u) | ((t & 0x10u) << 4) | ((t & 0x100u) << 8) | ((t & 0x1000u) << 12)) * 0xFFu;
-    return (pos & ~m) | (neg & m);
-}
-
-__device__ __forceinline__ uint8_t s4_to_e4m3_byte(uint32_t nib) {
-    return static_cast<uint8_t>(s4x4_to_e4m3x4(nib & 0xFu) & 0xFFu);
-}
 
 // The two conversions, as element types, 16-byte input vectors and a
 // vector / scalar conversion.
@@ -92,12 +30,7 @@ struct S8ToF16 {
     using Out = uint16_t;
     static constexpr int VEC = 16;  // elements per 16-byte input vector (32 output bytes)
     __device__ static const uint8_t *row_at(const uint8_t *row, int c0) { return row + c0; }
-    __device__ static void vector(const uint4 &x, uint4 &o0, uint4 &o1) {
-        s8x4_to_f16x4(x.x, o0.x, o0.y);
-        s8x4_to_f16x4(x.y, o0.z, o0.w);
-        s8x4_to_f16x4(x.z, o1.x, o1.y);
-        s8x4_to_f16x4(x.w, o1.z, o1.w);
-    }
+    __device__ static void vector(const uint4 &x, uint4 &o0, uint4 &o1) { cvt_s8_f16_x16(x, o0, o1); }
     __device__ static void scalar(const uint8_t *s, Out *d, int n) {
         for (int j = 0; j < n; ++j) d[j] = s8_to_f16_bits(static_cast<int8_t>(s[j]));
     }
@@ -107,12 +40,7 @@ struct S4ToE4M3 {
     using Out = uint8_t;
     static constexpr int VEC = 32;  // packed: 32 elements per 16-byte input vector (32 output bytes)
     __device__ static const uint8_t *row_at(const uint8_t *row, int c0) { return row + c0 / 2; }
-    __device__ static void vector(const uint4 &x, uint4 &o0, uint4 &o1) {
-        o0 = make_uint4(s4x4_to_e4m3x4(x.x & 0xFFFFu), s4x4_to_e4m3x4(x.x >> 16), s4x4_to_e4m3x4(x.y & 0xFFFFu),
-                        s4x4_to_e4m3x4(x.y >> 16));
-        o1 = make_uint4(s4x4_to_e4m3x4(x.z & 0xFFFFu), s4x4_to_e4m3x4(x.z >> 16), s4x4_to_e4m3x4(x.w & 0xFFFFu),
-                        s4x4_to_e4m3x4(x.w >> 16));
-    }
+    __device__ static void vector(const uint4 &x, uint4 &o0, uint4 &o1) { cvt_s4_e4m3_x32(x, o0, o1); }
     __device__ static void scalar(const uint8_t *s, Out *d, int n) {
         for (int j = 0; j < n; ++j) {
             const uint32_t b = s[j >> 1];

@@ -69,7 +69,9 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <type_traits>
 
+#include "convert.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -91,11 +93,20 @@ constexpr int KSTEPS = kRowBytes / KSTEP_BYTES; // MMAs per stage
 // stages of two K blocks (64 KiB each) by default or 7 stages of one K block
 // (32 KiB each): two-block stages take half as many barrier round trips per
 // byte and measured 3-6% faster.
+//
+// In-ring conversion (FU, one-CTA integer launches): the producer loads K
+// blocks of the raw operands (64 bytes per row: 64 s8 or 128 packed s4) into
+// a second ring of the same depth, and the epilogue warps, idle during the K
+// loop, convert each into the MMA ring stage.  Both rings fit 216 KiB: 6
+// stages for 64-wide tiles, 4 for 128-wide, 3 for 256-wide.
 constexpr int kRing1 = 4 * (kBM + kBN) * kRowBytes;  // one-CTA ring bytes
-template <int CTAS, int SUBK, int BN>
+constexpr int kRingFu = 216 * 1024;                  // both rings, in-ring conversion
+constexpr int kRawRow = 64;                          // raw operand bytes per row and K block
+template <int CTAS, int SUBK, int BN, bool FU = false>
 struct Cfg {
     static_assert(CTAS == 2 || SUBK == 1, "one CTA stages one K block at a time");
     static_assert(BN == kBN || (CTAS == 1 && (BN == 64 || BN == 128)), "narrow tiles are one-CTA tiles");
+    static_assert(!FU || CTAS == 1, "in-ring conversion in one-CTA launches");
     static constexpr int SUB = SUBK;  // K blocks per stage
     static constexpr int B_ROWS = BN / CTAS;
     static constexpr int A_BLOCK = kBM * kRowBytes;     // one K block of A
@@ -103,14 +114,19 @@ struct Cfg {
     static constexpr int A_STAGE = SUB * A_BLOCK;
     static constexpr int B_STAGE = SUB * B_BLOCK;
     static constexpr int STAGE = A_STAGE + B_STAGE;
-    static constexpr int STAGES = CTAS == 1 ? kRing1 / STAGE : (SUBK == 1 ? 7 : 3);
+    static constexpr int RAW_A = FU ? kBM * kRawRow : 0;          // raw A rows of a stage
+    static constexpr int RAW_STAGE = FU ? (kBM + BN) * kRawRow : 0;  // raw A, then raw B
+    static constexpr int STAGES = FU ? kRingFu / (STAGE + RAW_STAGE) : CTAS == 1 ? kRing1 / STAGE : (SUBK == 1 ? 7 : 3);
+    static constexpr int RING = STAGES * (STAGE + RAW_STAGE);        // bytes of both rings
     static constexpr int TMEM_COLS = 2 * BN;  // two accumulators of BN columns
 };
 
 template <int STAGES, int SUB>
 struct SharedTail {
-    uint64_t full[STAGES * SUB];  // per K block of a stage: its operands have landed
+    uint64_t full[STAGES * SUB];  // per K block of a stage: its operands have landed (or been converted)
     uint64_t empty[STAGES];       // per stage: its MMAs have read it
+    uint64_t rfull[STAGES];       // in-ring conversion: the raw stage has landed
+    uint64_t rempty[STAGES];      // ... and has been read by the converting warps
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
@@ -124,14 +140,22 @@ struct SharedTail {
 constexpr int kStageC = 32 * 32 * 4;
 constexpr int kStageWarp = 4 * kStageC;
 
-template <int CTAS, int SUBK, int BN = kBN>
+template <int CTAS, int SUBK, int BN = kBN, bool FU = false>
 constexpr size_t smem_bytes() {
-    return 1024 + size_t(Cfg<CTAS, SUBK, BN>::STAGES) * Cfg<CTAS, SUBK, BN>::STAGE +
-           sizeof(SharedTail<Cfg<CTAS, SUBK, BN>::STAGES, SUBK>);
+    return 1024 + size_t(Cfg<CTAS, SUBK, BN, FU>::RING) + sizeof(SharedTail<Cfg<CTAS, SUBK, BN, FU>::STAGES, SUBK>);
 }
 static_assert(smem_bytes<1, 1>() <= 232448 && smem_bytes<2, 1>() <= 232448 && smem_bytes<2, 2>() <= 232448 &&
-                  smem_bytes<1, 1, 128>() <= 232448 && smem_bytes<1, 1, 64>() <= 232448,
+                  smem_bytes<1, 1, 128>() <= 232448 && smem_bytes<1, 1, 64>() <= 232448 &&
+                  smem_bytes<1, 1, kBN, true>() <= 232448 && smem_bytes<1, 1, 128, true>() <= 232448 &&
+                  smem_bytes<1, 1, 64, true>() <= 232448,
               "shared memory budget");
+static_assert(Cfg<1, 1, 64, true>::STAGES == 6 && Cfg<1, 1, 128, true>::STAGES == 4 &&
+                  Cfg<1, 1, kBN, true>::STAGES == 3,
+              "in-ring conversion depths");
+// The ring staging of C and of K-split partial sums spans the first 128 KiB.
+static_assert(Cfg<1, 1, 64, true>::RING >= EPI_WARPS * kStageWarp && Cfg<1, 1, kBN, true>::RING >= kBM * kBN * 4 &&
+                  Cfg<1, 1, 128, true>::RING >= EPI_WARPS * kStageWarp,
+              "the rings hold the C staging and the partial sums");
 // A K-split cluster's partial sums: 128 rows of BN four-byte values, row r at
 // r * 4 BN bytes, its 16-byte piece j at piece j ^ (r & 7) (the writers, one
 // row per lane, and the readers, one piece per lane, do not conflict).
@@ -649,16 +673,17 @@ __device__ __forceinline__ void ksplit_complete(const GemmArgs &args, int mb, in
 // its full barriers collect both CTAs' copies, its commits arrive on both
 // CTAs' empty / accumulator-full barriers, and both CTAs' epilogues release
 // accumulator buffers on its acc_empty barriers.
-template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN>
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false>
 __global__ void __launch_bounds__(THREADS, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
     static_assert(!(B_MN && KIND == Kind::E4M3), "MN-major B is used by the FP16 path only");
     static_assert(KS == 1 || CTAS == 1, "K-split clusters of one-CTA tiles");
+    static_assert(!FU || (CTAS == 1 && EPI == EPI_INT && !B_MN), "in-ring conversion: one-CTA integer launches");
     constexpr bool INT_OUT = EPI == EPI_INT;
     constexpr int HALF = BN / 2;      // columns of an epilogue warp's slice
     constexpr int NCH = HALF / 32;    // 32-column chunks of a slice
-    using C_ = Cfg<CTAS, SUBK, BN>;
+    using C_ = Cfg<CTAS, SUBK, BN, FU>;
     constexpr int TMEM_COLS = C_::TMEM_COLS;
     constexpr int STAGES = C_::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -667,8 +692,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t *smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
     uint8_t *a_ring = smem;
     uint8_t *b_ring = smem + STAGES * C_::A_STAGE;
+    uint8_t *raw_ring = smem + STAGES * C_::STAGE;  // in-ring conversion only
     using Tail = SharedTail<STAGES, C_::SUB>;
-    Tail *st = reinterpret_cast<Tail *>(smem + STAGES * C_::STAGE);
+    Tail *st = reinterpret_cast<Tail *>(smem + C_::RING);
 
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
@@ -682,8 +708,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            for (int sb = 0; sb < C_::SUB; ++sb) mbar_init(&st->full[s * C_::SUB + sb], 1);
+            // In-ring conversion: a stage is full once every epilogue warp has
+            // converted its share of the raw stage into it.
+            for (int sb = 0; sb < C_::SUB; ++sb) mbar_init(&st->full[s * C_::SUB + sb], FU ? EPI_WARPS : 1);
             mbar_init(&st->empty[s], 1);
+            mbar_init(&st->rfull[s], 1);
+            mbar_init(&st->rempty[s], EPI_WARPS);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&st->acc_full[b], 1);
@@ -734,7 +764,9 @@ __global__ void __launch_bounds__(THREADS, 1)
                 const int m0 = wr.mb * (kBM * CTAS) + int(rank) * kBM;
                 const int n0 = wr.nb * BN + int(rank) * C_::B_ROWS;
                 for (int kb = wr.kb0; kb < wr.kb1; kb += C_::SUB) {
-                    if (!mbar_wait(&st->empty[s], ph ^ 1u, &st->abort, &g_error_word, limit)) {
+                    // The stage is free once its MMAs (in-ring conversion: its
+                    // converting warps) have read it.
+                    if (!mbar_wait(FU ? &st->rempty[s] : &st->empty[s], ph ^ 1u, &st->abort, &g_error_word, limit)) {
                         ok = false;
                         break;
                     }
@@ -743,7 +775,20 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (!stall) {
                         uint8_t *a_dst = a_ring + s * C_::A_STAGE;
                         uint8_t *b_dst = b_ring + s * C_::B_STAGE;
-                        if constexpr (CTAS == 1) {
+                        if constexpr (FU) {
+                            // Raw K block: 128 rows of A, then BN rows of B, 64 bytes each.
+                            uint8_t *r_dst = raw_ring + s * C_::RAW_STAGE;
+                            mbar_arrive_expect_tx(&st->rfull[s], C_::RAW_STAGE);
+                            if (hint) {
+                                tma_load_2d_hint(r_dst, &tmA, &st->rfull[s], kb * kRawRow, m0, pol_a);
+                                tma_load_2d_hint(r_dst + C_::RAW_A, &tmB, &st->rfull[s], kb * kRawRow, n0, pol_b);
+                            } else {
+                                tma_load_2d(r_dst, &tmA, &st->rfull[s], kb * kRawRow, m0);
+                                tma_load_2d(r_dst + C_::RAW_A, &tmB, &st->rfull[s], kb * kRawRow, n0);
+                            }
+                            outstanding |= 1u << s;
+                            out_phase = (out_phase & ~(1u << s)) | (ph << s);
+                        } else if constexpr (CTAS == 1) {
                             mbar_arrive_expect_tx(&st->full[s], C_::STAGE);
                             auto load = [&](void *dst, const CUtensorMap *map, int x, int y, uint64_t pol) {
                                 if (hint)
@@ -801,7 +846,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if constexpr (CTAS == 1) {
                     for (int q = 0; q < STAGES; ++q)
                         if (outstanding & (1u << q))
-                            mbar_wait(&st->full[q], (out_phase >> q) & 1u, nullptr, nullptr, limit);
+                            mbar_wait(FU ? &st->rfull[q] : &st->full[q], (out_phase >> q) & 1u, nullptr, nullptr, limit);
                 } else {
                     pause_ns(200000);  // copies complete on the even CTA's barrier: allow 200 us
                 }
@@ -914,6 +959,64 @@ __global__ void __launch_bounds__(THREADS, 1)
         int abuf = 0;
         uint32_t aph = 0;
         bool ok = true;
+        // In-ring conversion of K blocks [kb0, kb1) (the producer's and the MMA
+        // issuer's sequence of stages): each thread converts (128 + BN) / 64
+        // 16-byte raw pieces (row g = i / 4, piece p = i % 4 of 64 bytes) into
+        // the 16-byte chunks 2p and 2p + 1 of row g of the MMA stage, placed
+        // by the 128-byte swizzle (chunk j of row g at j ^ (g & 7)); the raw
+        // reads are contiguous and each quarter-warp's writes cover eight
+        // distinct chunks of two rows, so neither conflicts.  The writes reach
+        // the tensor cores through a proxy fence before the stage's barrier.
+        // (WIDE: all pieces of a thread in flight at once; the narrow form,
+        // one piece at a time, serves while the int32 sums occupy registers.)
+        int cs = 0;
+        uint32_t cph = 0;
+        auto convert = [&](int kb0, int kb1, auto wide) -> bool {
+            constexpr bool WIDE = decltype(wide)::value;
+            const int ctid = int(threadIdx.x) - 64;
+            for (int kb = kb0; kb < kb1; ++kb) {
+                if (!warp_wait(&st->rfull[cs], cph, &st->abort, limit, lane)) return false;
+                if (!warp_wait(&st->empty[cs], cph ^ 1u, &st->abort, limit, lane)) return false;
+                // Every lane observes both completed phases before its accesses.
+                mbar_try_wait(&st->rfull[cs], cph);
+                mbar_try_wait(&st->empty[cs], cph ^ 1u);
+                const uint32_t raw = smem_u32(raw_ring) + uint32_t(cs * C_::RAW_STAGE);
+                const uint32_t dst_a = smem_u32(a_ring) + uint32_t(cs * C_::A_STAGE);
+                const uint32_t dst_b = smem_u32(b_ring) + uint32_t(cs * C_::B_STAGE);
+                auto piece = [&](int it) {
+                    const int i = it * 256 + ctid;
+                    const int g = i >> 2, p = i & 3;
+                    const uint4 x = ld_shared_v4(raw + uint32_t(i) * 16u);
+                    uint4 o0, o1;
+                    if constexpr (KIND == Kind::F16)
+                        cvt_s8_f16_x16(x, o0, o1);
+                    else
+                        cvt_s4_e4m3_x32(x, o0, o1);
+                    // Pieces 0 .. 511 are A's 128 rows (it = 0, 1), the rest B's.
+                    const uint32_t row = it < 2 ? dst_a + uint32_t(g) * 128u : dst_b + uint32_t(g - kBM) * 128u;
+                    st_shared_v4(row + (uint32_t((2 * p) ^ (g & 7)) << 4), o0.x, o0.y, o0.z, o0.w);
+                    st_shared_v4(row + (uint32_t((2 * p + 1) ^ (g & 7)) << 4), o1.x, o1.y, o1.z, o1.w);
+                };
+                if constexpr (WIDE) {
+#pragma unroll
+                    for (int it = 0; it < (kBM + BN) / 64; ++it) piece(it);
+                } else {
+#pragma unroll 1
+                    for (int it = 0; it < (kBM + BN) / 64; ++it) piece(it);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&st->full[cs]);
+                    mbar_arrive(&st->rempty[cs]);
+                }
+                if (++cs == STAGES) {
+                    cs = 0;
+                    cph ^= 1u;
+                }
+            }
+            return true;
+        };
         if (CTAS == 2 && args.split_reduce && cluster < args.num_vunits) {
             // This cluster's last unit is the first K half of a split tile: zero
             // the tile's C (each warp its 32 x 128 slice) before the K loops run,
@@ -945,10 +1048,26 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int row = wr.mb * (kBM * CTAS) + int(rank) * kBM + 32 * q + lane;
             const int col0 = wr.nb * BN + h * HALF;
             if constexpr (INT_OUT) {
+                const int nchunks = (wr.kb1 - wr.kb0 + args.kb_per_chunk - 1) / args.kb_per_chunk;
+                // In-ring conversion of chunk c (its K blocks) precedes the fold
+                // of chunk c, and the fold of chunk c precedes the conversion of
+                // chunk c + 2, whose MMAs reuse chunk c's accumulator buffer:
+                // chunks 0 and 1 are converted first (while the int32 sums below
+                // hold nothing), then chunk c + 2 after each fold c.
+                auto convert_chunk = [&](int c, auto wide) {
+                    const int c0 = wr.kb0 + c * args.kb_per_chunk;
+                    return convert(c0, min(wr.kb1, c0 + args.kb_per_chunk), wide);
+                };
+                if constexpr (FU) {
+                    if ((nchunks > 0 && !convert_chunk(0, std::true_type{})) ||
+                        (nchunks > 1 && !convert_chunk(1, std::true_type{}))) {
+                        ok = false;
+                        break;
+                    }
+                }
                 int32_t acc[HALF];
 #pragma unroll
                 for (int j = 0; j < HALF; ++j) acc[j] = 0;
-                const int nchunks = (wr.kb1 - wr.kb0 + args.kb_per_chunk - 1) / args.kb_per_chunk;
                 for (int ch = 0; ch < nchunks; ++ch) {
                     if (!warp_wait(&st->acc_full[abuf], aph, &st->abort, limit, lane)) {
                         ok = false;
@@ -967,6 +1086,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if (++abuf == 2) {
                         abuf = 0;
                         aph ^= 1u;
+                    }
+                    if constexpr (FU) {
+                        if (ch + 2 < nchunks && !convert_chunk(ch + 2, std::false_type{})) {
+                            ok = false;
+                            break;
+                        }
                     }
                 }
                 if (!ok) break;
@@ -1173,12 +1298,12 @@ thread_local LastLaunch g_last;
 
 // Launch shape of one variant: dynamic shared memory, cluster dimension and
 // (optionally) programmatic stream serialization.
-template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN>
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false>
 void launch_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[2], bool pdl, cudaStream_t stream) {
     std::memset(&cfg, 0, sizeof(cfg));
     std::memset(attr, 0, sizeof(attr));
     cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = smem_bytes<CTAS, SUBK, BN>();
+    cfg.dynamicSmemBytes = smem_bytes<CTAS, SUBK, BN, FU>();
     cfg.stream = stream;
     cfg.attrs = attr;
     int n = 0;
@@ -1199,22 +1324,22 @@ void launch_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[2], bool
 
 // Clusters of the variant that can be resident at once on the current device
 // (cached per device; the shared-memory opt-in is set on first use).
-template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN>
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false>
 cudaError_t cluster_capacity(int sms, int *out) {
-    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS, SUBK, KS, BN>;
+    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU>;
     constexpr int CL = CTAS * KS;
     static thread_local LaunchCache cache;  // per device (re-queried when it changes)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev != cache.dev) {
-        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes<CTAS, SUBK, BN>()));
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem_bytes<CTAS, SUBK, BN, FU>()));
         if (e != cudaSuccess) return e;
         int clusters = sms / CL;
         if constexpr (CL > 1) {
             cudaLaunchConfig_t cfg;
             cudaLaunchAttribute attr[2];
-            launch_config<KIND, B_MN, EPI, CTAS, SUBK, KS, BN>(cfg, attr, false, nullptr);
+            launch_config<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU>(cfg, attr, false, nullptr);
             cfg.gridDim = dim3(CL * (sms / CL), 1, 1);
             int n = 0;
             e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
@@ -1229,17 +1354,17 @@ cudaError_t cluster_capacity(int sms, int *out) {
     return cudaSuccess;
 }
 
-template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN>
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false>
 cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args,
                        int sms, cudaMemPool_t pool, cudaStream_t stream) {
-    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS, SUBK, KS, BN>;
+    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU>;
     int maxc = 0;
-    cudaError_t e = cluster_capacity<KIND, B_MN, EPI, CTAS, SUBK, KS, BN>(sms, &maxc);
+    cudaError_t e = cluster_capacity<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU>(sms, &maxc);
     if (e != cudaSuccess) return e;
     if (KS > 1 && args.num_tiles > maxc) return cudaErrorInvalidConfiguration;  // one wave of clusters
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    launch_config<KIND, B_MN, EPI, CTAS, SUBK, KS, BN>(cfg, attr, args.pdl != 0, stream);
+    launch_config<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU>(cfg, attr, args.pdl != 0, stream);
     // Work list: split the last wave's tiles in K when they fill at most half
     // of the clusters (a lone partial wave included).  The halves exchange
     // partial sums through a stream-ordered workspace from `pool`: a counter
@@ -1278,7 +1403,7 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
     // threshold is split_min_kb K blocks (64 by default) with reductions on
     // the FP16 kind, twice that on the E4M3 kind or with the exchange.
     const int min_kb = a.split_min_kb * (reduce ? 1 : 2) * (KIND == Kind::E4M3 ? 2 : 1);
-    if (KS == 1 && BN == kBN && pool != nullptr && a.split_ok && a.num_kb > SUBK && a.num_kb >= min_kb &&
+    if (!FU && KS == 1 && BN == kBN && pool != nullptr && a.split_ok && a.num_kb > SUBK && a.num_kb >= min_kb &&
         tail > 0 && 2 * tail <= maxc) {
         const size_t slices = size_t(tail) * CTAS * EPI_WARPS;
         const size_t count_bytes = (slices * sizeof(uint32_t) + 255) / 256 * 256;
@@ -1386,12 +1511,33 @@ cudaError_t launch_gemm(Kind kind, bool b_mn_major, int epi, int ctas, const CUt
                : args.stage_kb == 1 ? launch_one<K, BMN, E, 2, 1, 1, kBN>(ta, tb, args, sms, pool, stream) \
                                     : launch_one<K, BMN, E, 2, 2, 1, kBN>(ta, tb, args, sms, pool, stream); \
     } while (0)
+#define PTC_LAUNCH_FU(K)                                                                                \
+    do {                                                                                                \
+        if (bn == 64 && ks == 4) return launch_one<K, false, EPI_INT, 1, 1, 4, 64, true>(ta, tb, args, sms, pool, stream); \
+        if (bn == 64 && ks == 2) return launch_one<K, false, EPI_INT, 1, 1, 2, 64, true>(ta, tb, args, sms, pool, stream); \
+        if (bn == 128 && ks == 4) return launch_one<K, false, EPI_INT, 1, 1, 4, 128, true>(ta, tb, args, sms, pool, stream); \
+        if (bn == 128 && ks == 2) return launch_one<K, false, EPI_INT, 1, 1, 2, 128, true>(ta, tb, args, sms, pool, stream); \
+        if (bn == 64) return launch_one<K, false, EPI_INT, 1, 1, 1, 64, true>(ta, tb, args, sms, pool, stream);   \
+        if (bn == 128) return launch_one<K, false, EPI_INT, 1, 1, 1, 128, true>(ta, tb, args, sms, pool, stream); \
+        if (ks == 8) return launch_one<K, false, EPI_INT, 1, 1, 8, kBN, true>(ta, tb, args, sms, pool, stream);   \
+        if (ks == 4) return launch_one<K, false, EPI_INT, 1, 1, 4, kBN, true>(ta, tb, args, sms, pool, stream);   \
+        if (ks == 2) return launch_one<K, false, EPI_INT, 1, 1, 2, kBN, true>(ta, tb, args, sms, pool, stream);   \
+        return launch_one<K, false, EPI_INT, 1, 1, 1, kBN, true>(ta, tb, args, sms, pool, stream);                \
+    } while (0)
     if (kind == Kind::F16 && b_mn_major && epi == EPI_F32) PTC_LAUNCH(Kind::F16, true, EPI_F32);
     if (kind == Kind::F16 && b_mn_major && epi == EPI_F16ACC) PTC_LAUNCH(Kind::F16, true, EPI_F16ACC);
+    if (args.in_ring != 0) {
+        // In-ring conversion: one-CTA integer launches with K-major B.
+        if (ctas != 1 || b_mn_major || epi != EPI_INT) return cudaErrorInvalidValue;
+        if (kind == Kind::F16) PTC_LAUNCH_FU(Kind::F16);
+        if (kind == Kind::E4M3) PTC_LAUNCH_FU(Kind::E4M3);
+        return cudaErrorInvalidValue;
+    }
     if (kind == Kind::F16 && !b_mn_major && epi == EPI_INT) PTC_LAUNCH(Kind::F16, false, EPI_INT);
     if (kind == Kind::F16 && b_mn_major && epi == EPI_INT) PTC_LAUNCH(Kind::F16, true, EPI_INT);
     if (kind == Kind::E4M3 && !b_mn_major && epi == EPI_INT) PTC_LAUNCH(Kind::E4M3, false, EPI_INT);
 #undef PTC_LAUNCH
+#undef PTC_LAUNCH_FU
     return cudaErrorInvalidValue;
 }
 

@@ -45,6 +45,9 @@ struct GemmArgs {
                            // in a cluster (0: chosen by size, 1: none, 2 / 4 / 8: that many
                            // when the launch allows it; tuning knob "ksplit")
     int pdl;               // 1: launched with programmatic stream serialization (knob "pdl")
+    int in_ring;           // 1: one-CTA integer launch whose tensor maps view the raw s8 / packed
+                           // s4 operands (boxes of 64 bytes x 128 rows of A, x bn rows of B, no
+                           // swizzle); the epilogue warps convert each K block in shared memory
     int split_ok;          // 1: the tail may be split (tuning knob "tail_split")
     int split_min_kb;      // ... when K spans at least this many K blocks
     int tail_split;
@@ -89,7 +92,9 @@ enum Epi : int {
 // `stream` and returned after the kernel; a null pool runs every tile whole.
 // One-CTA 256-wide launches run as K-split clusters when pick_ksplit(...,
 // args.ksplit, ...) returns more than 1 (no workspace).  args.pdl launches
-// with programmatic stream serialization.
+// with programmatic stream serialization.  args.in_ring (integer kinds, one
+// CTA, K-major B) converts the raw operands inside the kernel; such launches
+// never split the tail.
 cudaError_t launch_gemm(Kind kind, bool b_mn_major, int epi, int ctas, const CUtensorMap &ta,
                         const CUtensorMap &tb, const GemmArgs &args, int sms, cudaMemPool_t pool,
                         cudaStream_t stream);

@@ -6,7 +6,9 @@ Inputs are the seeded synthetic operands of the benchmark (FP16 normal/sqrt(K),
 INT8 and INT4 uniform).  Nothing is timed or checked here; use bench.py for
 numbers and the test suite for parity.  `--prec cublas_f16` runs the same FP16
 product through cuBLAS instead (torch.mm with FP32 output), as a library kernel
-to profile beside ours; it is not part of the library.
+to profile beside ours; it is not part of the library.  `--tune key=value`
+(repeatable) sets a library tuning knob first (ptc_set_tuning), e.g.
+`--tune in_ring=0` to profile the separate operand-conversion pass.
 """
 from __future__ import annotations
 
@@ -26,6 +28,7 @@ def main():
     p.add_argument("--prec", choices=["f16", "s8", "s4", "s8_noalloc", "cublas_f16"], default="f16")
     p.add_argument("--n", type=int, default=8192)
     p.add_argument("--reps", type=int, default=2)
+    p.add_argument("--tune", action="append", default=[], metavar="KEY=VALUE")
     a = p.parse_args()
 
     import torch
@@ -35,6 +38,9 @@ def main():
     from precision_tensor_core_gb300 import build as ptc_build
 
     ptc_build.build()
+    for kv in a.tune:
+        key, value = kv.split("=", 1)
+        ptc.ptc_set_tuning(key, int(value))
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     n = a.n

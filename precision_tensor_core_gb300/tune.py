@@ -18,7 +18,9 @@ policy, INT fold length), one knob at a time from the defaults: the ablation
 that shows the defaults are a local optimum.  `launch` compares launch shapes
 at small sizes (K-split clusters of 2, 4, 8 CTAs, programmatic launches on
 and off), reporting the median of 7 graph replays and the launch record
-(grid CTAs, CTAs per tile's K range) of each.  `sizes` times the three
+(grid CTAs, CTAs per tile's K range) of each; `--in-ring 0,1` repeats the
+integer rows with the operand conversion as a separate pass and inside the
+GEMM kernel.  `sizes` times the three
 entry points at each size with the library defaults.  `cublas` times gemm_f16
 against cuBLAS on the same FP16 operands (torch.mm with FP32 output, and with
 FP16 output), interleaved in one process so that both see the same clocks and
@@ -45,10 +47,10 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 DEFAULTS = {"cta_pair": 0, "group_m": 8, "l2_hint": 0, "s8_chunk_kb": 16, "s4_chunk_kb": 64, "tail_split": 1,
-            "split_min_kb": 64, "pair_stage_kb": 2, "ksplit": 0, "pdl": 1, "tile_n": 0}
+            "split_min_kb": 64, "pair_stage_kb": 2, "ksplit": 0, "pdl": 1, "tile_n": 0, "in_ring": 1}
 KNOBS = {"cta_pair": [1, 2], "pair_stage_kb": [1], "tail_split": [0], "split_min_kb": [32, 128],
          "group_m": [4, 16, 32], "l2_hint": [1, 2, 3], "s8_chunk_kb": [4, 8], "s4_chunk_kb": [2, 8, 16, 128],
-         "ksplit": [1, 2, 4, 8], "pdl": [0], "tile_n": [64, 128, 256]}
+         "ksplit": [1, 2, 4, 8], "pdl": [0], "tile_n": [64, 128, 256], "in_ring": [0]}
 # `launch` mode: launch-shape settings compared at small sizes, each timed as
 # the median of 7 replays of a CUDA graph of back-to-back calls.
 LAUNCH_SETTINGS = [("256-wide, plain launches", {"tile_n": 256, "ksplit": 1, "pdl": 0}),
@@ -75,6 +77,7 @@ def main():
     p.add_argument("--no-graph", action="store_true")
     p.add_argument("--json", default="")
     p.add_argument("--only", default="", help="comma-separated knob names to sweep (default: all)")
+    p.add_argument("--in-ring", default="1", help="launch mode: in_ring settings of the integer rows")
     a = p.parse_args()
 
     import torch
@@ -178,18 +181,22 @@ def main():
             ops = operands(n)
             calls = a.calls or max(20, min(200, int(2e11 / (2.0 * n ** 3))))
             results[str(n)] = {}
-            for prec in ("f16", "s8", "s4"):
+            rows = [("f16", 1)] + [(p, int(r)) for p in ("s8", "s4") for r in a.in_ring.split(",")]
+            for prec, ring in rows:
                 row = {}
                 for name, kv in LAUNCH_SETTINGS:
                     for k, v in kv.items():
                         ptc.ptc_set_tuning(k, v)
+                    ptc.ptc_set_tuning("in_ring", ring)
                     us = graph_median_us(call(prec, ops, n), calls)
                     grid, _, ks, bn = ptc.ptc_last_launch()
-                    row[name] = {"us": us, "grid": grid, "ksplit": ks, "tile_n": bn}
+                    row[name] = {"us": us, "grid": grid, "ksplit": ks, "tile_n": bn,
+                                 "conversion": ptc.ptc_last_conversion()}
                 for k, v in DEFAULTS.items():
                     ptc.ptc_set_tuning(k, v)
-                results[str(n)][prec] = row
-                print(f"{n:>6} {prec:>4} " + " ".join(
+                label = prec if prec == "f16" else f"{prec}/r{ring}"
+                results[str(n)][label] = row
+                print(f"{n:>6} {label:>5} " + " ".join(
                     f"{r['us']:>10.2f} ({r['grid']:>3}/{r['ksplit']}/{r['tile_n']:>3})" for r in row.values()),
                     flush=True)
     elif a.mode == "cublas":

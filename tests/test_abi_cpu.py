@@ -139,7 +139,7 @@ def test_status_strings_and_tuning(L):
     for key, bad, good in (("split_min_kb", 1, 64), ("tail_split", 2, 1), ("cta_pair", 3, 0),
                            ("s8_chunk_kb", 3, 16), ("s4_chunk_kb", 7, 64), ("pair_stage_kb", 3, 2),
                            ("ksplit", 3, 0), ("ksplit", 16, 0), ("pdl", 2, 1), ("split_reduce", 2, 1), ("tile_n", 32, 0),
-                           ("tile_n", 192, 0)):
+                           ("tile_n", 192, 0), ("in_ring", 3, 1), ("in_ring", -1, 1)):
         with pytest.raises(ptc.PtcError):
             ptc.ptc_set_tuning(key, bad)
         assert ptc.ptc_set_tuning(key, good) == 0
@@ -147,3 +147,5 @@ def test_status_strings_and_tuning(L):
     # no launch on this (GPU-less) thread yet: the launch record is empty
     assert ptc.ptc_last_launch() == (0, 0, 0, 0)
     assert L.ptc_last_launch(None, None, None, None) == ptc.PTC_ERR_INVALID
+    assert ptc.ptc_last_conversion() == 0
+    assert L.ptc_last_conversion(None) == ptc.PTC_ERR_INVALID

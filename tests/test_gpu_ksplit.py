@@ -83,7 +83,8 @@ def _check_launch(ks, M, N, num_kb):
     """The recorded launch is a K-split cluster launch when it must be: a
     forced KS with at most 8 tiles (clusters of 8 then always fit one wave)
     and at least KS K blocks; by size, 256-wide tiles only when each CTA sheds
-    8 or more K blocks, narrow tiles with at least two K blocks per CTA."""
+    8 or more K blocks, narrow tiles with at least two K blocks per CTA (one
+    when the integer operands are converted in the kernel's ring)."""
     grid, cluster, used, tile_n = ptc.ptc_last_launch()
     assert used in (1, 2, 4, 8) and grid > 0 and tile_n in (64, 128, 256)
     tiles = _tiles(M, N)
@@ -96,7 +97,8 @@ def _check_launch(ks, M, N, num_kb):
     elif used > 1 and tile_n == 256:
         assert num_kb - (num_kb + used - 1) // used >= 8
     elif used > 1:
-        assert num_kb >= 2 * used  # narrow tiles: at least two K blocks per CTA
+        # narrow tiles: at least two K blocks per CTA, or one with in-ring conversion
+        assert num_kb >= 2 * used or ptc.ptc_last_conversion() == 2
     if used > 1:
         tiles_bn = ((M + 127) // 128) * ((N + tile_n - 1) // tile_n)
         assert num_kb >= used and cluster == used and grid == used * tiles_bn

@@ -11,17 +11,20 @@ import precision_tensor_core_gb300 as ptc
 F16, S8, S4 = 0, 1, 2
 
 
+KNOBS = (("cta_pair", 0), ("tile_n", 0), ("ksplit", 0), ("in_ring", 1))
+
+
 @pytest.fixture(autouse=True)
 def default_knobs():
-    for k, v in (("cta_pair", 0), ("tile_n", 0), ("ksplit", 0)):
+    for k, v in KNOBS:
         ptc.ptc_set_tuning(k, v)
     yield
-    for k, v in (("cta_pair", 0), ("tile_n", 0), ("ksplit", 0)):
+    for k, v in KNOBS:
         ptc.ptc_set_tuning(k, v)
 
 
 @pytest.mark.parametrize("n,prec,shape", [
-    (512, F16, (1, 64, 4)), (512, S8, (1, 64, 4)), (512, S4, (1, 64, 1)),
+    (512, F16, (1, 64, 4)), (512, S8, (1, 64, 4)), (512, S4, (1, 64, 4)),
     (1024, F16, (1, 128, 2)), (1024, S8, (1, 128, 2)), (1024, S4, (1, 64, 1)),
     (1536, F16, (1, 128, 1)), (1536, S8, (1, 128, 1)), (1536, S4, (1, 128, 1)),
     (2048, F16, (2, 256, 1)), (2048, S8, (1, 256, 1)), (2048, S4, (1, 256, 1)),
@@ -72,3 +75,34 @@ def test_invalid_arguments():
         ptc.ptc_plan_shape(512, 512, 512, 3)
     with pytest.raises(ptc.PtcError):
         ptc.ptc_plan_shape(512, 512, 512, F16, sms=0)
+
+
+@pytest.mark.parametrize("n,prec,ring", [
+    (512, S8, True), (512, S4, True), (1024, S8, True), (1024, S4, False),
+    (1536, S8, False), (1536, S4, False), (2048, S8, False), (2048, S4, False),
+    (4096, S8, False), (8192, S4, False), (512, F16, False), (8192, F16, False),
+])
+def test_in_ring_choice_at_square_sizes(n, prec, ring):
+    """In-ring operand conversion where the launch-shape sweep of both paths
+    measured it faster (INT8 at N = 512 and 1024, INT4 at N = 512: 6.3 us
+    against 7.7 / 7.2 us with the separate pass at N = 512), the pass elsewhere
+    (its fixed cost is repaid once a CTA converts more than a few K blocks)."""
+    assert ptc.ptc_plan_shape(n, n, n, prec, with_ring=True)[3] is ring
+
+
+def test_in_ring_rules():
+    # odd K of packed s4 (a stray high nibble per row): never in ring
+    assert ptc.ptc_plan_shape(512, 512, 511, S4, with_ring=True)[3] is False
+    # a long K over few tiles: many K blocks per CTA, the pass
+    assert ptc.ptc_plan_shape(512, 512, 16384, S8, with_ring=True)[3] is False
+    # forced narrow tiles with more tiles than SMs: several units per CTA, the pass
+    ptc.ptc_set_tuning("tile_n", 64)
+    assert ptc.ptc_plan_shape(2048, 2048, 256, S8, with_ring=True)[3] is False
+    # the knob: 0 never, 2 on every one-CTA shape (not on CTA pairs)
+    ptc.ptc_set_tuning("in_ring", 2)
+    assert ptc.ptc_plan_shape(2048, 2048, 256, S8, with_ring=True)[3] is True
+    ptc.ptc_set_tuning("tile_n", 0)
+    assert ptc.ptc_plan_shape(8192, 8192, 8192, S8, with_ring=True)[3] is False
+    ptc.ptc_set_tuning("in_ring", 0)
+    assert ptc.ptc_plan_shape(512, 512, 512, S8, with_ring=True)[3] is False
+    assert ptc.ptc_plan_shape(512, 512, 512, S8) == (1, 64, 4)
