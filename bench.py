@@ -54,7 +54,7 @@ METRIC = "GEMM TFLOP/s / TOPS at N=8192 (FP16, INT8, INT4); fraction of GB300 de
 # an ncu capture of that kernel (`ncu --set full -k regex:gemm_kernel` on
 # `python -m precision_tensor_core_gb300.run --prec f16 --n 8192`); set to None
 # whenever that kernel changes, until it is captured again.
-F16_KERNEL_DRAM_BYTES = 1.0972e9 + 0.2566e9
+F16_KERNEL_DRAM_BYTES = 1.1052e9 + 0.2565e9
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
