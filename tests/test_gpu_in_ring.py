@@ -261,3 +261,26 @@ def test_in_ring_wait_timeout_and_recovery(knobs):
     torch.cuda.synchronize()
     assert np.array_equal(C.cpu().numpy(), oracle.wrap_s32(oracle.gemm_s8(A, Bt)))
     assert ptc.gemm_poll_device_error() == ptc.PTC_OK
+
+
+@pytest.mark.parametrize("prec", ["s8", "s4"])
+def test_in_ring_tall_output_many_units(prec, knobs):
+    """M = 2^20 rows, N = 40, K = 96 in forced 128 x 64 tiles with in-ring
+    conversion: 8192 tiles over at most one CTA per SM (dozens of units per
+    CTA, each converted, multiplied and stored in turn), sampled against the
+    oracle (the corners and the last row included)."""
+    knobs(tile_n=64, in_ring=2)
+    M, N, K = 1 << 20, 40, 96
+    ii, jj = sample_coords(M, N, 2000, seed=980)
+    if prec == "s8":
+        A, Bt = datagen.s8_operands(N, seed=981, m=M, k=K)
+        C = ptc.matmul_s8(padded_dev(A), padded_dev(Bt), out=out_padded(M, N))
+        assert ptc.ptc_last_conversion() == IN_RING
+        got = C.cpu().numpy()[ii, jj]
+        assert np.array_equal(got, oracle.wrap_s32(oracle.gemm_s8_at(A, Bt, ii, jj)))
+    else:
+        A, Bt = datagen.s4_operands(N, seed=982, m=M, k=K)
+        C = ptc.matmul_s4(padded_dev(A), padded_dev(Bt), K, out=out_padded(M, N))
+        assert ptc.ptc_last_conversion() == IN_RING
+        got = C.cpu().numpy()[ii, jj]
+        assert np.array_equal(got, oracle.wrap_s32(oracle.gemm_s4_at(A, Bt, K, ii, jj)))
