@@ -55,6 +55,7 @@ struct StageShape {
     static constexpr int K = KVALS;
     static constexpr bool B_RM = B_ROWMAJOR;
     static constexpr bool SL = SLICED;
+    static_assert(!(B_RM && SL), "row-major B tiles are never sliced");
     static constexpr int A_BYTES = SLICED ? 4 * BM * 32 : BM * PITCH;
     // FP16 B row-major: K rows of 64 halves (128 bytes) padded by 16 bytes.
     static constexpr int B_PITCH = B_ROWMAJOR ? (BN * 2 + 16) : PITCH;

@@ -118,6 +118,7 @@ struct Cfg {
     static constexpr int RAW_STAGE = FU ? (kBM + BN) * kRawRow : 0;  // raw A, then raw B
     static constexpr int STAGES = FU ? kRingFu / (STAGE + RAW_STAGE) : CTAS == 1 ? kRing1 / STAGE : (SUBK == 1 ? 7 : 3);
     static constexpr int RING = STAGES * (STAGE + RAW_STAGE);        // bytes of both rings
+    static_assert(RAW_A % 1024 == 0 && RAW_STAGE % 1024 == 0, "raw boxes start on 1024-byte boundaries");
     static constexpr int TMEM_COLS = 2 * BN;  // two accumulators of BN columns
 };
 
