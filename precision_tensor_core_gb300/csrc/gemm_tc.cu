@@ -55,6 +55,14 @@
 // of kb_per_chunk K blocks, each summed in its own accumulator buffer; the
 // epilogue converts each chunk's (integral) FP32 sums to int32 and adds them
 // in registers.  The int32 result is therefore the exact sum modulo 2^32.
+// The operands arrive converted (binary16 / E4M3 rows written by a separate
+// pass), or, with FU (one-CTA launches of small products), raw: the producer
+// loads 64-byte K blocks of the s8 / packed s4 rows into a second ring and the
+// epilogue warps, idle during the K loop, convert each into the MMA stage in
+// the 128-byte-swizzled layout (fence.proxy.async, then eight arrivals
+// complete the stage's full barrier).  They fold chunk c only after
+// converting it and convert chunk c + 2 only after folding chunk c, whose
+// accumulator buffer chunk c + 2 reuses, so the rings always drain.
 //
 // Tiles are spread over a persistent grid of at most one CTA per SM with no
 // dependency between clusters (no grid-wide spin barrier).  The kernel may be
