@@ -23,9 +23,11 @@ integer rows with the operand conversion as a separate pass and inside the
 GEMM kernel.  `sizes` times the three
 entry points at each size with the library defaults.  `cublas` times gemm_f16
 against cuBLAS on the same FP16 operands (torch.mm with FP32 output, and with
-FP16 output), interleaved in one process so that both see the same clocks and
-power state: 10 rounds of one CUDA-graph replay each, then ~1 s of back-to-back
-replays per kernel.
+FP16 output), or with `--prec s8` gemm_s8 against cuBLAS's INT8 GEMM
+(torch._int_mm, int32 output, whose result it first compares with ours),
+interleaved in one process so that both see the same clocks and power state:
+10 rounds of one CUDA-graph replay each, then ~1 s of back-to-back replays per
+kernel.
 
 Calls are captured in a CUDA graph (`--graph`, default on) and the graph is
 replayed, so that the host-side cost of a Python call does not hide the GPU
@@ -78,6 +80,8 @@ def main():
     p.add_argument("--json", default="")
     p.add_argument("--only", default="", help="comma-separated knob names to sweep (default: all)")
     p.add_argument("--in-ring", default="1", help="launch mode: in_ring settings of the integer rows")
+    p.add_argument("--prec", default="f16", choices=["f16", "s8"],
+                   help="cublas mode: FP16 (torch.mm) or INT8 (torch._int_mm, int32 C)")
     a = p.parse_args()
 
     import torch
@@ -202,10 +206,25 @@ def main():
     elif a.mode == "cublas":
         import statistics
         n = a.n
-        A, B, C = operands(n)["f16"]
-        fns = {"gemm_f16 (FP32 C)": lambda: ptc.matmul_f16(A, B, out=C),
-               "cuBLAS torch.mm (FP32 C)": lambda: torch.mm(A, B, out_dtype=torch.float32),
-               "cuBLAS torch.mm (FP16 C)": lambda: torch.mm(A, B)}
+        if a.prec == "f16":
+            A, B, C = operands(n)["f16"]
+            fns = {"gemm_f16 (FP32 C)": lambda: ptc.matmul_f16(A, B, out=C),
+                   "cuBLAS torch.mm (FP32 C)": lambda: torch.mm(A, B, out_dtype=torch.float32),
+                   "cuBLAS torch.mm (FP16 C)": lambda: torch.mm(A, B)}
+        else:
+            # INT8 -> int32 (B column-major: the K x N view of N rows of K).
+            A, Bt, C = operands(n)["s8"]
+            fns = {"gemm_s8 (int32 C)": lambda: ptc.matmul_s8(A, Bt, out=C)}
+            try:
+                ref = torch._int_mm(A, Bt.t())
+                torch.cuda.synchronize()
+                ptc.matmul_s8(A, Bt, out=C)
+                torch.cuda.synchronize()
+                print("torch._int_mm equals gemm_s8:", bool(torch.equal(ref, C)), flush=True)
+                del ref
+                fns["cuBLAS torch._int_mm"] = lambda: torch._int_mm(A, Bt.t())
+            except RuntimeError as exc:
+                print(f"torch._int_mm unavailable here: {exc}", flush=True)
         calls = a.calls or 20
         graphs = {}
         for k, fn in fns.items():
