@@ -106,3 +106,49 @@ def test_in_ring_rules():
     ptc.ptc_set_tuning("in_ring", 0)
     assert ptc.ptc_plan_shape(512, 512, 512, S8, with_ring=True)[3] is False
     assert ptc.ptc_plan_shape(512, 512, 512, S8) == (1, 64, 4)
+
+
+def test_plan_invariants_over_random_shapes():
+    """Every plan is launchable and consistent, over 3000 seeded shapes (sizes
+    log-uniform, so small products are as common as large ones) and all
+    three precisions: CTA pairs are 256-wide and never split or convert in
+    ring; narrow tiles fit one wave; a K-split fits the cluster capacity and
+    leaves every CTA a K block; in-ring conversion only for integer one-CTA
+    single-wave launches (packed s4: even K); products with one wave or more
+    of 128 x 256 tiles run on CTA pairs; with the knob at 0 nothing converts
+    in ring, at 2 every one-CTA integer plan does."""
+    import numpy as np
+    rng = np.random.default_rng(2024)
+    sms, caps = 152, (76, 36, 15)
+    cap_of = {2: caps[0], 4: caps[1], 8: caps[2]}
+    def log_uniform(hi):  # small products as often as large ones
+        return max(1, int(np.exp(rng.uniform(0.0, np.log(hi)))))
+
+    for _ in range(3000):
+        M, N, K = log_uniform(20000), log_uniform(20000), log_uniform(70000)
+        prec = int(rng.integers(0, 3))
+        ctas, bn, ks, ring = ptc.ptc_plan_shape(M, N, K, prec, with_ring=True)
+        num_kb = (K + (127 if prec == S4 else 63)) // (128 if prec == S4 else 64)
+        tiles = ((M + 127) // 128) * ((N + bn - 1) // bn)
+        t256 = ((M + 127) // 128) * ((N + 255) // 256)
+        assert ctas in (1, 2) and bn in (64, 128, 256) and ks in (1, 2, 4, 8)
+        if ctas == 2:
+            assert bn == 256 and ks == 1 and not ring
+        if t256 >= sms:
+            assert ctas == 2
+        if bn != 256:
+            assert ks in (1, 2, 4) and tiles <= sms
+        if ks > 1:
+            assert ctas == 1 and num_kb >= ks and tiles <= cap_of[ks]
+        if ring:
+            assert prec != F16 and ctas == 1 and tiles * ks <= sms
+            assert prec != S4 or K % 2 == 0
+    for value, expect in ((0, False), (2, True)):
+        ptc.ptc_set_tuning("in_ring", value)
+        for _ in range(300):
+            M, N = int(rng.integers(1, 3000)), int(rng.integers(1, 3000))
+            K = 2 * int(rng.integers(1, 8000))
+            prec = int(rng.integers(1, 3))
+            ctas, _, _, ring = ptc.ptc_plan_shape(M, N, K, prec, with_ring=True)
+            assert ring is (expect and ctas == 1)
+    ptc.ptc_set_tuning("in_ring", 1)
