@@ -149,3 +149,13 @@ def test_status_strings_and_tuning(L):
     assert L.ptc_last_launch(None, None, None, None) == ptc.PTC_ERR_INVALID
     assert ptc.ptc_last_conversion() == 0
     assert L.ptc_last_conversion(None) == ptc.PTC_ERR_INVALID
+    # the plan's in_ring output is optional; the others are not
+    import ctypes
+    c, n, k, r = (ctypes.c_int(0) for _ in range(4))
+    assert L.ptc_plan_shape(512, 512, 512, 1, 152, 76, 36, 15, ctypes.byref(c), ctypes.byref(n), ctypes.byref(k),
+                            None) == 0
+    assert (c.value, n.value, k.value) == ptc.ptc_plan_shape(512, 512, 512, 1)
+    assert L.ptc_plan_shape(512, 512, 512, 1, 152, 76, 36, 15, None, ctypes.byref(n), ctypes.byref(k),
+                            ctypes.byref(r)) == ptc.PTC_ERR_INVALID
+    assert L.ptc_plan_shape(512, 512, 512, 3, 152, 76, 36, 15, ctypes.byref(c), ctypes.byref(n), ctypes.byref(k),
+                            ctypes.byref(r)) == ptc.PTC_ERR_INVALID
