@@ -12,13 +12,16 @@ Reported (one JSON line from rank 0):
   value        2*N^3 multiply-adds counted as operations, summed over the three
                GEMMs of every step of every rank, divided by the max-over-ranks
                device time of the timed steps  [TOPS]
-  per_precision  TFLOP/s (FP16) and TOPS (INT8, INT4) of each call, averaged
-               over the timed steps (CUDA events on the launching stream)
+  per_precision  TFLOP/s / TOPS of each call: the median over 5 batches of
+               the batch's mean per-call time, and the best batch
   peak_fractions  each precision against its nominal dense peak, against the
                measured peak of the tensor-core kind it runs on, and against
-               that kind's nominal rate scaled to the run's median SM clock
+               that kind's dense per-SM rate x SMs x the SM clock its kernels
+               ran at (their CTAs' own cycle and global-timer counts)
   roofline     the FP16 GEMM kernel (one launch per gemm_f16 call) against the
-               measured bf16 tensor-core peak (FP16 runs at the bf16 rate)
+               measured bf16 tensor-core peak (FP16 runs at the bf16 rate):
+               the burst figure when the timed region is shorter than a
+               second, else the sustained one; both fractions are given
   e2e          the same metric through the public API with pinned host
                buffers (the host-buffer entry points, one stream per product):
                H2D of the operands, the GEMMs, D2H of the results, every step
@@ -50,12 +53,23 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "GEMM TFLOP/s / TOPS at N=8192 (FP16, INT8, INT4); fraction of GB300 dense peak"
-# DRAM read + write bytes of one launch of the FP16 GEMM kernel at N = 8192, from
-# an ncu capture of that kernel (`ncu --set full -k regex:gemm_kernel` on
-# `python -m precision_tensor_core_gb300.run --prec f16 --n 8192`); set to None
-# whenever that kernel changes, until it is captured again.
-F16_KERNEL_DRAM_BYTES = 1.1052e9 + 0.2565e9
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM read + write bytes of one launch of the FP16 GEMM kernel at N = 8192 come
+# from the record beside its ncu summary (made with
+# `ncu --set full --clock-control none -k regex:gemm_kernel -s 1 -c 1
+#  python -m precision_tensor_core_gb300.run --prec f16 --n 8192`), which names
+# the hash of the kernel sources it was captured from; a record of other sources
+# is stale and gives no traffic figure.
+TRAFFIC_RECORD = os.path.join(ROOT, "profiles", "traffic_gemm_f16_n8192.txt")
+KERNEL_SOURCES = ("gemm_tc.cu", "ptx.cuh", "internal.h", "convert.cuh")
+# Dense tensor-core rate per SM and clock: 8192 FLOP (M = 128, N = 256, K = 16
+# binary16 MMA, 2 * 128 * 256 * 16 FLOP, every 128 cycles) for the FP16 kind,
+# twice that for the E4M3 kind.
+PER_SM_CLOCK_FLOP = {"kind::f16": 8192.0, "kind::f8f6f4": 16384.0}
+BATCHES = 5
+# A timed region shorter than this is a burst: the kernel's clock has not
+# settled under the power cap, so the burst peak is the denominator.
+SUSTAINED_AFTER_MS = 1000.0
 
 
 def parse():
@@ -83,6 +97,32 @@ def load_peaks():
             d = json.load(f)
         return d, "measured"
     return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    """First 16 hex digits of the SHA-256 of the GEMM kernel's sources."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "precision_tensor_core_gb300", "csrc", name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record():
+    """(DRAM bytes per launch, note) of the FP16 kernel from the committed ncu
+    record, or (None, why) when it is absent or was taken from other sources."""
+    if not os.path.exists(TRAFFIC_RECORD):
+        return None, "no ncu traffic record"
+    rec = {}
+    with open(TRAFFIC_RECORD) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                rec[k.strip()] = v.strip()
+    if rec.get("source_sha256_16") != kernel_source_hash():
+        return None, "ncu traffic record is from other kernel sources (stale)"
+    return float(rec["dram_bytes_read"]) + float(rec["dram_bytes_write"]), "profiles/traffic_gemm_f16_n8192.txt"
 
 
 # ---------------------------------------------------------------- ranks
@@ -187,35 +227,66 @@ def run_ours(args, rank, world, dist):
     assert ptc.gemm_poll_device_error() == ptc.PTC_OK
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # Batch boundaries: the timed steps in BATCHES consecutive batches.
+    nb = max(1, min(BATCHES, args.steps))
+    bounds = [round(b * args.steps / nb) for b in range(nb + 1)]
+    bev = [torch.cuda.Event(enable_timing=True) for _ in range(nb + 1)]
     sampler = ClockSampler(local)
     sampler.start()
+    ptc.ptc_clock_probe_read()  # clear the clock record
+    ptc.ptc_set_tuning("clock_probe", 1)
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
     launches0 = ptc.ptc_kernel_launch_count()
-    start.record(stream)
-    for i in range(args.steps):
-        step(evs[i])
-    stop.record(stream)
+    bev[0].record(stream)
+    for b in range(nb):
+        for i in range(bounds[b], bounds[b + 1]):
+            step(evs[i])
+        bev[b + 1].record(stream)
     torch.cuda.synchronize()
     launches = ptc.ptc_kernel_launch_count() - launches0
     if dist:
         dist.barrier()
     clocks = sampler.stop()
-    elapsed_ms = start.elapsed_time(stop)
+    ptc.ptc_set_tuning("clock_probe", 0)
+    cyc, ns, ctas = ptc.ptc_clock_probe_read()
+    elapsed_ms = bev[0].elapsed_time(bev[nb])
+    batch_ms = [bev[b].elapsed_time(bev[b + 1]) / (bounds[b + 1] - bounds[b]) for b in range(nb)]
     t16 = [e[0].elapsed_time(e[1]) for e in evs]
     t8 = [e[1].elapsed_time(e[2]) for e in evs]
     t4 = [e[2].elapsed_time(e[3]) for e in evs]
     assert ptc.gemm_poll_device_error() == ptc.PTC_OK
     elapsed_ms = reduce_max(dist, elapsed_ms, dev)
 
+    def per_batch(ts):
+        """Mean per-call time of each batch (ms)."""
+        return [statistics.mean(ts[bounds[b]:bounds[b + 1]]) for b in range(nb)]
+
     ops = 2.0 * n ** 3
     value = throughput_tops(3 * ops, args.steps, world, elapsed_ms)
-    per = {"fp16_tflops": ops / (statistics.mean(t16) * 1e-3) / 1e12,
-           "int8_tops": ops / (statistics.mean(t8) * 1e-3) / 1e12,
-           "int4_tops": ops / (statistics.mean(t4) * 1e-3) / 1e12,
-           "ms": {"fp16": statistics.mean(t16), "int8": statistics.mean(t8), "int4": statistics.mean(t4)}}
+    ms = {"fp16": per_batch(t16), "int8": per_batch(t8), "int4": per_batch(t4)}
+    med = {k: statistics.median(v) for k, v in ms.items()}
+    best = {k: min(v) for k, v in ms.items()}
+    per = {"fp16_tflops": ops / (med["fp16"] * 1e-3) / 1e12,
+           "int8_tops": ops / (med["int8"] * 1e-3) / 1e12,
+           "int4_tops": ops / (med["int4"] * 1e-3) / 1e12,
+           "ms": med, "ms_min": best,
+           "best": {"fp16_tflops": ops / (best["fp16"] * 1e-3) / 1e12,
+                    "int8_tops": ops / (best["int8"] * 1e-3) / 1e12,
+                    "int4_tops": ops / (best["int4"] * 1e-3) / 1e12},
+           "statistic": f"median over {nb} batches of the batch's mean per-call time (CUDA events on the "
+                        f"launching stream); ms_min / best: the fastest batch"}
+    batches = {"batches": nb, "ms_per_step_median": statistics.median(batch_ms),
+               "ms_per_step_min": min(batch_ms), "ms_per_step_each": batch_ms}
+    # Mean SM clock each GEMM kernel family ran at, from its CTAs' own cycle and
+    # global-timer counts.
+    kernel_mhz = {fam: (1e3 * cyc[i] / ns[i] if ns[i] else None)
+                  for i, fam in enumerate(("fp16", "int8", "int4"))}
+    clocks["kernel_sm_mhz"] = kernel_mhz
+    clocks["kernel_sm_mhz_how"] = ("sum of %clock64 cycles / sum of %globaltimer ns over every CTA of every "
+                                   "timed GEMM kernel launch (thread 0, start of work to exit)")
+    clocks["kernel_ctas"] = {fam: int(ctas[i]) for i, fam in enumerate(("fp16", "int8", "int4"))}
 
     # e2e through the public API with pinned host buffers
     e2e_steps = args.e2e_steps or min(args.steps, 20)
@@ -258,44 +329,52 @@ def run_ours(args, rank, world, dist):
            "how": "gemm_f16_host / gemm_s8_host / gemm_s4_host on pinned host buffers, one stream each"}
 
     peaks, src = load_peaks()
-    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    traffic = F16_KERNEL_DRAM_BYTES if n == 8192 else None
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    is_burst = elapsed_ms < SUSTAINED_AFTER_MS
+    peak = burst if is_burst else sustained
+    traffic, traffic_note = traffic_record() if n == 8192 else (None, "recorded for N = 8192 only")
+    if traffic is not None:
+        traffic_note += " (one ncu capture, cold L2)"
     achieved = per["fp16_tflops"]
-    roofline = {"bound": "tensor", "kernel": "gemm_kernel<F16, B MN-major, f32 out> (gemm_f16)",
+    roofline = {"bound": "tensor", "kernel": "gemm_kernel<F16, B MN-major, f32 out, CTA pair> (gemm_f16)",
                 "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "peak_source": f"bf16_tflops_sustained of {src} MEASURED_PEAKS.json (FP16 = bf16 rate)",
-                "traffic": traffic,
+                "peak_source": (f"{'bf16_tflops (burst)' if is_burst else 'bf16_tflops_sustained'} of {src} "
+                                f"MEASURED_PEAKS.json, FP16 = bf16 rate; the timed region lasted "
+                                f"{elapsed_ms:.0f} ms ({'<' if is_burst else '>='} {SUSTAINED_AFTER_MS:.0f} ms)"),
+                "frac_of_burst": achieved / burst, "frac_of_sustained": achieved / sustained,
+                "traffic": traffic, "traffic_source": traffic_note,
                 "int8_frac_of_f16_peak": per["int8_tops"] / peak,
                 "int4_frac_of_fp8_peak": per["int4_tops"] / (2 * peak)}
-    fractions = peak_fractions(per, peak, clocks)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    fractions = peak_fractions(per, peak, kernel_mhz, sms)
     return {"value": value, "elapsed_ms": elapsed_ms, "per": per, "e2e": e2e, "roofline": roofline,
-            "clocks": clocks, "launches": int(launches), "fractions": fractions}
+            "clocks": clocks, "launches": int(launches), "fractions": fractions, "batches": batches}
 
 
 # Nominal dense tensor-core rates of GB300 quoted with the metric (TFLOP/s or
-# TOPS): FP16 about 2.25 P, INT8 about 4.5 P; INT4 is quoted as INT8's.  The
-# FP8 (E4M3) kind is nominally twice the FP16 kind.
+# TOPS): FP16 about 2.25 P, INT8 about 4.5 P; INT4 is quoted as INT8's.
 NOMINAL = {"fp16": 2250.0, "int8": 4500.0, "int4": 4500.0}
-PIPE_NOMINAL = {"kind::f16": 2250.0, "kind::f8f6f4": 4500.0}
 
 
-def peak_fractions(per, measured_f16_peak, clocks):
+def peak_fractions(per, measured_f16_peak, kernel_mhz, sms):
     """Each precision's throughput against the denominators of the metric:
-    the nominal dense peak of its precision, the tensor-core kind it actually
-    runs on (measured sustained bf16 rate for kind::f16, twice that for the
-    E4M3 kind), and that kind's nominal rate scaled by the median SM clock of
-    the run over the maximum clock (nominal rates taken at the maximum clock)."""
-    mhz, mhz_max = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
-    scale = (mhz / mhz_max) if (mhz and mhz_max) else None
+    the nominal dense peak of its precision; the measured peak of the
+    tensor-core kind it actually runs on (the cuBLAS bf16 rate for kind::f16,
+    FP16 and the INT8 route; twice that for the E4M3 kind of the INT4 route);
+    and that kind's dense per-SM rate x SMs x the mean SM clock its own
+    kernels ran at during the timed region (the clock record)."""
     rows = {"fp16": ("fp16_tflops", "kind::f16", measured_f16_peak),
             "int8": ("int8_tops", "kind::f16", measured_f16_peak),
             "int4": ("int4_tops", "kind::f8f6f4", 2 * measured_f16_peak)}
     out = {}
     for prec, (key, kind, pipe_peak) in rows.items():
         a = per[key]
-        clock_peak = PIPE_NOMINAL[kind] * scale if scale else None
+        mhz = kernel_mhz.get(prec)
+        clock_peak = PER_SM_CLOCK_FLOP[kind] * sms * mhz * 1e6 / 1e12 if mhz else None
         out[prec] = {"achieved": a, "nominal_peak": NOMINAL[prec], "frac_nominal": a / NOMINAL[prec],
                      "pipe": kind, "pipe_peak_measured": pipe_peak, "frac_pipe_measured": a / pipe_peak,
+                     "kernel_sm_mhz": mhz,
                      "pipe_peak_clock_adjusted": clock_peak,
                      "frac_pipe_clock_adjusted": (a / clock_peak) if clock_peak else None}
     return out
@@ -516,6 +595,7 @@ def main():
                                    "one step = one GEMM of each",
                        "N": args.n, "l2": "inputs larger than L2 (~1.2 GB per step), no flush",
                        "parallelism": f"replicas x{world}"},
+            "batches": res["batches"],
             "per_precision": res["per"], "peak_fractions": res["fractions"], "roofline": res["roofline"],
             "cpu_baseline": cpu,
             "e2e": res["e2e"], "gpu_launches": res["launches"], "clocks": res["clocks"],

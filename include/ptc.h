@@ -38,8 +38,9 @@
  *     PTC_ERR_INVALID  negative or too-large size (each of M, N, K must be
  *                      <= 2^30, and C must have fewer than 2^31 output tiles
  *                      of 128 x 256), NULL pointer where data is needed, a leading
- *                      dimension below its minimum, an odd INT4 leading
- *                      dimension
+ *                      dimension below its minimum or above 2^36 elements
+ *                      (the operands' when K > 0, C's always), an odd INT4
+ *                      leading dimension
  *     PTC_ERR_ALIGN    a base pointer not 16-byte aligned, or a row pitch in
  *                      bytes that is not a multiple of 16
  *     PTC_ERR_OVERLAP  C's byte range intersects A's or B's
@@ -213,9 +214,14 @@ int gemm_s4_scaled(int64_t M, int64_t N, int64_t K,
  * otherwise the call returns PTC_ERR_INVALID and launches nothing.
  * The first call on each device (with that device current) looks up the
  * array's device address with cudaGetSymbolAddress; make it before any stream
- * capture begins.  Every call uses the same array: calls whose kernels
- * overlap on the GPU (other streams, other host threads) race on it and give
- * wrong results, so serialise them.
+ * capture begins.  Under CUDA's default lazy module loading that first lookup
+ * also loads the library's device code and commits the array's 32 MiB on the
+ * GPU, so make the first call (or set CUDA_MODULE_LOADING=EAGER) before the
+ * application's own allocator reserves the device's memory; later calls
+ * allocate nothing.  If that set-up fails the call returns PTC_ERR_DEVICE and
+ * the next call tries it again.  Every call uses the same array: calls whose
+ * kernels overlap on the GPU (other streams, other host threads) race on it
+ * and give wrong results, so serialise them.
  */
 int gemm_s8_noalloc(int64_t M, int64_t N, int64_t K,
                     const int8_t *A, int64_t lda,
@@ -305,6 +311,21 @@ int gemm_poll_device_error(void);
  * all threads).  Lets callers count the GPU work behind a sequence of calls. */
 uint64_t ptc_kernel_launch_count(void);
 
+/* Clock record of the GEMM kernels (tuning key "clock_probe" = 1 turns it on):
+ * thread 0 of every CTA of a GEMM kernel launched while it is on adds the SM
+ * clock cycles (%clock64) and the global-timer nanoseconds between its start
+ * of work and its exit, and 1, to the record of its kernel family, so that
+ * cycles / ns is the mean SM clock (GHz) the tensor-core kernels ran at.
+ * Families: [0] FP16 operands (gemm_f16, gemm_f16_f16acc), [1] the INT8
+ * route, [2] the INT4 route.  Fills cycles[3], ns[3], ctas[3] for the current
+ * device, then clears the record.  Synchronises the device.  The timing
+ * methodology of the study (wall-clock times of repeated launches, section
+ * III-B of "Hand-Written PTX Tensor-Core GEMM Kernels: A Multi-Precision Study
+ * on NVIDIA L4") leaves the clock implicit; this makes it explicit.  Returns
+ * PTC_OK, PTC_ERR_INVALID for a NULL pointer, PTC_ERR_DEVICE, or
+ * PTC_ERR_LAUNCH. */
+int ptc_clock_probe_read(uint64_t *cycles, uint64_t *ns, uint64_t *ctas);
+
 /* Test hook, not for production use.  Sets the pipeline-wait time limit (in
  * nanoseconds, 0 restores the default of one second) and, when stall_tile >= 0,
  * makes the next launched GEMM kernel withhold the operands of output tile
@@ -350,11 +371,13 @@ int ptc_last_conversion(int *mode);
  *   "s8_chunk_kb"  INT8 route: K blocks (64 values each) whose FP32 partial
  *                  sum is folded into int32 at a time, default 16 (1024
  *                  values: |partial| <= 2^24, so every FP32 partial sum is an
- *                  exactly representable integer)
+ *                  exactly representable integer); at most 16
  *   "s4_chunk_kb"  INT4 route: K blocks (128 values each) per fold, default 64
- *                  (8192 values: |partial| <= 2^19)
+ *                  (8192 values: |partial| <= 2^19); at most 2048 (2^24)
  *                  Both fold lengths must be even (CTA pairs stage two K
- *                  blocks at a time); odd values return PTC_ERR_INVALID.
+ *                  blocks at a time); odd values, and values above the
+ *                  exactness limits (which could let an FP32 partial sum
+ *                  round), return PTC_ERR_INVALID.
  *   "l2_hint"      L2 eviction policy of operand loads: 0 (default) none;
  *                  1 A evict-last / B evict-first; 2 A evict-last; 3 both
  *                  evict-normal (all measured slower than 0 on GB300)
@@ -423,6 +446,8 @@ int ptc_last_conversion(int *mode);
  *                  barriers and tensor memory) while the previous kernel of
  *                  the stream finishes; it waits for that kernel before its
  *                  first global-memory access.  0: plain stream order.
+ *   "clock_probe"  0 (default) or 1: GEMM kernels add their SM cycles and
+ *                  nanoseconds to the clock record (ptc_clock_probe_read)
  *   "in_ring"      gemm_s8 / gemm_s4 (and their scaled forms) on one-CTA
  *                  shapes may load K blocks of the raw operands and convert
  *                  them to the MMA input type in the GEMM kernel's shared
@@ -432,8 +457,7 @@ int ptc_last_conversion(int *mode);
  *                  (single-wave launches with few K blocks per CTA: small
  *                  products such as N = 512); 0: never; 2: on every one-CTA
  *                  shape.  Results do not depend on the choice.
- * Values above the defaults can make gemm_s8 / gemm_s4 inexact for adversarial
- * inputs; they exist to measure the tensor cores' accumulation width. */
+ * No accepted value of any key changes an INT8 or INT4 result. */
 int ptc_set_tuning(const char *key, int64_t value);
 
 #ifdef __cplusplus

@@ -98,6 +98,9 @@ def lib() -> ctypes.CDLL:
         L.ptc_last_launch.argtypes = [_ip, _ip, _ip, _ip]
         L.ptc_last_conversion.restype = ctypes.c_int
         L.ptc_last_conversion.argtypes = [_ip]
+        _u64p = ctypes.POINTER(ctypes.c_uint64)
+        L.ptc_clock_probe_read.restype = ctypes.c_int
+        L.ptc_clock_probe_read.argtypes = [_u64p, _u64p, _u64p]
         L.ptc_plan_shape.restype = ctypes.c_int
         L.ptc_plan_shape.argtypes = [_i64, _i64, _i64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, _ip, _ip, _ip, _ip]
@@ -185,6 +188,15 @@ def gemm_poll_device_error() -> int:
 
 def ptc_kernel_launch_count() -> int:
     return int(lib().ptc_kernel_launch_count())
+
+
+def ptc_clock_probe_read():
+    """Clock record of the GEMM kernels launched with the "clock_probe" knob
+    set, per family (FP16, INT8 route, INT4 route): lists of SM cycles,
+    nanoseconds and CTAs summed over CTAs.  Read and cleared; synchronous."""
+    cyc, ns, ctas = (ctypes.c_uint64 * 3)(), (ctypes.c_uint64 * 3)(), (ctypes.c_uint64 * 3)()
+    _check(lib().ptc_clock_probe_read(cyc, ns, ctas))
+    return list(cyc), list(ns), list(ctas)
 
 
 def ptc_debug_set_wait_limit(timeout_ns: int, stall_tile: int = -1) -> int:

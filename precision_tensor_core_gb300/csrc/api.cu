@@ -37,6 +37,8 @@ thread_local char g_msg[512];
 // int32 every kb_per_chunk K blocks of 128 bytes; see gemm_tc.cu.
 std::atomic<int> g_chunk_s8{16};  // 1024 K values: |partial| <= 1024 * 2^14 = 2^24
 std::atomic<int> g_chunk_s4{64};  // 8192 K values: |partial| <= 8192 * 2^6  = 2^19
+constexpr int kMaxChunkS8 = 16;   // 2^24 / (64 * 2^14): the longest exact INT8 fold
+constexpr int kMaxChunkS4 = 2048; // 2^24 / (128 * 2^6): the longest exact INT4 fold
 std::atomic<int> g_group_m{8};
 std::atomic<int> g_l2_hint{0};
 std::atomic<int> g_cta_pair{0};     // 0: by problem size, 1: one CTA per tile, 2: CTA pairs
@@ -50,6 +52,7 @@ std::atomic<int> g_pdl{1};            // programmatic stream serialization of th
 std::atomic<int> g_in_ring{1};        // integer routes: operands converted in the GEMM kernel's shared
                                       // memory where estimated faster (0: never, 2: on every one-CTA shape)
 thread_local int g_last_conv = 0;     // operand conversion of this thread's last GEMM call
+std::atomic<int> g_clock_probe{0};   // 1: GEMM kernels add to the clock record
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 std::atomic<int64_t> g_stall_tile{-1};
 
@@ -162,15 +165,30 @@ int make_tmap(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool overlaps(const void *a, uint64_t alen, const void *b, uint64_t blen) {
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    const unsigned __int128 a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
     return a0 < b0 + blen && b0 < a0 + alen;
 }
 
+// Leading dimensions above 2^36 elements (256 GiB rows of 4-byte values, more
+// than a GB300 holds) are rejected, as are sizes above 2^30.
+constexpr int64_t kMaxLd = int64_t(1) << 36;
+
+int check_ld(int64_t lda, int64_t ldb, int64_t ldc) {
+    if (lda > kMaxLd || ldb > kMaxLd || ldc > kMaxLd) {
+        std::snprintf(g_msg, sizeof(g_msg), "leading dimensions must be <= 2^36 elements");
+        return PTC_ERR_INVALID;
+    }
+    return PTC_OK;
+}
+
 // Bytes spanned by `rows` rows of `cols` elements at `ld` elements pitch, for
-// an element of `num`/`den` bytes (den = 2 for nibbles).
+// an element of `num`/`den` bytes (den = 2 for nibbles).  Sizes are at most
+// 2^30 and pitches at most kMaxLd, so the product fits 128-bit arithmetic;
+// the result saturates at 2^64 - 1.
 uint64_t span_bytes(int64_t rows, int64_t cols, int64_t ld, int num, int den) {
-    const int64_t elems = (rows - 1) * ld + cols;
-    return uint64_t((elems * num + den - 1) / den);
+    const __int128 elems = __int128(rows - 1) * ld + cols;
+    const __int128 b = (elems * num + den - 1) / den;
+    return b > __int128(UINT64_MAX) ? UINT64_MAX : uint64_t(b);
 }
 
 int check_sizes(int64_t M, int64_t N, int64_t K) {
@@ -380,6 +398,7 @@ GemmArgs base_args(int64_t M, int64_t N, int64_t K, int k_elems_per_block, void 
     a.split_reduce = g_split_reduce.load();
     a.pdl = g_pdl.load();
     a.wait_limit_ns = g_wait_ns.load();
+    a.probe = g_clock_probe.load();
     return a;
 }
 
@@ -428,6 +447,7 @@ int f16_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const 
     int rc = check_sizes(M, N, K);
     if (rc) return rc;
     if (M == 0 || N == 0) return PTC_OK;
+    if ((rc = check_ld(K > 0 ? lda : 0, K > 0 ? ldb : 0, ldc))) return rc;
     const int eb = epi == ptc::EPI_F16ACC ? 2 : 4;
     if (!C || ldc < N) return fail(PTC_ERR_INVALID, "C is NULL or ldc < N");
     if (K > 0 && (!A || !B)) return fail(PTC_ERR_INVALID, "A or B is NULL");
@@ -491,6 +511,7 @@ int int_gemm(bool s4, int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     int rc = check_sizes(M, N, K);
     if (rc) return rc;
     if (M == 0 || N == 0) return PTC_OK;
+    if ((rc = check_ld(K > 0 ? lda : 0, K > 0 ? ldb : 0, ldc))) return rc;
     const int eb = out_bytes(mode);
     if (!C || ldc < N) return fail(PTC_ERR_INVALID, "C is NULL or ldc < N");
     if (K > 0 && (!A || !B)) return fail(PTC_ERR_INVALID, "A or B is NULL");
@@ -604,6 +625,7 @@ int s8_rowb_gemm(int64_t M, int64_t N, int64_t K, const int8_t *A, int64_t lda, 
     int rc = check_sizes(M, N, K);
     if (rc) return rc;
     if (M == 0 || N == 0) return PTC_OK;
+    if ((rc = check_ld(K > 0 ? lda : 0, K > 0 ? ldb : 0, ldc))) return rc;
     if (!C || ldc < N) return fail(PTC_ERR_INVALID, "C is NULL or ldc < N");
     if (K > 0 && (!A || !B)) return fail(PTC_ERR_INVALID, "A or B is NULL");
     if (K > 0 && (lda < K || ldb < N)) return fail(PTC_ERR_INVALID, "lda < K or ldb < N");
@@ -711,6 +733,7 @@ int host_gemm(int prec, int64_t M, int64_t N, int64_t K, const void *A, int64_t 
     int rc = check_sizes(M, N, K);
     if (rc) return rc;
     if (M == 0 || N == 0) return PTC_OK;
+    if ((rc = check_ld(K > 0 ? lda : 0, K > 0 ? ldb : 0, ldc))) return rc;
     const bool f16 = prec == 0, s4 = prec == 2;
     if (!C || ldc < N) return fail(PTC_ERR_INVALID, "C is NULL or ldc < N");
     if (K > 0 && (!A || !B)) return fail(PTC_ERR_INVALID, "A or B is NULL");
@@ -950,6 +973,7 @@ int gemm_baseline(int variant, int64_t M, int64_t N, int64_t K, const void *A, i
     int rc = check_sizes(M, N, K);
     if (rc) return rc;
     if (M == 0 || N == 0) return PTC_OK;
+    if ((rc = check_ld(K > 0 ? lda : 0, K > 0 ? ldb : 0, ldc))) return rc;
     const bool f16 = v == ptc::BASE_F16_WMMA || v == ptc::BASE_F16_MMA;
     const bool s4 = v == ptc::BASE_S4_WMMA || v == ptc::BASE_S4_MMA;
     const int kmult = ptc::baseline_k_multiple(v);
@@ -1009,6 +1033,23 @@ int gemm_poll_device_error(void) {
 
 uint64_t ptc_kernel_launch_count(void) { return g_launches.load(); }
 
+int ptc_clock_probe_read(uint64_t *cycles, uint64_t *ns, uint64_t *ctas) {
+    if (!cycles || !ns || !ctas) return fail(PTC_ERR_INVALID, "NULL pointer");
+    int dev;
+    DevInfo *d;
+    int rc = current_device(&dev, &d);
+    if (rc) return rc;
+    unsigned long long v[9];
+    cudaError_t e = ptc::read_and_clear_clock_probe(v);
+    if (e != cudaSuccess) return fail_cuda(e, "reading the clock record");
+    for (int f = 0; f < 3; ++f) {
+        cycles[f] = v[3 * f];
+        ns[f] = v[3 * f + 1];
+        ctas[f] = v[3 * f + 2];
+    }
+    return PTC_OK;
+}
+
 int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile) {
     g_wait_ns.store(timeout_ns ? timeout_ns : kDefaultWaitNs);
     g_stall_tile.store(stall_tile);
@@ -1058,13 +1099,23 @@ int ptc_last_conversion(int *mode) {
 
 int ptc_set_tuning(const char *key, int64_t value) {
     if (!key) return fail(PTC_ERR_INVALID, "key is NULL");
-    if (std::strcmp(key, "s8_chunk_kb") == 0 && value > 0 && value % 2 == 0 && value < (1 << 30)) {
-        g_chunk_s8.store(int(value));
-        return PTC_OK;
+    // Fold lengths stay within exactness: every FP32 partial sum of a chunk is
+    // an integer of magnitude <= 2^24 (s8: 64 values of |ab| <= 2^14 per K
+    // block, so at most 16 blocks; E4M3 route: 128 values of |ab| <= 2^6, at
+    // most 2048 blocks).
+    if (std::strcmp(key, "s8_chunk_kb") == 0) {
+        if (value > 0 && value % 2 == 0 && value <= kMaxChunkS8) {
+            g_chunk_s8.store(int(value));
+            return PTC_OK;
+        }
+        return fail(PTC_ERR_INVALID, "s8_chunk_kb must be even and in 2 .. 16 (exact FP32 partial sums)");
     }
-    if (std::strcmp(key, "s4_chunk_kb") == 0 && value > 0 && value % 2 == 0 && value < (1 << 30)) {
-        g_chunk_s4.store(int(value));
-        return PTC_OK;
+    if (std::strcmp(key, "s4_chunk_kb") == 0) {
+        if (value > 0 && value % 2 == 0 && value <= kMaxChunkS4) {
+            g_chunk_s4.store(int(value));
+            return PTC_OK;
+        }
+        return fail(PTC_ERR_INVALID, "s4_chunk_kb must be even and in 2 .. 2048 (exact FP32 partial sums)");
     }
     if (std::strcmp(key, "group_m") == 0 && value > 0 && value < (1 << 20)) {
         g_group_m.store(int(value));
@@ -1104,6 +1155,10 @@ int ptc_set_tuning(const char *key, int64_t value) {
     }
     if (std::strcmp(key, "in_ring") == 0 && value >= 0 && value <= 2) {
         g_in_ring.store(int(value));
+        return PTC_OK;
+    }
+    if (std::strcmp(key, "clock_probe") == 0 && (value == 0 || value == 1)) {
+        g_clock_probe.store(int(value));
         return PTC_OK;
     }
     if (std::strcmp(key, "cta_pair") == 0 && value >= 0 && value <= 2) {

@@ -17,7 +17,12 @@
 // so the first call on each device, with that device current, asks the
 // runtime for the array's device address with cudaGetSymbolAddress and keeps
 // it; later calls on that device reuse it.  Make that first call before any
-// stream capture begins.
+// stream capture begins.  Under CUDA's default lazy module loading, that first
+// lookup is also what loads the library's device code onto the GPU and
+// commits the array's memory: make the first call (or run with
+// CUDA_MODULE_LOADING=EAGER) before the application's allocator reserves the
+// device's memory.  A failed set-up is not remembered: the next call on that
+// device tries again.
 //
 // All calls share the one array, and it keeps whatever the last call wrote.
 // Nothing has to start at zero: each call writes every workspace element its
@@ -28,6 +33,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstdio>
 #include <cstring>
@@ -47,16 +53,16 @@ constexpr int kGroupM = 16;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 struct DeviceScratch {
-    std::once_flag once;
-    int ok = 0;
+    std::atomic<int> ok{0};  // set once the set-up below has succeeded
     int sms = 0;
     void *ptr = nullptr;  // device address of g_scratch on this device
-    char why[160] = {0};
 };
 DeviceScratch g_dev[kMaxDevices];
+std::mutex g_setup;
 
-// Once per device, with that device current: check it and look up the
-// scratch array's device address.
+// With the device current: check it and look up the scratch array's device
+// address.  Done once per device on success; a failure is reported to the
+// caller and retried by the next call.
 int device_scratch(DeviceScratch **out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -65,34 +71,38 @@ int device_scratch(DeviceScratch **out) {
         return PTC_ERR_DEVICE;
     }
     DeviceScratch &d = g_dev[dev];
-    std::call_once(d.once, [&] {
-        int major = 0, minor = 0, sms = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-            cudaGetLastError();
-            std::snprintf(d.why, sizeof(d.why), "device %d attributes unavailable", dev);
-            return;
+    if (!d.ok.load(std::memory_order_acquire)) {
+        std::lock_guard<std::mutex> lock(g_setup);
+        if (!d.ok.load(std::memory_order_relaxed)) {
+            char why[160];
+            int major = 0, minor = 0, sms = 0;
+            if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+                cudaGetLastError();
+                std::snprintf(why, sizeof(why), "device %d attributes unavailable", dev);
+                ptc::set_message(why);
+                return PTC_ERR_DEVICE;
+            }
+            if (!(major == 10 && minor == 3 && sms > 0)) {
+                std::snprintf(why, sizeof(why), "device %d is not a compute capability 10.3 GPU", dev);
+                ptc::set_message(why);
+                return PTC_ERR_DEVICE;
+            }
+            void *p = nullptr;
+            const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
+            if (e != cudaSuccess || p == nullptr) {
+                std::snprintf(why, sizeof(why),
+                              "cudaGetSymbolAddress of the scratch array failed (retried on the next call): %s",
+                              cudaGetErrorString(e));
+                cudaGetLastError();
+                ptc::set_message(why);
+                return PTC_ERR_DEVICE;
+            }
+            d.sms = sms;
+            d.ptr = p;
+            d.ok.store(1, std::memory_order_release);
         }
-        if (!(major == 10 && minor == 3 && sms > 0)) {
-            std::snprintf(d.why, sizeof(d.why), "device %d is not a compute capability 10.3 GPU", dev);
-            return;
-        }
-        void *p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_scratch);
-        if (e != cudaSuccess || p == nullptr) {
-            std::snprintf(d.why, sizeof(d.why), "cudaGetSymbolAddress of the scratch array failed: %s",
-                          cudaGetErrorString(e));
-            cudaGetLastError();
-            return;
-        }
-        d.sms = sms;
-        d.ptr = p;
-        d.ok = 1;
-    });
-    if (!d.ok) {
-        ptc::set_message(d.why[0] ? d.why : "device set-up failed");
-        return PTC_ERR_DEVICE;
     }
     *out = &d;
     return PTC_OK;
@@ -101,8 +111,14 @@ int device_scratch(DeviceScratch **out) {
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool overlaps(const void *a, uint64_t alen, const void *b, uint64_t blen) {
-    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    const unsigned __int128 a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
     return a0 < b0 + blen && b0 < a0 + alen;
+}
+
+// Bytes spanned by `rows` rows of `cols` elements of `esize` bytes at a pitch
+// of `ld` elements (sizes <= 2^30, pitches <= 2^36: exact in 128 bits).
+uint64_t span(int64_t rows, int64_t cols, int64_t ld, int esize) {
+    return uint64_t((__int128(rows - 1) * ld + cols) * esize);
 }
 
 int reject(int code, const char *text) {
@@ -126,12 +142,14 @@ extern "C" int gemm_s8_noalloc(int64_t M, int64_t N, int64_t K, const int8_t *A,
     if (!C || ldc < N) return reject(PTC_ERR_INVALID, "C is NULL or ldc < N");
     if (K > 0 && (!A || !B)) return reject(PTC_ERR_INVALID, "A or B is NULL");
     if (K > 0 && (lda < K || ldb < K)) return reject(PTC_ERR_INVALID, "lda < K or ldb < K");
+    const int64_t kMaxLd = int64_t(1) << 36;
+    if (ldc > kMaxLd || (K > 0 && (lda > kMaxLd || ldb > kMaxLd)))
+        return reject(PTC_ERR_INVALID, "leading dimensions must be <= 2^36 elements");
     if (!aligned16(C) || ldc % 4) return reject(PTC_ERR_ALIGN, "C must be 16-byte aligned, ldc % 4 == 0");
     if (K > 0 && (!aligned16(A) || !aligned16(B) || lda % 16 || ldb % 16))
         return reject(PTC_ERR_ALIGN, "A, B must be 16-byte aligned, lda % 16 == 0, ldb % 16 == 0");
-    const uint64_t cbytes = uint64_t(((M - 1) * ldc + N) * 4);
-    if (K > 0 && (overlaps(C, cbytes, A, uint64_t((M - 1) * lda + K)) ||
-                  overlaps(C, cbytes, B, uint64_t((N - 1) * ldb + K))))
+    const uint64_t cbytes = span(M, N, ldc, 4);
+    if (K > 0 && (overlaps(C, cbytes, A, span(M, K, lda, 1)) || overlaps(C, cbytes, B, span(N, K, ldb, 1))))
         return reject(PTC_ERR_OVERLAP, "C overlaps A or B");
 
     // Workspace layout of gemm_s8: A then B as binary16 rows of K, pitch

@@ -86,6 +86,9 @@
 namespace ptc {
 
 __device__ uint32_t g_error_word;
+// Clock record: per kernel family, SM cycles, nanoseconds and CTAs (see
+// read_and_clear_clock_probe).
+__device__ unsigned long long g_clock_probe[3][3];
 
 namespace {
 
@@ -139,6 +142,7 @@ struct SharedTail {
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
+    uint64_t probe_c0, probe_t0;  // clock record: SM cycles and ns at the start of work
     uint32_t tmem_base;
     AbortState abort;
 };
@@ -749,6 +753,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     // Global memory from here on: after the previous kernel of the stream.
     griddep_wait();
     griddep_launch_dependents();
+    if (args.clock_probe != nullptr && threadIdx.x == 0) {
+        st->probe_t0 = globaltimer_ns();
+        st->probe_c0 = sm_clock64();
+    }
 
     constexpr int K_ELEMS = (KIND == Kind::F16) ? kRowBytes / 2 : kRowBytes;
 
@@ -1283,6 +1291,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         cluster_sync();
     tc_fence_after_sync();
     if (warp == 1) tmem_dealloc<CTAS>(tmem_base, TMEM_COLS);
+    if (args.clock_probe != nullptr && threadIdx.x == 0) {
+        const uint64_t c1 = sm_clock64(), t1 = globaltimer_ns();
+        atomicAdd(args.clock_probe + 0, static_cast<unsigned long long>(c1 - st->probe_c0));
+        atomicAdd(args.clock_probe + 1, static_cast<unsigned long long>(t1 - st->probe_t0));
+        atomicAdd(args.clock_probe + 2, 1ull);
+    }
 }
 
 template <typename T>
@@ -1363,6 +1377,25 @@ cudaError_t cluster_capacity(int sms, int *out) {
     return cudaSuccess;
 }
 
+// Device address of g_clock_probe on the current device (cached per device
+// and thread).
+cudaError_t clock_probe_base(unsigned long long **out) {
+    static thread_local int dev_cached = -1;
+    static thread_local unsigned long long *addr = nullptr;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev != dev_cached) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_clock_probe);
+        if (e != cudaSuccess) return e;
+        addr = static_cast<unsigned long long *>(p);
+        dev_cached = dev;
+    }
+    *out = addr;
+    return cudaSuccess;
+}
+
 template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false>
 cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args,
                        int sms, cudaMemPool_t pool, cudaStream_t stream) {
@@ -1379,6 +1412,14 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
     // partial sums through a stream-ordered workspace from `pool`: a counter
     // per epilogue warp slice (zeroed here) and two slices of partial sums.
     GemmArgs a = args;
+    a.clock_probe = nullptr;
+    if (a.probe) {
+        unsigned long long *base = nullptr;
+        e = clock_probe_base(&base);
+        if (e != cudaSuccess) return e;
+        const int family = KIND == Kind::E4M3 ? 2 : EPI == EPI_INT ? 1 : 0;
+        a.clock_probe = base + 3 * family;
+    }
     // 32-byte C stores (whole L2 sectors) when C's base and row pitch allow them.
     const int64_t esize = (EPI == EPI_F16ACC || (EPI == EPI_INT && (a.out_mode == OUT_BF16 || a.out_mode == OUT_F16))) ? 2 : 4;
     a.c_wide = (reinterpret_cast<uintptr_t>(a.C) % 32 == 0 && (a.ldc * esize) % 32 == 0) ? 1 : 0;
@@ -1556,6 +1597,16 @@ cudaError_t launch_zero_fill(void *C, int64_t ldc, int M, int N, int esize, int 
     else
         zero_fill_kernel<uint32_t><<<grid, 256, 0, stream>>>(static_cast<uint32_t *>(C), ldc, M, N);
     return cudaGetLastError();
+}
+
+cudaError_t read_and_clear_clock_probe(unsigned long long out[9]) {
+    unsigned long long v[3][3];
+    cudaError_t e = cudaMemcpyFromSymbol(v, g_clock_probe, sizeof(v));
+    if (e != cudaSuccess) return e;
+    const unsigned long long zero[3][3] = {};
+    e = cudaMemcpyToSymbol(g_clock_probe, zero, sizeof(zero));
+    std::memcpy(out, v, sizeof(v));
+    return e;
 }
 
 cudaError_t read_and_clear_error_word(uint32_t *out) {

@@ -58,6 +58,11 @@ struct GemmArgs {
                            // epilogue warp slice); no partial-sum workspace
     uint32_t *split_count;
     float *split_part;
+    // Clock record (knob "clock_probe"): when set, thread 0 of every CTA adds
+    // its SM clock cycles, its global-timer nanoseconds and 1 to clock_probe[0..2]
+    // (set by launch_gemm from `probe`).
+    int probe;
+    unsigned long long *clock_probe;
     // Integer routes only: output of the epilogue.
     int out_mode;          // OUT_S32, or OUT_F32 / OUT_BF16 / OUT_F16 (scaled)
     const float *scale_a;  // M row scales (scaled modes; NULL: 1)
@@ -127,6 +132,13 @@ cudaError_t launch_zero_fill(void *C, int64_t ldc, int M, int N, int esize, int 
 
 // Reads and clears the device error word of the current device.
 cudaError_t read_and_clear_error_word(uint32_t *out);
+
+// Clock record of the GEMM kernels on the current device, per kernel family
+// (0: FP16 kind with FP32 / FP16 output, 1: FP16 kind with integer folds
+// (INT8), 2: E4M3 kind (INT4)): SM clock cycles, global-timer nanoseconds and
+// CTAs, summed over the CTAs of every launch made with args.probe set.  Reads
+// and clears the record (synchronous).
+cudaError_t read_and_clear_clock_probe(unsigned long long out[9]);
 
 // Operand preparation for the integer routes: exact element conversion into
 // dense, 128-byte-pitched workspace matrices of `cols` columns.

@@ -139,7 +139,9 @@ def test_status_strings_and_tuning(L):
     for key, bad, good in (("split_min_kb", 1, 64), ("tail_split", 2, 1), ("cta_pair", 3, 0),
                            ("s8_chunk_kb", 3, 16), ("s4_chunk_kb", 7, 64), ("pair_stage_kb", 3, 2),
                            ("ksplit", 3, 0), ("ksplit", 16, 0), ("pdl", 2, 1), ("split_reduce", 2, 1), ("tile_n", 32, 0),
-                           ("tile_n", 192, 0), ("in_ring", 3, 1), ("in_ring", -1, 1)):
+                           ("tile_n", 192, 0), ("in_ring", 3, 1), ("in_ring", -1, 1),
+                           ("s8_chunk_kb", 18, 16), ("s8_chunk_kb", 1 << 20, 16),
+                           ("s4_chunk_kb", 2050, 64), ("s4_chunk_kb", 1 << 20, 64)):
         with pytest.raises(ptc.PtcError):
             ptc.ptc_set_tuning(key, bad)
         assert ptc.ptc_set_tuning(key, good) == 0
@@ -159,3 +161,51 @@ def test_status_strings_and_tuning(L):
                             ctypes.byref(r)) == ptc.PTC_ERR_INVALID
     assert L.ptc_plan_shape(512, 512, 512, 3, 152, 76, 36, 15, ctypes.byref(c), ctypes.byref(n), ctypes.byref(k),
                             ctypes.byref(r)) == ptc.PTC_ERR_INVALID
+
+
+def test_fold_lengths_are_bounded_by_exactness(L):
+    """The fold-length knobs accept exactly the even lengths whose FP32 partial
+    sums stay exact integers (|partial| <= 2^24): s8 K blocks of 64 values with
+    |ab| <= 2^14 allow at most 16, E4M3 K blocks of 128 values with |ab| <= 2^6
+    at most 2048.  A longer fold is refused with PTC_ERR_INVALID and leaves the
+    previous value in place."""
+    assert L.ptc_set_tuning(b"s8_chunk_kb", 18) == ptc.PTC_ERR_INVALID
+    assert "16" in ptc.gemm_status_string(ptc.PTC_ERR_INVALID)
+    assert L.ptc_set_tuning(b"s4_chunk_kb", 2050) == ptc.PTC_ERR_INVALID
+    for v in (2, 16):
+        assert L.ptc_set_tuning(b"s8_chunk_kb", v) == ptc.PTC_OK
+    for v in (2, 2048):
+        assert L.ptc_set_tuning(b"s4_chunk_kb", v) == ptc.PTC_OK
+    assert 16 * 64 * 2 ** 14 == 2 ** 24 and 2048 * 128 * 2 ** 6 == 2 ** 24
+    assert L.ptc_set_tuning(b"s8_chunk_kb", 16) == ptc.PTC_OK
+    assert L.ptc_set_tuning(b"s4_chunk_kb", 64) == ptc.PTC_OK
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_leading_dimension_above_limit_is_invalid(L, name):
+    """A leading dimension above 2^36 elements is refused before any CUDA call
+    (so that the byte extents used by the overlap check cannot overflow)."""
+    args = good_args(name)
+    for key in ("lda", "ldb", "ldc"):
+        if key not in args:
+            continue
+        bad = dict(args)
+        bad[key] = (1 << 36) + 16 * 64
+        assert call(L, name, **bad) == ptc.PTC_ERR_INVALID, key
+
+
+def test_noalloc_leading_dimension_above_limit_is_invalid(L):
+    g = good_args("gemm_s8")
+    for key in ("lda", "ldb", "ldc"):
+        assert call(L, "gemm_s8_noalloc", **{**g, key: (1 << 36) + 1024}) == ptc.PTC_ERR_INVALID, key
+
+
+def test_clock_probe_read_without_device(L):
+    import ctypes
+    v = (ctypes.c_uint64 * 3)()
+    assert L.ptc_clock_probe_read(None, v, v) == ptc.PTC_ERR_INVALID
+    if not torch.cuda.is_available():
+        assert L.ptc_clock_probe_read(v, v, v) == ptc.PTC_ERR_DEVICE
+    for bad in (2, -1):
+        assert L.ptc_set_tuning(b"clock_probe", bad) == ptc.PTC_ERR_INVALID
+    assert L.ptc_set_tuning(b"clock_probe", 0) == ptc.PTC_OK

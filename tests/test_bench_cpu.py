@@ -84,17 +84,35 @@ def test_reference_arm_other_ranks_exit_quietly():
 
 def test_peak_fractions_denominators():
     per = {"fp16_tflops": 1500.0, "int8_tops": 1125.0, "int4_tops": 2250.0}
-    f = bench.peak_fractions(per, 1500.0, {"sm_mhz": 1035.0, "sm_max_mhz": 2070.0})
+    mhz = {"fp16": 1500.0, "int8": 1800.0, "int4": 1800.0}
+    f = bench.peak_fractions(per, 1500.0, mhz, 152)
     assert f["fp16"]["frac_nominal"] == pytest.approx(1500 / 2250)
     assert f["int8"]["frac_nominal"] == pytest.approx(1125 / 4500)
     assert f["fp16"]["frac_pipe_measured"] == pytest.approx(1.0)
     assert f["int8"]["pipe"] == "kind::f16" and f["int8"]["frac_pipe_measured"] == pytest.approx(0.75)
     assert f["int4"]["pipe"] == "kind::f8f6f4" and f["int4"]["pipe_peak_measured"] == pytest.approx(3000.0)
-    # half the maximum clock halves the nominal rate of the kind
-    assert f["fp16"]["pipe_peak_clock_adjusted"] == pytest.approx(1125.0)
-    assert f["int4"]["frac_pipe_clock_adjusted"] == pytest.approx(2250 / 2250)
-    g = bench.peak_fractions(per, 1500.0, {"sm_mhz": None, "sm_max_mhz": None})
+    # per-SM rate x SMs x the kernel's own clock: 8192 FLOP per clock for the
+    # FP16 kind, 16384 for the E4M3 kind
+    assert f["fp16"]["pipe_peak_clock_adjusted"] == pytest.approx(8192 * 152 * 1.5e9 / 1e12)
+    assert f["int8"]["pipe_peak_clock_adjusted"] == pytest.approx(8192 * 152 * 1.8e9 / 1e12)
+    assert f["int4"]["pipe_peak_clock_adjusted"] == pytest.approx(16384 * 152 * 1.8e9 / 1e12)
+    assert f["int4"]["frac_pipe_clock_adjusted"] == pytest.approx(2250 / (16384 * 152 * 1.8e9 / 1e12))
+    g = bench.peak_fractions(per, 1500.0, {"fp16": None, "int8": None, "int4": None}, 152)
     assert g["fp16"]["pipe_peak_clock_adjusted"] is None and g["fp16"]["frac_pipe_clock_adjusted"] is None
+
+
+def test_traffic_record_is_tied_to_the_kernel_sources(tmp_path, monkeypatch):
+    rec = tmp_path / "traffic.txt"
+    rec.write_text(f"kernel: x\nsource_sha256_16: {bench.kernel_source_hash()}\n"
+                   "dram_bytes_read: 1.0e9\ndram_bytes_write: 0.25e9\n")
+    monkeypatch.setattr(bench, "TRAFFIC_RECORD", str(rec))
+    t, _ = bench.traffic_record()
+    assert t == pytest.approx(1.25e9)
+    rec.write_text("kernel: x\nsource_sha256_16: 0000000000000000\ndram_bytes_read: 1\ndram_bytes_write: 1\n")
+    t, why = bench.traffic_record()
+    assert t is None and "stale" in why
+    monkeypatch.setattr(bench, "TRAFFIC_RECORD", str(tmp_path / "absent.txt"))
+    assert bench.traffic_record()[0] is None
 
 
 def test_sweep_oracle_time_measured_and_extrapolated():

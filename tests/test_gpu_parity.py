@@ -458,3 +458,29 @@ def test_pair_ring_stage_depths(M, N, K, stage_kb):
     finally:
         ptc.ptc_set_tuning("pair_stage_kb", 2)
         ptc.ptc_set_tuning("cta_pair", 0)
+
+
+def test_clock_probe_records_each_kernel_family():
+    """With the clock record on, each GEMM family's CTAs add their cycle and
+    nanosecond counts; the ratio is a plausible SM clock and the results are
+    unchanged."""
+    ptc.ptc_clock_probe_read()
+    ptc.ptc_set_tuning("clock_probe", 1)
+    try:
+        A, B = datagen.f16_operands(1024, "normal")
+        C16 = run_f16(A, B)
+        A8, Bt8 = datagen.s8_operands(1024)
+        C8 = run_s8(A8, Bt8)
+        A4, Bt4 = datagen.s4_operands(1024)
+        C4 = run_s4(A4, Bt4, 1024)
+    finally:
+        ptc.ptc_set_tuning("clock_probe", 0)
+    cyc, ns, ctas = ptc.ptc_clock_probe_read()
+    for f in range(3):
+        assert ctas[f] > 0 and ns[f] > 0
+        mhz = 1e3 * cyc[f] / ns[f]
+        assert 300.0 < mhz < 2500.0, (f, mhz)
+    assert ptc.ptc_clock_probe_read()[2] == [0, 0, 0]  # read and cleared
+    check_f16(C16, A, B)
+    assert np.array_equal(C8, oracle.wrap_s32(oracle.gemm_s8(A8, Bt8)))
+    assert np.array_equal(C4, oracle.wrap_s32(oracle.gemm_s4(A4, Bt4, 1024)))

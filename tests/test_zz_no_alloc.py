@@ -3,8 +3,11 @@ allocate device memory (for example an application whose own allocator has
 reserved the GPU's memory).  Its workspace is a fixed device array shared by
 every call, so the test runs two different problems back to back: the second
 call starts with the first call's data still in the array.  Each result must
-equal what gemm_s8 (the pool-allocating entry point) returns for the same
-inputs, bit for bit, as all INT8 results in this suite must.
+equal the CPU oracle's exact sums and what gemm_s8 (the pool-allocating entry
+point) returns for the same inputs, bit for bit, as all INT8 results in this
+suite must.  A further test checks the property the entry point exists for:
+once a first call has set it up, calls change neither the device's free
+memory nor any allocator's holdings.
 
 This file is collected last on purpose: if it fails, a run that stops at the
 first failure has already run every other test.
@@ -14,6 +17,7 @@ import pytest
 import torch
 
 import datagen
+import oracle
 import precision_tensor_core_gb300 as ptc
 
 pytestmark = pytest.mark.gpu
@@ -32,6 +36,7 @@ def built():
 
 def _both(M, N, K, seed):
     A, Bt = datagen.s8_operands(N, seed=seed, m=M, k=K)
+    exact = oracle.wrap_s32(oracle.gemm_s8(A, Bt))
     Ad = torch.from_numpy(A).to(DEV)
     Bd = torch.from_numpy(Bt).to(DEV)
     ref = torch.empty((M, N), dtype=torch.int32, device=DEV)
@@ -42,16 +47,18 @@ def _both(M, N, K, seed):
     ptc.gemm_s8_noalloc(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K, got.data_ptr(), N, s)
     launched = ptc.ptc_kernel_launch_count() - before
     torch.cuda.synchronize()
-    return got.cpu().numpy(), ref.cpu().numpy(), launched
+    return got.cpu().numpy(), ref.cpu().numpy(), exact, launched
 
 
 def test_noalloc_matches_gemm_s8_on_two_calls_in_a_row():
     # call 1: the INT8 workload shape of the study, 2048^3 (16 MiB of workspace)
-    got, ref, launched = _both(2048, 2048, 2048, seed=datagen.config_seed("s8", 2048))
+    got, ref, exact, launched = _both(2048, 2048, 2048, seed=datagen.config_seed("s8", 2048))
     assert launched == 3  # two conversions and the tensor-core kernel
+    assert np.array_equal(got, exact)
     assert np.array_equal(got, ref)
     # call 2: a smaller ragged problem over the array the first call filled
-    got, ref, _ = _both(300, 520, 208, seed=12345)
+    got, ref, exact, _ = _both(300, 520, 208, seed=12345)
+    assert np.array_equal(got, exact)
     assert np.array_equal(got, ref)
     assert ptc.gemm_poll_device_error() == ptc.PTC_OK
 
@@ -67,3 +74,31 @@ def test_noalloc_rejects_problems_beyond_the_scratch():
     assert e.value.status == ptc.PTC_ERR_INVALID
     assert "static scratch" in str(e.value)
     assert ptc.ptc_kernel_launch_count() == before
+
+
+def test_noalloc_calls_allocate_nothing():
+    """After a first call on the device (the set-up), repeated calls leave the
+    device's free memory, torch's caching allocator and the library's
+    workspace pool (whose memory would show in the free figure) unchanged."""
+    M, N, K = 1024, 1536, 2048
+    A, Bt = datagen.s8_operands(N, seed=777, m=M, k=K)
+    Ad = torch.from_numpy(A).to(DEV)
+    Bd = torch.from_numpy(Bt).to(DEV)
+    C = torch.empty((M, N), dtype=torch.int32, device=DEV)
+    s = torch.cuda.current_stream().cuda_stream
+
+    def call():
+        ptc.gemm_s8_noalloc(M, N, K, Ad.data_ptr(), K, Bd.data_ptr(), K, C.data_ptr(), N, s)
+
+    call()  # set-up and first use of these kernels
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    reserved0, allocated0 = torch.cuda.memory_reserved(), torch.cuda.memory_allocated()
+    for _ in range(5):
+        call()
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    assert torch.cuda.memory_reserved() == reserved0 and torch.cuda.memory_allocated() == allocated0
+    assert np.array_equal(C.cpu().numpy(), oracle.wrap_s32(oracle.gemm_s8(A, Bt)))
+    assert ptc.gemm_poll_device_error() == ptc.PTC_OK
