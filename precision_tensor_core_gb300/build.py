@@ -67,5 +67,53 @@ def build(force: bool = False, verbose: bool = False) -> str:
     return LIB
 
 
+_GEMM_ARGS = ("kind", "B", "epi", "CTAs", "K blocks per stage", "K-split", "tile N", "in-ring")
+
+
+def _gemm_label(mangled: str) -> str | None:
+    """Readable template arguments of a gemm_kernel instantiation."""
+    import re
+    m = re.search(r"gemm_kernelILNS_4KindE(\d)ELb(\d)ELi(\d)ELi(\d)ELi(\d)ELi(\d)ELi(\d+)ELb(\d)", mangled)
+    if not m:
+        return None
+    kind, bmn, epi, ctas, subk, ks, bn, fu = m.groups()
+    return (f"gemm_kernel<{'F16' if kind == '0' else 'E4M3'}, B {'MN' if bmn == '1' else 'K'}-major, "
+            f"{['EPI_F32', 'EPI_INT', 'EPI_F16ACC'][int(epi)]}, CTAS={ctas}, SUBK={subk}, KS={ks}, "
+            f"BN={bn}{', in-ring' if fu == '1' else ''}>")
+
+
+def ptxas_summary(log_path: str = os.path.join(BUILD, "ptxas.log")) -> str:
+    """Markdown table of every kernel in the last build's ptxas report:
+    registers, barriers, static shared memory, stack frame and spills."""
+    import re
+    text = open(log_path).read()
+    rows = []
+    pat = re.compile(r"Compiling entry function '(\S+)' for '(\w+)'\n"
+                     r"ptxas info\s+: Function properties for \S+\n"
+                     r"\s+(\d+) bytes stack frame, (\d+) bytes spill stores, (\d+) bytes spill loads\n"
+                     r"ptxas info\s+: Used (\d+) registers(.*)")
+    for name, arch, stack, sst, sld, regs, rest in pat.findall(text):
+        smem = re.search(r"(\d+) bytes smem", rest)
+        label = _gemm_label(name)
+        if label is None:
+            r = subprocess.run(["c++filt", name], capture_output=True, text=True)
+            label = (r.stdout.strip() or name) if r.returncode == 0 else name
+            label = label.replace("(anonymous namespace)::", "").replace("ptc::", "")
+            label = re.sub(r"^void ", "", re.sub(r"\([^()]*\)$", "", label))
+        rows.append((label, int(regs), int(smem.group(1)) if smem else 0, int(stack), int(sst), int(sld)))
+    rows.sort()
+    out = ["| kernel | registers | static smem (B) | stack (B) | spill stores (B) | spill loads (B) |",
+           "|---|---|---|---|---|---|"]
+    out += [f"| `{a}` | {b} | {c} | {d} | {e} | {f} |" for a, b, c, d, e, f in rows]
+    spilling = sum(1 for r in rows if r[4] or r[5])
+    out.append("")
+    out.append(f"{len(rows)} kernels, {spilling} with spills.")
+    return "\n".join(out)
+
+
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    if "--ptxas-summary" in sys.argv:
+        build(force="--force" in sys.argv)
+        print(ptxas_summary())
+    else:
+        print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
