@@ -446,6 +446,15 @@ int ptc_last_conversion(int *mode);
  *                  barriers and tensor memory) while the previous kernel of
  *                  the stream finishes; it waits for that kernel before its
  *                  first global-memory access.  0: plain stream order.
+ *   "pair_in_ring" gemm_s8 / gemm_s4 on CTA pairs (products whose 128 x 256
+ *                  tiles would fill the SMs): 0 (default) converts the
+ *                  operands in a separate pass; 2 converts each K block of the
+ *                  raw operands inside the pair kernel, by six dedicated
+ *                  converter warps per CTA.  Measured on GB300 at N = 8192,
+ *                  the in-kernel route is ~3x slower (the conversion and the
+ *                  proxy fence that publishes each converted block take
+ *                  longer than the block's MMAs), so it is not the default.
+ *                  Results do not depend on the choice.
  *   "clock_probe"  0 (default) or 1: GEMM kernels add their SM cycles and
  *                  nanoseconds to the clock record (ptc_clock_probe_read)
  *   "in_ring"      gemm_s8 / gemm_s4 (and their scaled forms) on one-CTA

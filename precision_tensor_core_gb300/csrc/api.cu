@@ -53,6 +53,8 @@ std::atomic<int> g_in_ring{1};        // integer routes: operands converted in t
                                       // memory where estimated faster (0: never, 2: on every one-CTA shape)
 thread_local int g_last_conv = 0;     // operand conversion of this thread's last GEMM call
 std::atomic<int> g_clock_probe{0};   // 1: GEMM kernels add to the clock record
+std::atomic<int> g_pair_in_ring{0};  // integer routes on CTA pairs: 0 a separate conversion pass,
+                                     // 2 conversion inside the pair kernel (dedicated converter warps)
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
 std::atomic<int64_t> g_stall_tile{-1};
 
@@ -549,7 +551,9 @@ int int_gemm(bool s4, int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     // workspace and no separate pass.  Packed s4 needs an even K (no stray
     // high nibble).
     const int conv = s4 ? (K % 2 == 0 ? 2 : 0) : 1;
-    const Shape sh = choose_shape(M, N, ldw / k_elems, d->sms, false, eb, conv);
+    Shape sh = choose_shape(M, N, ldw / k_elems, d->sms, false, eb, conv);
+    // CTA pairs convert inside the kernel when the pair_in_ring knob says so.
+    if (sh.ctas == 2 && conv != 0 && g_pair_in_ring.load() == 2) sh.ring = true;
     const int chunk = s4 ? g_chunk_s4.load() : g_chunk_s8.load();
     if (sh.ring) {
         const uint64_t kbytes = uint64_t(s4 ? K / 2 : K);
@@ -558,7 +562,7 @@ int int_gemm(bool s4, int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
                        ptc::kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
         if (!rc)
             rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, B, kbytes, uint64_t(N), uint64_t(s4 ? ldb / 2 : ldb),
-                           64, uint32_t(sh.bn), CU_TENSOR_MAP_SWIZZLE_NONE);
+                           64, uint32_t(sh.bn / sh.ctas), CU_TENSOR_MAP_SWIZZLE_NONE);
         if (rc) return rc;
         GemmArgs args = base_args(M, N, K, k_elems, C, ldc, sh);
         args.kb_per_chunk = chunk > 0 ? chunk : 1;
@@ -566,7 +570,7 @@ int int_gemm(bool s4, int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
         args.scale_a = sa;
         args.scale_b = sb;
         args.in_ring = 1;
-        rc = launch_gemm_checked(s4 ? Kind::E4M3 : Kind::F16, false, ptc::EPI_INT, 1, ta, tb, args, *d, s);
+        rc = launch_gemm_checked(s4 ? Kind::E4M3 : Kind::F16, false, ptc::EPI_INT, sh.ctas, ta, tb, args, *d, s);
         if (!rc) g_last_conv = 2;
         return rc;
     }
@@ -1155,6 +1159,10 @@ int ptc_set_tuning(const char *key, int64_t value) {
     }
     if (std::strcmp(key, "in_ring") == 0 && value >= 0 && value <= 2) {
         g_in_ring.store(int(value));
+        return PTC_OK;
+    }
+    if (std::strcmp(key, "pair_in_ring") == 0 && (value == 0 || value == 2)) {
+        g_pair_in_ring.store(int(value));
         return PTC_OK;
     }
     if (std::strcmp(key, "clock_probe") == 0 && (value == 0 || value == 1)) {

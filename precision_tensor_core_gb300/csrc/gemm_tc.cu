@@ -93,7 +93,20 @@ __device__ unsigned long long g_clock_probe[3][3];
 namespace {
 
 constexpr int EPI_WARPS = 8;
-constexpr int THREADS = 64 + 32 * EPI_WARPS;
+constexpr int THREADS = 64 + 32 * EPI_WARPS;  // warps 0, 1 and the epilogue warps 2 .. 9
+// CTA pairs with in-ring conversion: 16 warps.  Warpgroup 0 holds the producer
+// (warp 0), the MMA issuer (warp 1) and two idle warps, warpgroups 1 and 2 the
+// epilogue warps (4 .. 11), warpgroup 3 four converter warps (12 .. 15).  The
+// launch grants 128 registers per thread (65,536 / 512); warpgroups 0 and 3
+// give back all but kRegsLow (the producer, MMA and converter code fits in
+// 80 without spills), the epilogue warpgroups take kRegsHigh (their 128 int32
+// partial sums and the tensor-memory loads in flight):
+// 8 warps x 80 + 8 warps x 176 = 16 warps x 128 registers per lane.
+constexpr int PAIR_FU_THREADS = 512;
+constexpr int CONV_WARPS = 4;
+constexpr uint32_t kRegsLow = 80, kRegsHigh = 176;
+static_assert(8 * kRegsLow + 8 * kRegsHigh == (PAIR_FU_THREADS / 32) * (65536 / PAIR_FU_THREADS),
+              "warpgroup register budgets sum to the launch's registers");
 constexpr int KSTEP_BYTES = 32;                 // K bytes per tcgen05.mma (16 f16 / 32 e4m3)
 constexpr int KSTEPS = kRowBytes / KSTEP_BYTES; // MMAs per stage
 
@@ -105,19 +118,28 @@ constexpr int KSTEPS = kRowBytes / KSTEP_BYTES; // MMAs per stage
 // (32 KiB each): two-block stages take half as many barrier round trips per
 // byte and measured 3-6% faster.
 //
-// In-ring conversion (FU, one-CTA integer launches): the producer loads K
-// blocks of the raw operands (64 bytes per row: 64 s8 or 128 packed s4) into
-// a second ring of the same depth, and the epilogue warps, idle during the K
-// loop, convert each into the MMA ring stage.  Both rings fit 216 KiB: 6
-// stages for 64-wide tiles, 4 for 128-wide, 3 for 256-wide.
+// In-ring conversion (FU, integer launches): the producer loads K blocks of
+// the raw operands (64 bytes per row: 64 s8 or 128 packed s4) into a second
+// ring, and converting warps write each into an MMA ring stage.  One CTA per
+// tile: the epilogue warps, idle during the K loop, convert; both rings have
+// the same depth and fit 216 KiB (6 stages for 64-wide tiles, 4 for 128-wide,
+// 3 for 256-wide).  CTA pairs: four dedicated converter warps per CTA (the
+// epilogue warps of a multi-wave product fold and store while the next tile is
+// multiplied); 8 raw stages of 16 KiB (half the bytes of a converted K block,
+// so twice the K blocks in flight per byte) and 3 MMA stages of 32 KiB.
 constexpr int kRing1 = 4 * (kBM + kBN) * kRowBytes;  // one-CTA ring bytes
 constexpr int kRingFu = 216 * 1024;                  // both rings, in-ring conversion
 constexpr int kRawRow = 64;                          // raw operand bytes per row and K block
+constexpr int kPairFuStages = 3, kPairFuRawStages = 8;
 template <int CTAS, int SUBK, int BN, bool FU = false>
 struct Cfg {
     static_assert(CTAS == 2 || SUBK == 1, "one CTA stages one K block at a time");
     static_assert(BN == kBN || (CTAS == 1 && (BN == 64 || BN == 128)), "narrow tiles are one-CTA tiles");
-    static_assert(!FU || CTAS == 1, "in-ring conversion in one-CTA launches");
+    static_assert(!FU || CTAS == 1 || SUBK == 1, "in-ring conversion stages one K block at a time");
+    static constexpr bool PFU = FU && CTAS == 2;  // pair with dedicated converter warps
+    static constexpr int THREADS_ = PFU ? PAIR_FU_THREADS : THREADS;
+    static constexpr int EPI_WARP0 = PFU ? 4 : 2;  // first epilogue warp
+    static constexpr int CONV_WARP0 = 12;          // first converter warp (PFU)
     static constexpr int SUB = SUBK;  // K blocks per stage
     static constexpr int B_ROWS = BN / CTAS;
     static constexpr int A_BLOCK = kBM * kRowBytes;     // one K block of A
@@ -125,20 +147,23 @@ struct Cfg {
     static constexpr int A_STAGE = SUB * A_BLOCK;
     static constexpr int B_STAGE = SUB * B_BLOCK;
     static constexpr int STAGE = A_STAGE + B_STAGE;
-    static constexpr int RAW_A = FU ? kBM * kRawRow : 0;          // raw A rows of a stage
-    static constexpr int RAW_STAGE = FU ? (kBM + BN) * kRawRow : 0;  // raw A, then raw B
-    static constexpr int STAGES = FU ? kRingFu / (STAGE + RAW_STAGE) : CTAS == 1 ? kRing1 / STAGE : (SUBK == 1 ? 7 : 3);
-    static constexpr int RING = STAGES * (STAGE + RAW_STAGE);        // bytes of both rings
+    static constexpr int RAW_A = FU ? kBM * kRawRow : 0;              // raw A rows of a stage
+    static constexpr int RAW_STAGE = FU ? (kBM + B_ROWS) * kRawRow : 0;  // raw A, then raw B
+    static constexpr int STAGES = PFU ? kPairFuStages
+                                  : FU ? kRingFu / (STAGE + RAW_STAGE)
+                                       : CTAS == 1 ? kRing1 / STAGE : (SUBK == 1 ? 7 : 3);
+    static constexpr int RSTAGES = PFU ? kPairFuRawStages : FU ? STAGES : 1;  // raw ring depth
+    static constexpr int RING = STAGES * STAGE + (FU ? RSTAGES * RAW_STAGE : 0);  // bytes of both rings
     static_assert(RAW_A % 1024 == 0 && RAW_STAGE % 1024 == 0, "raw boxes start on 1024-byte boundaries");
     static constexpr int TMEM_COLS = 2 * BN;  // two accumulators of BN columns
 };
 
-template <int STAGES, int SUB>
+template <int STAGES, int SUB, int RSTAGES = STAGES>
 struct SharedTail {
     uint64_t full[STAGES * SUB];  // per K block of a stage: its operands have landed (or been converted)
     uint64_t empty[STAGES];       // per stage: its MMAs have read it
-    uint64_t rfull[STAGES];       // in-ring conversion: the raw stage has landed
-    uint64_t rempty[STAGES];      // ... and has been read by the converting warps
+    uint64_t rfull[RSTAGES];      // in-ring conversion: the raw stage has landed
+    uint64_t rempty[RSTAGES];     // ... and has been read by the converting warps
     uint64_t acc_full[2];
     uint64_t acc_empty[2];
     uint64_t drain;
@@ -155,12 +180,13 @@ constexpr int kStageWarp = 4 * kStageC;
 
 template <int CTAS, int SUBK, int BN = kBN, bool FU = false>
 constexpr size_t smem_bytes() {
-    return 1024 + size_t(Cfg<CTAS, SUBK, BN, FU>::RING) + sizeof(SharedTail<Cfg<CTAS, SUBK, BN, FU>::STAGES, SUBK>);
+    using C_ = Cfg<CTAS, SUBK, BN, FU>;
+    return 1024 + size_t(C_::RING) + sizeof(SharedTail<C_::STAGES, SUBK, C_::RSTAGES>);
 }
 static_assert(smem_bytes<1, 1>() <= 232448 && smem_bytes<2, 1>() <= 232448 && smem_bytes<2, 2>() <= 232448 &&
                   smem_bytes<1, 1, 128>() <= 232448 && smem_bytes<1, 1, 64>() <= 232448 &&
                   smem_bytes<1, 1, kBN, true>() <= 232448 && smem_bytes<1, 1, 128, true>() <= 232448 &&
-                  smem_bytes<1, 1, 64, true>() <= 232448,
+                  smem_bytes<1, 1, 64, true>() <= 232448 && smem_bytes<2, 1, kBN, true>() <= 232448,
               "shared memory budget");
 static_assert(Cfg<1, 1, 64, true>::STAGES == 6 && Cfg<1, 1, 128, true>::STAGES == 4 &&
                   Cfg<1, 1, kBN, true>::STAGES == 3,
@@ -687,12 +713,12 @@ __device__ __forceinline__ void ksplit_complete(const GemmArgs &args, int mb, in
 // CTAs' empty / accumulator-full barriers, and both CTAs' epilogues release
 // accumulator buffers on its acc_empty barriers.
 template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
     static_assert(!(B_MN && KIND == Kind::E4M3), "MN-major B is used by the FP16 path only");
     static_assert(KS == 1 || CTAS == 1, "K-split clusters of one-CTA tiles");
-    static_assert(!FU || (CTAS == 1 && EPI == EPI_INT && !B_MN), "in-ring conversion: one-CTA integer launches");
+    static_assert(!FU || (EPI == EPI_INT && !B_MN), "in-ring conversion: integer launches with K-major B");
     constexpr bool INT_OUT = EPI == EPI_INT;
     constexpr int HALF = BN / 2;      // columns of an epilogue warp's slice
     constexpr int NCH = HALF / 32;    // 32-column chunks of a slice
@@ -706,7 +732,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint8_t *a_ring = smem;
     uint8_t *b_ring = smem + STAGES * C_::A_STAGE;
     uint8_t *raw_ring = smem + STAGES * C_::STAGE;  // in-ring conversion only
-    using Tail = SharedTail<STAGES, C_::SUB>;
+    using Tail = SharedTail<STAGES, C_::SUB, C_::RSTAGES>;
+    constexpr bool PFU = C_::PFU;
+    constexpr int EPI_WARP0 = C_::EPI_WARP0;
+    constexpr int PSTAGES = FU ? C_::RSTAGES : STAGES;  // the producer's ring
     Tail *st = reinterpret_cast<Tail *>(smem + C_::RING);
 
     const int warp = threadIdx.x / 32;
@@ -720,13 +749,17 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int nclusters = gridDim.x / CL;
 
     if (threadIdx.x == 0) {
+        // In-ring conversion: a stage is full once every converting warp has
+        // converted its share of the raw stage into it (a pair's converter
+        // warps of both CTAs arrive on the even CTA's barrier).
+        constexpr uint32_t conv_arrivals = PFU ? (CONV_WARPS + 2) * CTAS : EPI_WARPS;
         for (int s = 0; s < STAGES; ++s) {
-            // In-ring conversion: a stage is full once every epilogue warp has
-            // converted its share of the raw stage into it.
-            for (int sb = 0; sb < C_::SUB; ++sb) mbar_init(&st->full[s * C_::SUB + sb], FU ? EPI_WARPS : 1);
+            for (int sb = 0; sb < C_::SUB; ++sb) mbar_init(&st->full[s * C_::SUB + sb], FU ? conv_arrivals : 1);
             mbar_init(&st->empty[s], 1);
+        }
+        for (int s = 0; s < C_::RSTAGES; ++s) {
             mbar_init(&st->rfull[s], 1);
-            mbar_init(&st->rempty[s], EPI_WARPS);
+            mbar_init(&st->rempty[s], PFU ? CONV_WARPS + 2 : EPI_WARPS);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&st->acc_full[b], 1);
@@ -760,206 +793,294 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     constexpr int K_ELEMS = (KIND == Kind::F16) ? kRowBytes / 2 : kRowBytes;
 
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            // L2 policies: A panels are re-read by every N tile of a raster group,
-            // B panels only by the M tiles of one group running at the same time.
-            const bool hint = args.l2_hint != 0;
-            uint64_t pol_a = 0, pol_b = 0;
-            if (args.l2_hint == 1 || args.l2_hint == 2) pol_a = l2_policy_evict_last();
-            if (args.l2_hint == 1) pol_b = l2_policy_evict_first();
-            if (args.l2_hint == 2) pol_b = l2_policy_evict_normal();
-            if (args.l2_hint == 3) pol_a = pol_b = l2_policy_evict_normal();
-            int s = 0;
-            uint32_t ph = 0;
-            uint32_t outstanding = 0, out_phase = 0;  // per-stage bits of issued copies
-            bool ok = true;
-            for (int t = cluster; t < args.num_vunits && ok; t += nclusters) {
-                WorkRef wr = work_unit(t, args, C_::SUB);
-                if constexpr (KS > 1) ksplit_range(wr, krank, KS);
-                const int m0 = wr.mb * (kBM * CTAS) + int(rank) * kBM;
-                const int n0 = wr.nb * BN + int(rank) * C_::B_ROWS;
-                for (int kb = wr.kb0; kb < wr.kb1; kb += C_::SUB) {
-                    // The stage is free once its MMAs (in-ring conversion: its
-                    // converting warps) have read it.
-                    if (!mbar_wait(FU ? &st->rempty[s] : &st->empty[s], ph ^ 1u, &st->abort, &g_error_word, limit)) {
-                        ok = false;
-                        break;
-                    }
-                    outstanding &= ~(1u << s);
-                    const bool stall = (t == args.stall_tile && kb == wr.kb0 && rank == 0);
-                    if (!stall) {
-                        uint8_t *a_dst = a_ring + s * C_::A_STAGE;
-                        uint8_t *b_dst = b_ring + s * C_::B_STAGE;
-                        if constexpr (FU) {
-                            // Raw K block: 128 rows of A, then BN rows of B, 64 bytes each.
-                            uint8_t *r_dst = raw_ring + s * C_::RAW_STAGE;
-                            mbar_arrive_expect_tx(&st->rfull[s], C_::RAW_STAGE);
-                            if (hint) {
-                                tma_load_2d_hint(r_dst, &tmA, &st->rfull[s], kb * kRawRow, m0, pol_a);
-                                tma_load_2d_hint(r_dst + C_::RAW_A, &tmB, &st->rfull[s], kb * kRawRow, n0, pol_b);
-                            } else {
-                                tma_load_2d(r_dst, &tmA, &st->rfull[s], kb * kRawRow, m0);
-                                tma_load_2d(r_dst + C_::RAW_A, &tmB, &st->rfull[s], kb * kRawRow, n0);
-                            }
-                            outstanding |= 1u << s;
-                            out_phase = (out_phase & ~(1u << s)) | (ph << s);
-                        } else if constexpr (CTAS == 1) {
-                            mbar_arrive_expect_tx(&st->full[s], C_::STAGE);
-                            auto load = [&](void *dst, const CUtensorMap *map, int x, int y, uint64_t pol) {
-                                if (hint)
-                                    tma_load_2d_hint(dst, map, &st->full[s], x, y, pol);
-                                else
-                                    tma_load_2d(dst, map, &st->full[s], x, y);
-                            };
-                            load(a_dst, &tmA, kb * K_ELEMS, m0, pol_a);
-                            if constexpr (B_MN) {
-#pragma unroll
-                                for (int i = 0; i < C_::B_ROWS / 64; ++i)
-                                    load(b_dst + i * (K_ELEMS * 128), &tmB, n0 + 64 * i, kb * K_ELEMS, pol_b);
-                            } else {
-                                load(b_dst, &tmB, kb * K_ELEMS, n0, pol_b);
-                            }
-                            outstanding |= 1u << s;
-                            out_phase = (out_phase & ~(1u << s)) | (ph << s);
-                        } else {
-                            // Both CTAs' copies of a K block complete on the even CTA's
-                            // full barrier of that block, which alone expects the pair's
-                            // bytes; each block has its own barrier, so that the MMAs
-                            // start on the first block of a stage while the second lands.
-                            // A block past K reads as zeros.
-#pragma unroll
-                            for (int sb = 0; sb < C_::SUB; ++sb) {
-                                uint64_t *fb = &st->full[s * C_::SUB + sb];
-                                if (rank == 0) mbar_arrive_expect_tx(fb, CTAS * (C_::A_BLOCK + C_::B_BLOCK));
-                                const uint32_t bar = mapa_shared(smem_u32(fb), 0);
+    if (warp < EPI_WARP0 || (PFU && warp >= C_::CONV_WARP0)) {
+        // Producer, MMA issuer, idle and converter warps.  With the 16-warp layout
+        // their warpgroups (0 and 3) first lower their register budget together.
+        if constexpr (PFU) regs_dec<kRegsLow>();
+        if (warp == 0) {
+            // ------------------------------------------------------ TMA producer
+            if (lane == 0) {
+                // L2 policies: A panels are re-read by every N tile of a raster group,
+                // B panels only by the M tiles of one group running at the same time.
+                const bool hint = args.l2_hint != 0;
+                uint64_t pol_a = 0, pol_b = 0;
+                if (args.l2_hint == 1 || args.l2_hint == 2) pol_a = l2_policy_evict_last();
+                if (args.l2_hint == 1) pol_b = l2_policy_evict_first();
+                if (args.l2_hint == 2) pol_b = l2_policy_evict_normal();
+                if (args.l2_hint == 3) pol_a = pol_b = l2_policy_evict_normal();
+                int s = 0;
+                uint32_t ph = 0;
+                uint32_t outstanding = 0, out_phase = 0;  // per-stage bits of issued copies
+                bool ok = true;
+                for (int t = cluster; t < args.num_vunits && ok; t += nclusters) {
+                    WorkRef wr = work_unit(t, args, C_::SUB);
+                    if constexpr (KS > 1) ksplit_range(wr, krank, KS);
+                    const int m0 = wr.mb * (kBM * CTAS) + int(rank) * kBM;
+                    const int n0 = wr.nb * BN + int(rank) * C_::B_ROWS;
+                    for (int kb = wr.kb0; kb < wr.kb1; kb += C_::SUB) {
+                        // The stage is free once its MMAs (in-ring conversion: its
+                        // converting warps) have read it.
+                        if (!mbar_wait(FU ? &st->rempty[s] : &st->empty[s], ph ^ 1u, &st->abort, &g_error_word, limit)) {
+                            ok = false;
+                            break;
+                        }
+                        outstanding &= ~(1u << s);
+                        const bool stall = (t == args.stall_tile && kb == wr.kb0 && rank == 0);
+                        if (!stall) {
+                            uint8_t *a_dst = a_ring + s * C_::A_STAGE;
+                            uint8_t *b_dst = b_ring + s * C_::B_STAGE;
+                            if constexpr (FU) {
+                                // Raw K block: 128 rows of A, then BN rows of B, 64 bytes each.
+                                uint8_t *r_dst = raw_ring + s * C_::RAW_STAGE;
+                                mbar_arrive_expect_tx(&st->rfull[s], C_::RAW_STAGE);
+                                if (hint) {
+                                    tma_load_2d_hint(r_dst, &tmA, &st->rfull[s], kb * kRawRow, m0, pol_a);
+                                    tma_load_2d_hint(r_dst + C_::RAW_A, &tmB, &st->rfull[s], kb * kRawRow, n0, pol_b);
+                                } else {
+                                    tma_load_2d(r_dst, &tmA, &st->rfull[s], kb * kRawRow, m0);
+                                    tma_load_2d(r_dst + C_::RAW_A, &tmB, &st->rfull[s], kb * kRawRow, n0);
+                                }
+                                outstanding |= 1u << s;
+                                out_phase = (out_phase & ~(1u << s)) | (ph << s);
+                            } else if constexpr (CTAS == 1) {
+                                mbar_arrive_expect_tx(&st->full[s], C_::STAGE);
                                 auto load = [&](void *dst, const CUtensorMap *map, int x, int y, uint64_t pol) {
                                     if (hint)
-                                        tma_load_2d_pair_hint(dst, map, bar, x, y, pol);
+                                        tma_load_2d_hint(dst, map, &st->full[s], x, y, pol);
                                     else
-                                        tma_load_2d_pair(dst, map, bar, x, y);
+                                        tma_load_2d(dst, map, &st->full[s], x, y);
                                 };
-                                load(a_dst + sb * C_::A_BLOCK, &tmA, (kb + sb) * K_ELEMS, m0, pol_a);
+                                load(a_dst, &tmA, kb * K_ELEMS, m0, pol_a);
                                 if constexpr (B_MN) {
-#pragma unroll
+    #pragma unroll
                                     for (int i = 0; i < C_::B_ROWS / 64; ++i)
-                                        load(b_dst + sb * C_::B_BLOCK + i * (K_ELEMS * 128), &tmB, n0 + 64 * i,
-                                             (kb + sb) * K_ELEMS, pol_b);
+                                        load(b_dst + i * (K_ELEMS * 128), &tmB, n0 + 64 * i, kb * K_ELEMS, pol_b);
                                 } else {
-                                    load(b_dst + sb * C_::B_BLOCK, &tmB, (kb + sb) * K_ELEMS, n0, pol_b);
+                                    load(b_dst, &tmB, kb * K_ELEMS, n0, pol_b);
+                                }
+                                outstanding |= 1u << s;
+                                out_phase = (out_phase & ~(1u << s)) | (ph << s);
+                            } else {
+                                // Both CTAs' copies of a K block complete on the even CTA's
+                                // full barrier of that block, which alone expects the pair's
+                                // bytes; each block has its own barrier, so that the MMAs
+                                // start on the first block of a stage while the second lands.
+                                // A block past K reads as zeros.
+    #pragma unroll
+                                for (int sb = 0; sb < C_::SUB; ++sb) {
+                                    uint64_t *fb = &st->full[s * C_::SUB + sb];
+                                    if (rank == 0) mbar_arrive_expect_tx(fb, CTAS * (C_::A_BLOCK + C_::B_BLOCK));
+                                    const uint32_t bar = mapa_shared(smem_u32(fb), 0);
+                                    auto load = [&](void *dst, const CUtensorMap *map, int x, int y, uint64_t pol) {
+                                        if (hint)
+                                            tma_load_2d_pair_hint(dst, map, bar, x, y, pol);
+                                        else
+                                            tma_load_2d_pair(dst, map, bar, x, y);
+                                    };
+                                    load(a_dst + sb * C_::A_BLOCK, &tmA, (kb + sb) * K_ELEMS, m0, pol_a);
+                                    if constexpr (B_MN) {
+    #pragma unroll
+                                        for (int i = 0; i < C_::B_ROWS / 64; ++i)
+                                            load(b_dst + sb * C_::B_BLOCK + i * (K_ELEMS * 128), &tmB, n0 + 64 * i,
+                                                 (kb + sb) * K_ELEMS, pol_b);
+                                    } else {
+                                        load(b_dst + sb * C_::B_BLOCK, &tmB, (kb + sb) * K_ELEMS, n0, pol_b);
+                                    }
                                 }
                             }
                         }
-                    }
-                    if (++s == STAGES) {
-                        s = 0;
-                        ph ^= 1u;
-                    }
-                }
-            }
-            if (!ok) {
-                // Abort: let every copy this thread issued land before the CTA exits.
-                if constexpr (CTAS == 1) {
-                    for (int q = 0; q < STAGES; ++q)
-                        if (outstanding & (1u << q))
-                            mbar_wait(FU ? &st->rfull[q] : &st->full[q], (out_phase >> q) & 1u, nullptr, nullptr, limit);
-                } else {
-                    pause_ns(200000);  // copies complete on the even CTA's barrier: allow 200 us
-                }
-            }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------ MMA issuer
-        if (lane == 0 && rank == 0) {
-            constexpr uint32_t IDESC =
-                instr_desc(EPI == EPI_F16ACC ? 0u : 1u, 0u, 0u, B_MN, kBM * CTAS,
-                           BN);  // F16 x F16 or E4M3 x E4M3 -> F32 (or F16 accumulators)
-            const uint32_t a_base = smem_u32(a_ring);
-            const uint32_t b_base = smem_u32(b_ring);
-            int s = 0;
-            uint32_t ph = 0;
-            int abuf = 0;
-            uint32_t aph = 0;
-            bool ok = true;
-            for (int t = cluster; t < args.num_vunits && ok; t += nclusters) {
-                WorkRef wr = work_unit(t, args, C_::SUB);
-                if constexpr (KS > 1) ksplit_range(wr, krank, KS);
-                const int nchunks = (wr.kb1 - wr.kb0 + args.kb_per_chunk - 1) / args.kb_per_chunk;
-                for (int ch = 0; ch < nchunks && ok; ++ch) {
-                    if (!mbar_wait(&st->acc_empty[abuf], aph ^ 1u, &st->abort, &g_error_word, limit)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const uint32_t d_tmem = tmem_base + uint32_t(abuf * BN);
-                    const int kb0 = wr.kb0 + ch * args.kb_per_chunk;
-                    const int kb1 = min(wr.kb1, kb0 + args.kb_per_chunk);
-                    for (int kb = kb0; kb < kb1 && ok; kb += C_::SUB) {
-                        const uint32_t a_addr = a_base + s * C_::A_STAGE;
-                        const uint32_t b_addr = b_base + s * C_::B_STAGE;
-#pragma unroll
-                        for (int kk = 0; kk < KSTEPS * C_::SUB; ++kk) {
-                            const int k = kk % KSTEPS;
-                            if (k == 0) {
-                                // The next K block of the stage has landed.
-                                if (!mbar_wait(&st->full[s * C_::SUB + kk / KSTEPS], ph, &st->abort, &g_error_word,
-                                               limit)) {
-                                    ok = false;
-                                    break;
-                                }
-                                tc_fence_after_sync();
-                            }
-                            const uint32_t a_blk = a_addr + (kk / KSTEPS) * C_::A_BLOCK;
-                            const uint32_t b_blk = b_addr + (kk / KSTEPS) * C_::B_BLOCK;
-                            const uint64_t adesc = smem_desc_sw128(a_blk + k * KSTEP_BYTES, 16, 1024);
-                            uint64_t bdesc;
-                            if constexpr (B_MN)
-                                bdesc = smem_desc_sw128(b_blk + k * (16 * 128), K_ELEMS * 128, 1024);
-                            else
-                                bdesc = smem_desc_sw128(b_blk + k * KSTEP_BYTES, 16, 1024);
-                            const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
-                            mma<CTAS, KIND == Kind::E4M3>(d_tmem, adesc, bdesc, IDESC, acc);
-                        }
-                        if (!ok) break;
-                        if constexpr (CTAS == 1)
-                            mma_commit<1>(&st->empty[s]);
-                        else
-                            mma_commit_pair(&st->empty[s], 0x3);
-                        if (++s == STAGES) {
+                        if (++s == PSTAGES) {
                             s = 0;
                             ph ^= 1u;
                         }
                     }
-                    if (!ok) break;
-                    if constexpr (CTAS == 1)
-                        mma_commit<1>(&st->acc_full[abuf]);
-                    else
-                        mma_commit_pair(&st->acc_full[abuf], 0x3);
-                    if (++abuf == 2) {
-                        abuf = 0;
-                        aph ^= 1u;
+                }
+                if (!ok) {
+                    // Abort: let every copy this thread issued land before the CTA exits.
+                    if constexpr (CTAS == 1 || FU) {
+                        for (int q = 0; q < PSTAGES; ++q)
+                            if (outstanding & (1u << q))
+                                mbar_wait(FU ? &st->rfull[q] : &st->full[q], (out_phase >> q) & 1u, nullptr, nullptr, limit);
+                    } else {
+                        pause_ns(200000);  // copies complete on the even CTA's barrier: allow 200 us
                     }
                 }
             }
-            if (!ok) {
-                // Abort: wait for the MMAs already issued before tensor memory is freed.
-                mma_commit<CTAS>(&st->drain);
-                mbar_wait(&st->drain, 0, nullptr, nullptr, limit);
+            __syncwarp();
+        } else if (warp == 1) {
+            // ------------------------------------------------------ MMA issuer
+            if (lane == 0 && rank == 0) {
+                constexpr uint32_t IDESC =
+                    instr_desc(EPI == EPI_F16ACC ? 0u : 1u, 0u, 0u, B_MN, kBM * CTAS,
+                               BN);  // F16 x F16 or E4M3 x E4M3 -> F32 (or F16 accumulators)
+                const uint32_t a_base = smem_u32(a_ring);
+                const uint32_t b_base = smem_u32(b_ring);
+                int s = 0;
+                uint32_t ph = 0;
+                int abuf = 0;
+                uint32_t aph = 0;
+                bool ok = true;
+                for (int t = cluster; t < args.num_vunits && ok; t += nclusters) {
+                    WorkRef wr = work_unit(t, args, C_::SUB);
+                    if constexpr (KS > 1) ksplit_range(wr, krank, KS);
+                    const int nchunks = (wr.kb1 - wr.kb0 + args.kb_per_chunk - 1) / args.kb_per_chunk;
+                    for (int ch = 0; ch < nchunks && ok; ++ch) {
+                        if (!mbar_wait(&st->acc_empty[abuf], aph ^ 1u, &st->abort, &g_error_word, limit)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        const uint32_t d_tmem = tmem_base + uint32_t(abuf * BN);
+                        const int kb0 = wr.kb0 + ch * args.kb_per_chunk;
+                        const int kb1 = min(wr.kb1, kb0 + args.kb_per_chunk);
+                        for (int kb = kb0; kb < kb1 && ok; kb += C_::SUB) {
+                            const uint32_t a_addr = a_base + s * C_::A_STAGE;
+                            const uint32_t b_addr = b_base + s * C_::B_STAGE;
+    #pragma unroll
+                            for (int kk = 0; kk < KSTEPS * C_::SUB; ++kk) {
+                                const int k = kk % KSTEPS;
+                                if (k == 0) {
+                                    // The next K block of the stage has landed.
+                                    if (!mbar_wait(&st->full[s * C_::SUB + kk / KSTEPS], ph, &st->abort, &g_error_word,
+                                                   limit)) {
+                                        ok = false;
+                                        break;
+                                    }
+                                    tc_fence_after_sync();
+                                }
+                                const uint32_t a_blk = a_addr + (kk / KSTEPS) * C_::A_BLOCK;
+                                const uint32_t b_blk = b_addr + (kk / KSTEPS) * C_::B_BLOCK;
+                                const uint64_t adesc = smem_desc_sw128(a_blk + k * KSTEP_BYTES, 16, 1024);
+                                uint64_t bdesc;
+                                if constexpr (B_MN)
+                                    bdesc = smem_desc_sw128(b_blk + k * (16 * 128), K_ELEMS * 128, 1024);
+                                else
+                                    bdesc = smem_desc_sw128(b_blk + k * KSTEP_BYTES, 16, 1024);
+                                const uint32_t acc = (kb > kb0 || kk > 0) ? 1u : 0u;
+                                mma<CTAS, KIND == Kind::E4M3>(d_tmem, adesc, bdesc, IDESC, acc);
+                            }
+                            if (!ok) break;
+                            if constexpr (CTAS == 1)
+                                mma_commit<1>(&st->empty[s]);
+                            else
+                                mma_commit_pair(&st->empty[s], 0x3);
+                            if (++s == STAGES) {
+                                s = 0;
+                                ph ^= 1u;
+                            }
+                        }
+                        if (!ok) break;
+                        if constexpr (CTAS == 1)
+                            mma_commit<1>(&st->acc_full[abuf]);
+                        else
+                            mma_commit_pair(&st->acc_full[abuf], 0x3);
+                        if (++abuf == 2) {
+                            abuf = 0;
+                            aph ^= 1u;
+                        }
+                    }
+                }
+                if (!ok) {
+                    // Abort: wait for the MMAs already issued before tensor memory is freed.
+                    mma_commit<CTAS>(&st->drain);
+                    mbar_wait(&st->drain, 0, nullptr, nullptr, limit);
+                }
             }
+            __syncwarp();
+        } else if (PFU && warp >= 2) {
+            // ------------------------------------------------------ converters
+            // CTA pairs with in-ring conversion: six converter warps (2, 3 and
+            // 12 .. 15) write each K block of this CTA's raw A (128 rows) and
+            // raw B (128 rows), 64 bytes per row, into the MMA stage in the
+            // operand type: a 16-byte piece i (row g = i / 4, piece p = i % 4)
+            // becomes chunks 2p and 2p + 1 of row g, placed by the 128-byte
+            // swizzle (chunk j of row g at j ^ (g & 7)).
+            // The raw and MMA rings have their own depths and phases.  The pair's
+            // MMAs read both CTAs' stages: each warp's arrival on the even CTA's
+            // full barrier follows a proxy fence.
+            if constexpr (PFU) {
+                // Converter threads: warps 2, 3 and 12 .. 15 (192 threads); thread
+                // ctid takes pieces ctid, ctid + 192, ... of each K block, four
+                // loads in flight before their conversions and stores.
+                constexpr int CT = 32 * (CONV_WARPS + 2);
+                constexpr int PIECES = (kBM + C_::B_ROWS) * kRawRow / 16;
+                constexpr int ITERS = (PIECES + CT - 1) / CT;
+                const int ctid = warp < EPI_WARP0 ? int(threadIdx.x) - 64 : int(threadIdx.x) - 32 * C_::CONV_WARP0 + 64;
+                int q = 0, r = 0;
+                uint32_t qph = 0, rph = 0;
+                bool ok = true;
+                for (int t = cluster; t < args.num_vunits && ok; t += nclusters) {
+                    const WorkRef wr = work_unit(t, args, C_::SUB);
+                    for (int kb = wr.kb0; kb < wr.kb1; ++kb) {
+                        if (!warp_wait(&st->rfull[r], rph, &st->abort, limit, lane) ||
+                            !warp_wait(&st->empty[q], qph ^ 1u, &st->abort, limit, lane)) {
+                            ok = false;
+                            break;
+                        }
+                        // Every lane observes both completed phases before its accesses.
+                        mbar_try_wait(&st->rfull[r], rph);
+                        mbar_try_wait(&st->empty[q], qph ^ 1u);
+                        const uint32_t raw = smem_u32(raw_ring) + uint32_t(r * C_::RAW_STAGE);
+                        const uint32_t dst_a = smem_u32(a_ring) + uint32_t(q * C_::A_STAGE);
+                        const uint32_t dst_b = smem_u32(b_ring) + uint32_t(q * C_::B_STAGE);
+#pragma unroll
+                        for (int it0 = 0; it0 < ITERS; it0 += 4) {
+                            uint4 x[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int i = (it0 + u) * CT + ctid;
+                                if (it0 + u < ITERS && i < PIECES) x[u] = ld_shared_v4(raw + uint32_t(i) * 16u);
+                            }
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int i = (it0 + u) * CT + ctid;
+                                if (it0 + u >= ITERS || i >= PIECES) continue;
+                                const int g = i >> 2, p = i & 3;
+                                uint4 o0, o1;
+                                if constexpr (KIND == Kind::F16)
+                                    cvt_s8_f16_x16(x[u], o0, o1);
+                                else
+                                    cvt_s4_e4m3_x32(x[u], o0, o1);
+                                const uint32_t row = g < kBM ? dst_a + uint32_t(g) * 128u : dst_b + uint32_t(g - kBM) * 128u;
+                                st_shared_v4(row + (uint32_t((2 * p) ^ (g & 7)) << 4), o0.x, o0.y, o0.z, o0.w);
+                                st_shared_v4(row + (uint32_t((2 * p + 1) ^ (g & 7)) << 4), o1.x, o1.y, o1.z, o1.w);
+                            }
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            if (rank == 0)
+                                mbar_arrive(&st->full[q]);
+                            else
+                                mbar_arrive_cluster(mapa_shared(smem_u32(&st->full[q]), 0));
+                            mbar_arrive(&st->rempty[r]);
+                        }
+                        if (++q == STAGES) {
+                            q = 0;
+                            qph ^= 1u;
+                        }
+                        if (++r == C_::RSTAGES) {
+                            r = 0;
+                            rph ^= 1u;
+                        }
+                    }
+                }
+            }
+            __syncwarp();
         }
-        __syncwarp();
     } else {
+        // The epilogue warpgroups raise their register budget (16-warp layout).
+        if constexpr (PFU) regs_inc<kRegsHigh>();
         // ------------------------------------------------------ epilogue
+        const int ew = warp - EPI_WARP0;    // epilogue warp 0 .. 7
         const int q = warp & 3;             // tensor-memory lane quarter
-        const int h = (warp - 2) >> 2;      // column half of the tile
+        const int h = ew >> 2;              // column half of the tile
         // The unit whose 4-byte C goes out by TMA stores (this cluster's last, or
         // none), and this warp's four C staging blocks in the idle ring.
         const int tma_t = (EPI == EPI_F32 && args.c_tma && cluster < args.num_vunits)
                               ? cluster + (args.num_vunits - 1 - cluster) / nclusters * nclusters
                               : -1;
-        const uint32_t stg = smem_u32(smem) + uint32_t(warp - 2) * uint32_t(kStageWarp);
+        const uint32_t stg = smem_u32(smem) + uint32_t(ew) * uint32_t(kStageWarp);
         bool stg_pending = false;           // TMA stores may still be reading the blocks
         const uint32_t t_lane = tmem_base + (uint32_t(32 * q) << 16) + uint32_t(h * HALF);
         // Accumulator buffers are released on the issuing (even) CTA's barriers.
@@ -990,7 +1111,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t cph = 0;
         auto convert = [&](int kb0, int kb1, auto wide) -> bool {
             constexpr bool WIDE = decltype(wide)::value;
-            const int ctid = int(threadIdx.x) - 64;
+            const int ctid = int(threadIdx.x) - 32 * EPI_WARP0;
             for (int kb = kb0; kb < kb1; ++kb) {
                 if (!warp_wait(&st->rfull[cs], cph, &st->abort, limit, lane)) return false;
                 if (!warp_wait(&st->empty[cs], cph ^ 1u, &st->abort, limit, lane)) return false;
@@ -1075,7 +1196,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int c0 = wr.kb0 + c * args.kb_per_chunk;
                     return convert(c0, min(wr.kb1, c0 + args.kb_per_chunk), wide);
                 };
-                if constexpr (FU) {
+                if constexpr (FU && !PFU) {
                     if ((nchunks > 0 && !convert_chunk(0, std::true_type{})) ||
                         (nchunks > 1 && !convert_chunk(1, std::true_type{}))) {
                         ok = false;
@@ -1104,7 +1225,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         abuf = 0;
                         aph ^= 1u;
                     }
-                    if constexpr (FU) {
+                    if constexpr (FU && !PFU) {
                         if (ch + 2 < nchunks && !convert_chunk(ch + 2, std::false_type{})) {
                             ok = false;
                             break;
@@ -1278,9 +1399,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         // Every CTA's partial sums are in its ring (barrier release / acquire at
         // cluster scope); each completes its rows of the tile from all of them.
         cluster_sync();
-        if (warp >= 2 && cluster < args.num_vunits) {
+        if (warp >= EPI_WARP0 && warp < EPI_WARP0 + EPI_WARPS && cluster < args.num_vunits) {
             const WorkRef wr = work_unit(cluster, args, C_::SUB);
-            ksplit_complete<EPI, KS, BN>(args, wr.mb, wr.nb, krank, smem_u32(smem), warp - 2, lane);
+            ksplit_complete<EPI, KS, BN>(args, wr.mb, wr.nb, krank, smem_u32(smem), warp - EPI_WARP0, lane);
         }
     }
     // A K-split cluster's peers read this CTA's ring until this barrier.
@@ -1325,7 +1446,7 @@ template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, boo
 void launch_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[2], bool pdl, cudaStream_t stream) {
     std::memset(&cfg, 0, sizeof(cfg));
     std::memset(attr, 0, sizeof(attr));
-    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.blockDim = dim3(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1, 1);
     cfg.dynamicSmemBytes = smem_bytes<CTAS, SUBK, BN, FU>();
     cfg.stream = stream;
     cfg.attrs = attr;
@@ -1563,6 +1684,7 @@ cudaError_t launch_gemm(Kind kind, bool b_mn_major, int epi, int ctas, const CUt
     } while (0)
 #define PTC_LAUNCH_FU(K)                                                                                \
     do {                                                                                                \
+        if (ctas == 2) return launch_one<K, false, EPI_INT, 2, 1, 1, kBN, true>(ta, tb, args, sms, pool, stream); \
         if (bn == 64 && ks == 4) return launch_one<K, false, EPI_INT, 1, 1, 4, 64, true>(ta, tb, args, sms, pool, stream); \
         if (bn == 64 && ks == 2) return launch_one<K, false, EPI_INT, 1, 1, 2, 64, true>(ta, tb, args, sms, pool, stream); \
         if (bn == 128 && ks == 4) return launch_one<K, false, EPI_INT, 1, 1, 4, 128, true>(ta, tb, args, sms, pool, stream); \
@@ -1577,8 +1699,9 @@ cudaError_t launch_gemm(Kind kind, bool b_mn_major, int epi, int ctas, const CUt
     if (kind == Kind::F16 && b_mn_major && epi == EPI_F32) PTC_LAUNCH(Kind::F16, true, EPI_F32);
     if (kind == Kind::F16 && b_mn_major && epi == EPI_F16ACC) PTC_LAUNCH(Kind::F16, true, EPI_F16ACC);
     if (args.in_ring != 0) {
-        // In-ring conversion: one-CTA integer launches with K-major B.
-        if (ctas != 1 || b_mn_major || epi != EPI_INT) return cudaErrorInvalidValue;
+        // In-ring conversion: integer launches with K-major B (one CTA per
+        // tile, or CTA pairs with dedicated converter warps).
+        if (b_mn_major || epi != EPI_INT) return cudaErrorInvalidValue;
         if (kind == Kind::F16) PTC_LAUNCH_FU(Kind::F16);
         if (kind == Kind::E4M3) PTC_LAUNCH_FU(Kind::E4M3);
         return cudaErrorInvalidValue;

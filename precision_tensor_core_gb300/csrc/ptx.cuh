@@ -157,6 +157,13 @@ __device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap *map, uint32
 // Orders this thread's view of global memory written through the generic
 // proxy (ordinary stores, here made visible to it by an acquire) before its
 // later asynchronous-proxy (TMA) accesses of global memory.
+// Orders this thread's generic-proxy writes (any state space) before later
+// async-proxy accesses: used before a CTA pair's tensor cores read shared
+// memory that threads of either CTA wrote.
+__device__ __forceinline__ void fence_proxy_async_all() {
+    asm volatile("fence.proxy.async;" ::: "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
@@ -403,6 +410,21 @@ __device__ __forceinline__ void tmem_ld_16cols(uint32_t taddr, uint32_t (&r)[16]
 
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- registers
+// Per-warpgroup register budget (all four warps of the warpgroup execute the
+// same instruction): .dec returns registers to the CTA's pool, .inc waits
+// until the pool holds enough and takes them.  The budgets of the CTA's
+// warpgroups must sum to at most the registers it was launched with.  ptxas
+// allocates the code that an instruction dominates within its budget.
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
 }
 
 // ---------------------------------------------------------------- descriptors
