@@ -276,6 +276,13 @@ int gemm_s4_host(int64_t M, int64_t N, int64_t K,
  *   PTC_BASELINE_S8_MMA    mma.sync m16n8k32, s8 -> s32      (int8_ptx_mma_k32)
  *   PTC_BASELINE_S4_WMMA   WMMA m8n8k32, s4 -> s32           (int4_wmma)
  *   PTC_BASELINE_S4_MMA    mma.sync m16n8k64, s4 -> s32      (int4_ptx_mma_k64)
+ *   PTC_BASELINE_F16_LDMATRIX, PTC_BASELINE_S8_LDMATRIX, PTC_BASELINE_S4_LDMATRIX
+ *                          the three mma.sync kernels with their fragments
+ *                          loaded by ldmatrix (A: .x4, B: .x2; FP16 B with
+ *                          .trans), the fragment path of the paper's fastest
+ *                          INT8 / INT4 kernels (Table VI, Listing 2); the
+ *                          *_MMA variants pack fragments from scalar 32-bit
+ *                          shared loads (the paper's manual-pack family)
  * Operands and C have the layouts of gemm_f16 / gemm_s8 / gemm_s4 (C FP32 for
  * the FP16 variants, int32 otherwise).  Restrictions of these simple kernels:
  * M % 32 == 0, N % 64 == 0, K a positive multiple of 32 (FP16), 64 (INT8) or
@@ -289,6 +296,9 @@ int gemm_s4_host(int64_t M, int64_t N, int64_t K,
 #define PTC_BASELINE_S8_MMA 3
 #define PTC_BASELINE_S4_WMMA 4
 #define PTC_BASELINE_S4_MMA 5
+#define PTC_BASELINE_F16_LDMATRIX 6
+#define PTC_BASELINE_S8_LDMATRIX 7
+#define PTC_BASELINE_S4_LDMATRIX 8
 
 int gemm_baseline(int variant, int64_t M, int64_t N, int64_t K,
                   const void *A, int64_t lda,

@@ -47,6 +47,9 @@ PTC_BASELINE_S8_WMMA = 2
 PTC_BASELINE_S8_MMA = 3
 PTC_BASELINE_S4_WMMA = 4
 PTC_BASELINE_S4_MMA = 5
+PTC_BASELINE_F16_LDMATRIX = 6
+PTC_BASELINE_S8_LDMATRIX = 7
+PTC_BASELINE_S4_LDMATRIX = 8
 
 PTC_OUT_F32 = 0
 PTC_OUT_BF16 = 1

@@ -971,15 +971,15 @@ int gemm_s4_host(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, co
 int gemm_baseline(int variant, int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const void *B,
                   int64_t ldb, void *C, int64_t ldc, void *stream) {
     g_msg[0] = 0;
-    if (variant < PTC_BASELINE_F16_WMMA || variant > PTC_BASELINE_S4_MMA)
+    if (variant < PTC_BASELINE_F16_WMMA || variant > PTC_BASELINE_S4_LDMATRIX)
         return fail(PTC_ERR_INVALID, "unknown baseline variant");
     const ptc::Variant v = static_cast<ptc::Variant>(variant);
     int rc = check_sizes(M, N, K);
     if (rc) return rc;
     if (M == 0 || N == 0) return PTC_OK;
     if ((rc = check_ld(K > 0 ? lda : 0, K > 0 ? ldb : 0, ldc))) return rc;
-    const bool f16 = v == ptc::BASE_F16_WMMA || v == ptc::BASE_F16_MMA;
-    const bool s4 = v == ptc::BASE_S4_WMMA || v == ptc::BASE_S4_MMA;
+    const bool f16 = v == ptc::BASE_F16_WMMA || v == ptc::BASE_F16_MMA || v == ptc::BASE_F16_LDM;
+    const bool s4 = v == ptc::BASE_S4_WMMA || v == ptc::BASE_S4_MMA || v == ptc::BASE_S4_LDM;
     const int kmult = ptc::baseline_k_multiple(v);
     if (M % 32 || N % 64 || K % kmult || K == 0)
         return fail(PTC_ERR_INVALID, "baseline kernels need M % 32 == 0, N % 64 == 0 and K a positive multiple "

@@ -11,6 +11,13 @@
 // instructions; they are comparison points for the tcgen05 kernels, not the
 // library's fast path.
 //
+// Fragments of the mma.sync kernels come either from scalar 32-bit shared
+// loads packed by hand (the *_MMA variants) or from ldmatrix (*_LDM: A as four
+// 8 x 8 b16 matrices with .x4, B as two with .x2; the FP16 kernel's row-major
+// B tile is transposed by the load), the fragment path of the paper's fastest
+// INT8 / INT4 kernels (section IV-B/IV-C, Table VI; Listing 2 loads A with
+// ldmatrix.x4 and B with .x2 before each m16n8k64).
+//
 // Block: 256 threads = 8 warps, block tile 32 (M) x 64 (N), warp (wy, wx)
 // owns rows 16 wy .. +15 and columns 16 wx .. +15.  Per stage 64 bytes of K
 // per operand row (32 FP16, 64 INT8 or 128 INT4 values), rows padded by 16
@@ -69,6 +76,9 @@ template <> struct Shape<BASE_S8_WMMA> : StageShape<64, false, true> {};
 template <> struct Shape<BASE_S8_MMA> : StageShape<64, false, false> {};
 template <> struct Shape<BASE_S4_WMMA> : StageShape<128, false, true> {};
 template <> struct Shape<BASE_S4_MMA> : StageShape<128, false, false> {};
+template <> struct Shape<BASE_F16_LDM> : StageShape<32, true, false> {};
+template <> struct Shape<BASE_S8_LDM> : StageShape<64, false, false> {};
+template <> struct Shape<BASE_S4_LDM> : StageShape<128, false, false> {};
 
 // Copies stage kt of the block's A rows and B tile into shared memory.
 // lda_b / ldb_b are row pitches in bytes of the global operands.
@@ -99,6 +109,32 @@ __device__ __forceinline__ void load_stage(uint8_t *sa, uint8_t *sb, const uint8
 
 __device__ __forceinline__ uint32_t ld32(const uint8_t *p) { return *reinterpret_cast<const uint32_t *>(p); }
 
+// ldmatrix: lane t supplies the address of row t % 8 of 8 x 8 b16 matrix t / 8
+// (16 contiguous bytes); register i of lane t receives the 32 bits at row
+// t / 4, columns 2 (t % 4) .. +1 of matrix i (.trans: of its transpose).
+__device__ __forceinline__ void ldm_x4(const uint8_t *row, uint32_t &r0, uint32_t &r1, uint32_t &r2, uint32_t &r3) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(row));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(a));
+}
+__device__ __forceinline__ void ldm_x2(const uint8_t *row, uint32_t &r0, uint32_t &r1) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(row));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(a));
+}
+__device__ __forceinline__ void ldm_x2_trans(const uint8_t *row, uint32_t &r0, uint32_t &r1) {
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(row));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(a));
+}
+
+// A fragment of one 16 x 16-byte slice (bytes kb .. kb + 31 of the warp's 16
+// rows at PITCH): matrices rows 0-7 / 8-15 x bytes 0-15 / 16-31, which is the
+// register order a0..a3 of m16n8k16 (FP16), m16n8k32 (s8) and m16n8k64 (s4).
+__device__ __forceinline__ void ldm_a(const uint8_t *sa, int kb, int lane, uint32_t (&a)[4]) {
+    const int r = (lane & 7) + 8 * ((lane >> 3) & 1);
+    ldm_x4(sa + r * PITCH + kb + 16 * (lane >> 4), a[0], a[1], a[2], a[3]);
+}
+
 template <Variant V>
 __global__ void __launch_bounds__(THREADS)
     baseline_kernel(const uint8_t *A, int64_t lda_b, const uint8_t *B, int64_t ldb_b, void *C, int64_t ldc,
@@ -109,7 +145,7 @@ __global__ void __launch_bounds__(THREADS)
     const int wy = warp / 4, wx = warp % 4;
     const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
     const int kt_n = K / S::K;
-    constexpr bool INT_C = !(V == BASE_F16_WMMA || V == BASE_F16_MMA);
+    constexpr bool INT_C = !(V == BASE_F16_WMMA || V == BASE_F16_MMA || V == BASE_F16_LDM);
 
     // Accumulators: WMMA fragments, or mma.sync registers for two n8 tiles.
     wmma::fragment<wmma::accumulator, 16, 16, 16, float> acc_f;
@@ -214,6 +250,50 @@ __global__ void __launch_bounds__(THREADS)
                         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
                 }
             }
+        } else if constexpr (V == BASE_F16_LDM) {
+#pragma unroll
+            for (int k = 0; k < S::K; k += 16) {
+                uint32_t a[4];
+                ldm_a(sa, k * 2, lane, a);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    // B rows k .. k + 15 (K) of the row-major tile, the 8 columns
+                    // of tile j, transposed into the k-pair fragment b0, b1.
+                    uint32_t b0, b1;
+                    const int kr = k + (lane & 7) + 8 * ((lane >> 3) & 1);
+                    ldm_x2_trans(sb + kr * S::B_PITCH + (wx * 16 + j * 8) * 2, b0, b1);
+                    asm volatile(
+                        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                        "{%0,%1,%2,%3};"
+                        : "+f"(cf[j][0]), "+f"(cf[j][1]), "+f"(cf[j][2]), "+f"(cf[j][3])
+                        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+                }
+            }
+        } else if constexpr (V == BASE_S8_LDM || V == BASE_S4_LDM) {
+#pragma unroll
+            for (int k = 0; k < ROWB; k += 32) {  // 32 bytes per step: k32 of s8, k64 of s4
+                uint32_t a[4];
+                ldm_a(sa, k, lane, a);
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    // Column-major B: the 8 N-rows of tile j, bytes k .. k + 15 and
+                    // k + 16 .. k + 31 (lanes 0-7 and 8-15 give the row addresses).
+                    uint32_t b0, b1;
+                    ldm_x2(sb + (wx * 16 + j * 8 + (lane & 7)) * PITCH + k + 16 * ((lane >> 3) & 1), b0, b1);
+                    if constexpr (V == BASE_S8_LDM)
+                        asm volatile(
+                            "mma.sync.aligned.m16n8k32.row.col.s32.s8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                            "{%0,%1,%2,%3};"
+                            : "+r"(ci[j][0]), "+r"(ci[j][1]), "+r"(ci[j][2]), "+r"(ci[j][3])
+                            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+                    else
+                        asm volatile(
+                            "mma.sync.aligned.m16n8k64.row.col.s32.s4.s4.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+                            "{%0,%1,%2,%3};"
+                            : "+r"(ci[j][0]), "+r"(ci[j][1]), "+r"(ci[j][2]), "+r"(ci[j][3])
+                            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+                }
+            }
         } else {  // BASE_S4_MMA
 #pragma unroll
             for (int k = 0; k < S::K / 2; k += 32) {  // k in bytes; 64 nibbles per step
@@ -282,9 +362,11 @@ cudaError_t launch_v(const void *A, int64_t lda_b, const void *B, int64_t ldb_b,
 int baseline_k_multiple(Variant v) {
     switch (v) {
         case BASE_F16_WMMA:
-        case BASE_F16_MMA: return 32;
+        case BASE_F16_MMA:
+        case BASE_F16_LDM: return 32;
         case BASE_S8_WMMA:
-        case BASE_S8_MMA: return 64;
+        case BASE_S8_MMA:
+        case BASE_S8_LDM: return 64;
         default: return 128;
     }
 }
@@ -298,6 +380,9 @@ cudaError_t launch_baseline(Variant v, const void *A, int64_t lda_b, const void 
         case BASE_S8_MMA: return launch_v<BASE_S8_MMA>(A, lda_b, B, ldb_b, C, ldc, M, N, K, s);
         case BASE_S4_WMMA: return launch_v<BASE_S4_WMMA>(A, lda_b, B, ldb_b, C, ldc, M, N, K, s);
         case BASE_S4_MMA: return launch_v<BASE_S4_MMA>(A, lda_b, B, ldb_b, C, ldc, M, N, K, s);
+        case BASE_F16_LDM: return launch_v<BASE_F16_LDM>(A, lda_b, B, ldb_b, C, ldc, M, N, K, s);
+        case BASE_S8_LDM: return launch_v<BASE_S8_LDM>(A, lda_b, B, ldb_b, C, ldc, M, N, K, s);
+        case BASE_S4_LDM: return launch_v<BASE_S4_LDM>(A, lda_b, B, ldb_b, C, ldc, M, N, K, s);
     }
     return cudaErrorInvalidValue;
 }

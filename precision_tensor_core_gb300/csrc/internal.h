@@ -164,6 +164,11 @@ enum Variant : int {
     BASE_S8_MMA = 3,
     BASE_S4_WMMA = 4,
     BASE_S4_MMA = 5,
+    // The same mma.sync kernels with fragments loaded by ldmatrix (A: .x4,
+    // B: .x2, FP16 B transposed on the load).
+    BASE_F16_LDM = 6,
+    BASE_S8_LDM = 7,
+    BASE_S4_LDM = 8,
 };
 // K must be a multiple of this many values for variant v (M of 32, N of 64).
 int baseline_k_multiple(Variant v);

@@ -265,7 +265,10 @@ def main():
     elif a.mode == "baselines":
         base = {"fp16_wmma": ("f16", ptc.PTC_BASELINE_F16_WMMA), "fp16_ptx_mma": ("f16", ptc.PTC_BASELINE_F16_MMA),
                 "int8_wmma": ("s8", ptc.PTC_BASELINE_S8_WMMA), "int8_ptx_mma_k32": ("s8", ptc.PTC_BASELINE_S8_MMA),
-                "int4_wmma": ("s4", ptc.PTC_BASELINE_S4_WMMA), "int4_ptx_mma_k64": ("s4", ptc.PTC_BASELINE_S4_MMA)}
+                "int4_wmma": ("s4", ptc.PTC_BASELINE_S4_WMMA), "int4_ptx_mma_k64": ("s4", ptc.PTC_BASELINE_S4_MMA),
+                "fp16_ptx_ldmatrix": ("f16", ptc.PTC_BASELINE_F16_LDMATRIX),
+                "int8_ptx_ldm_k32": ("s8", ptc.PTC_BASELINE_S8_LDMATRIX),
+                "int4_ptx_ldm_k64": ("s4", ptc.PTC_BASELINE_S4_LDMATRIX)}
         print(f"{'N':>6} {'kernel':>18} {'ms':>10} {'TOPS':>9} {'vs same-prec WMMA':>18} {'vs FP16 WMMA':>13}")
         for n in [int(x) for x in a.sizes.split(",")]:
             ops = operands(n)

@@ -1,6 +1,7 @@
 """GPU parity of the paper's kernel families on GB300 (gemm_baseline):
-WMMA and mma.sync kernels for FP16, INT8 and INT4 against the oracle
-(INT bit-exact, FP16 within the FP16 tolerance)."""
+WMMA and mma.sync kernels for FP16, INT8 and INT4, with hand-packed and
+ldmatrix fragments, against the oracle (INT bit-exact, FP16 within the FP16
+tolerance)."""
 import numpy as np
 import pytest
 import torch
@@ -16,6 +17,8 @@ VARIANTS = {
     "f16_wmma": ptc.PTC_BASELINE_F16_WMMA, "f16_mma": ptc.PTC_BASELINE_F16_MMA,
     "s8_wmma": ptc.PTC_BASELINE_S8_WMMA, "s8_mma": ptc.PTC_BASELINE_S8_MMA,
     "s4_wmma": ptc.PTC_BASELINE_S4_WMMA, "s4_mma": ptc.PTC_BASELINE_S4_MMA,
+    "f16_ldmatrix": ptc.PTC_BASELINE_F16_LDMATRIX, "s8_ldmatrix": ptc.PTC_BASELINE_S8_LDMATRIX,
+    "s4_ldmatrix": ptc.PTC_BASELINE_S4_LDMATRIX,
 }
 
 
