@@ -12,6 +12,8 @@ memory nor any allocator's holdings.
 This file is collected last on purpose: if it fails, a run that stops at the
 first failure has already run every other test.
 """
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -92,6 +94,7 @@ def test_noalloc_calls_allocate_nothing():
 
     call()  # set-up and first use of these kernels
     torch.cuda.synchronize()
+    gc.collect()  # tensors of earlier tests are freed now, not during the calls
     free0, _ = torch.cuda.mem_get_info()
     reserved0, allocated0 = torch.cuda.memory_reserved(), torch.cuda.memory_allocated()
     for _ in range(5):
@@ -99,6 +102,8 @@ def test_noalloc_calls_allocate_nothing():
     torch.cuda.synchronize()
     free1, _ = torch.cuda.mem_get_info()
     assert free1 == free0
-    assert torch.cuda.memory_reserved() == reserved0 and torch.cuda.memory_allocated() == allocated0
+    # torch's caching allocator holds the same memory and hands out no more
+    # (the library never calls it).
+    assert torch.cuda.memory_reserved() == reserved0 and torch.cuda.memory_allocated() <= allocated0
     assert np.array_equal(C.cpu().numpy(), oracle.wrap_s32(oracle.gemm_s8(A, Bt)))
     assert ptc.gemm_poll_device_error() == ptc.PTC_OK
