@@ -2,6 +2,7 @@
 
     python -m precision_tensor_core_gb300.tune --mode knobs --n 8192
     python -m precision_tensor_core_gb300.tune --mode sizes --sizes 512,1024,2048,4096,8192
+    python -m precision_tensor_core_gb300.tune --mode ab --n 8192 --settings "defaults;pair_in_ring=2"
 
 `baselines` times the paper's kernel families on GB300 (gemm_baseline: WMMA
 and mma.sync) beside the library's tcgen05 entry points at each size, and
@@ -29,6 +30,13 @@ interleaved in one process so that both see the same clocks and power state:
 10 rounds of one CUDA-graph replay each, then ~1 s of back-to-back replays per
 kernel.
 
+`ab` compares whole settings of the tuning knobs (`--settings`, separated by
+semicolons, each a comma-separated list of key=value; "defaults" is the
+library's defaults) in one process: `--rounds` rounds, each running every
+setting in a shuffled order for every precision of `--precs`, with the clock
+record on; it prints the median per call, the throughput, the median SM clock
+the GEMM kernels ran at and the throughput per GHz of that clock.
+
 Calls are captured in a CUDA graph (`--graph`, default on) and the graph is
 replayed, so that the host-side cost of a Python call does not hide the GPU
 time at small sizes; times are CUDA-event times of the replay divided by the
@@ -49,7 +57,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 DEFAULTS = {"cta_pair": 0, "group_m": 8, "l2_hint": 0, "s8_chunk_kb": 16, "s4_chunk_kb": 64, "tail_split": 1,
-            "split_min_kb": 64, "pair_stage_kb": 2, "ksplit": 0, "pdl": 1, "tile_n": 0, "in_ring": 1}
+            "split_min_kb": 64, "pair_stage_kb": 2, "ksplit": 0, "pdl": 1, "tile_n": 0, "in_ring": 1,
+            "pair_in_ring": 0}
 KNOBS = {"cta_pair": [1, 2], "pair_stage_kb": [1], "tail_split": [0], "split_min_kb": [32, 128],
          "group_m": [4, 16, 32], "l2_hint": [1, 2, 3], "s8_chunk_kb": [4, 8], "s4_chunk_kb": [2, 8, 16, 128],
          "ksplit": [1, 2, 4, 8], "pdl": [0], "tile_n": [64, 128, 256], "in_ring": [0]}
@@ -72,7 +81,11 @@ LAUNCH_SETTINGS = [("256-wide, plain launches", {"tile_n": 256, "ksplit": 1, "pd
 
 def main():
     p = argparse.ArgumentParser()
-    p.add_argument("--mode", choices=["knobs", "sizes", "variants", "baselines", "cublas", "launch"], default="sizes")
+    p.add_argument("--mode", choices=["knobs", "sizes", "variants", "baselines", "cublas", "launch", "ab"],
+                   default="sizes")
+    p.add_argument("--settings", default="defaults", help="ab mode: knob settings separated by ';'")
+    p.add_argument("--precs", default="f16,s8,s4", help="ab mode: precisions")
+    p.add_argument("--rounds", type=int, default=10, help="ab mode: shuffled rounds")
     p.add_argument("--n", type=int, default=8192)
     p.add_argument("--sizes", default="512,1024,2048,4096,8192")
     p.add_argument("--calls", type=int, default=0, help="calls per timing (0: by size)")
@@ -153,7 +166,48 @@ def main():
         return out
 
     results = {}
-    if a.mode == "launch":
+    if a.mode == "ab":
+        import random
+        import statistics
+
+        settings = []
+        for text in a.settings.split(";"):
+            text = text.strip()
+            kv = {} if text in ("", "defaults") else dict(x.split("=") for x in text.split(","))
+            settings.append((text or "defaults", {k: int(v) for k, v in kv.items()}))
+        precs = a.precs.split(",")
+        ops = operands(a.n)
+        calls = a.calls or max(4, min(200, int(2e13 / (2.0 * a.n ** 3))))
+        fam = {"f16": 0, "s8": 1, "s4": 2}
+        us = {(i, p): [] for i in range(len(settings)) for p in precs}
+        mhz = {(i, p): [] for i in range(len(settings)) for p in precs}
+        for r in range(a.rounds):
+            order = list(range(len(settings)))
+            random.Random(r).shuffle(order)
+            for i in order:
+                for k, v in settings[i][1].items():
+                    ptc.ptc_set_tuning(k, v)
+                for prec in precs:
+                    ptc.ptc_clock_probe_read()
+                    ptc.ptc_set_tuning("clock_probe", 1)
+                    ms = time_ms(call(prec, ops, a.n), calls)
+                    ptc.ptc_set_tuning("clock_probe", 0)
+                    cyc, ns, _ = ptc.ptc_clock_probe_read()
+                    us[(i, prec)].append(ms * 1e3)
+                    mhz[(i, prec)].append(1e3 * cyc[fam[prec]] / max(1, ns[fam[prec]]))
+                for k, v in DEFAULTS.items():
+                    ptc.ptc_set_tuning(k, v)
+        print(f"{'N':>6} {'setting':>28} {'prec':>5} {'us/call':>9} {'TOPS':>8} {'MHz':>6} {'TOPS/GHz':>9}")
+        for i, (name, _) in enumerate(settings):
+            results[name] = {}
+            for prec in precs:
+                u = statistics.median(us[(i, prec)])
+                m = statistics.median(mhz[(i, prec)])
+                tops = 2.0 * a.n ** 3 / (u * 1e-6) / 1e12
+                results[name][prec] = {"us": u, "tops": tops, "mhz": m, "rounds": us[(i, prec)]}
+                print(f"{a.n:>6} {name:>28} {prec:>5} {u:>9.1f} {tops:>8.1f} {m:>6.0f} {tops / m * 1e3:>9.1f}",
+                      flush=True)
+    elif a.mode == "launch":
         import statistics
 
         def graph_median_us(fn, calls):
