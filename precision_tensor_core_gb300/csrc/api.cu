@@ -994,8 +994,9 @@ int gemm_baseline(int variant, int64_t M, int64_t N, int64_t K, const void *A, i
     if ((reinterpret_cast<uintptr_t>(C) & 31u) || ldc % 8)
         return fail(PTC_ERR_ALIGN, "C must be 32-byte aligned, ldc % 8 == 0");
     const uint64_t cbytes = span_bytes(M, N, ldc, 4, 1);
-    if (overlaps(C, cbytes, A, uint64_t((M - 1) * lda_b) + uint64_t(f16 ? K * 2 : (s4 ? (K + 1) / 2 : K))) ||
-        overlaps(C, cbytes, B, uint64_t(((f16 ? K : N) - 1) * ldb_b) + uint64_t(f16 ? N * 2 : (s4 ? (K + 1) / 2 : K))))
+    const int64_t a_row_bytes = f16 ? K * 2 : (s4 ? (K + 1) / 2 : K);
+    if (overlaps(C, cbytes, A, span_bytes(M, a_row_bytes, lda_b, 1, 1)) ||
+        overlaps(C, cbytes, B, f16 ? span_bytes(K, N * 2, ldb_b, 1, 1) : span_bytes(N, a_row_bytes, ldb_b, 1, 1)))
         return fail(PTC_ERR_OVERLAP, "C overlaps A or B");
     int dev;
     DevInfo *d;

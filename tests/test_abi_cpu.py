@@ -210,3 +210,20 @@ def test_clock_probe_read_without_device(L):
     for bad in (2, -1):
         assert L.ptc_set_tuning(b"clock_probe", bad) == ptc.PTC_ERR_INVALID
     assert L.ptc_set_tuning(b"clock_probe", 0) == ptc.PTC_OK
+
+
+def test_baseline_argument_checks(L):
+    """gemm_baseline: unknown variants, a leading dimension above 2^36 and C
+    overlapping A are refused before any CUDA call."""
+    args = dict(M=64, N=64, K=128, A=BASE, lda=128, B=BASE + (1 << 30), ldb=128, C=BASE + (1 << 31), ldc=64)
+
+    def base(v, **kw):
+        a = {**args, **kw}
+        return L.gemm_baseline(v, a["M"], a["N"], a["K"], a["A"], a["lda"], a["B"], a["ldb"], a["C"], a["ldc"], None)
+
+    assert base(9) == ptc.PTC_ERR_INVALID and base(-1) == ptc.PTC_ERR_INVALID
+    for v in (ptc.PTC_BASELINE_S8_MMA, ptc.PTC_BASELINE_S8_LDMATRIX):
+        assert base(v, ldc=(1 << 36) + 64) == ptc.PTC_ERR_INVALID
+        assert base(v, C=BASE + 64 * 64) == ptc.PTC_ERR_OVERLAP
+        # a pitch so large that (M - 1) * pitch leaves 64 bits is refused, not wrapped
+        assert base(v, lda=(1 << 36) + 16) == ptc.PTC_ERR_INVALID
