@@ -20,6 +20,9 @@
 //               blocks staged in the then idle ring and written by TMA stores
 //               where nothing hides the epilogue (4-byte C of a single-wave
 //               launch, and the last tile of each cluster in FP32 C).
+//   (CTA pairs that convert integer operands in the kernel run 16 warps:
+//   producer, MMA issuer, converter warps 2-3, epilogue warps 4-11 and
+//   converter warps 12-15; see Cfg::PFU.)
 //
 // Shapes of the same kernel:
 //   CTAS = 1    one CTA per 128 x BN output tile (M = 128 MMAs): BN = 256 with
@@ -95,15 +98,15 @@ namespace {
 constexpr int EPI_WARPS = 8;
 constexpr int THREADS = 64 + 32 * EPI_WARPS;  // warps 0, 1 and the epilogue warps 2 .. 9
 // CTA pairs with in-ring conversion: 16 warps.  Warpgroup 0 holds the producer
-// (warp 0), the MMA issuer (warp 1) and two idle warps, warpgroups 1 and 2 the
-// epilogue warps (4 .. 11), warpgroup 3 four converter warps (12 .. 15).  The
+// (warp 0), the MMA issuer (warp 1) and converter warps 2 and 3, warpgroups 1
+// and 2 the epilogue warps (4 .. 11), warpgroup 3 converter warps 12 .. 15.  The
 // launch grants 128 registers per thread (65,536 / 512); warpgroups 0 and 3
 // give back all but kRegsLow (the producer, MMA and converter code fits in
 // 80 without spills), the epilogue warpgroups take kRegsHigh (their 128 int32
 // partial sums and the tensor-memory loads in flight):
 // 8 warps x 80 + 8 warps x 176 = 16 warps x 128 registers per lane.
 constexpr int PAIR_FU_THREADS = 512;
-constexpr int CONV_WARPS = 4;
+constexpr int CONV_WARPS = 4;  // converter warps of warpgroup 3 (warpgroup 0 adds two more)
 constexpr uint32_t kRegsLow = 80, kRegsHigh = 176;
 static_assert(8 * kRegsLow + 8 * kRegsHigh == (PAIR_FU_THREADS / 32) * (65536 / PAIR_FU_THREADS),
               "warpgroup register budgets sum to the launch's registers");
@@ -123,10 +126,13 @@ constexpr int KSTEPS = kRowBytes / KSTEP_BYTES; // MMAs per stage
 // ring, and converting warps write each into an MMA ring stage.  One CTA per
 // tile: the epilogue warps, idle during the K loop, convert; both rings have
 // the same depth and fit 216 KiB (6 stages for 64-wide tiles, 4 for 128-wide,
-// 3 for 256-wide).  CTA pairs: four dedicated converter warps per CTA (the
+// 3 for 256-wide).  CTA pairs: six dedicated converter warps per CTA (the
 // epilogue warps of a multi-wave product fold and store while the next tile is
 // multiplied); 8 raw stages of 16 KiB (half the bytes of a converted K block,
-// so twice the K blocks in flight per byte) and 3 MMA stages of 32 KiB.
+// so twice the K blocks in flight per byte) and 3 MMA stages of 32 KiB.  That
+// route is slower than the separate conversion pass for CTA pairs (the
+// conversion and its proxy fence take longer than a K block's MMAs) and runs
+// only when the pair_in_ring knob asks for it.
 constexpr int kRing1 = 4 * (kBM + kBN) * kRowBytes;  // one-CTA ring bytes
 constexpr int kRingFu = 216 * 1024;                  // both rings, in-ring conversion
 constexpr int kRawRow = 64;                          // raw operand bytes per row and K block
@@ -139,7 +145,7 @@ struct Cfg {
     static constexpr bool PFU = FU && CTAS == 2;  // pair with dedicated converter warps
     static constexpr int THREADS_ = PFU ? PAIR_FU_THREADS : THREADS;
     static constexpr int EPI_WARP0 = PFU ? 4 : 2;  // first epilogue warp
-    static constexpr int CONV_WARP0 = 12;          // first converter warp (PFU)
+    static constexpr int CONV_WARP0 = 12;          // first converter warp of warpgroup 3 (PFU)
     static constexpr int SUB = SUBK;  // K blocks per stage
     static constexpr int B_ROWS = BN / CTAS;
     static constexpr int A_BLOCK = kBM * kRowBytes;     // one K block of A
@@ -794,7 +800,7 @@ __global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
     constexpr int K_ELEMS = (KIND == Kind::F16) ? kRowBytes / 2 : kRowBytes;
 
     if (warp < EPI_WARP0 || (PFU && warp >= C_::CONV_WARP0)) {
-        // Producer, MMA issuer, idle and converter warps.  With the 16-warp layout
+        // Producer, MMA issuer and converter warps.  With the 16-warp layout
         // their warpgroups (0 and 3) first lower their register budget together.
         if constexpr (PFU) regs_dec<kRegsLow>();
         if (warp == 0) {
