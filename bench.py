@@ -99,13 +99,27 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
-    """First 16 hex digits of the SHA-256 of the GEMM kernel's sources."""
+def code_of(text: str) -> str:
+    """C++/CUDA source without comments and with whitespace runs collapsed, so
+    that a comment edit does not change the kernel's identity."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def kernel_source_hash(read=None) -> str:
+    """First 16 hex digits of the SHA-256 of the GEMM kernel's sources (their
+    code, comments removed).  `read(name)` supplies a file's text (default: the
+    working tree)."""
     import hashlib
+    if read is None:
+        def read(name):
+            with open(os.path.join(ROOT, "precision_tensor_core_gb300", "csrc", name)) as f:
+                return f.read()
     h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "precision_tensor_core_gb300", "csrc", name), "rb") as f:
-            h.update(name.encode() + b"\0" + f.read())
+        h.update(name.encode() + b"\0" + code_of(read(name)).encode())
     return h.hexdigest()[:16]
 
 

@@ -123,3 +123,19 @@ def test_sweep_oracle_time_measured_and_extrapolated():
     part = bench._oracle_time("s8", A, B, 64, 2, budget_s=0.0)
     assert part["rows_timed"] == 2 and part["extrapolated"]
     assert part["tops"] == pytest.approx(2.0 * 64 ** 3 / part["seconds"] / 1e12)
+
+
+def test_kernel_identity_ignores_comments_only():
+    """The traffic record is tied to the kernel's code: comment and
+    whitespace edits keep its hash, any code edit changes it."""
+    import os
+    base = {n: open(os.path.join(bench.ROOT, "precision_tensor_core_gb300", "csrc", n)).read()
+            for n in bench.KERNEL_SOURCES}
+    h0 = bench.kernel_source_hash(lambda n: base[n])
+    assert h0 == bench.kernel_source_hash()
+    commented = dict(base)
+    commented["gemm_tc.cu"] = "// a new comment\n" + base["gemm_tc.cu"].replace("\n", "\n\n", 3) + "/* tail */\n"
+    assert bench.kernel_source_hash(lambda n: commented[n]) == h0
+    edited = dict(base)
+    edited["ptx.cuh"] = base["ptx.cuh"] + "\nstatic int unused_symbol;\n"
+    assert bench.kernel_source_hash(lambda n: edited[n]) != h0
