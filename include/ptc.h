@@ -465,6 +465,16 @@ int ptc_last_conversion(int *mode);
  *                  proxy fence that publishes each converted block take
  *                  longer than the block's MMAs), so it is not the default.
  *                  Results do not depend on the choice.
+ *   "multicast"    CTA-pair products (256 x 256 tiles): 0 (default) one pair
+ *                  per thread-block cluster; 1 two pairs per cluster of four
+ *                  CTAs, computing adjacent tile columns of one tile row and
+ *                  sharing A by TMA multicast (each CTA loads half of its 128
+ *                  A rows into its own shared memory and its counterpart's in
+ *                  the other pair), which cuts the operand bytes the SMs read
+ *                  from L2 by a quarter.  Clusters of four fit 144 of the
+ *                  152 SMs, and the last-wave K split is not used.  The
+ *                  in-kernel pair conversion ("pair_in_ring" 2) keeps one
+ *                  pair per cluster.  Results do not depend on the choice.
  *   "clock_probe"  0 (default) or 1: GEMM kernels add their SM cycles and
  *                  nanoseconds to the clock record (ptc_clock_probe_read)
  *   "in_ring"      gemm_s8 / gemm_s4 (and their scaled forms) on one-CTA

@@ -53,6 +53,7 @@ std::atomic<int> g_in_ring{1};        // integer routes: operands converted in t
                                       // memory where estimated faster (0: never, 2: on every one-CTA shape)
 thread_local int g_last_conv = 0;     // operand conversion of this thread's last GEMM call
 std::atomic<int> g_clock_probe{0};   // 1: GEMM kernels add to the clock record
+std::atomic<int> g_multicast{0};     // 1: CTA-pair products run two pairs per cluster sharing A
 std::atomic<int> g_pair_in_ring{0};  // integer routes on CTA pairs: 0 a separate conversion pass,
                                      // 2 conversion inside the pair kernel (dedicated converter warps)
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
@@ -401,6 +402,7 @@ GemmArgs base_args(int64_t M, int64_t N, int64_t K, int k_elems_per_block, void 
     a.pdl = g_pdl.load();
     a.wait_limit_ns = g_wait_ns.load();
     a.probe = g_clock_probe.load();
+    a.pairs = 1;
     return a;
 }
 
@@ -470,12 +472,14 @@ int f16_gemm(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, const 
     if (K == 0) return zero_c(C, ldc, M, N, eb, *d, s);
 
     const Shape sh = choose_shape(M, N, (K + 63) / 64, d->sms, true, eb);
+    const int pairs = (sh.ctas == 2 && g_multicast.load() == 1) ? 2 : 1;
     CUtensorMap ta, tb;
-    if ((rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, uint64_t(lda) * 2, 64, ptc::kBM)))
+    if ((rc = make_tmap(&ta, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A, K, M, uint64_t(lda) * 2, 64, ptc::kBM / pairs)))
         return rc;
     if ((rc = make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, N, K, uint64_t(ldb) * 2, 64, 64)))
         return rc;
     GemmArgs args = base_args(M, N, K, 64, C, ldc, sh);
+    args.pairs = pairs;
     return launch_gemm_checked(Kind::F16, true, epi, sh.ctas, ta, tb, args, *d, s);
 }
 
@@ -604,11 +608,13 @@ int int_gemm(bool s4, int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     else
         g_launches.fetch_add(1);
     const CUtensorMapDataType dt = s4 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const int pairs = (sh.ctas == 2 && g_multicast.load() == 1) ? 2 : 1;
     CUtensorMap ta, tb;
-    if (!rc) rc = make_tmap(&ta, dt, aw, K, M, uint64_t(ldw) * wsize, k_elems, ptc::kBM);
+    if (!rc) rc = make_tmap(&ta, dt, aw, K, M, uint64_t(ldw) * wsize, k_elems, ptc::kBM / pairs);
     if (!rc) rc = make_tmap(&tb, dt, bw, K, N, uint64_t(ldw) * wsize, k_elems, sh.bn / sh.ctas);
     if (!rc) {
         GemmArgs args = base_args(M, N, K, k_elems, C, ldc, sh);
+        args.pairs = pairs;
         args.kb_per_chunk = chunk > 0 ? chunk : 1;
         args.out_mode = mode;
         args.scale_a = sa;
@@ -1160,6 +1166,10 @@ int ptc_set_tuning(const char *key, int64_t value) {
     }
     if (std::strcmp(key, "in_ring") == 0 && value >= 0 && value <= 2) {
         g_in_ring.store(int(value));
+        return PTC_OK;
+    }
+    if (std::strcmp(key, "multicast") == 0 && (value == 0 || value == 1)) {
+        g_multicast.store(int(value));
         return PTC_OK;
     }
     if (std::strcmp(key, "pair_in_ring") == 0 && (value == 0 || value == 2)) {

@@ -718,13 +718,15 @@ __device__ __forceinline__ void ksplit_complete(const GemmArgs &args, int mb, in
 // its full barriers collect both CTAs' copies, its commits arrive on both
 // CTAs' empty / accumulator-full barriers, and both CTAs' epilogues release
 // accumulator buffers on its acc_empty barriers.
-template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false>
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false, int PAIRS = 1>
 __global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
     static_assert(!(B_MN && KIND == Kind::E4M3), "MN-major B is used by the FP16 path only");
     static_assert(KS == 1 || CTAS == 1, "K-split clusters of one-CTA tiles");
     static_assert(!FU || (EPI == EPI_INT && !B_MN), "in-ring conversion: integer launches with K-major B");
+    static_assert(PAIRS == 1 || (CTAS == 2 && SUBK == 2 && KS == 1 && BN == kBN && !FU),
+                  "two pairs per cluster: two-block pair stages, operands converted by the pass");
     constexpr bool INT_OUT = EPI == EPI_INT;
     constexpr int HALF = BN / 2;      // columns of an epilogue warp's slice
     constexpr int NCH = HALF / 32;    // 32-column chunks of a slice
@@ -747,10 +749,17 @@ __global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     const uint64_t limit = args.wait_limit_ns;
-    constexpr int CL = CTAS * KS;  // CTAs per cluster
+    constexpr int CL = CTAS * KS * PAIRS;  // CTAs per cluster
     const uint32_t crank = (CL == 1) ? 0u : cluster_ctarank();
-    const uint32_t rank = (CTAS == 1) ? 0u : crank;  // CTA of a pair
+    const uint32_t rank = (CTAS == 1) ? 0u : (PAIRS == 1 ? crank : (crank & 1u));  // CTA of a pair
     const int krank = (KS == 1) ? 0 : int(crank);    // K share of a K-split cluster
+    // Two pairs per cluster (PAIRS = 2): pair pp computes tile column 2 nb + pp of
+    // unit (mb, nb); both pairs use the same rows of A, and each CTA loads half of
+    // its rows and multicasts them to itself and its counterpart in the other pair.
+    const uint32_t pp = (PAIRS == 2) ? (crank >> 1) : 0u;
+    const uint32_t leader = (PAIRS == 2) ? (crank & ~1u) : 0u;  // even CTA of this CTA's pair
+    constexpr uint16_t kAllMask = uint16_t((1u << CL) - 1u);
+    const uint16_t pair_mask = uint16_t(0x3u << (2u * pp));
     const int cluster = blockIdx.x / CL;
     const int nclusters = gridDim.x / CL;
 
@@ -761,7 +770,7 @@ __global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
         constexpr uint32_t conv_arrivals = PFU ? (CONV_WARPS + 2) * CTAS : EPI_WARPS;
         for (int s = 0; s < STAGES; ++s) {
             for (int sb = 0; sb < C_::SUB; ++sb) mbar_init(&st->full[s * C_::SUB + sb], FU ? conv_arrivals : 1);
-            mbar_init(&st->empty[s], 1);
+            mbar_init(&st->empty[s], PAIRS);  // one MMA commit per pair reading the stage
         }
         for (int s = 0; s < C_::RSTAGES; ++s) {
             mbar_init(&st->rfull[s], 1);
@@ -822,7 +831,7 @@ __global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
                     WorkRef wr = work_unit(t, args, C_::SUB);
                     if constexpr (KS > 1) ksplit_range(wr, krank, KS);
                     const int m0 = wr.mb * (kBM * CTAS) + int(rank) * kBM;
-                    const int n0 = wr.nb * BN + int(rank) * C_::B_ROWS;
+                    const int n0 = (wr.nb * PAIRS + int(pp)) * BN + int(rank) * C_::B_ROWS;
                     for (int kb = wr.kb0; kb < wr.kb1; kb += C_::SUB) {
                         // The stage is free once its MMAs (in-ring conversion: its
                         // converting warps) have read it.
@@ -876,14 +885,22 @@ __global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
                                 for (int sb = 0; sb < C_::SUB; ++sb) {
                                     uint64_t *fb = &st->full[s * C_::SUB + sb];
                                     if (rank == 0) mbar_arrive_expect_tx(fb, CTAS * (C_::A_BLOCK + C_::B_BLOCK));
-                                    const uint32_t bar = mapa_shared(smem_u32(fb), 0);
+                                    const uint32_t bar = mapa_shared(smem_u32(fb), leader);
                                     auto load = [&](void *dst, const CUtensorMap *map, int x, int y, uint64_t pol) {
                                         if (hint)
                                             tma_load_2d_pair_hint(dst, map, bar, x, y, pol);
                                         else
                                             tma_load_2d_pair(dst, map, bar, x, y);
                                     };
-                                    load(a_dst + sb * C_::A_BLOCK, &tmA, (kb + sb) * K_ELEMS, m0, pol_a);
+                                    if constexpr (PAIRS == 2) {
+                                        // Half pp of this CTA's 128 A rows (a 64-row box), to
+                                        // this CTA and its counterpart in the other pair.
+                                        tma_load_2d_pair_mc(a_dst + sb * C_::A_BLOCK + pp * (C_::A_BLOCK / 2), &tmA, bar,
+                                                            (kb + sb) * K_ELEMS, m0 + int(pp) * (kBM / 2),
+                                                            uint16_t((1u << rank) | (1u << (rank + 2))));
+                                    } else {
+                                        load(a_dst + sb * C_::A_BLOCK, &tmA, (kb + sb) * K_ELEMS, m0, pol_a);
+                                    }
                                     if constexpr (B_MN) {
     #pragma unroll
                                         for (int i = 0; i < C_::B_ROWS / 64; ++i)
@@ -969,7 +986,7 @@ __global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
                             if constexpr (CTAS == 1)
                                 mma_commit<1>(&st->empty[s]);
                             else
-                                mma_commit_pair(&st->empty[s], 0x3);
+                                mma_commit_pair(&st->empty[s], kAllMask);  // every CTA that writes the stage
                             if (++s == STAGES) {
                                 s = 0;
                                 ph ^= 1u;
@@ -979,7 +996,7 @@ __global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
                         if constexpr (CTAS == 1)
                             mma_commit<1>(&st->acc_full[abuf]);
                         else
-                            mma_commit_pair(&st->acc_full[abuf], 0x3);
+                            mma_commit_pair(&st->acc_full[abuf], pair_mask);
                         if (++abuf == 2) {
                             abuf = 0;
                             aph ^= 1u;
@@ -1058,7 +1075,7 @@ __global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
                             if (rank == 0)
                                 mbar_arrive(&st->full[q]);
                             else
-                                mbar_arrive_cluster(mapa_shared(smem_u32(&st->full[q]), 0));
+                                mbar_arrive_cluster(mapa_shared(smem_u32(&st->full[q]), leader));
                             mbar_arrive(&st->rempty[r]);
                         }
                         if (++q == STAGES) {
@@ -1097,7 +1114,7 @@ __global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
                 if constexpr (CTAS == 1)
                     mbar_arrive(&st->acc_empty[b]);
                 else
-                    mbar_arrive_cluster(mapa_shared(smem_u32(&st->acc_empty[b]), 0));
+                    mbar_arrive_cluster(mapa_shared(smem_u32(&st->acc_empty[b]), leader));
             }
         };
         int abuf = 0;
@@ -1161,7 +1178,7 @@ __global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
             }
             return true;
         };
-        if (CTAS == 2 && args.split_reduce && cluster < args.num_vunits) {
+        if (CTAS == 2 && PAIRS == 1 && args.split_reduce && cluster < args.num_vunits) {
             // This cluster's last unit is the first K half of a split tile: zero
             // the tile's C (each warp its 32 x 128 slice) before the K loops run,
             // for both halves to add into.
@@ -1190,7 +1207,7 @@ __global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
             WorkRef wr = work_unit(t, args, C_::SUB);
             if constexpr (KS > 1) ksplit_range(wr, krank, KS);
             const int row = wr.mb * (kBM * CTAS) + int(rank) * kBM + 32 * q + lane;
-            const int col0 = wr.nb * BN + h * HALF;
+            const int col0 = (wr.nb * PAIRS + int(pp)) * BN + h * HALF;
             if constexpr (INT_OUT) {
                 const int nchunks = (wr.kb1 - wr.kb0 + args.kb_per_chunk - 1) / args.kb_per_chunk;
                 // In-ring conversion of chunk c (its K blocks) precedes the fold
@@ -1250,14 +1267,14 @@ __global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
                 }
                 // A split tile of int32 C: both K halves add into the zeroed C
                 // by int32 TMA reductions (modulo 2^32, like every partial sum).
-                const bool add = CTAS == 2 && wr.part != 0 && args.split_reduce;
+                const bool add = CTAS == 2 && PAIRS == 1 && wr.part != 0 && args.split_reduce;
                 if (add) {
                     const int slice = ((wr.slot * CTAS + int(rank)) * 4 + q) * 2 + h;
                     if (!split_zeroed_wait(args.split_count + slice, &st->abort, limit, lane)) {
                         ok = false;
                         break;
                     }
-                } else if (BN == kBN && wr.part != 0) {
+                } else if (BN == kBN && PAIRS == 1 && wr.part != 0) {
                     // Sum of the two K halves, wrapping like every int32 partial sum.
                     const int slice = ((wr.slot * CTAS + int(rank)) * 4 + q) * 2 + h;
                     uint32_t *cnt = args.split_count + slice;
@@ -1341,7 +1358,7 @@ __global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
                     // A split tile of FP32 C: both K halves add into the zeroed C
                     // by FP32 TMA reductions (0 + a + b: the same bits in either
                     // order).
-                    const bool add = CTAS == 2 && EPI == EPI_F32 && wr.part != 0 && args.split_reduce;
+                    const bool add = CTAS == 2 && PAIRS == 1 && EPI == EPI_F32 && wr.part != 0 && args.split_reduce;
                     if (add) {
                         const int slice = ((wr.slot * CTAS + int(rank)) * 4 + q) * 2 + h;
                         ok = split_zeroed_wait(args.split_count + slice, &st->abort, limit, lane);
@@ -1448,7 +1465,7 @@ thread_local LastLaunch g_last;
 
 // Launch shape of one variant: dynamic shared memory, cluster dimension and
 // (optionally) programmatic stream serialization.
-template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false>
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false, int PAIRS = 1>
 void launch_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[2], bool pdl, cudaStream_t stream) {
     std::memset(&cfg, 0, sizeof(cfg));
     std::memset(attr, 0, sizeof(attr));
@@ -1457,9 +1474,9 @@ void launch_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[2], bool
     cfg.stream = stream;
     cfg.attrs = attr;
     int n = 0;
-    if constexpr (CTAS * KS > 1) {
+    if constexpr (CTAS * KS * PAIRS > 1) {
         attr[n].id = cudaLaunchAttributeClusterDimension;
-        attr[n].val.clusterDim.x = CTAS * KS;
+        attr[n].val.clusterDim.x = CTAS * KS * PAIRS;
         attr[n].val.clusterDim.y = 1;
         attr[n].val.clusterDim.z = 1;
         ++n;
@@ -1474,10 +1491,10 @@ void launch_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[2], bool
 
 // Clusters of the variant that can be resident at once on the current device
 // (cached per device; the shared-memory opt-in is set on first use).
-template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false>
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false, int PAIRS = 1>
 cudaError_t cluster_capacity(int sms, int *out) {
-    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU>;
-    constexpr int CL = CTAS * KS;
+    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU, PAIRS>;
+    constexpr int CL = CTAS * KS * PAIRS;
     static thread_local LaunchCache cache;  // per device (re-queried when it changes)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1489,7 +1506,7 @@ cudaError_t cluster_capacity(int sms, int *out) {
         if constexpr (CL > 1) {
             cudaLaunchConfig_t cfg;
             cudaLaunchAttribute attr[2];
-            launch_config<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU>(cfg, attr, false, nullptr);
+            launch_config<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU, PAIRS>(cfg, attr, false, nullptr);
             cfg.gridDim = dim3(CL * (sms / CL), 1, 1);
             int n = 0;
             e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
@@ -1523,17 +1540,24 @@ cudaError_t clock_probe_base(unsigned long long **out) {
     return cudaSuccess;
 }
 
-template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false>
-cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args,
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false, int PAIRS = 1>
+cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args_in,
                        int sms, cudaMemPool_t pool, cudaStream_t stream) {
-    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU>;
+    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU, PAIRS>;
     int maxc = 0;
-    cudaError_t e = cluster_capacity<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU>(sms, &maxc);
+    cudaError_t e = cluster_capacity<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU, PAIRS>(sms, &maxc);
     if (e != cudaSuccess) return e;
+    GemmArgs args = args_in;
+    if constexpr (PAIRS == 2) {
+        // Work units of two pairs: tile columns 2 nb and 2 nb + 1 of tile row mb
+        // (the second is empty past N when the columns are odd).
+        args.tiles_n = (args.tiles_n + 1) / 2;
+        args.num_tiles = args.tiles_m * args.tiles_n;
+    }
     if (KS > 1 && args.num_tiles > maxc) return cudaErrorInvalidConfiguration;  // one wave of clusters
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    launch_config<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU>(cfg, attr, args.pdl != 0, stream);
+    launch_config<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU, PAIRS>(cfg, attr, args.pdl != 0, stream);
     // Work list: split the last wave's tiles in K when they fill at most half
     // of the clusters (a lone partial wave included).  The halves exchange
     // partial sums through a stream-ordered workspace from `pool`: a counter
@@ -1580,7 +1604,8 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
     // threshold is split_min_kb K blocks (64 by default) with reductions on
     // the FP16 kind, twice that on the E4M3 kind or with the exchange.
     const int min_kb = a.split_min_kb * (reduce ? 1 : 2) * (KIND == Kind::E4M3 ? 2 : 1);
-    if (!FU && KS == 1 && BN == kBN && pool != nullptr && a.split_ok && a.num_kb > SUBK && a.num_kb >= min_kb &&
+    if (!FU && PAIRS == 1 && KS == 1 && BN == kBN && pool != nullptr && a.split_ok && a.num_kb > SUBK &&
+        a.num_kb >= min_kb &&
         tail > 0 && 2 * tail <= maxc) {
         const size_t slices = size_t(tail) * CTAS * EPI_WARPS;
         const size_t count_bytes = (slices * sizeof(uint32_t) + 255) / 256 * 256;
@@ -1606,11 +1631,11 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
     // staged in the idle ring (its epilogue is exposed); earlier units use
     // 32-byte stores, which leave the TMA engine to the operand loads while the
     // next tile runs.
-    cfg.gridDim = dim3(CTAS * KS * clusters, 1, 1);
+    cfg.gridDim = dim3(CTAS * KS * PAIRS * clusters, 1, 1);
     e = cudaLaunchKernelEx(&cfg, fn, ta, tb, tc, a);
     if (e == cudaSuccess) {
-        g_last.grid = CTAS * KS * clusters;
-        g_last.cluster = CTAS * KS;
+        g_last.grid = CTAS * KS * PAIRS * clusters;
+        g_last.cluster = CTAS * KS * PAIRS;
         g_last.ksplit = KS;
         g_last.bn = BN;
     }
@@ -1685,6 +1710,7 @@ cudaError_t launch_gemm(Kind kind, bool b_mn_major, int epi, int ctas, const CUt
         if (ks == 4) return launch_one<K, BMN, E, 1, 1, 4, kBN>(ta, tb, args, sms, pool, stream);   \
         if (ks == 2) return launch_one<K, BMN, E, 1, 1, 2, kBN>(ta, tb, args, sms, pool, stream);   \
         return ctas == 1 ? launch_one<K, BMN, E, 1, 1, 1, kBN>(ta, tb, args, sms, pool, stream)     \
+               : args.pairs == 2  ? launch_one<K, BMN, E, 2, 2, 1, kBN, false, 2>(ta, tb, args, sms, pool, stream) \
                : args.stage_kb == 1 ? launch_one<K, BMN, E, 2, 1, 1, kBN>(ta, tb, args, sms, pool, stream) \
                                     : launch_one<K, BMN, E, 2, 2, 1, kBN>(ta, tb, args, sms, pool, stream); \
     } while (0)

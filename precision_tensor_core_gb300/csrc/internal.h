@@ -63,6 +63,10 @@ struct GemmArgs {
     // (set by launch_gemm from `probe`).
     int probe;
     unsigned long long *clock_probe;
+    // CTA pairs per thread-block cluster (knob "multicast"): 1, or 2 pairs that
+    // compute two adjacent tile columns and share A by TMA multicast (the A
+    // tensor map then has boxes of 64 rows).
+    int pairs;
     // Integer routes only: output of the epilogue.
     int out_mode;          // OUT_S32, or OUT_F32 / OUT_BF16 / OUT_F16 (scaled)
     const float *scale_a;  // M row scales (scaled modes; NULL: 1)

@@ -215,6 +215,21 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                  : "memory");
 }
 
+// 2-D tiled TMA load multicast into the shared memory of every CTA of
+// `cta_mask` (same offset in each) in a cluster of CTA pairs: the completion
+// of each destination's copy is signalled on the mbarrier at the offset of
+// `bar_cluster_addr` in the even CTA of that destination's pair (measured on
+// GB300: each pair leader's barrier received exactly its pair's bytes).
+__device__ __forceinline__ void tma_load_2d_pair_mc(void *smem_dst, const CUtensorMap *map,
+                                                    uint32_t bar_cluster_addr, int32_t x, int32_t y,
+                                                    uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
+        ".cta_group::2 [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar_cluster_addr), "h"(cta_mask)
+        : "memory");
+}
+
 // 2-D tiled TMA load into this CTA's shared memory whose completion is
 // signalled on an mbarrier of either CTA of the pair (shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(void *smem_dst, const CUtensorMap *map,

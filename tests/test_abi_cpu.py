@@ -142,7 +142,8 @@ def test_status_strings_and_tuning(L):
                            ("tile_n", 192, 0), ("in_ring", 3, 1), ("in_ring", -1, 1),
                            ("s8_chunk_kb", 18, 16), ("s8_chunk_kb", 1 << 20, 16),
                            ("s4_chunk_kb", 2050, 64), ("s4_chunk_kb", 1 << 20, 64),
-                           ("pair_in_ring", 1, 0), ("pair_in_ring", 3, 0)):
+                           ("pair_in_ring", 1, 0), ("pair_in_ring", 3, 0),
+                           ("multicast", 2, 0), ("multicast", -1, 0)):
         with pytest.raises(ptc.PtcError):
             ptc.ptc_set_tuning(key, bad)
         assert ptc.ptc_set_tuning(key, good) == 0
