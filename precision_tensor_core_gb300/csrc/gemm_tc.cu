@@ -681,8 +681,12 @@ __device__ __forceinline__ void ksplit_finish(const GemmArgs &args, int row, int
 // Completion of a K-split tile of BN columns: this CTA (`krank` of KS) owns
 // local rows krank * 128/KS .. of the tile (mb, nb), BN / 4 16-byte pieces per
 // row.  The 256 epilogue threads take consecutive pieces (a warp covers 512
-// contiguous bytes of C per store), two at a time with all 2 x KS peer loads
-// in flight before the sums (distributed shared memory is latency-bound).
+// contiguous bytes of C per store), two at a time with all 2 x KS loads in
+// flight before the sums (distributed shared memory is latency-bound; this
+// CTA's own partial sums are read locally).  Every thread makes the same
+// number of passes; once the last pass's loads are done the thread arrives on
+// the cluster barrier (it reads no peer's memory after that), so that the
+// barrier's latency overlaps the last sums and stores.
 template <int EPI, int KS, int BN>
 __device__ __forceinline__ void ksplit_complete(const GemmArgs &args, int mb, int nb, int krank, uint32_t base,
                                                 int ew, int lane) {
@@ -701,8 +705,10 @@ __device__ __forceinline__ void ksplit_complete(const GemmArgs &args, int mb, in
             const int piece = idx % PPR;
             const uint32_t addr = base + uint32_t(lr) * PROW + (uint32_t(piece ^ (lr & 7)) << 4);
 #pragma unroll
-            for (int k = 0; k < KS; ++k) p[u][k] = ld_shared_cluster_v4(mapa_shared(addr, uint32_t(k)));
+            for (int k = 0; k < KS; ++k)
+                p[u][k] = k == krank ? ld_shared_v4(addr) : ld_shared_cluster_v4(mapa_shared(addr, uint32_t(k)));
         }
+        if (i0 + 2 * NT >= R * PPR) cluster_arrive();
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const int idx = i0 + u * NT;
@@ -1421,19 +1427,27 @@ __global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
     if constexpr (KS > 1) {
         // Every CTA's partial sums are in its ring (barrier release / acquire at
         // cluster scope); each completes its rows of the tile from all of them.
+        // Peers read this CTA's ring until the second barrier, on which the
+        // completing threads arrive after their last loads and every other
+        // thread here.
         cluster_sync();
+        tc_fence_before_sync();
         if (warp >= EPI_WARP0 && warp < EPI_WARP0 + EPI_WARPS && cluster < args.num_vunits) {
             const WorkRef wr = work_unit(cluster, args, C_::SUB);
             ksplit_complete<EPI, KS, BN>(args, wr.mb, wr.nb, krank, smem_u32(smem), warp - EPI_WARP0, lane);
+        } else {
+            cluster_arrive();
         }
+        cluster_wait();
+        tc_fence_after_sync();
+    } else {
+        tc_fence_before_sync();
+        if constexpr (CL == 1)
+            __syncthreads();
+        else
+            cluster_sync();
+        tc_fence_after_sync();
     }
-    // A K-split cluster's peers read this CTA's ring until this barrier.
-    tc_fence_before_sync();
-    if constexpr (CL == 1)
-        __syncthreads();
-    else
-        cluster_sync();
-    tc_fence_after_sync();
     if (warp == 1) tmem_dealloc<CTAS>(tmem_base, TMEM_COLS);
     if (args.clock_probe != nullptr && threadIdx.x == 0) {
         const uint64_t c1 = sm_clock64(), t1 = globaltimer_ns();

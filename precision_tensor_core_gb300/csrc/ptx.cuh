@@ -199,6 +199,15 @@ __device__ __forceinline__ void cluster_sync() {
                      "memory");
 }
 
+// The two halves of cluster_sync, for work between them (every thread of
+// the cluster arrives once, then waits).
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // 16 bytes from shared::cluster address `addr` (this CTA's or a peer's).
 __device__ __forceinline__ uint4 ld_shared_cluster_v4(uint32_t addr) {
     uint4 v;
