@@ -340,8 +340,11 @@ int ptc_clock_probe_read(uint64_t *cycles, uint64_t *ns, uint64_t *ctas);
  * nanoseconds, 0 restores the default of one second) and, when stall_tile >= 0,
  * makes the next launched GEMM kernel withhold the operands of output tile
  * `stall_tile`, so that the wait for them runs out and the kernel reports
- * PTC_ERR_TIMEOUT through gemm_poll_device_error().  The stall applies to one
- * launch only.  Returns PTC_OK. */
+ * PTC_ERR_TIMEOUT through gemm_poll_device_error().  stall_tile = -2 makes the
+ * converter warps of the next integer launch with conversion in the GEMM
+ * kernel (tuning key "conv_fused") withhold the first piece they would
+ * convert, so that the producers waiting for it run out.  The stall applies to
+ * one launch only.  Returns PTC_OK. */
 int ptc_debug_set_wait_limit(uint64_t timeout_ns, int64_t stall_tile);
 
 /* The launch shape the library would choose for an M x N x K product of
@@ -370,7 +373,9 @@ int ptc_last_launch(int *grid, int *cluster, int *ksplit, int *tile_n);
 /* Operand conversion of the calling thread's last GEMM call through this
  * library: *mode = 0 none (FP16 operands, a call that launched nothing, or no
  * call yet), 1 a separate conversion pass into a workspace, 2 conversion
- * inside the GEMM kernel's shared memory.  Host-side only.  Returns PTC_OK,
+ * inside the GEMM kernel's shared memory, 3 conversion into the workspace by
+ * the GEMM kernel's converter warps (tuning key "conv_fused").  Host-side
+ * only.  Returns PTC_OK,
  * or PTC_ERR_INVALID when the pointer is NULL. */
 int ptc_last_conversion(int *mode);
 
@@ -465,6 +470,19 @@ int ptc_last_conversion(int *mode);
  *                  proxy fence that publishes each converted block take
  *                  longer than the block's MMAs), so it is not the default.
  *                  Results do not depend on the choice.
+ *   "conv_fused"   gemm_s8 / gemm_s4 (and their scaled forms) on 256-wide tiles
+ *                  without a K split that would use the separate conversion
+ *                  pass: 0 (default) keeps the pass; 1 converts the operands
+ *                  into the same workspace inside the GEMM kernel, by six
+ *                  converter warps per CTA (16-warp CTAs; CTAs without a tile
+ *                  convert too), panel slice by panel slice in the order the
+ *                  tiles need them, each slice loaded once its counter holds
+ *                  all its pieces.  Measured on GB300 it is slower than the
+ *                  pass (N = 8192: INT8 673 against 625 us, INT4 392 against
+ *                  325 us; N = 2048: 31 against 21 us): the converter warps'
+ *                  loads in flight limit their rate, and their HBM traffic
+ *                  slows the GEMM's operand loads.  Results do not depend on
+ *                  the choice.
  *   "multicast"    CTA-pair products (256 x 256 tiles): 0 (default) one pair
  *                  per thread-block cluster; 1 two pairs per cluster of four
  *                  CTAs, computing adjacent tile columns of one tile row and

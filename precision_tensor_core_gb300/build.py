@@ -73,14 +73,15 @@ _GEMM_ARGS = ("kind", "B", "epi", "CTAs", "K blocks per stage", "K-split", "tile
 def _gemm_label(mangled: str) -> str | None:
     """Readable template arguments of a gemm_kernel instantiation."""
     import re
-    m = re.search(r"gemm_kernelILNS_4KindE(\d)ELb(\d)ELi(\d)ELi(\d)ELi(\d)ELi(\d)ELi(\d+)ELb(\d)ELi(\d)",
-                  mangled)
+    m = re.search(r"gemm_kernelILNS_4KindE(\d)ELb(\d)ELi(\d)ELi(\d)ELi(\d)ELi(\d)ELi(\d+)ELb(\d)ELi(\d)"
+                  r"(?:ELb(\d))?", mangled)
     if not m:
         return None
-    kind, bmn, epi, ctas, subk, ks, bn, fu, pairs = m.groups()
+    kind, bmn, epi, ctas, subk, ks, bn, fu, pairs, gc = m.groups()
     return (f"gemm_kernel<{'F16' if kind == '0' else 'E4M3'}, B {'MN' if bmn == '1' else 'K'}-major, "
             f"{['EPI_F32', 'EPI_INT', 'EPI_F16ACC'][int(epi)]}, CTAS={ctas}, SUBK={subk}, KS={ks}, "
-            f"BN={bn}{', in-ring' if fu == '1' else ''}{', 2 pairs, A multicast' if pairs == '2' else ''}>")
+            f"BN={bn}{', in-ring' if fu == '1' else ''}{', 2 pairs, A multicast' if pairs == '2' else ''}"
+            f"{', converter warps' if gc == '1' else ''}>")
 
 
 def ptxas_summary(log_path: str = os.path.join(BUILD, "ptxas.log")) -> str:

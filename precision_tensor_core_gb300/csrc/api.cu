@@ -54,6 +54,7 @@ std::atomic<int> g_in_ring{1};        // integer routes: operands converted in t
 thread_local int g_last_conv = 0;     // operand conversion of this thread's last GEMM call
 std::atomic<int> g_clock_probe{0};   // 1: GEMM kernels add to the clock record
 std::atomic<int> g_multicast{0};     // 1: CTA-pair products run two pairs per cluster sharing A
+std::atomic<int> g_conv_fused{0};    // 1: integer routes convert in the GEMM kernel's converter warps
 std::atomic<int> g_pair_in_ring{0};  // integer routes on CTA pairs: 0 a separate conversion pass,
                                      // 2 conversion inside the pair kernel (dedicated converter warps)
 std::atomic<uint64_t> g_wait_ns{kDefaultWaitNs};
@@ -582,10 +583,16 @@ int int_gemm(bool s4, int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
 
     // Workspace: A and B as rows of K in the MMA input type (binary16 for
     // INT8, E4M3 for INT4), pitch rounded to 128 bytes, blocks 1024-aligned.
+    // With the conversion in the GEMM kernel (knob "conv_fused": 256-wide
+    // tiles without a K split, one pair per cluster) the converter warps write
+    // it, and the counters of converted pieces follow it.
+    const int pairs = (sh.ctas == 2 && g_multicast.load() == 1) ? 2 : 1;
+    const bool fused = g_conv_fused.load() == 1 && sh.bn == ptc::kBN && sh.ks <= 1 && pairs == 1;
     const int64_t a_bytes = round_up(M * ldw * wsize, 1024);
     const int64_t b_bytes = round_up(N * ldw * wsize, 1024);
+    const int64_t c_bytes = fused ? round_up(ptc::conv_counter_words(M, N, K) * 4, 256) : 0;
     void *ws = nullptr;
-    cudaError_t e = cudaMallocFromPoolAsync(&ws, size_t(a_bytes + b_bytes), d->pool, s);
+    cudaError_t e = cudaMallocFromPoolAsync(&ws, size_t(a_bytes + b_bytes + c_bytes), d->pool, s);
     if (e != cudaSuccess) {
         cudaGetLastError();
         return fail(PTC_ERR_ALLOC, "workspace allocation failed");
@@ -594,7 +601,9 @@ int int_gemm(bool s4, int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     uint8_t *bw = aw + a_bytes;
     const int cgrid = d->sms * 16;  // 16 CTAs per SM: measured 6% faster than 8 at N = 8192
     rc = PTC_OK;
-    if (s4)
+    if (fused)
+        e = cudaSuccess;
+    else if (s4)
         e = ptc::launch_s4_to_e4m3_pair(static_cast<const uint8_t *>(A), lda / 2, int(M),
                                         static_cast<const uint8_t *>(B), ldb / 2, int(N), int(K), aw, bw,
                                         ldw, cgrid, s, g_pdl.load() != 0);
@@ -605,10 +614,9 @@ int int_gemm(bool s4, int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
                                        ldw, cgrid, s, g_pdl.load() != 0);
     if (e != cudaSuccess)
         rc = fail_cuda(e, "operand conversion launch");
-    else
+    else if (!fused)
         g_launches.fetch_add(1);
     const CUtensorMapDataType dt = s4 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const int pairs = (sh.ctas == 2 && g_multicast.load() == 1) ? 2 : 1;
     CUtensorMap ta, tb;
     if (!rc) rc = make_tmap(&ta, dt, aw, K, M, uint64_t(ldw) * wsize, k_elems, ptc::kBM / pairs);
     if (!rc) rc = make_tmap(&tb, dt, bw, K, N, uint64_t(ldw) * wsize, k_elems, sh.bn / sh.ctas);
@@ -619,8 +627,19 @@ int int_gemm(bool s4, int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
         args.out_mode = mode;
         args.scale_a = sa;
         args.scale_b = sb;
+        if (fused) {
+            args.conv = 1;
+            args.conv_a = static_cast<const uint8_t *>(A);
+            args.conv_b = static_cast<const uint8_t *>(B);
+            args.conv_lda = s4 ? lda / 2 : lda;
+            args.conv_ldb = s4 ? ldb / 2 : ldb;
+            args.conv_wa = aw;
+            args.conv_wb = bw;
+            args.conv_ldw = ldw;
+            args.conv_count = reinterpret_cast<uint32_t *>(bw + b_bytes);
+        }
         rc = launch_gemm_checked(s4 ? Kind::E4M3 : Kind::F16, false, ptc::EPI_INT, sh.ctas, ta, tb, args, *d, s);
-        if (!rc) g_last_conv = 1;
+        if (!rc) g_last_conv = fused ? 3 : 1;
     }
     cudaFreeAsync(ws, s);
     return rc;
@@ -1170,6 +1189,10 @@ int ptc_set_tuning(const char *key, int64_t value) {
     }
     if (std::strcmp(key, "multicast") == 0 && (value == 0 || value == 1)) {
         g_multicast.store(int(value));
+        return PTC_OK;
+    }
+    if (std::strcmp(key, "conv_fused") == 0 && (value == 0 || value == 1)) {
+        g_conv_fused.store(int(value));
         return PTC_OK;
     }
     if (std::strcmp(key, "pair_in_ring") == 0 && (value == 0 || value == 2)) {

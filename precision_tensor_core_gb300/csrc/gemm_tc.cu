@@ -137,15 +137,19 @@ constexpr int kRing1 = 4 * (kBM + kBN) * kRowBytes;  // one-CTA ring bytes
 constexpr int kRingFu = 216 * 1024;                  // both rings, in-ring conversion
 constexpr int kRawRow = 64;                          // raw operand bytes per row and K block
 constexpr int kPairFuStages = 3, kPairFuRawStages = 8;
-template <int CTAS, int SUBK, int BN, bool FU = false>
+template <int CTAS, int SUBK, int BN, bool FU = false, bool GC = false>
 struct Cfg {
     static_assert(CTAS == 2 || SUBK == 1, "one CTA stages one K block at a time");
     static_assert(BN == kBN || (CTAS == 1 && (BN == 64 || BN == 128)), "narrow tiles are one-CTA tiles");
     static_assert(!FU || CTAS == 1 || SUBK == 1, "in-ring conversion stages one K block at a time");
+    static_assert(!(FU && GC), "operands converted in the ring or in global memory, not both");
     static constexpr bool PFU = FU && CTAS == 2;  // pair with dedicated converter warps
-    static constexpr int THREADS_ = PFU ? PAIR_FU_THREADS : THREADS;
-    static constexpr int EPI_WARP0 = PFU ? 4 : 2;  // first epilogue warp
-    static constexpr int CONV_WARP0 = 12;          // first converter warp of warpgroup 3 (PFU)
+    // 16 warps with per-warpgroup register budgets: pairs converting in the
+    // ring, and launches converting the operands in global memory (GC).
+    static constexpr bool WIDE = PFU || GC;
+    static constexpr int THREADS_ = WIDE ? PAIR_FU_THREADS : THREADS;
+    static constexpr int EPI_WARP0 = WIDE ? 4 : 2;  // first epilogue warp
+    static constexpr int CONV_WARP0 = 12;           // first converter warp of warpgroup 3 (WIDE)
     static constexpr int SUB = SUBK;  // K blocks per stage
     static constexpr int B_ROWS = BN / CTAS;
     static constexpr int A_BLOCK = kBM * kRowBytes;     // one K block of A
@@ -304,6 +308,194 @@ __device__ __forceinline__ bool split_publish(uint32_t *cnt, int lane) {
 
 __device__ __forceinline__ void st_release_gpu(uint32_t *p, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// ---------------------------------------------------------------- conversion
+// Integer launches that convert their operands themselves (GC): converter
+// warps rewrite the raw s8 / packed s4 rows of A and B into the workspace rows
+// that the tensor maps read, one element at a time exactly as the separate
+// pass does, in items of 2 KiB of raw operand (a few rows x kConvSlice K
+// elements).  Each (panel of kConvPanel rows, K slice) has a counter that its
+// items raise; a producer loads a slice of a panel once the counter holds all
+// the items.  Items go in the order the tiles need them (GemmArgs::conv), so
+// the first wave's MMAs start after the first slice of their panels.
+constexpr int kConvSlice = 256;  // K elements per slice
+constexpr int kConvPanel = 128;  // rows per panel
+constexpr int kConvWarps = 6;    // converter warps per CTA (2, 3 and 12 .. 15)
+
+template <Kind KIND>
+struct ConvItem {
+    static constexpr int ROWS = KIND == Kind::F16 ? 8 : 16;       // rows of 256 s8 or 128 packed-s4 bytes
+    static constexpr int ITEMS = kConvPanel / ROWS;               // items per (panel, slice)
+    static constexpr int VPR = 128 / ROWS;                        // 16-byte raw vectors per row
+    static constexpr int EPV = KIND == Kind::F16 ? 16 : 32;       // elements per raw vector
+    static constexpr int OUT = KIND == Kind::F16 ? 2 : 1;         // workspace bytes per element
+    static_assert(VPR * EPV == kConvSlice && ROWS * VPR == 128, "an item is 128 vectors of 16 bytes");
+};
+
+struct ConvGeom {
+    int S, PA, PB;  // K slices, panels of A, panels of B
+    __device__ __forceinline__ explicit ConvGeom(const GemmArgs &a)
+        : S((a.K + kConvSlice - 1) / kConvSlice), PA((a.M + kConvPanel - 1) / kConvPanel),
+          PB((a.N + kConvPanel - 1) / kConvPanel) {}
+    __device__ __forceinline__ int units() const { return (PA + PB) * S; }
+    // Counter of (operand, panel, slice): A panels first, then B panels.
+    __device__ __forceinline__ int counter(bool b, int p, int s) const { return ((b ? PA : 0) + p) * S + s; }
+};
+
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Unit u of the conversion order: the first wave's panels (fa of A, fb of B)
+// slice by slice, then the other B panels, then the other A panels, each
+// panel slice by slice.
+__device__ __forceinline__ void conv_unit(const ConvGeom &g, int fa, int fb, int u, bool &is_b, int &p, int &s) {
+    const int front = (fa + fb) * g.S;
+    if (u < front) {
+        s = u / (fa + fb);
+        const int i = u - s * (fa + fb);
+        is_b = i >= fa;
+        p = is_b ? i - fa : i;
+        return;
+    }
+    u -= front;
+    const int rest_b = (g.PB - fb) * g.S;
+    is_b = u < rest_b;
+    if (!is_b) u -= rest_b;
+    p = (is_b ? fb : fa) + u / g.S;
+    s = u % g.S;
+}
+
+// Vector v (0 .. 127) of an item of unit (is_b, p, sl), item q of the unit:
+// its raw source, its workspace destination and the elements below K that it
+// holds (0: none, EPV: the whole vector).
+template <Kind KIND>
+__device__ __forceinline__ int conv_vec(const GemmArgs &a, bool is_b, int p, int sl, int q, int v, const uint8_t *&src,
+                                        uint8_t *&dst) {
+    using CI = ConvItem<KIND>;
+    const int row = p * kConvPanel + q * CI::ROWS + v / CI::VPR;
+    const int c = sl * kConvSlice + (v % CI::VPR) * CI::EPV;
+    src = (is_b ? a.conv_b : a.conv_a) + int64_t(row) * (is_b ? a.conv_ldb : a.conv_lda) +
+          (KIND == Kind::F16 ? c : c / 2);
+    dst = static_cast<uint8_t *>(is_b ? a.conv_wb : a.conv_wa) + (int64_t(row) * a.conv_ldw + c) * CI::OUT;
+    return row < (is_b ? a.N : a.M) ? max(0, min(CI::EPV, a.K - c)) : 0;
+}
+
+// Converter warp g of G: items g, g + G, ..., in batches of four: two items'
+// loads in flight together, converted and stored, then the next two (whose
+// loads overlap the first stores' drain); one device-scope fence per batch,
+// then relaxed additions to the counts (fence-based release; the producers
+// read the counts relaxed and fence before their loads).  Only the loaded
+// vectors and the items' indices stay live across the loads (the converter
+// warpgroups run in 80 registers).
+template <Kind KIND>
+__device__ void convert_global(const GemmArgs &a, int g, int G, int lane, AbortState *ab) {
+    using CI = ConvItem<KIND>;
+    const ConvGeom geom(a);
+    const int total = geom.units() * CI::ITEMS;
+    auto item = [&](int i) { return (i >= total || (a.stall_tile == -2 && i == 0)) ? -1 : i; };  // test hook: item 0
+    for (int i0 = g; i0 < total; i0 += 4 * G) {
+        if (ab->flag) return;
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+            uint4 x[2][4];
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+                const int it = item(i0 + (2 * half + w) * G);
+                if (it < 0) continue;
+                bool is_b;
+                int p, sl;
+                conv_unit(geom, a.conv_front_a, a.conv_front_b, it / CI::ITEMS, is_b, p, sl);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint8_t *src;
+                    uint8_t *dst;
+                    if (conv_vec<KIND>(a, is_b, p, sl, it % CI::ITEMS, lane + 32 * j, src, dst) == CI::EPV)
+                        x[w][j] = __ldcs(reinterpret_cast<const uint4 *>(src));
+                }
+            }
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+                const int it = item(i0 + (2 * half + w) * G);
+                if (it < 0) continue;
+                bool is_b;
+                int p, sl;
+                conv_unit(geom, a.conv_front_a, a.conv_front_b, it / CI::ITEMS, is_b, p, sl);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint8_t *src;
+                    uint8_t *dst;
+                    const int n = conv_vec<KIND>(a, is_b, p, sl, it % CI::ITEMS, lane + 32 * j, src, dst);
+                    if (n == CI::EPV) {
+                        uint4 o0, o1;
+                        if constexpr (KIND == Kind::F16)
+                            cvt_s8_f16_x16(x[w][j], o0, o1);
+                        else
+                            cvt_s4_e4m3_x32(x[w][j], o0, o1);
+                        reinterpret_cast<uint4 *>(dst)[0] = o0;
+                        reinterpret_cast<uint4 *>(dst)[1] = o1;
+                    } else {
+                        for (int e = 0; e < n; ++e) {  // the ragged end of a row: no byte past K is read
+                            if constexpr (KIND == Kind::F16) {
+                                reinterpret_cast<uint16_t *>(dst)[e] = s8_to_f16_bits(static_cast<int8_t>(src[e]));
+                            } else {
+                                const uint32_t b = src[e >> 1];
+                                dst[e] = s4_to_e4m3_byte((e & 1) ? (b >> 4) : b);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) {
+            int n = 0;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const int it = item(i0 + w * G);
+                if (it < 0) continue;
+                bool is_b;
+                int p, sl;
+                conv_unit(geom, a.conv_front_a, a.conv_front_b, it / CI::ITEMS, is_b, p, sl);
+                atomicAdd(a.conv_count + geom.counter(is_b, p, sl), 1u);
+                ++n;
+            }
+            if (n) atomicAdd(a.conv_count + geom.units(), uint32_t(n));
+        }
+        __syncwarp();
+    }
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
+// Bounded wait of a producer until the counters i0 .. i2 (-1: none) hold
+// `need` items each (`seen`: their values read earlier, relaxed); then acquire
+// (fence) and order its coming TMA loads after the converters' stores (proxy
+// fence).  False on timeout or abort.
+__device__ __forceinline__ bool conv_wait(const uint32_t *cnt, int i0, int i1, int i2, uint32_t need, uint32_t seen,
+                                          AbortState *ab, uint64_t limit) {
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t m = seen;;) {
+        if (m >= need) break;
+        const uint32_t a = i0 >= 0 ? ld_relaxed_gpu(cnt + i0) : need;
+        const uint32_t b = i1 >= 0 ? ld_relaxed_gpu(cnt + i1) : need;
+        const uint32_t c = i2 >= 0 ? ld_relaxed_gpu(cnt + i2) : need;
+        m = min(a, min(b, c));
+        if (m >= need) break;
+        if (ab->flag) return false;
+        if (globaltimer_ns() - t0 > limit) {
+            ab->flag = 1;
+            atomicCAS(&g_error_word, 0u, kErrTimeout);
+            return false;
+        }
+    }
+    fence_acq_rel_gpu();
+    fence_proxy_async_global();
+    return true;
 }
 
 // Split tiles added into C by TMA reductions: the first half's cluster zeroes
@@ -724,19 +916,22 @@ __device__ __forceinline__ void ksplit_complete(const GemmArgs &args, int mb, in
 // its full barriers collect both CTAs' copies, its commits arrive on both
 // CTAs' empty / accumulator-full barriers, and both CTAs' epilogues release
 // accumulator buffers on its acc_empty barriers.
-template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false, int PAIRS = 1>
-__global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false, int PAIRS = 1,
+          bool GC = false>
+__global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU, GC>::THREADS_, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmC, const GemmArgs args) {
     static_assert(!(B_MN && KIND == Kind::E4M3), "MN-major B is used by the FP16 path only");
     static_assert(KS == 1 || CTAS == 1, "K-split clusters of one-CTA tiles");
     static_assert(!FU || (EPI == EPI_INT && !B_MN), "in-ring conversion: integer launches with K-major B");
-    static_assert(PAIRS == 1 || (CTAS == 2 && SUBK == 2 && KS == 1 && BN == kBN && !FU),
+    static_assert(PAIRS == 1 || (CTAS == 2 && SUBK == 2 && KS == 1 && BN == kBN && !FU && !GC),
                   "two pairs per cluster: two-block pair stages, operands converted by the pass");
+    static_assert(!GC || (EPI == EPI_INT && !B_MN && KS == 1 && BN == kBN && PAIRS == 1),
+                  "conversion in global memory: integer launches of 256-wide tiles with K-major B");
     constexpr bool INT_OUT = EPI == EPI_INT;
     constexpr int HALF = BN / 2;      // columns of an epilogue warp's slice
     constexpr int NCH = HALF / 32;    // 32-column chunks of a slice
-    using C_ = Cfg<CTAS, SUBK, BN, FU>;
+    using C_ = Cfg<CTAS, SUBK, BN, FU, GC>;
     constexpr int TMEM_COLS = C_::TMEM_COLS;
     constexpr int STAGES = C_::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -748,6 +943,7 @@ __global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
     uint8_t *raw_ring = smem + STAGES * C_::STAGE;  // in-ring conversion only
     using Tail = SharedTail<STAGES, C_::SUB, C_::RSTAGES>;
     constexpr bool PFU = C_::PFU;
+    constexpr bool WIDE = C_::WIDE;
     constexpr int EPI_WARP0 = C_::EPI_WARP0;
     constexpr int PSTAGES = FU ? C_::RSTAGES : STAGES;  // the producer's ring
     Tail *st = reinterpret_cast<Tail *>(smem + C_::RING);
@@ -813,11 +1009,12 @@ __global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
     }
 
     constexpr int K_ELEMS = (KIND == Kind::F16) ? kRowBytes / 2 : kRowBytes;
+    static_assert(!GC || kConvSlice % (K_ELEMS * C_::SUB) == 0, "a stage lies within one conversion slice");
 
-    if (warp < EPI_WARP0 || (PFU && warp >= C_::CONV_WARP0)) {
+    if (warp < EPI_WARP0 || (WIDE && warp >= C_::CONV_WARP0)) {
         // Producer, MMA issuer and converter warps.  With the 16-warp layout
         // their warpgroups (0 and 3) first lower their register budget together.
-        if constexpr (PFU) regs_dec<kRegsLow>();
+        if constexpr (WIDE) regs_dec<kRegsLow>();
         if (warp == 0) {
             // ------------------------------------------------------ TMA producer
             if (lane == 0) {
@@ -833,11 +1030,28 @@ __global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
                 uint32_t ph = 0;
                 uint32_t outstanding = 0, out_phase = 0;  // per-stage bits of issued copies
                 bool ok = true;
+                // Conversion in global memory: once every item is done no slice
+                // is checked again; until then each new slice of this CTA's A
+                // panel and B panel(s) is awaited before its loads.
+                bool conv_all = !GC;
                 for (int t = cluster; t < args.num_vunits && ok; t += nclusters) {
                     WorkRef wr = work_unit(t, args, C_::SUB);
                     if constexpr (KS > 1) ksplit_range(wr, krank, KS);
                     const int m0 = wr.mb * (kBM * CTAS) + int(rank) * kBM;
                     const int n0 = (wr.nb * PAIRS + int(pp)) * BN + int(rank) * C_::B_ROWS;
+                    int conv_sl = -1, conv_pre_sl = -1;
+                    uint32_t conv_pre = 0;
+                    if constexpr (GC) {
+                        if (!conv_all) {
+                            const ConvGeom geom(args);
+                            conv_all = ld_relaxed_gpu(args.conv_count + geom.units()) >=
+                                       uint32_t(geom.units() * ConvItem<KIND>::ITEMS);
+                            if (conv_all) {
+                                fence_acq_rel_gpu();
+                                fence_proxy_async_global();
+                            }
+                        }
+                    }
                     for (int kb = wr.kb0; kb < wr.kb1; kb += C_::SUB) {
                         // The stage is free once its MMAs (in-ring conversion: its
                         // converting warps) have read it.
@@ -846,6 +1060,41 @@ __global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
                             break;
                         }
                         outstanding &= ~(1u << s);
+                        if constexpr (GC) {
+                            const int sl = kb * K_ELEMS / kConvSlice;  // a stage lies within one slice
+                            if (!conv_all && sl != conv_sl) {
+                                const ConvGeom geom(args);
+                                const int pa = m0 / kConvPanel, pb = n0 / kConvPanel;
+                                auto idx = [&](int s2, int &ia, int &ib0, int &ib1) {
+                                    ia = pa < geom.PA ? geom.counter(false, pa, s2) : -1;
+                                    ib0 = pb < geom.PB ? geom.counter(true, pb, s2) : -1;
+                                    ib1 = (C_::B_ROWS > kConvPanel && pb + 1 < geom.PB) ? geom.counter(true, pb + 1, s2)
+                                                                                       : -1;
+                                };
+                                int ia, ib0, ib1;
+                                idx(sl, ia, ib0, ib1);
+                                // The counts read a slice ago, when they were for this slice.
+                                const uint32_t seen = conv_pre_sl == sl ? conv_pre : 0u;
+                                if (!conv_wait(args.conv_count, ia, ib0, ib1, uint32_t(ConvItem<KIND>::ITEMS), seen,
+                                               &st->abort, limit)) {
+                                    ok = false;
+                                    break;
+                                }
+                                conv_sl = sl;
+                                // Read the next slice's counts now (relaxed: the value is
+                                // used at that slice, so this load does not stall here).
+                                conv_pre_sl = -1;
+                                if (sl + 1 < geom.S) {
+                                    idx(sl + 1, ia, ib0, ib1);
+                                    const uint32_t need = ConvItem<KIND>::ITEMS;
+                                    const uint32_t a0 = ia >= 0 ? ld_relaxed_gpu(args.conv_count + ia) : need;
+                                    const uint32_t b0 = ib0 >= 0 ? ld_relaxed_gpu(args.conv_count + ib0) : need;
+                                    const uint32_t b1 = ib1 >= 0 ? ld_relaxed_gpu(args.conv_count + ib1) : need;
+                                    conv_pre = min(a0, min(b0, b1));
+                                    conv_pre_sl = sl + 1;
+                                }
+                            }
+                        }
                         const bool stall = (t == args.stall_tile && kb == wr.kb0 && rank == 0);
                         if (!stall) {
                             uint8_t *a_dst = a_ring + s * C_::A_STAGE;
@@ -1096,10 +1345,19 @@ __global__ void __launch_bounds__(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1)
                 }
             }
             __syncwarp();
+        } else if (GC && warp >= 2) {
+            // ------------------------------------------------------ converters
+            // Conversion in global memory: warps 2, 3 and 12 .. 15 of every CTA.
+            if constexpr (GC) {
+                const int cw = warp < 4 ? warp - 2 : warp - C_::CONV_WARP0 + 2;
+                convert_global<KIND>(args, int(blockIdx.x) * kConvWarps + cw, int(gridDim.x) * kConvWarps, lane,
+                                     &st->abort);
+            }
+            __syncwarp();
         }
     } else {
         // The epilogue warpgroups raise their register budget (16-warp layout).
-        if constexpr (PFU) regs_inc<kRegsHigh>();
+        if constexpr (WIDE) regs_inc<kRegsHigh>();
         // ------------------------------------------------------ epilogue
         const int ew = warp - EPI_WARP0;    // epilogue warp 0 .. 7
         const int q = warp & 3;             // tensor-memory lane quarter
@@ -1473,13 +1731,15 @@ __global__ void zero_fill_kernel(T *C, int64_t ldc, int M, int N) {
 // lets the GEMM start its setup at once; the GEMM's own wait then orders its
 // first counter access after these stores.  (A memset between the two kernels
 // would end the overlap: ~5 us between them at N = 4096, against ~0.7 us.)
-__global__ void __launch_bounds__(256) clear_words_kernel(uint32_t *p, int n) {
+__global__ void __launch_bounds__(256) clear_words_kernel(uint32_t *p, int n, uint32_t *p2, int n2) {
     griddep_wait();
     griddep_launch_dependents();
     for (int i = int(threadIdx.x); i < n; i += int(blockDim.x)) p[i] = 0u;
+    for (int i = int(threadIdx.x); i < n2; i += int(blockDim.x)) p2[i] = 0u;
 }
 
-cudaError_t launch_clear_words(uint32_t *p, int n, bool pdl, cudaStream_t stream) {
+// Zeroes n words at p and n2 at p2 (either count may be 0).
+cudaError_t launch_clear_words(uint32_t *p, int n, uint32_t *p2, int n2, bool pdl, cudaStream_t stream) {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     std::memset(&cfg, 0, sizeof(cfg));
@@ -1493,9 +1753,20 @@ cudaError_t launch_clear_words(uint32_t *p, int n, bool pdl, cudaStream_t stream
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.numAttrs = 1;
     }
-    cudaError_t e = cudaLaunchKernelEx(&cfg, clear_words_kernel, p, n);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, clear_words_kernel, p, n, p2, n2);
     if (e == cudaSuccess) note_launches(1);
     return e;
+}
+
+// The work list's tile coordinates (tile_coords), on the host.
+void host_tile_coords(int t, const GemmArgs &a, int &mb, int &nb) {
+    const int per_group = a.group_m * a.tiles_n;
+    const int g = t / per_group;
+    const int first_m = g * a.group_m;
+    const int gsz = a.tiles_m - first_m < a.group_m ? a.tiles_m - first_m : a.group_m;
+    const int r = t - g * per_group;
+    mb = first_m + r % gsz;
+    nb = r / gsz;
 }
 
 struct LaunchCache {
@@ -1510,11 +1781,12 @@ thread_local LastLaunch g_last;
 
 // Launch shape of one variant: dynamic shared memory, cluster dimension and
 // (optionally) programmatic stream serialization.
-template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false, int PAIRS = 1>
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false, int PAIRS = 1,
+          bool GC = false>
 void launch_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[2], bool pdl, cudaStream_t stream) {
     std::memset(&cfg, 0, sizeof(cfg));
     std::memset(attr, 0, sizeof(attr));
-    cfg.blockDim = dim3(Cfg<CTAS, SUBK, BN, FU>::THREADS_, 1, 1);
+    cfg.blockDim = dim3(Cfg<CTAS, SUBK, BN, FU, GC>::THREADS_, 1, 1);
     cfg.dynamicSmemBytes = smem_bytes<CTAS, SUBK, BN, FU>();
     cfg.stream = stream;
     cfg.attrs = attr;
@@ -1536,9 +1808,10 @@ void launch_config(cudaLaunchConfig_t &cfg, cudaLaunchAttribute (&attr)[2], bool
 
 // Clusters of the variant that can be resident at once on the current device
 // (cached per device; the shared-memory opt-in is set on first use).
-template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false, int PAIRS = 1>
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false, int PAIRS = 1,
+          bool GC = false>
 cudaError_t cluster_capacity(int sms, int *out) {
-    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU, PAIRS>;
+    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU, PAIRS, GC>;
     constexpr int CL = CTAS * KS * PAIRS;
     static thread_local LaunchCache cache;  // per device (re-queried when it changes)
     int dev = 0;
@@ -1551,7 +1824,7 @@ cudaError_t cluster_capacity(int sms, int *out) {
         if constexpr (CL > 1) {
             cudaLaunchConfig_t cfg;
             cudaLaunchAttribute attr[2];
-            launch_config<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU, PAIRS>(cfg, attr, false, nullptr);
+            launch_config<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU, PAIRS, GC>(cfg, attr, false, nullptr);
             cfg.gridDim = dim3(CL * (sms / CL), 1, 1);
             int n = 0;
             e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
@@ -1585,12 +1858,13 @@ cudaError_t clock_probe_base(unsigned long long **out) {
     return cudaSuccess;
 }
 
-template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false, int PAIRS = 1>
+template <Kind KIND, bool B_MN, int EPI, int CTAS, int SUBK, int KS, int BN, bool FU = false, int PAIRS = 1,
+          bool GC = false>
 cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmArgs &args_in,
                        int sms, cudaMemPool_t pool, cudaStream_t stream) {
-    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU, PAIRS>;
+    auto *fn = gemm_kernel<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU, PAIRS, GC>;
     int maxc = 0;
-    cudaError_t e = cluster_capacity<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU, PAIRS>(sms, &maxc);
+    cudaError_t e = cluster_capacity<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU, PAIRS, GC>(sms, &maxc);
     if (e != cudaSuccess) return e;
     GemmArgs args = args_in;
     if constexpr (PAIRS == 2) {
@@ -1602,7 +1876,7 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
     if (KS > 1 && args.num_tiles > maxc) return cudaErrorInvalidConfiguration;  // one wave of clusters
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[2];
-    launch_config<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU, PAIRS>(cfg, attr, args.pdl != 0, stream);
+    launch_config<KIND, B_MN, EPI, CTAS, SUBK, KS, BN, FU, PAIRS, GC>(cfg, attr, args.pdl != 0, stream);
     // Work list: split the last wave's tiles in K when they fill at most half
     // of the clusters (a lone partial wave included).  The halves exchange
     // partial sums through a stream-ordered workspace from `pool`: a counter
@@ -1638,6 +1912,7 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
     a.split_count = nullptr;
     a.split_part = nullptr;
     void *ws = nullptr;
+    int split_words = 0;  // split-tile counters to zero before the launch
     // The split saves about half of a tile's K loop (~0.35 us per K block
     // under the power cap).  Adding the halves into C by TMA reductions costs
     // ~4 us after the last MMA; exchanging partial sums through the workspace
@@ -1656,12 +1931,7 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
         const size_t count_bytes = (slices * sizeof(uint32_t) + 255) / 256 * 256;
         const size_t bytes = count_bytes + (reduce ? 0 : slices * 2 * kSliceWords * sizeof(float));
         if (cudaMallocFromPoolAsync(&ws, bytes, pool, stream) == cudaSuccess) {
-            e = launch_clear_words(static_cast<uint32_t *>(ws), int(count_bytes / sizeof(uint32_t)), a.pdl != 0,
-                                   stream);
-            if (e != cudaSuccess) {
-                cudaFreeAsync(ws, stream);
-                return e;
-            }
+            split_words = int(count_bytes / sizeof(uint32_t));
             a.tail_split = tail;
             a.split_reduce = reduce ? 1 : 0;
             a.split_count = static_cast<uint32_t *>(ws);
@@ -1672,7 +1942,32 @@ cudaError_t launch_one(const CUtensorMap &ta, const CUtensorMap &tb, const GemmA
         }
     }
     a.num_vunits = a.num_tiles + a.tail_split;
-    const int clusters = a.num_vunits < maxc ? a.num_vunits : maxc;
+    // Conversion in global memory: every resident cluster is launched (CTAs
+    // without a tile convert too), and the panels the first wave's tiles use
+    // are converted first.
+    const int clusters = GC ? maxc : (a.num_vunits < maxc ? a.num_vunits : maxc);
+    int conv_words = 0;
+    if constexpr (GC) {
+        int max_mb = 0, max_nb = 0;
+        const int wave = a.num_tiles < clusters ? a.num_tiles : clusters;
+        for (int t = 0; t < wave; ++t) {
+            int mb, nb;
+            host_tile_coords(t, a, mb, nb);
+            max_mb = mb > max_mb ? mb : max_mb;
+            max_nb = nb > max_nb ? nb : max_nb;
+        }
+        const int pa = (a.M + kConvPanel - 1) / kConvPanel, pb = (a.N + kConvPanel - 1) / kConvPanel;
+        a.conv_front_a = (max_mb + 1) * CTAS < pa ? (max_mb + 1) * CTAS : pa;
+        a.conv_front_b = (max_nb + 1) * (BN / kConvPanel) < pb ? (max_nb + 1) * (BN / kConvPanel) : pb;
+        conv_words = int(conv_counter_words(a.M, a.N, a.K));
+    }
+    if (split_words > 0 || conv_words > 0) {
+        e = launch_clear_words(a.conv_count, conv_words, a.split_count, split_words, a.pdl != 0, stream);
+        if (e != cudaSuccess) {
+            if (ws != nullptr) cudaFreeAsync(ws, stream);
+            return e;
+        }
+    }
     // Each cluster's last unit writes 4-byte C by TMA stores (or reductions)
     // staged in the idle ring (its epilogue is exposed); earlier units use
     // 32-byte stores, which leave the TMA engine to the operand loads while the
@@ -1728,6 +2023,11 @@ int pick_ksplit(int tiles, int num_kb, int knob, int sms) {
     return pick_ksplit_pure(tiles, num_kb, knob, sms, cluster_caps(sms));
 }
 
+int64_t conv_counter_words(int64_t M, int64_t N, int64_t K) {
+    const int64_t slices = (K + kConvSlice - 1) / kConvSlice;
+    return ((M + kConvPanel - 1) / kConvPanel + (N + kConvPanel - 1) / kConvPanel) * slices + 1;
+}
+
 size_t gemm_smem_bytes(int ctas) { return ctas == 2 ? smem_bytes<2, 2>() : smem_bytes<1, 1>(); }
 
 // One-CTA launches of 256-wide tiles run as K-split clusters when pick_ksplit
@@ -1776,6 +2076,18 @@ cudaError_t launch_gemm(Kind kind, bool b_mn_major, int epi, int ctas, const CUt
     } while (0)
     if (kind == Kind::F16 && b_mn_major && epi == EPI_F32) PTC_LAUNCH(Kind::F16, true, EPI_F32);
     if (kind == Kind::F16 && b_mn_major && epi == EPI_F16ACC) PTC_LAUNCH(Kind::F16, true, EPI_F16ACC);
+    if (args.conv != 0) {
+        // Conversion in the GEMM kernel's converter warps: integer launches with
+        // K-major B, 256-wide tiles, no K split (one CTA, or CTA pairs).
+        if (b_mn_major || epi != EPI_INT || bn != kBN || args.pairs != 1) return cudaErrorInvalidValue;
+        if (kind == Kind::F16)
+            return ctas == 1 ? launch_one<Kind::F16, false, EPI_INT, 1, 1, 1, kBN, false, 1, true>(ta, tb, args, sms, pool, stream)
+                             : launch_one<Kind::F16, false, EPI_INT, 2, 2, 1, kBN, false, 1, true>(ta, tb, args, sms, pool, stream);
+        if (kind == Kind::E4M3)
+            return ctas == 1 ? launch_one<Kind::E4M3, false, EPI_INT, 1, 1, 1, kBN, false, 1, true>(ta, tb, args, sms, pool, stream)
+                             : launch_one<Kind::E4M3, false, EPI_INT, 2, 2, 1, kBN, false, 1, true>(ta, tb, args, sms, pool, stream);
+        return cudaErrorInvalidValue;
+    }
     if (args.in_ring != 0) {
         // In-ring conversion: integer launches with K-major B (one CTA per
         // tile, or CTA pairs with dedicated converter warps).

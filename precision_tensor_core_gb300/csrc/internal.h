@@ -67,6 +67,23 @@ struct GemmArgs {
     // compute two adjacent tile columns and share A by TMA multicast (the A
     // tensor map then has boxes of 64 rows).
     int pairs;
+    // Integer routes with the conversion inside the GEMM (conv = 1): converter
+    // warps rewrite the raw operands (s8, or packed s4) into the workspace rows
+    // that the tensor maps read (binary16 / E4M3, conv_ldw elements per row),
+    // in items of a few rows x kConvSlice K elements, in the order the tiles
+    // need them: the K slices of the panels (128 rows) of A and B that the
+    // first wave uses (conv_front_a / conv_front_b panels) slice by slice,
+    // then the other B panels, then the other A panels.  Each item adds 1 to
+    // the counter of its (panel, slice) (A panels first, then B) and to the
+    // last counter; the producer loads a slice of a panel once its counter
+    // holds all its items.  The counters are zero at launch.
+    int conv;
+    const uint8_t *conv_a, *conv_b;  // raw A (M rows) and B (N rows of K)
+    int64_t conv_lda, conv_ldb;      // their row pitches in bytes
+    void *conv_wa, *conv_wb;         // workspace rows
+    int64_t conv_ldw;                // workspace row pitch in elements
+    uint32_t *conv_count;            // (panels of A + panels of B) x slices counters, then one more
+    int conv_front_a, conv_front_b;
     // Integer routes only: output of the epilogue.
     int out_mode;          // OUT_S32, or OUT_F32 / OUT_BF16 / OUT_F16 (scaled)
     const float *scale_a;  // M row scales (scaled modes; NULL: 1)
@@ -80,6 +97,9 @@ enum OutMode : int { OUT_S32 = 0, OUT_F32 = 1, OUT_BF16 = 2, OUT_F16 = 3 };
 // Dynamic shared memory the GEMM kernel needs (ctas = 1: one CTA per
 // 128 x 256 tile; ctas = 2: a CTA pair per 256 x 256 tile).
 size_t gemm_smem_bytes(int ctas);
+// Counters an integer launch with conversion in the GEMM kernel uses (one per
+// panel of 128 rows of A or B and K slice, plus one), zeroed by that launch.
+int64_t conv_counter_words(int64_t M, int64_t N, int64_t K);
 
 // Epilogues of the tensor-core GEMM kernel.
 enum Epi : int {

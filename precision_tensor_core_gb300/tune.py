@@ -58,7 +58,7 @@ if ROOT not in sys.path:
 
 DEFAULTS = {"cta_pair": 0, "group_m": 8, "l2_hint": 0, "s8_chunk_kb": 16, "s4_chunk_kb": 64, "tail_split": 1,
             "split_min_kb": 64, "pair_stage_kb": 2, "ksplit": 0, "pdl": 1, "tile_n": 0, "in_ring": 1,
-            "pair_in_ring": 0, "multicast": 0}
+            "pair_in_ring": 0, "multicast": 0, "conv_fused": 0}
 KNOBS = {"cta_pair": [1, 2], "pair_stage_kb": [1], "tail_split": [0], "split_min_kb": [32, 128],
          "group_m": [4, 16, 32], "l2_hint": [1, 2, 3], "s8_chunk_kb": [4, 8], "s4_chunk_kb": [2, 8, 16, 128],
          "ksplit": [1, 2, 4, 8], "pdl": [0], "tile_n": [64, 128, 256], "in_ring": [0]}

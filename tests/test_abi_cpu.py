@@ -143,7 +143,7 @@ def test_status_strings_and_tuning(L):
                            ("s8_chunk_kb", 18, 16), ("s8_chunk_kb", 1 << 20, 16),
                            ("s4_chunk_kb", 2050, 64), ("s4_chunk_kb", 1 << 20, 64),
                            ("pair_in_ring", 1, 0), ("pair_in_ring", 3, 0),
-                           ("multicast", 2, 0), ("multicast", -1, 0)):
+                           ("multicast", 2, 0), ("multicast", -1, 0), ("conv_fused", 2, 0), ("conv_fused", -1, 0)):
         with pytest.raises(ptc.PtcError):
             ptc.ptc_set_tuning(key, bad)
         assert ptc.ptc_set_tuning(key, good) == 0
