@@ -587,7 +587,8 @@ int int_gemm(bool s4, int64_t M, int64_t N, int64_t K, const void *A, int64_t ld
     // tiles without a K split, one pair per cluster) the converter warps write
     // it, and the counters of converted pieces follow it.
     const int pairs = (sh.ctas == 2 && g_multicast.load() == 1) ? 2 : 1;
-    const bool fused = g_conv_fused.load() == 1 && sh.bn == ptc::kBN && sh.ks <= 1 && pairs == 1;
+    const bool fused = g_conv_fused.load() == 1 && sh.bn == ptc::kBN && sh.ks <= 1 && pairs == 1 &&
+                       ptc::conv_counter_words(M, N, K) < (int64_t(1) << 30);
     const int64_t a_bytes = round_up(M * ldw * wsize, 1024);
     const int64_t b_bytes = round_up(N * ldw * wsize, 1024);
     const int64_t c_bytes = fused ? round_up(ptc::conv_counter_words(M, N, K) * 4, 256) : 0;
