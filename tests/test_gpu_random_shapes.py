@@ -1,0 +1,84 @@
+"""GPU parity on seeded random shapes: M, N, K drawn from 1 .. 1500 (K even for
+packed s4), each precision, on the shape the planner picks (narrow tiles,
+K-split clusters, in-ring conversion, CTA pairs) and with CTA pairs forced.
+FP16 within the FP16 tolerance, INT8 / INT4 bit-exact against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import datagen
+import oracle
+import precision_tensor_core_gb300 as ptc
+from tests.gpu_util import DEV, check_f16, f16_dev, int_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    torch.cuda.set_device(DEV)
+    yield
+    assert ptc.gemm_poll_device_error() == ptc.PTC_OK
+
+
+@pytest.fixture(params=[0, 2], ids=["planner", "pairs"])
+def cta_mode(request):
+    ptc.ptc_set_tuning("cta_pair", request.param)
+    yield request.param
+    ptc.ptc_set_tuning("cta_pair", 0)
+
+
+def shapes(n=30, seed=2026):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        # half log-uniform (small and ragged shapes), half uniform (several tiles and waves)
+        if i % 2 == 0:
+            m, nn, k = (int(np.exp(rng.uniform(0, np.log(1500)))) for _ in range(3))
+        else:
+            m, nn, k = (int(rng.integers(1, 1501)) for _ in range(3))
+        out.append((max(1, m), max(1, nn), max(1, k)))
+    return out
+
+
+SHAPES = shapes()
+
+
+def padded(a: np.ndarray, per: int) -> np.ndarray:
+    rows, cols = a.shape
+    w = max(per, (cols + per - 1) // per * per)
+    out = np.zeros((rows, w), dtype=a.dtype)
+    out[:, :cols] = a
+    return out
+
+
+def out_padded(M, N, dtype=torch.int32):
+    per = 16 // torch.empty((), dtype=dtype).element_size()
+    return torch.empty((M, (N + per - 1) // per * per), dtype=dtype, device=DEV)[:, :N]
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_random_shape_f16(M, N, K, cta_mode):
+    A, B = datagen.f16_operands(N, "normal", seed=M * 7919 + N * 31 + K, m=M, k=K)
+    Ad = f16_dev(padded(A, 8))[:, :K]
+    Bd = f16_dev(padded(B, 8))[:, :N]
+    C = ptc.matmul_f16(Ad, Bd, out=out_padded(M, N, torch.float32))
+    torch.cuda.synchronize()
+    check_f16(C.cpu().numpy(), A, B)
+
+
+@pytest.mark.parametrize("M,N,K", SHAPES)
+def test_random_shape_int(M, N, K, cta_mode):
+    A, Bt = datagen.s8_operands(N, seed=M * 104729 + N * 37 + K, m=M, k=K)
+    C = ptc.matmul_s8(int_dev(padded(A, 16))[:, :K], int_dev(padded(Bt, 16))[:, :K], out=out_padded(M, N))
+    torch.cuda.synchronize()
+    assert np.array_equal(C.cpu().numpy(), oracle.wrap_s32(oracle.gemm_s8(A, Bt)))
+    K4 = K + (K & 1)
+    A4, Bt4 = datagen.s4_operands(N, seed=M * 1299709 + N * 41 + K4, m=M, k=K4)
+    C4 = ptc.matmul_s4(int_dev(padded(A4, 16))[:, :K4 // 2], int_dev(padded(Bt4, 16))[:, :K4 // 2], K4,
+                       out=out_padded(M, N))
+    torch.cuda.synchronize()
+    assert np.array_equal(C4.cpu().numpy(), oracle.wrap_s32(oracle.gemm_s4(A4, Bt4, K4)))
