@@ -524,7 +524,7 @@ __device__ __forceinline__ bool split_zeroed_wait(const uint32_t *flag, AbortSta
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast.
+// Warp-uniform bounded wait: lane 0 polls, the outcome is broadcast.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, AbortState *ab,
                                           uint64_t limit, int lane) {
     uint32_t ok = 0;

@@ -156,7 +156,7 @@ def test_sampled_checker_catches_nan(case):
 
 # ------------------------------------------------ planted checker mistakes
 def scenarios(case):
-    """(C, Cref, S, verdict the stated rule gives) for the cases above."""
+    """(C, Cref, S, outcome the stated rule gives) for the cases above."""
     _, _, Cref, S = case
     out = [(Cref.astype(np.float32), Cref, S, True)]
     i, j = 17, 33
