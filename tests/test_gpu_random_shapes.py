@@ -1,7 +1,9 @@
 """GPU parity on seeded random shapes: M, N, K drawn from 1 .. 1500 (K even for
 packed s4), each precision, on the shape the planner picks (narrow tiles,
 K-split clusters, in-ring conversion, CTA pairs) and with CTA pairs forced.
-FP16 within the FP16 tolerance, INT8 / INT4 bit-exact against the oracle."""
+FP16 within the FP16 tolerance, INT8 / INT4 bit-exact against the oracle; on
+half of the shapes also the FP16-accumulator product (within its bound), the
+dequantising epilogues (bit-exact) and the host-buffer entry points."""
 import numpy as np
 import pytest
 import torch
@@ -82,3 +84,68 @@ def test_random_shape_int(M, N, K, cta_mode):
                        out=out_padded(M, N))
     torch.cuda.synchronize()
     assert np.array_equal(C4.cpu().numpy(), oracle.wrap_s32(oracle.gemm_s4(A4, Bt4, K4)))
+
+
+SUBSET = SHAPES[::2]
+
+
+@pytest.mark.parametrize("M,N,K", SUBSET)
+def test_random_shape_f16acc(M, N, K, cta_mode):
+    """FP16 accumulators: within one binary16 rounding per 16-deep step
+    (|C - sum| <= (ceil(K/16) + 1) 2^-10 S + ceil(K/16) 2^-24)."""
+    A, B = datagen.f16_operands(N, "uniform", seed=M * 3 + N * 5 + K, m=M, k=K)
+    C = ptc.matmul_f16_f16acc(f16_dev(padded(A, 8))[:, :K], f16_dev(padded(B, 8))[:, :N],
+                              out=out_padded(M, N, torch.float16))
+    torch.cuda.synchronize()
+    Cref, S = oracle.gemm_f16(A, B)
+    steps = -(-K // 16)
+    bound = (steps + 1) * 2.0 ** -10 * S + steps * 2.0 ** -24
+    assert np.all(np.abs(C.cpu().numpy().astype(np.float64) - Cref) <= bound)
+
+
+@pytest.mark.parametrize("i,M,N,K", [(i,) + s for i, s in enumerate(SUBSET)])
+def test_random_shape_scaled(i, M, N, K, cta_mode):
+    """Dequantising epilogues, the output type rotating over FP32, BF16, FP16:
+    bit-exact against the oracle's rounding order."""
+    out = (torch.float32, torch.bfloat16, torch.float16)[i % 3]
+    code = {torch.float32: oracle.OUT_F32, torch.bfloat16: oracle.OUT_BF16, torch.float16: oracle.OUT_F16}[out]
+    rng = np.random.default_rng(i)
+    sa = rng.uniform(0.25, 4.0, M).astype(np.float32)
+    sb = rng.uniform(0.25, 4.0, N).astype(np.float32)
+    A, Bt = datagen.s8_operands(N, seed=M + N + K + 17, m=M, k=K)
+    C = ptc.matmul_s8_scaled(int_dev(padded(A, 16))[:, :K], int_dev(padded(Bt, 16))[:, :K],
+                             torch.from_numpy(sa).to(DEV), torch.from_numpy(sb).to(DEV), out=out_padded(M, N, out))
+    K4 = K + (K & 1)
+    A4, Bt4 = datagen.s4_operands(N, seed=M + N + K4 + 23, m=M, k=K4)
+    C4 = ptc.matmul_s4_scaled(int_dev(padded(A4, 16))[:, :K4 // 2], int_dev(padded(Bt4, 16))[:, :K4 // 2], K4,
+                              torch.from_numpy(sa).to(DEV), torch.from_numpy(sb).to(DEV), out=out_padded(M, N, out))
+    torch.cuda.synchronize()
+
+    def bits(t):
+        return (t.cpu().view(torch.int32).numpy().view(np.uint32) if out == torch.float32
+                else t.cpu().view(torch.int16).numpy().view(np.uint16))
+    assert np.array_equal(bits(C), oracle.dequant(oracle.gemm_s8(A, Bt), sa, sb, code))
+    assert np.array_equal(bits(C4), oracle.dequant(oracle.gemm_s4(A4, Bt4, K4), sa, sb, code))
+
+
+@pytest.mark.parametrize("M,N,K", SUBSET)
+def test_random_shape_host_buffers(M, N, K):
+    """The host-buffer entry points (pinned host operands and results,
+    pipelined copies inside the library)."""
+    A, B = datagen.f16_operands(N, "normal", seed=M * 11 + N + K, m=M, k=K)
+    hA = torch.from_numpy(padded(A, 8).view(np.float16)).pin_memory()[:, :K]
+    hB = torch.from_numpy(padded(B, 8).view(np.float16)).pin_memory()[:, :N]
+    hC = torch.empty((M, (N + 3) // 4 * 4), dtype=torch.float32).pin_memory()[:, :N]
+    C = ptc.matmul_f16(hA, hB, out=hC)
+    check_f16(C.numpy(), A, B)
+    A8, Bt8 = datagen.s8_operands(N, seed=M * 13 + N + K, m=M, k=K)
+    h8 = torch.empty((M, (N + 3) // 4 * 4), dtype=torch.int32).pin_memory()[:, :N]
+    C8 = ptc.matmul_s8(torch.from_numpy(padded(A8, 16)).pin_memory()[:, :K],
+                       torch.from_numpy(padded(Bt8, 16)).pin_memory()[:, :K], out=h8)
+    assert np.array_equal(C8.numpy(), oracle.wrap_s32(oracle.gemm_s8(A8, Bt8)))
+    K4 = K + (K & 1)
+    A4, Bt4 = datagen.s4_operands(N, seed=M * 17 + N + K4, m=M, k=K4)
+    h4 = torch.empty((M, (N + 3) // 4 * 4), dtype=torch.int32).pin_memory()[:, :N]
+    C4 = ptc.matmul_s4(torch.from_numpy(padded(A4, 16)).pin_memory()[:, :K4 // 2],
+                       torch.from_numpy(padded(Bt4, 16)).pin_memory()[:, :K4 // 2], K4, out=h4)
+    assert np.array_equal(C4.numpy(), oracle.wrap_s32(oracle.gemm_s4(A4, Bt4, K4)))
