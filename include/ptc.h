@@ -489,10 +489,14 @@ int ptc_last_conversion(int *mode);
  *                  sharing A by TMA multicast (each CTA loads half of its 128
  *                  A rows into its own shared memory and its counterpart's in
  *                  the other pair), which cuts the operand bytes the SMs read
- *                  from L2 by a quarter.  Clusters of four fit 144 of the
- *                  152 SMs, and the last-wave K split is not used.  The
- *                  in-kernel pair conversion ("pair_in_ring" 2) keeps one
- *                  pair per cluster.  Results do not depend on the choice.
+ *                  from L2 by a quarter (not the bytes each SM receives).
+ *                  Clusters of four fit 144 of the 152 SMs, and the
+ *                  last-wave K split is not used.  Measured on GB300 it is
+ *                  no faster (N = 8192: FP16 +3.9%, INT8 +2.2%, INT4 -1.0%
+ *                  time; N = 4096 and 6144 within +-4%), so it is off by
+ *                  default.  The in-kernel pair conversion ("pair_in_ring" 2)
+ *                  keeps one pair per cluster.  Results do not depend on the
+ *                  choice.
  *   "clock_probe"  0 (default) or 1: GEMM kernels add their SM cycles and
  *                  nanoseconds to the clock record (ptc_clock_probe_read)
  *   "in_ring"      gemm_s8 / gemm_s4 (and their scaled forms) on one-CTA
