@@ -149,3 +149,16 @@ def test_random_shape_host_buffers(M, N, K):
     C4 = ptc.matmul_s4(torch.from_numpy(padded(A4, 16)).pin_memory()[:, :K4 // 2],
                        torch.from_numpy(padded(Bt4, 16)).pin_memory()[:, :K4 // 2], K4, out=h4)
     assert np.array_equal(C4.numpy(), oracle.wrap_s32(oracle.gemm_s4(A4, Bt4, K4)))
+
+
+@pytest.mark.parametrize("M,N,K", SUBSET)
+def test_random_shape_s8_rowmajor_b(M, N, K, cta_mode):
+    """INT8 with B row-major (K x N), read MN-major: bit-exact."""
+    A, Bt = datagen.s8_operands(N, seed=M * 19 + N + K, m=M, k=K)
+    B_kn = np.ascontiguousarray(Bt.T)
+    Ad, Bd = int_dev(padded(A, 16)), int_dev(padded(B_kn, 16))
+    C = out_padded(M, N)
+    ptc.gemm_s8_b_rowmajor(M, N, K, Ad.data_ptr(), Ad.shape[1], Bd.data_ptr(), Bd.shape[1], C.data_ptr(),
+                           C.stride(0), torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert np.array_equal(C.cpu().numpy(), oracle.wrap_s32(oracle.gemm_s8(A, Bt)))

@@ -107,3 +107,23 @@ def test_noalloc_calls_allocate_nothing():
     assert torch.cuda.memory_reserved() == reserved0 and torch.cuda.memory_allocated() <= allocated0
     assert np.array_equal(C.cpu().numpy(), oracle.wrap_s32(oracle.gemm_s8(A, Bt)))
     assert ptc.gemm_poll_device_error() == ptc.PTC_OK
+
+
+@pytest.mark.parametrize("M,N,K", [(3, 107, 30), (120, 556, 966), (324, 749, 3), (8, 1178, 834), (43, 419, 26),
+                                   (1130, 691, 509), (1, 26, 14), (995, 248, 294), (61, 23, 724), (1407, 625, 1196)])
+def test_noalloc_random_shapes_exact(M, N, K):
+    """Seeded random shapes (after the first-call tests above), pitches padded
+    to 16 bytes: bit-exact against the oracle."""
+    A, Bt = datagen.s8_operands(N, seed=M * 7 + N * 3 + K, m=M, k=K)
+    lda = max(16, (K + 15) // 16 * 16)
+    Ap = np.zeros((M, lda), np.int8)
+    Ap[:, :K] = A
+    Bp = np.zeros((N, lda), np.int8)
+    Bp[:, :K] = Bt
+    ldc = (N + 3) // 4 * 4
+    Ad, Bd = torch.from_numpy(Ap).to(DEV), torch.from_numpy(Bp).to(DEV)
+    C = torch.full((M, ldc), -1, dtype=torch.int32, device=DEV)
+    ptc.gemm_s8_noalloc(M, N, K, Ad.data_ptr(), lda, Bd.data_ptr(), lda, C.data_ptr(), ldc,
+                        torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert np.array_equal(C.cpu().numpy()[:, :N], oracle.wrap_s32(oracle.gemm_s8(A, Bt)))
